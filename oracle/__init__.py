@@ -1,0 +1,193 @@
+"""ctypes access to the plain C oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the package smoke check
+in ``__graft_entry__.py`` and by the CPU-baseline leg of ``bench.py``. The
+CUDA library never imports, links or calls anything here, and the oracle
+imports nothing from the CUDA side.
+
+Arrays cross as numpy buffers; bf16 tensors are ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (-O2, plain scalar code, IEEE semantics)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-fno-fast-math", "-ffp-contract=off",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+            lib.oracle_bf16_from_double.argtypes = [f64]
+            lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = f64
+            lib.oracle_gate_logits.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
+            lib.oracle_gate_logits.restype = None
+            lib.oracle_select.argtypes = [i32, i32, P, P, P]
+            lib.oracle_select.restype = None
+            lib.oracle_shared_weight.argtypes = [f64, f32]
+            lib.oracle_shared_weight.restype = f32
+            lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, f32, P, i64, P, P, P,
+                                         P, P, P, P, P, P]
+            lib.oracle_route.restype = None
+            lib.oracle_select_block_size.argtypes = [i32, i32, i32]
+            lib.oracle_select_block_size.restype = i32
+            lib.oracle_align_capacity.argtypes = [i64, i32, i32]
+            lib.oracle_align_capacity.restype = i64
+            lib.oracle_align.argtypes = [P, i64, i32, i32, P, i64, P, i64, P]
+            lib.oracle_align.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+# --- scalar helpers -----------------------------------------------------------
+
+def bf16_from_double(v: float) -> int:
+    return int(_load().oracle_bf16_from_double(float(v)))
+
+
+def bf16_to_double(b: int) -> float:
+    return float(_load().oracle_bf16_to_double(int(b) & 0xFFFF))
+
+
+def bf16_round(values: np.ndarray) -> np.ndarray:
+    """Round each double to bf16 (RNE), returned as doubles."""
+    lib = _load()
+    flat = np.asarray(values, dtype=np.float64).ravel()
+    out = np.array([lib.oracle_bf16_to_double(lib.oracle_bf16_from_double(float(v)))
+                    for v in flat], dtype=np.float64)
+    return out.reshape(np.shape(values))
+
+
+# --- route ---------------------------------------------------------------------
+
+def gate_logits(x: np.ndarray, w: np.ndarray, bias: Optional[np.ndarray] = None):
+    """fp64 logits z [M,E] and sum|x*W| [M,E] for bf16-bit inputs."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    M, H = x.shape
+    E = w.shape[0]
+    z = np.empty((M, E), dtype=np.float64)
+    ad = np.empty((M, E), dtype=np.float64)
+    _load().oracle_gate_logits(M, H, E, _ptr(x), H, _ptr(w), _ptr(_c(bias, np.float32)),
+                               _ptr(z), _ptr(ad))
+    return z, ad
+
+
+def select(zhat_row: np.ndarray, k: int):
+    """Top-k (value desc, id asc) and renormalised softmax of one row."""
+    z = _c(zhat_row, np.float64)
+    ids = np.empty(k, dtype=np.int32)
+    w = np.empty(k, dtype=np.float32)
+    _load().oracle_select(z.shape[0], k, _ptr(z), _ptr(ids), _ptr(w))
+    return ids, w
+
+
+def select_rows(zhat: np.ndarray, k: int):
+    zhat = _c(zhat, np.float64)
+    M = zhat.shape[0]
+    ids = np.empty((M, k), dtype=np.int32)
+    w = np.empty((M, k), dtype=np.float32)
+    for t in range(M):
+        ids[t], w[t] = select(zhat[t], k)
+    return ids, w
+
+
+def shared_weight(s: float, scale: float) -> float:
+    return float(_load().oracle_shared_weight(float(s), float(scale)))
+
+
+class RouteResult:
+    def __init__(self, ids, w, zhat, z, absdot, s):
+        self.ids, self.w, self.zhat, self.z, self.absdot, self.s = ids, w, zhat, z, absdot, s
+
+
+def route(x: np.ndarray, w: np.ndarray, ws: Optional[np.ndarray], bias: Optional[np.ndarray],
+          topk: int, scale: float = 1.0, rows: Optional[np.ndarray] = None) -> RouteResult:
+    """Full oracle route. ``rows`` restricts it to a subset of token rows."""
+    x = _c(x, np.uint16)
+    if rows is not None:
+        x = np.ascontiguousarray(x[np.asarray(rows)])
+    w = _c(w, np.uint16)
+    ws = _c(ws, np.uint16)
+    bias = _c(bias, np.float32)
+    M, H = x.shape
+    E = w.shape[0]
+    S = 1 if ws is not None else 0
+    width = topk + S
+    ids = np.empty((M, width), dtype=np.int32)
+    wt = np.empty((M, width), dtype=np.float32)
+    zhat = np.empty((M, E), dtype=np.float64)
+    z = np.empty((M, E), dtype=np.float64)
+    ad = np.empty((M, E), dtype=np.float64)
+    s = np.zeros(M, dtype=np.float64)
+    _load().oracle_route(M, H, E, topk, S, float(scale), _ptr(x), H, _ptr(w), _ptr(ws),
+                         _ptr(bias), _ptr(ids), _ptr(wt), _ptr(zhat), _ptr(z), _ptr(ad),
+                         _ptr(s))
+    return RouteResult(ids, wt, zhat, z, ad, s)
+
+
+# --- align ---------------------------------------------------------------------
+
+def select_block_size(num_tokens: int, topk: int, num_experts: int) -> int:
+    return int(_load().oracle_select_block_size(num_tokens, topk, num_experts))
+
+
+def align_capacity(numel: int, num_experts: int, A: int) -> int:
+    return int(_load().oracle_align_capacity(numel, num_experts, A))
+
+
+class AlignResult:
+    def __init__(self, sorted_ids, expert_ids, npp):
+        self.sorted_ids, self.expert_ids, self.npp = sorted_ids, expert_ids, npp
+
+
+def align(ids: np.ndarray, num_experts: int, A: int) -> AlignResult:
+    """Sequential moe_align_block_size. Returns only the defined prefixes."""
+    flat = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).ravel())
+    numel = flat.shape[0]
+    cap = align_capacity(numel, num_experts, A)
+    sorted_ids = np.full(max(cap, 1), -7, dtype=np.int32)
+    expert_ids = np.full(max((cap + A - 1) // A, 1), -7, dtype=np.int32)
+    npp = np.zeros(1, dtype=np.int32)
+    rc = _load().oracle_align(_ptr(flat), numel, num_experts, A, _ptr(sorted_ids), cap,
+                              _ptr(expert_ids), expert_ids.shape[0], _ptr(npp))
+    if rc != 0:
+        raise ValueError("oracle_align: id out of range or capacity too small")
+    n = int(npp[0])
+    return AlignResult(sorted_ids[:n].copy(), expert_ids[: n // A].copy(), n)

@@ -1,0 +1,232 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for the MoE routing front-end.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or calls
+ * this file; only the tests, the package smoke check and the CPU-baseline leg
+ * of the benchmark do. It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * Every step is the plain definition, evaluated in fp64, in the order the
+ * pages give it:
+ *
+ *  1. gate GEMM: z[t,e] = sum_h x[t,h] * W[e,h] (+ bias[e]), summed in double.
+ *     "[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950",
+ *     Modifications (one launch computes the 513 gate rows: 512 routed plus
+ *     the shared-expert gate, read in place) and Accuracy Tests (the
+ *     fp64-then-bf16 reference).
+ *  2. the routed logits are rounded to bf16 (round to nearest even) straight
+ *     from the double, with no intermediate fp32 rounding. Same page,
+ *     Modifications ("rounds the routed logits to bf16") and Accuracy Tests.
+ *  3. top-k over the rounded logits; equal values go to the lowest expert id,
+ *     and slots are ordered by (value desc, id asc), the order k successive
+ *     argmax passes produce. Same page, Motivation and Modifications.
+ *  4. softmax over the E experts followed by renormalising the k selected
+ *     weights, which equals a softmax over the selected logits (the full
+ *     denominator cancels). Same page, Motivation.
+ *  5. shared slot k = (E, scale * sigmoid(shared logit)); the shared logit is
+ *     the unrounded fp64 dot (only the routed logits are rounded). Same page,
+ *     Modifications; expert id E = 512 as the shared expert also in the
+ *     vLLM "--monokernel decode" pull request (#60833), Details (Launches).
+ *  6. moe_align_block_size: per-expert counts over all slots, padded prefix
+ *     sum off[e+1] = off[e] + ceil(cnt[e]/A)*A, num_tokens_post_padded =
+ *     off[E_al], stable scatter of flat slot indices, sentinel padding and one
+ *     expert id per block. "[ROCm][Kernel] W4A16 MoE prefill: M-aware
+ *     moe_align block size", Purpose.
+ *  7. M-aware tier: A = 64 while num_tokens*topk/E is below one full
+ *     128-row block per expert, else 128. Same page, Purpose (commit 2) and
+ *     Scope and safety (2048+ tokens keep the large tier).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+/* ---------------------------------------------------------------- bf16 --- */
+
+/* bf16: 1 sign bit, 8 exponent bits (bias 127), 7 stored fraction bits.
+ * Normal numbers carry 8 significant bits; below 2^-126 the spacing is fixed
+ * at 2^-133 (subnormals). The largest finite value is (2 - 2^-7) * 2^127. */
+ORACLE_API uint16_t oracle_bf16_from_double(double v)
+{
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    int e2;
+    frexp(a, &e2);                 /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;                /* a in [2^e, 2^(e+1)) */
+    if (e < -126) e = -126;        /* subnormal range: fixed spacing */
+    double q = ldexp(1.0, e - 7);  /* spacing of bf16 values near a */
+    double n = nearbyint(a / q);   /* a/q is exact; default mode is RNE */
+    double r = n * q;
+    if (r >= ldexp(2.0, 127)) return (uint16_t)(sign | 0x7F80);  /* overflow */
+    float f = (float)r;            /* exact: r has <= 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    return (uint16_t)(sign | ((bits >> 16) & 0x7FFF));
+}
+
+ORACLE_API double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+/* --------------------------------------------------------- gate GEMM --- */
+
+/* z[t*E + e] = sum_h x[t,h]*W[e,h] + bias[e] in double; absdot (optional)
+ * gets sum_h |x[t,h]*W[e,h]| + |bias[e]|, the scale of the rounding error a
+ * finite-precision accumulation of the same sum can make. */
+ORACLE_API void oracle_gate_logits(int M, int H, int E, const uint16_t *x, int64_t ld_x,
+                                   const uint16_t *W, const float *bias,
+                                   double *z, double *absdot)
+{
+    for (int t = 0; t < M; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0, aacc = 0.0;
+            for (int h = 0; h < H; ++h) {
+                double p = oracle_bf16_to_double(x[(int64_t)t * ld_x + h]) *
+                           oracle_bf16_to_double(W[(int64_t)e * H + h]);
+                acc += p;
+                aacc += fabs(p);
+            }
+            if (bias) {
+                acc += (double)bias[e];
+                aacc += fabs((double)bias[e]);
+            }
+            z[(int64_t)t * E + e] = acc;
+            if (absdot) absdot[(int64_t)t * E + e] = aacc;
+        }
+    }
+}
+
+/* ------------------------------------------------- top-k and softmax --- */
+
+typedef struct { double v; int id; } scored;
+
+/* (value desc, id asc); -0 and +0 compare equal as values. */
+static int by_value_then_id(const void *pa, const void *pb)
+{
+    const scored *a = (const scored *)pa, *b = (const scored *)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id);
+}
+
+/* One token row: zhat[E] are the bf16-rounded logits (as doubles). Writes
+ * ids[k] (slot order: value desc, id asc) and w[k] = softmax over the
+ * selected logits, computed in double and rounded once to fp32. */
+ORACLE_API void oracle_select(int E, int k, const double *zhat, int32_t *ids, float *w)
+{
+    scored *s = (scored *)malloc(sizeof(scored) * (size_t)E);
+    for (int e = 0; e < E; ++e) { s[e].v = zhat[e]; s[e].id = e; }
+    qsort(s, (size_t)E, sizeof(scored), by_value_then_id);
+    double zmax = s[0].v;
+    double denom = 0.0;
+    for (int i = 0; i < k; ++i) denom += exp(s[i].v - zmax);
+    for (int i = 0; i < k; ++i) {
+        ids[i] = s[i].id;
+        w[i] = (float)(exp(s[i].v - zmax) / denom);
+    }
+    free(s);
+}
+
+/* Shared slot weight: scale * sigmoid(s), s the unrounded shared logit. */
+ORACLE_API float oracle_shared_weight(double s, float scale)
+{
+    return (float)((double)scale * (1.0 / (1.0 + exp(-s))));
+}
+
+/* Full route for M rows. Outputs ids/w are [M, k+S] row-major. Optional:
+ * zhat_out [M,E] (rounded logits as doubles), z_out [M,E] (unrounded),
+ * absdot_out [M,E], s_out [M] (shared logit). */
+ORACLE_API void oracle_route(int M, int H, int E, int k, int has_shared, float scale,
+                             const uint16_t *x, int64_t ld_x, const uint16_t *W,
+                             const uint16_t *Ws, const float *bias,
+                             int32_t *ids, float *w,
+                             double *zhat_out, double *z_out, double *absdot_out,
+                             double *s_out)
+{
+    int width = k + (has_shared ? 1 : 0);
+    double *z = (double *)malloc(sizeof(double) * (size_t)E);
+    double *zh = (double *)malloc(sizeof(double) * (size_t)E);
+    double *ad = absdot_out ? (double *)malloc(sizeof(double) * (size_t)E) : NULL;
+    for (int t = 0; t < M; ++t) {
+        const uint16_t *xt = x + (int64_t)t * ld_x;
+        oracle_gate_logits(1, H, E, xt, ld_x, W, bias, z, ad);
+        for (int e = 0; e < E; ++e)
+            zh[e] = oracle_bf16_to_double(oracle_bf16_from_double(z[e]));
+        oracle_select(E, k, zh, ids + (int64_t)t * width, w + (int64_t)t * width);
+        if (has_shared) {
+            double s;
+            oracle_gate_logits(1, H, 1, xt, ld_x, Ws, NULL, &s, NULL);
+            ids[(int64_t)t * width + k] = E;
+            w[(int64_t)t * width + k] = oracle_shared_weight(s, scale);
+            if (s_out) s_out[t] = s;
+        }
+        if (zhat_out) memcpy(zhat_out + (int64_t)t * E, zh, sizeof(double) * (size_t)E);
+        if (z_out) memcpy(z_out + (int64_t)t * E, z, sizeof(double) * (size_t)E);
+        if (absdot_out) memcpy(absdot_out + (int64_t)t * E, ad, sizeof(double) * (size_t)E);
+    }
+    free(z);
+    free(zh);
+    free(ad);
+}
+
+/* ------------------------------------------------------------- align --- */
+
+/* M-aware alignment tier: 64 below one full 128-row block of routed rows per
+ * expert (num_tokens*topk/E < 128), 128 at or above it. */
+ORACLE_API int oracle_select_block_size(int num_tokens, int topk, int num_experts)
+{
+    return ((int64_t)num_tokens * topk < (int64_t)128 * num_experts) ? 64 : 128;
+}
+
+/* Worst-case num_tokens_post_padded: every slot plus A-1 padding rows per
+ * expert (the workspace num_slots of the alignment page). */
+ORACLE_API int64_t oracle_align_capacity(int64_t numel, int num_experts, int A)
+{
+    return numel + (int64_t)num_experts * (A - 1);
+}
+
+/* Sequential moe_align_block_size. ids[numel] hold expert ids in
+ * [0, num_experts); the flat slot index i = t*width + s is the value stored.
+ * sorted[0, npp) and expert_ids[0, npp/A) are written; padding = numel.
+ * Returns 0, or -1 if an id is out of range or a capacity is too small. */
+ORACLE_API int oracle_align(const int32_t *ids, int64_t numel, int num_experts, int A,
+                            int32_t *sorted, int64_t sorted_cap,
+                            int32_t *expert_ids, int64_t expert_cap, int32_t *npp_out)
+{
+    int64_t *cnt = (int64_t *)calloc((size_t)num_experts, sizeof(int64_t));
+    int64_t *off = (int64_t *)calloc((size_t)num_experts + 1, sizeof(int64_t));
+    int64_t *cur = (int64_t *)calloc((size_t)num_experts, sizeof(int64_t));
+    int rc = 0;
+    /* per-expert counts */
+    for (int64_t i = 0; i < numel; ++i) {
+        if (ids[i] < 0 || ids[i] >= num_experts) { rc = -1; goto done; }
+        cnt[ids[i]] += 1;
+    }
+    /* padded prefix sum */
+    for (int e = 0; e < num_experts; ++e)
+        off[e + 1] = off[e] + (cnt[e] + A - 1) / A * A;
+    if (off[num_experts] > sorted_cap || off[num_experts] / A > expert_cap) { rc = -1; goto done; }
+    /* stable scatter in ascending flat index */
+    for (int e = 0; e < num_experts; ++e) cur[e] = off[e];
+    for (int64_t i = 0; i < numel; ++i) sorted[cur[ids[i]]++] = (int32_t)i;
+    /* padding rows and per-block expert ids */
+    for (int e = 0; e < num_experts; ++e) {
+        for (int64_t p = off[e] + cnt[e]; p < off[e + 1]; ++p) sorted[p] = (int32_t)numel;
+        for (int64_t b = off[e] / A; b < off[e + 1] / A; ++b) expert_ids[b] = e;
+    }
+    *npp_out = (int32_t)off[num_experts];
+done:
+    free(cnt);
+    free(off);
+    free(cur);
+    return rc;
+}
