@@ -1,0 +1,170 @@
+/*
+ * smr.h -- C ABI of the GB300 (sm_103a) MoE routing front-end.
+ *
+ * The library computes, for M tokens with hidden size H, E routed experts and
+ * an optional shared expert (S = 1):
+ *
+ *   route  : gate GEMM [M,H] x [E+S,H] (bf16 in, fp32 accumulation), the
+ *            routed logits rounded to bf16, top-k with the lowest expert id
+ *            winning ties, softmax + renormalisation over the k selected,
+ *            and the shared slot k = (E, sigmoid(shared logit) * scale).
+ *            "[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950",
+ *            Motivation and Modifications.
+ *   align  : moe_align_block_size -- per-expert counts, padded prefix sum,
+ *            sorted_token_ids, one expert id per block and
+ *            num_tokens_post_padded = sum over touched experts of
+ *            ceil(tokens_e / A) * A, with the M-aware choice of A.
+ *            "[ROCm][Kernel] W4A16 MoE prefill: M-aware moe_align block size
+ *            (1.6x TTFT)", Purpose and Scope and safety.
+ *
+ * Conventions (all entry points):
+ *  - Every tensor argument is a DEVICE pointer owned by the caller. The
+ *    library never allocates, frees, looks up symbols, touches the file
+ *    system or synchronises the host on a launch path; kernels are enqueued
+ *    on the caller's stream (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream). The same pointers and sizes replay correctly inside a
+ *    captured CUDA graph ("Netra Kernel ...", Compile exact contracts, not
+ *    model names: fixed pointers, no allocation or host sync on replay).
+ *  - Calls outside the supported contract are refused before any launch with
+ *    SMR_ERR_INVALID_ARG or SMR_ERR_UNSUPPORTED; smr_last_error() then lists
+ *    every reason, so the caller can fall back to another implementation
+ *    ("[AMD] One-launch small-M MoE router ...", Modifications: guarded call,
+ *    everything else takes the existing path).
+ *  - Workspace: a caller-owned device buffer of at least the size the
+ *    matching *_workspace_size() returns, 256-byte aligned, ZEROED ONCE by
+ *    the caller before its first use (cudaMemsetAsync). The library leaves
+ *    its counters at zero after every call, so the buffer can be reused by
+ *    later calls and graph replays without clearing. Calls that share a
+ *    workspace must not run concurrently.
+ *  - Inputs must be finite. NaN or Inf in hidden states, gate weights or
+ *    bias give unspecified (but in-bounds) results.
+ */
+#ifndef SMR_H_
+#define SMR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SMR_API __attribute__((visibility("default")))
+#else
+#define SMR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum smr_status {
+    SMR_OK = 0,
+    SMR_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, too-small capacity */
+    SMR_ERR_UNSUPPORTED = 2,  /* valid request outside the implemented contract */
+    SMR_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
+    SMR_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    SMR_ERR_DEVICE = 5        /* no usable sm_103 device is current */
+} smr_status;
+
+/* Route problem. Row-major tensors; sizes in elements unless stated. */
+typedef struct smr_route_args {
+    int32_t M;               /* tokens, >= 0 */
+    int32_t H;               /* hidden size, multiple of 8, 8..16384 */
+    int32_t E;               /* routed experts, 1..1024 */
+    int32_t topk;            /* routed top-k, 1..E, topk + has_shared <= 32 */
+    int32_t has_shared;      /* S: 1 = shared expert with id E, 0 = none */
+    float shared_scale;      /* multiplies sigmoid(shared logit) */
+    int32_t renormalize;     /* must be 1 (softmax renormalised over the top-k) */
+    const void *hidden;      /* bf16 [M, ld_hidden], 16-byte aligned */
+    int64_t ld_hidden;       /* row stride of hidden in elements, >= H, multiple of 8 */
+    const void *gate_w;      /* bf16 [E, H] contiguous (nn.Linear layout), 16-byte aligned */
+    const void *shared_w;    /* bf16 [1, H], 16-byte aligned; NULL iff has_shared == 0 */
+    const float *bias;       /* fp32 [E] added to each routed fp32 logit before the
+                                bf16 rounding, or NULL */
+    int32_t *topk_ids;       /* out: int32 [M, topk + S]; slots 0..topk-1 in order of
+                                (rounded logit desc, id asc); slot topk = E if S */
+    float *topk_weights;     /* out: fp32 [M, topk + S] */
+    uint16_t *logits_out;    /* optional out: bf16 bits [M, E] of the rounded routed
+                                logits (bias included); NULL to skip */
+} smr_route_args;
+
+/* Align problem over a [num_tokens, width] id matrix. */
+typedef struct smr_align_args {
+    const int32_t *topk_ids;      /* int32 [num_tokens, width], ids in [0, num_experts) */
+    int32_t num_tokens;           /* >= 0 */
+    int32_t width;                /* slots per token (topk + S), >= 1 */
+    int32_t num_experts;          /* E_al = E + S, 1..1024 */
+    int32_t routed_topk;          /* k and E used by the M-aware tier (block_size == 0) */
+    int32_t routed_experts;
+    int32_t block_size;           /* A >= 1, or 0 = smr_select_block_size(num_tokens,
+                                     routed_topk, routed_experts) */
+    int32_t *sorted_token_ids;    /* out: int32 [sorted_cap]; [0, npp) defined: flat slot
+                                     index t*width+s grouped by expert, ascending inside
+                                     each expert, padding rows = num_tokens*width */
+    int64_t sorted_cap;           /* >= smr_align_capacity(num_tokens*width, num_experts, A) */
+    int32_t *expert_ids;          /* out: int32 [expert_cap]; [0, npp/A) defined */
+    int64_t expert_cap;           /* >= ceil(smr_align_capacity(...) / A) */
+    int32_t *num_tokens_post_padded;  /* out: device int32 [1] = npp */
+} smr_align_args;
+
+/* M-aware alignment tier (host, no device work): 64 if
+ * num_tokens * topk < 128 * num_experts (fewer than one full 128-row block of
+ * routed rows per expert), else 128. Returns -1 on non-positive topk or
+ * num_experts or negative num_tokens. */
+SMR_API int32_t smr_select_block_size(int32_t num_tokens, int32_t topk, int32_t num_experts);
+
+/* Worst-case num_tokens_post_padded: numel + num_experts * (A - 1) (the
+ * workspace num_slots formula of the alignment page, Scope and safety).
+ * Returns -1 on invalid arguments. */
+SMR_API int64_t smr_align_capacity(int64_t numel, int32_t num_experts, int32_t block_size);
+
+/* Workspace bytes for one call with these arguments (0 if none is needed);
+ * pointers inside args are not read. */
+SMR_API size_t smr_route_workspace_size(const smr_route_args *args);
+SMR_API size_t smr_align_workspace_size(const smr_align_args *args);
+SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const smr_align_args *align);
+
+/* Route only. One kernel launch for M <= 16 (gate rows split across CTAs,
+ * last CTA does top-k); for M > 16 one tcgen05 GEMM launch with the top-k
+ * fused into its epilogue, which requires E % 32 == 0 and 32 <= E <= 512
+ * (other E with M > 16 are refused with SMR_ERR_UNSUPPORTED).
+ * M == 0 launches nothing. */
+SMR_API smr_status smr_route(const smr_route_args *args, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* Align only: reads topk_ids, writes sorted_token_ids, expert_ids and
+ * num_tokens_post_padded. An id outside [0, num_experts) is skipped and sets
+ * the sticky device error word (see smr_get_device_error). */
+SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* Route then align on the route's output. align->topk_ids must equal
+ * route->topk_ids, align->num_tokens == route->M, align->width == topk + S,
+ * align->num_experts == E + S; routed_topk/routed_experts are taken from the
+ * route. For M <= 16 both run in ONE launch. */
+SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_args *align,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Sticky device error word of a workspace: synchronises `stream`, then copies
+ * the word to *code_out (0 = no error; bit 0 = an id out of range in align,
+ * bit 1 = a bounded wait inside a kernel gave up). Not for launch paths. */
+SMR_API smr_status smr_get_device_error(const void *workspace, void *stream, int32_t *code_out);
+
+/* Clears the sticky device error word (stream-ordered memset). */
+SMR_API smr_status smr_clear_device_error(void *workspace, void *stream);
+
+/* Static string for a status; thread-local text of the last refusal (every
+ * reason, "; "-separated) or CUDA error on this thread, "" if none. */
+SMR_API const char *smr_status_string(smr_status status);
+SMR_API const char *smr_last_error(void);
+
+/* Library version, 0xMMmmpp. */
+SMR_API int32_t smr_version(void);
+
+/* Number of kernels the most recent successful smr_route / smr_align /
+ * smr_route_align call on this thread enqueued (0 after a refusal). */
+SMR_API int32_t smr_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMR_H_ */

@@ -1,0 +1,115 @@
+// smr_align.cu -- moe_align_block_size kernels.
+//
+// "[ROCm][Kernel] W4A16 MoE prefill: M-aware moe_align block size (1.6x
+// TTFT)", Purpose: every touched expert is padded up to a full alignment
+// block of A rows; num_tokens_post_padded = sum over touched experts of
+// ceil(tokens_e / A) * A. The output order inside an expert is ascending flat
+// slot index, so results are deterministic and bit-identical across runs.
+//
+//  - numel <= kAlignSingleMax: one CTA of 512 threads does count, scan,
+//    scatter and padding (one launch);
+//  - larger inputs: align_hist_kernel writes per-tile expert counts to the
+//    workspace, then align_scatter_kernel (one CTA per tile) derives the
+//    global segment offsets from all tile counts (a short fixed-order loop),
+//    scatters its tile and writes its share of padding rows and block expert
+//    ids (two launches, no inter-CTA waiting).
+#include "smr_device.cuh"
+#include "smr_launch.h"
+
+namespace smr {
+
+constexpr int kAlignThreads = 512;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+__global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const AlignLaunch a) {
+    extern __shared__ int sm[];
+    uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
+    AlignSmem s = align_carve(sm, a.E_al);
+    align_count(a.ids, a.numel, a.E_al, s, err);
+    const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
+    align_scatter(a.ids, a.numel, a.E_al, 0, s, false, a.sorted);
+    align_blocks(npp, a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids, threadIdx.x >> 5,
+                 kAlignWarps);
+    if (threadIdx.x == 0) *a.npp = npp;
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLaunch a) {
+    extern __shared__ int cnt[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
+    for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int beg = blockIdx.x * kAlignTile, end = min(beg + kAlignTile, a.numel);
+    for (int b = beg + warp * 32; b < end; b += kAlignThreads) {
+        const int i = b + lane;
+        int e = (i < end) ? a.ids[i] : -1;
+        if (i < end && (unsigned)e >= (unsigned)a.E_al) {
+            set_error(err, kErrBadId);
+            e = -1;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[e], __popc(peers));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E_al; e += blockDim.x)
+        a.tile_counts[(int64_t)blockIdx.x * a.E_al + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const AlignLaunch a) {
+    extern __shared__ int sm[];
+    uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
+    AlignSmem s = align_carve(sm, a.E_al);
+    const int t = blockIdx.x, ntiles = gridDim.x;
+    const int beg = t * kAlignTile, n = min(beg + kAlignTile, a.numel) - beg;
+    align_count(a.ids + beg, n, a.E_al, s, err);  // per-warp starts inside this tile
+    for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) {
+        int base = 0, tot = 0;
+        for (int u = 0; u < ntiles; ++u) {
+            const int c = a.tile_counts[(int64_t)u * a.E_al + e];
+            base += (u < t) ? c : 0;
+            tot += c;
+        }
+        s.base[e] = base;
+        s.cnt[e] = tot;
+    }
+    __syncthreads();
+    const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
+    align_scatter(a.ids + beg, n, a.E_al, beg, s, true, a.sorted);
+    align_blocks(npp, a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids,
+                 t * kAlignWarps + (threadIdx.x >> 5), ntiles * kAlignWarps);
+    if (t == 0 && threadIdx.x == 0) *a.npp = npp;
+}
+
+static cudaError_t set_smem(const void *kern, size_t bytes) {
+    static bool done[3][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int slot = kern == (const void *)align_single_kernel ? 0
+             : kern == (const void *)align_scatter_kernel ? 1 : 2;
+    if (dev < 64 && !done[slot][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)bytes);
+        if (e != cudaSuccess) return e;
+        done[slot][dev] = true;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream) {
+    const size_t smem = (size_t)align_smem_words(kAlignWarps, a.E_al) * 4;
+    const size_t smem_max = (size_t)align_smem_words(kAlignWarps, 1025) * 4;
+    cudaError_t e;
+    if (a.numel <= kAlignSingleMax) {
+        if ((e = set_smem((const void *)align_single_kernel, smem_max)) != cudaSuccess) return e;
+        align_single_kernel<<<1, kAlignThreads, smem, stream>>>(a);
+        return cudaGetLastError();
+    }
+    const int ntiles = align_num_tiles(a.numel);
+    align_hist_kernel<<<ntiles, kAlignThreads, (size_t)a.E_al * 4, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = set_smem((const void *)align_scatter_kernel, smem_max)) != cudaSuccess) return e;
+    align_scatter_kernel<<<ntiles, kAlignThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace smr

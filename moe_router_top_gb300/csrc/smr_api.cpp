@@ -1,0 +1,409 @@
+// smr_api.cpp -- the C ABI (include/smr.h): argument validation with every
+// refusal reason, workspace layout, dispatch to the kernels, error reporting.
+//
+// Dispatch ("[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950",
+// Modifications, for the guarded single launch; "[ROCm][Kernel] W4A16 MoE
+// prefill: M-aware moe_align block size", Purpose, for the alignment tier):
+//   route_align, M <= 16 : 1 launch  (small route + fused align)
+//   route_align, M > 16  : 1 tcgen05 route launch + 1 or 2 align launches
+//   route        : 1 launch;  align : 1 launch (numel <= 8192) or 2.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "smr.h"
+#include "smr_launch.h"
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kWsAlign = 256;
+constexpr int kMaxH = 16384;
+constexpr int kMaxExperts = 1024;
+
+thread_local std::string g_last_error;
+thread_local int g_last_launches = 0;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Reasons {
+    std::vector<std::string> invalid, unsupported;
+    void bad(const std::string &s) { invalid.push_back(s); }
+    void unsup(const std::string &s) { unsupported.push_back(s); }
+    bool ok() const { return invalid.empty() && unsupported.empty(); }
+    smr_status finish(const char *what) {
+        std::string msg;
+        for (auto &r : invalid) msg += (msg.empty() ? "" : "; ") + r;
+        for (auto &r : unsupported) msg += (msg.empty() ? "" : "; ") + r;
+        g_last_error = std::string(what) + ": " + msg;
+        g_last_launches = 0;
+        return invalid.empty() ? SMR_ERR_UNSUPPORTED : SMR_ERR_INVALID_ARG;
+    }
+};
+
+smr_status cuda_fail(const char *what, cudaError_t e) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    g_last_launches = 0;
+    return SMR_ERR_CUDA;
+}
+
+// The kernels are built for sm_103a only.
+smr_status check_device() {
+    static int cached[64] = {};  // 0 unknown, 1 ok, 2 bad
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        g_last_error = std::string("no current CUDA device: ") + cudaGetErrorString(e);
+        return SMR_ERR_DEVICE;
+    }
+    if (dev < 64 && cached[dev] == 1) return SMR_OK;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    const bool ok = (major == 10 && minor == 3);
+    if (dev < 64) cached[dev] = ok ? 1 : 2;
+    if (!ok) {
+        g_last_error = "device " + std::to_string(dev) + " is sm_" + std::to_string(major) +
+                       std::to_string(minor) + "; this library is built for sm_103a (GB300)";
+        return SMR_ERR_DEVICE;
+    }
+    return SMR_OK;
+}
+
+// --- route ------------------------------------------------------------------
+
+void check_route(const smr_route_args *a, Reasons &r) {
+    if (a->M < 0) r.bad("M must be >= 0 (got " + std::to_string(a->M) + ")");
+    if (a->H < 8 || a->H > kMaxH || a->H % 8 != 0)
+        r.bad("H must be a multiple of 8 in [8, 16384] (got " + std::to_string(a->H) + ")");
+    if (a->E < 1 || a->E > kMaxExperts)
+        r.bad("E must be in [1, 1024] (got " + std::to_string(a->E) + ")");
+    if (a->has_shared != 0 && a->has_shared != 1)
+        r.bad("has_shared must be 0 or 1 (got " + std::to_string(a->has_shared) + ")");
+    const int S = a->has_shared ? 1 : 0;
+    if (a->topk < 1 || a->topk > a->E)
+        r.bad("topk must be in [1, E] (got " + std::to_string(a->topk) + ")");
+    else if (a->topk + S > 32)
+        r.unsup("topk + has_shared must be <= 32 (got " + std::to_string(a->topk + S) + ")");
+    if (a->renormalize != 1)
+        r.unsup("only renormalize == 1 (softmax renormalised over the top-k) is implemented");
+    if (!std::isfinite(a->shared_scale)) r.bad("shared_scale must be finite");
+    if (a->M > 0) {
+        if (!a->hidden) r.bad("hidden is NULL");
+        else if (!aligned(a->hidden, 16)) r.bad("hidden must be 16-byte aligned");
+        if (a->ld_hidden < a->H || a->ld_hidden % 8 != 0)
+            r.bad("ld_hidden must be >= H and a multiple of 8 (got " + std::to_string(a->ld_hidden) + ")");
+        if (!a->gate_w) r.bad("gate_w is NULL");
+        else if (!aligned(a->gate_w, 16)) r.bad("gate_w must be 16-byte aligned");
+        if (S && !a->shared_w) r.bad("shared_w is NULL but has_shared == 1");
+        if (S && a->shared_w && !aligned(a->shared_w, 16)) r.bad("shared_w must be 16-byte aligned");
+        if (!S && a->shared_w) r.bad("shared_w must be NULL when has_shared == 0");
+        if (a->bias && !aligned(a->bias, 4)) r.bad("bias must be 4-byte aligned");
+        if (!a->topk_ids) r.bad("topk_ids is NULL");
+        else if (!aligned(a->topk_ids, 4)) r.bad("topk_ids must be 4-byte aligned");
+        if (!a->topk_weights) r.bad("topk_weights is NULL");
+        else if (!aligned(a->topk_weights, 4)) r.bad("topk_weights must be 4-byte aligned");
+        if (a->logits_out && !aligned(a->logits_out, 16)) r.bad("logits_out must be 16-byte aligned");
+    }
+    if (a->M > smr::kSmallMaxM && r.invalid.empty() &&
+        !smr::tc_route_supported(a->H, a->E, a->topk, S))
+        r.unsup("M > 16 uses the tcgen05 path, which needs E % 32 == 0 and 32 <= E <= 512 (got E=" +
+                std::to_string(a->E) + ")");
+}
+
+size_t route_scratch_bytes(const smr_route_args *a) {
+    if (a->M <= 0 || a->M > smr::kSmallMaxM) return 0;
+    return round_up((size_t)a->M * (size_t)(a->E + (a->has_shared ? 1 : 0)) * 4, kWsAlign);
+}
+
+// --- align ------------------------------------------------------------------
+
+int effective_block_size(const smr_align_args *a) {
+    if (a->block_size > 0) return a->block_size;
+    return smr_select_block_size(a->num_tokens, a->routed_topk, a->routed_experts);
+}
+
+void check_align(const smr_align_args *a, Reasons &r, bool ids_from_route) {
+    if (a->num_tokens < 0) r.bad("num_tokens must be >= 0");
+    if (a->width < 1) r.bad("width must be >= 1");
+    if (a->num_experts < 1 || a->num_experts > kMaxExperts + 1)
+        r.bad("num_experts must be in [1, 1025] (got " + std::to_string(a->num_experts) + ")");
+    if (a->block_size < 0 || a->block_size > 4096)
+        r.bad("block_size must be 0 (M-aware tier) or in [1, 4096] (got " +
+              std::to_string(a->block_size) + ")");
+    if (a->block_size == 0 && !ids_from_route && (a->routed_topk < 1 || a->routed_experts < 1))
+        r.bad("block_size == 0 needs routed_topk >= 1 and routed_experts >= 1");
+    if (!r.invalid.empty()) return;
+    const int64_t numel = (int64_t)a->num_tokens * a->width;
+    if (numel > (int64_t)1 << 30) r.unsup("num_tokens * width must be <= 2^30");
+    const int A = effective_block_size(a);
+    if (A < 1) {
+        r.bad("cannot derive a block size");
+        return;
+    }
+    const int64_t cap = smr_align_capacity(numel, a->num_experts, A);
+    if (!ids_from_route) {
+        if (numel > 0 && !a->topk_ids) r.bad("topk_ids is NULL");
+        else if (a->topk_ids && !aligned(a->topk_ids, 4)) r.bad("topk_ids must be 4-byte aligned");
+    }
+    if (!a->sorted_token_ids) r.bad("sorted_token_ids is NULL");
+    if (!a->expert_ids) r.bad("expert_ids is NULL");
+    if (!a->num_tokens_post_padded) r.bad("num_tokens_post_padded is NULL");
+    if (a->sorted_cap < cap)
+        r.bad("sorted_cap " + std::to_string(a->sorted_cap) + " < required " + std::to_string(cap));
+    if (a->expert_cap < (cap + A - 1) / A)
+        r.bad("expert_cap " + std::to_string(a->expert_cap) + " < required " +
+              std::to_string((cap + A - 1) / A));
+    if (cap > INT32_MAX) r.unsup("capacity exceeds int32 indexing");
+}
+
+size_t align_scratch_bytes(const smr_align_args *a) {
+    const int64_t numel = (int64_t)a->num_tokens * a->width;
+    if (numel <= smr::kAlignSingleMax) return 0;
+    return round_up((size_t)smr::align_num_tiles((int)numel) * (size_t)a->num_experts * 4, kWsAlign);
+}
+
+smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
+    if (!ws) {
+        g_last_error = std::string(what) + ": workspace is NULL";
+        return SMR_ERR_WORKSPACE;
+    }
+    if (!aligned(ws, kWsAlign)) {
+        g_last_error = std::string(what) + ": workspace must be 256-byte aligned";
+        return SMR_ERR_WORKSPACE;
+    }
+    if (bytes < need) {
+        g_last_error = std::string(what) + ": workspace has " + std::to_string(bytes) +
+                       " bytes, needs " + std::to_string(need);
+        return SMR_ERR_WORKSPACE;
+    }
+    return SMR_OK;
+}
+
+smr::AlignLaunch make_align_launch(const smr_align_args *a, const int32_t *ids, void *ws,
+                                   size_t align_off) {
+    smr::AlignLaunch L{};
+    L.ids = ids;
+    L.numel = a->num_tokens * a->width;
+    L.E_al = a->num_experts;
+    L.A = effective_block_size(a);
+    L.sorted = a->sorted_token_ids;
+    L.expert_ids = a->expert_ids;
+    L.npp = a->num_tokens_post_padded;
+    L.hdr = ws;
+    L.tile_counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + align_off);
+    return L;
+}
+
+smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
+                     const smr_align_args *fused_align, int *launches) {
+    const int S = a->has_shared ? 1 : 0;
+    if (a->M <= smr::kSmallMaxM) {
+        smr::SmallRouteLaunch L{};
+        L.x = static_cast<const uint16_t *>(a->hidden);
+        L.ld = a->ld_hidden;
+        L.w = static_cast<const uint16_t *>(a->gate_w);
+        L.ws = static_cast<const uint16_t *>(a->shared_w);
+        L.bias = a->bias;
+        L.M = a->M; L.H = a->H; L.E = a->E; L.S = S; L.k = a->topk;
+        L.scale = a->shared_scale;
+        L.ids = a->topk_ids;
+        L.wts = a->topk_weights;
+        L.logits_out = a->logits_out;
+        L.scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kHeaderBytes);
+        L.hdr = ws;
+        if (fused_align) {
+            L.A = effective_block_size(fused_align);
+            L.sorted = fused_align->sorted_token_ids;
+            L.expert_ids = fused_align->expert_ids;
+            L.npp = fused_align->num_tokens_post_padded;
+        }
+        cudaError_t e = smr::launch_small_route(L, stream);
+        if (e != cudaSuccess) return cuda_fail("small-M route launch", e);
+        *launches += 1;
+        return SMR_OK;
+    }
+    smr::TcRouteLaunch L{};
+    L.x = static_cast<const uint16_t *>(a->hidden);
+    L.ld = a->ld_hidden;
+    L.w = static_cast<const uint16_t *>(a->gate_w);
+    L.ws = static_cast<const uint16_t *>(a->shared_w);
+    L.bias = a->bias;
+    L.M = a->M; L.H = a->H; L.E = a->E; L.S = S; L.k = a->topk;
+    L.scale = a->shared_scale;
+    L.ids = a->topk_ids;
+    L.wts = a->topk_weights;
+    L.logits_out = a->logits_out;
+    L.hdr = ws;
+    cudaError_t e = smr::launch_tc_route(L, stream);
+    if (e != cudaSuccess) return cuda_fail("tcgen05 route launch", e);
+    *launches += 1;
+    return SMR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SMR_API int32_t smr_select_block_size(int32_t num_tokens, int32_t topk, int32_t num_experts) {
+    if (num_tokens < 0 || topk < 1 || num_experts < 1) return -1;
+    return ((int64_t)num_tokens * topk < (int64_t)128 * num_experts) ? 64 : 128;
+}
+
+SMR_API int64_t smr_align_capacity(int64_t numel, int32_t num_experts, int32_t block_size) {
+    if (numel < 0 || num_experts < 1 || block_size < 1) return -1;
+    return numel + (int64_t)num_experts * (block_size - 1);
+}
+
+SMR_API size_t smr_route_workspace_size(const smr_route_args *args) {
+    if (!args) return 0;
+    return kHeaderBytes + route_scratch_bytes(args);
+}
+
+SMR_API size_t smr_align_workspace_size(const smr_align_args *args) {
+    if (!args) return 0;
+    return kHeaderBytes + align_scratch_bytes(args);
+}
+
+SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const smr_align_args *align) {
+    if (!route || !align) return 0;
+    smr_align_args al = *align;
+    al.num_tokens = route->M;
+    al.width = route->topk + (route->has_shared ? 1 : 0);
+    al.num_experts = route->E + (route->has_shared ? 1 : 0);
+    return kHeaderBytes + route_scratch_bytes(route) + align_scratch_bytes(&al);
+}
+
+SMR_API smr_status smr_route(const smr_route_args *args, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    g_last_launches = 0;
+    if (!args) {
+        g_last_error = "smr_route: args is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    Reasons r;
+    check_route(args, r);
+    if (!r.ok()) return r.finish("smr_route");
+    if (args->M == 0) return SMR_OK;
+    smr_status st = check_ws(workspace, workspace_bytes, smr_route_workspace_size(args), "smr_route");
+    if (st != SMR_OK) return st;
+    if ((st = check_device()) != SMR_OK) return st;
+    int launches = 0;
+    st = run_route(args, workspace, static_cast<cudaStream_t>(stream), nullptr, &launches);
+    if (st == SMR_OK) g_last_launches = launches;
+    return st;
+}
+
+SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    g_last_launches = 0;
+    if (!args) {
+        g_last_error = "smr_align: args is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    Reasons r;
+    check_align(args, r, false);
+    if (!r.ok()) return r.finish("smr_align");
+    smr_status st = check_ws(workspace, workspace_bytes, smr_align_workspace_size(args), "smr_align");
+    if (st != SMR_OK) return st;
+    if ((st = check_device()) != SMR_OK) return st;
+    smr::AlignLaunch L = make_align_launch(args, args->topk_ids, workspace, kHeaderBytes);
+    cudaError_t e = smr::launch_align(L, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("align launch", e);
+    g_last_launches = L.numel <= smr::kAlignSingleMax ? 1 : 2;
+    return SMR_OK;
+}
+
+SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_args *align,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_launches = 0;
+    if (!route || !align) {
+        g_last_error = "smr_route_align: route or align args is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    Reasons r;
+    check_route(route, r);
+    const int S = route->has_shared ? 1 : 0;
+    smr_align_args al = *align;
+    al.routed_topk = route->topk;
+    al.routed_experts = route->E;
+    if (align->topk_ids != route->topk_ids) r.bad("align.topk_ids must equal route.topk_ids");
+    if (align->num_tokens != route->M) r.bad("align.num_tokens must equal route.M");
+    if (align->width != route->topk + S) r.bad("align.width must equal route.topk + has_shared");
+    if (align->num_experts != route->E + S) r.bad("align.num_experts must equal route.E + has_shared");
+    check_align(&al, r, true);
+    if (!r.ok()) return r.finish("smr_route_align");
+    smr_status st = check_ws(workspace, workspace_bytes, smr_route_align_workspace_size(route, &al),
+                             "smr_route_align");
+    if (st != SMR_OK) return st;
+    if ((st = check_device()) != SMR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    if (route->M >= 1 && route->M <= smr::kSmallMaxM) {
+        st = run_route(route, workspace, s, &al, &launches);
+        if (st == SMR_OK) g_last_launches = launches;
+        return st;
+    }
+    if (route->M > 0) {
+        st = run_route(route, workspace, s, nullptr, &launches);
+        if (st != SMR_OK) return st;
+    }
+    smr::AlignLaunch L = make_align_launch(&al, route->topk_ids, workspace,
+                                           kHeaderBytes + route_scratch_bytes(route));
+    cudaError_t e = smr::launch_align(L, s);
+    if (e != cudaSuccess) return cuda_fail("align launch", e);
+    launches += L.numel <= smr::kAlignSingleMax ? 1 : 2;
+    g_last_launches = launches;
+    return SMR_OK;
+}
+
+SMR_API smr_status smr_get_device_error(const void *workspace, void *stream, int32_t *code_out) {
+    if (!workspace || !code_out) {
+        g_last_error = "smr_get_device_error: workspace or code_out is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("smr_get_device_error", e);
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, static_cast<const uint8_t *>(workspace) + 4, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("smr_get_device_error", e);
+    *code_out = (int32_t)word;
+    return SMR_OK;
+}
+
+SMR_API smr_status smr_clear_device_error(void *workspace, void *stream) {
+    if (!workspace) {
+        g_last_error = "smr_clear_device_error: workspace is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    cudaError_t e = cudaMemsetAsync(static_cast<uint8_t *>(workspace) + 4, 0, 4,
+                                    static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("smr_clear_device_error", e);
+    return SMR_OK;
+}
+
+SMR_API const char *smr_status_string(smr_status status) {
+    switch (status) {
+        case SMR_OK: return "SMR_OK";
+        case SMR_ERR_INVALID_ARG: return "SMR_ERR_INVALID_ARG";
+        case SMR_ERR_UNSUPPORTED: return "SMR_ERR_UNSUPPORTED";
+        case SMR_ERR_WORKSPACE: return "SMR_ERR_WORKSPACE";
+        case SMR_ERR_CUDA: return "SMR_ERR_CUDA";
+        case SMR_ERR_DEVICE: return "SMR_ERR_DEVICE";
+    }
+    return "SMR_ERR_UNKNOWN";
+}
+
+SMR_API const char *smr_last_error(void) { return g_last_error.c_str(); }
+
+SMR_API int32_t smr_version(void) { return 0x000100; }
+
+SMR_API int32_t smr_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,400 @@
+// smr_device.cuh -- device helpers shared by the routing kernels (sm_103a).
+//
+// Contents: workspace header, bf16 rounding and the ordered selection key,
+// inline-PTX wrappers (mbarrier, TMA, tcgen05), and the single-CTA
+// moe_align_block_size routine used by the fused small-M kernel and by the
+// standalone align kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace smr {
+
+// ------------------------------------------------------------ workspace --
+
+// Sticky error bits in the workspace header.
+constexpr uint32_t kErrBadId = 1u;        // align saw an id outside [0, E_al)
+constexpr uint32_t kErrWaitTimeout = 2u;  // a bounded wait gave up
+
+// First 256 bytes of every workspace. Zeroed once by the caller; kernels
+// return the counters to zero before they exit.
+struct WsHeader {
+    uint32_t ticket;  // small route: CTAs that finished their gate rows
+    uint32_t error;   // sticky error bits (kErr*)
+    uint32_t reserved[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// ------------------------------------------------------ bf16 and keys ----
+
+// Round an fp32 logit to bf16 (round to nearest even) and return it as fp32.
+// -0 is folded into +0 (adding +0.0f under round-to-nearest), so that equal
+// values compare and tie-break by id only.
+__device__ __forceinline__ float round_bf16(float z) {
+    return __bfloat162float(__float2bfloat16_rn(z)) + 0.0f;
+}
+
+// Ordered 32-bit selection key of a bf16-valued logit and its expert id:
+// the high half maps the bf16 bit pattern to an unsigned order that matches
+// the numeric order; the low half is 0xFFFF - id, so among equal values the
+// lower id has the larger key. One unsigned max then selects by
+// (value desc, id asc) -- the argmax key of "Netra Kernel ...", Sampling:
+// make small batches large enough, restated for bf16 logits. Valid keys are
+// never 0 (id <= 1024), so 0 marks an empty or removed entry.
+__device__ __forceinline__ uint32_t make_key(float zr, int id) {
+    uint32_t b = __float_as_uint(zr) >> 16;
+    uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+    return (ord << 16) | (0xFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ int key_id(uint32_t key) { return (int)(0xFFFFu - (key & 0xFFFFu)); }
+__device__ __forceinline__ float key_value(uint32_t key) {
+    uint32_t ord = key >> 16;
+    uint32_t b = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
+    return __uint_as_float(b << 16);
+}
+
+// sigmoid(s) = 1 / (1 + exp(-s)), evaluated as exp(s) / (1 + exp(s)) for
+// s < 0 so that tiny results keep their (possibly subnormal) value instead of
+// flushing through 1 / (1 + inf).
+__device__ __forceinline__ float sigmoid_stable(float s) {
+    if (s >= 0.0f) return 1.0f / (1.0f + expf(-s));
+    const float e = expf(s);
+    return e / (1.0f + e);
+}
+
+// Unpack 8 bf16 (one 16-byte chunk) to fp32.
+__device__ __forceinline__ void unpack8(const uint4 &v, float f[8]) {
+    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Streaming 16-byte load of read-only data that is used once (gate weights).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void set_error(uint32_t *err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ------------------------------------------------------------ mbarrier ---
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 " selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^32 SM cycles (about 2 s at the maximum
+// clock) or as soon as *abort becomes non-zero; on giving up it sets *abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > (1ll << 32)) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- TMA ---
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// ------------------------------------------------------------- tcgen05 ---
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation, one CTA.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive on an mbarrier once all previously issued MMAs of this thread finish.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
+// lane (base lane + i), columns [col, col+32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma: K-major operand whose rows
+// are 128 bytes (64 bf16) with the 128-byte swizzle that TMA writes; rows are
+// packed, so 8-row groups are 1024 bytes apart. Fields: start address >> 4
+// (bits 0-13), leading byte offset >> 4 (16-29, unused for swizzled K-major),
+// stride byte offset >> 4 (32-45), descriptor version 1 (46-47), base offset
+// 0 (49-51, tile bases are 1024-byte aligned), layout 2 = 128B swizzle (61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+// ------------------------------------------------------ align building blocks --
+//
+// moe_align_block_size over flat slot indices i = t*width + s ("[ROCm][Kernel]
+// W4A16 MoE prefill: M-aware moe_align block size", Purpose): count slots per
+// expert, pad each count to a multiple of A, exclusive-scan the padded counts
+// into segment offsets, scatter slot indices into their expert's segment in
+// ascending order, fill the rest of each segment with the sentinel numel and
+// record the expert of every A-row block.
+//
+// Stability without a sort: each warp owns a contiguous range of slots; a
+// first pass counts per (warp, expert), an exclusive prefix over warps gives
+// each warp its start inside every expert segment, and a second pass ranks
+// equal ids inside each 32-slot step with match_any + popc.
+
+struct AlignSmem {
+    int *wcnt;     // [nwarps][E_al] per-warp counts, then per-warp starts
+    int *cnt;      // [E_al] counts of this CTA's slots (then reused as totals)
+    int *off;      // [E_al + 1] padded segment offsets
+    int *base;     // [E_al] extra per-expert offset of this CTA's slots
+    int *scratch;  // [32] scan scratch
+};
+
+__host__ __device__ constexpr int align_smem_words(int nwarps, int num_experts) {
+    return nwarps * num_experts + num_experts + (num_experts + 1) + num_experts + 32;
+}
+
+__device__ __forceinline__ AlignSmem align_carve(int *smem, int num_experts) {
+    const int nw = blockDim.x >> 5;
+    AlignSmem s;
+    s.wcnt = smem;
+    s.cnt = s.wcnt + nw * num_experts;
+    s.off = s.cnt + num_experts;
+    s.base = s.off + num_experts + 1;
+    s.scratch = s.base + num_experts;
+    return s;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Slots [warp*L, min((warp+1)*L, n)) belong to warp `warp`; L is a multiple of 32.
+__device__ __forceinline__ int align_warp_span(int n) {
+    const int nw = blockDim.x >> 5;
+    return ((n + nw - 1) / nw + 31) & ~31;
+}
+
+// Pass 1: per-warp counts -> s.wcnt, then per-expert exclusive prefix over
+// warps (in s.wcnt) and the CTA total (in s.cnt). Ids outside [0, E_al) are
+// skipped and flagged.
+__device__ __forceinline__ void align_count(const int32_t *ids, int n, int E_al,
+                                            const AlignSmem &s, uint32_t *err) {
+    const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < nw * E_al; i += blockDim.x) s.wcnt[i] = 0;
+    __syncthreads();
+    const int L = align_warp_span(n);
+    const int beg = warp * L, end = min(beg + L, n);
+    int *wc = s.wcnt + warp * E_al;
+    for (int b = beg; b < end; b += 32) {
+        const int i = b + lane;
+        int e = (i < end) ? ids[i] : -1;
+        if (i < end && (unsigned)e >= (unsigned)E_al) {
+            set_error(err, kErrBadId);
+            e = -1;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E_al; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < nw; ++w) {
+            const int c = s.wcnt[w * E_al + e];
+            s.wcnt[w * E_al + e] = run;
+            run += c;
+        }
+        s.cnt[e] = run;
+    }
+    __syncthreads();
+}
+
+// Exclusive scan over the CTA of one int per thread; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        scratch[lane] = t;
+    }
+    __syncthreads();
+    const int excl = x - v + (warp > 0 ? scratch[warp - 1] : 0);
+    *total = scratch[nw - 1];
+    __syncthreads();
+    return excl;
+}
+
+// Padded segment offsets from per-expert totals tot[]: off[e] = sum over
+// e' < e of ceil(tot[e']/A)*A; returns npp = off[E_al]. Each thread scans a
+// contiguous run of experts so the order of the sum is fixed.
+__device__ __forceinline__ int align_offsets(const int *tot, int E_al, int A, const AlignSmem &s) {
+    const int per = (E_al + blockDim.x - 1) / blockDim.x;
+    const int e0 = threadIdx.x * per, e1 = min(e0 + per, E_al);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (tot[e] + A - 1) / A * A;
+    int total;
+    int run = block_exclusive_scan(local, s.scratch, &total);
+    for (int e = e0; e < e1; ++e) {
+        s.off[e] = run;
+        run += (tot[e] + A - 1) / A * A;
+    }
+    if (threadIdx.x == 0) s.off[E_al] = total;
+    __syncthreads();
+    return total;
+}
+
+// Pass 2: stable scatter of this CTA's n slots (flat indices flat0 + i) to
+// sorted[off[e] + base[e] + warp start + rank]. Consumes s.wcnt.
+__device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_al, int flat0,
+                                              const AlignSmem &s, bool use_base,
+                                              int32_t *sorted) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = align_warp_span(n);
+    const int beg = warp * L, end = min(beg + L, n);
+    int *wc = s.wcnt + warp * E_al;
+    const uint32_t lt = lanemask_lt();
+    for (int b = beg; b < end; b += 32) {
+        const int i = b + lane;
+        int e = (i < end) ? ids[i] : -1;
+        if ((unsigned)e >= (unsigned)E_al) e = -1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0) {
+            const int pos = s.off[e] + (use_base ? s.base[e] : 0) + wc[e] + __popc(peers & lt);
+            sorted[pos] = flat0 + i;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Blocks b = first, first+stride, ... < npp/A: expert_ids[b] = owner of the
+// block, sorted[p] = sentinel for the block's rows past the owner's last
+// slot. One warp per block; tot[] are the per-expert totals.
+__device__ __forceinline__ void align_blocks(int npp, int A, int E_al, const int *tot,
+                                             const AlignSmem &s, int sentinel, int32_t *sorted,
+                                             int32_t *expert_ids, int first, int stride) {
+    const int lane = threadIdx.x & 31;
+    const int nblocks = npp / A;
+    for (int b = first; b < nblocks; b += stride) {
+        const int p0 = b * A;
+        int lo = 0, hi = E_al;  // largest e with off[e] <= p0 (and off[e+1] > p0)
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s.off[mid] <= p0) lo = mid; else hi = mid;
+        }
+        const int e = lo;
+        if (lane == 0) expert_ids[b] = e;
+        const int fill0 = max(p0, s.off[e] + tot[e]);
+        for (int p = fill0 + lane; p < p0 + A; p += 32) sorted[p] = sentinel;
+    }
+}
+
+}  // namespace smr

@@ -1,0 +1,457 @@
+// smr_tc.cu -- large-M route: tcgen05 gate GEMM with the top-k fused into the
+// epilogue.
+//
+// Computes the same route as the small-M kernel ("[AMD] One-launch small-M
+// MoE router for Qwen3.5 on gfx950", Modifications: fp32-accumulated gate
+// logits, bf16 rounding of the routed logits, top-k with the lowest id winning
+// ties, softmax + renormalisation, shared slot (E, sigmoid(s) * scale)), but
+// for many tokens, where the gate GEMM is a dense contraction
+// (M=16384: 2*16384*4096*513 = 68.9 GFLOP) and belongs on the tensor cores.
+//
+// One CTA per 128-token tile, 192 threads:
+//   warp 0     TMA producer: x tile [128 x 64] and the whole gate [E x 64] per
+//              k-block, 128-byte swizzle, into a ring of shared-memory stages;
+//   warp 1     allocates TMEM (E fp32 columns x 128 lanes) and issues
+//              tcgen05.mma (M=128, N<=256 per instruction, K=16) from one
+//              thread; tcgen05.commit frees each stage;
+//   warps 2-5  meanwhile compute the shared-expert logit of their row from the
+//              staged x tile (CUDA cores, fp32 per k-block, compensated sum
+//              across k-blocks); then the epilogue: thread = token row, reads
+//              its E logits from TMEM (tcgen05.ld 32x32b), rounds them to
+//              bf16, and selects the top-k in three steps:
+//                1. maxima of NG column classes (c mod NG) -> threshold T =
+//                   k-th largest class maximum (at least k logits >= T, so
+//                   every top-k logit, ties included, is >= T);
+//                2. collect the logits >= T as ordered keys (about 1.5k of
+//                   them on random data) into a per-thread shared list;
+//                3. k max-extractions over that short list (exact fallback
+//                   over all E logits if the list overflows).
+// Every mbarrier wait is bounded; on timeout the kernel sets the workspace's
+// error bit, skips its outputs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "smr_device.cuh"
+#include "smr_launch.h"
+
+namespace smr {
+
+constexpr int kTcBM = 128;
+constexpr int kTcBK = 64;
+constexpr int kTcThreads = 192;
+constexpr int kCandCap = 32;
+constexpr int kTcSmemLimit = 232448;  // 227 KiB opt-in per CTA
+
+struct TcParams {
+    int M, H, E, S, k, width;
+    float scale;
+    const float *bias;
+    const uint16_t *ws;
+    int32_t *ids;
+    float *wts;
+    uint16_t *logits_out;
+    uint32_t *err;
+    int num_kb, stages, n_pieces, piece_n, b_box_rows, n_b_boxes;
+    uint32_t tmem_cols, stage_bytes, tx_bytes, misc_bias_off, misc_ws_off;
+};
+
+// Compensated (two-sum) accumulation of k-block partial sums.
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
+    const float t = hi + x;
+    const float bp = t - hi;
+    const float err = (hi - (t - bp)) + (x - bp);
+    hi = t;
+    lo += err;
+}
+
+// Descending sort of N floats (bitonic network, N a power of two).
+template <int N>
+__device__ __forceinline__ void sort_desc(float (&a)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = ((i & size) == 0);
+                    const float x = a[i], y = a[j];
+                    const float hi = fmaxf(x, y), lo = fminf(x, y);
+                    a[i] = desc ? hi : lo;
+                    a[j] = desc ? lo : hi;
+                }
+            }
+        }
+    }
+}
+
+template <int NG>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const int ST = p.stages;
+    uint8_t *misc = smem + (size_t)ST * p.stage_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc);
+    uint64_t *empty = full + ST;
+    uint64_t *accum = empty + ST;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
+    uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTcBM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1 + (p.S ? 4 : 0));
+        }
+        mbar_init(smem_u32(accum), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+        tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i < p.E; i += kTcThreads) bias_s[i] = p.bias ? p.bias[i] : 0.0f;
+    if (p.S) {
+        const int nch = p.H >> 3;
+        for (int c = threadIdx.x; c < nch; c += kTcThreads)
+            reinterpret_cast<uint4 *>(ws_s)[c] = reinterpret_cast<const uint4 *>(p.ws)[c];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            int kb = 0;
+            for (; kb < p.num_kb; ++kb) {
+                const int s = kb % ST;
+                const uint32_t ph = (uint32_t)(kb / ST) & 1u;
+                if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag)) break;
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, p.tx_bytes);
+                const uint32_t a_dst = smem_u32(smem + (size_t)s * p.stage_bytes);
+                tma_load_2d(a_dst, &tm_x, kb * kTcBK, m0, fb);
+                const uint32_t b_dst = a_dst + kTcBM * kTcBK * 2;
+                for (int bb = 0; bb < p.n_b_boxes; ++bb)
+                    tma_load_2d(b_dst + (uint32_t)(bb * p.b_box_rows * kTcBK * 2), &tm_w,
+                                kb * kTcBK, bb * p.b_box_rows, fb);
+            }
+            if (kb < p.num_kb) {
+                // gave up: let the copies already issued land before exiting
+                set_error(p.err, kErrWaitTimeout);
+                for (int j = kb - 1; j >= 0 && j >= kb - ST; --j) {
+                    const uint32_t fb = smem_u32(&full[j % ST]);
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(fb, (uint32_t)(j / ST) & 1u) &&
+                           clock64() - t0 < (1ll << 28)) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer -----
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTcBM, p.piece_n);
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % ST;
+                const uint32_t ph = (uint32_t)(kb / ST) & 1u;
+                if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag)) {
+                    set_error(p.err, kErrWaitTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + (size_t)s * p.stage_bytes);
+                const uint32_t b_base = a_base + kTcBM * kTcBK * 2;
+#pragma unroll
+                for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                    const uint64_t adesc = smem_desc_sw128(a_base + kk * 32);
+                    for (int pc = 0; pc < p.n_pieces; ++pc) {
+                        const uint64_t bdesc =
+                            smem_desc_sw128(b_base + (uint32_t)(pc * p.piece_n * 128) + kk * 32);
+                        tc_mma_bf16(tmem + (uint32_t)(pc * p.piece_n), adesc, bdesc, idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                tc_commit(smem_u32(&empty[s]));
+            }
+            tc_commit(smem_u32(accum));
+        }
+    } else {
+        // ------------------------------------------- epilogue warps 2-5 ---
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const int grow = m0 + row;
+        const bool valid = grow < p.M;
+        float s_hi = 0.0f, s_lo = 0.0f;
+        if (p.S) {
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % ST;
+                const uint32_t ph = (uint32_t)(kb / ST) & 1u;
+                // warp-uniform: either every lane saw the stage or the warp stops
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag)))
+                    break;
+                const uint8_t *arow = smem + (size_t)s * p.stage_bytes + row * (kTcBK * 2);
+                float part = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int h = kb * kTcBK + c * 8;
+                    if (h < p.H) {
+                        const uint4 xa = *reinterpret_cast<const uint4 *>(arow + ((c ^ (row & 7)) << 4));
+                        const uint4 wa = *reinterpret_cast<const uint4 *>(ws_s + h);
+                        float xf[8], wf[8];
+                        unpack8(xa, xf);
+                        unpack8(wa, wf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
+                    }
+                }
+                two_sum_acc(s_hi, s_lo, part);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            }
+        }
+        bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
+        tc_fence_after();
+        // all four epilogue warps are past the shared-dot reads of the stage
+        // ring before any of them reuses it as scratch
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag ? 1 : 0, 0) != 0;  // one decision per warp
+        if (ok) {
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+            const int nchunks = p.E >> 5;
+            uint32_t *cand = reinterpret_cast<uint32_t *>(smem);          // [kCandCap][128]
+            uint32_t *sel = cand + kCandCap * kTcBM;                        // [32][128]
+            // 1. class maxima and threshold
+            float gmax[NG];
+#pragma unroll
+            for (int g = 0; g < NG; ++g) gmax[g] = -INFINITY;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                float v[32];
+                tmem_ld32(taddr + (uint32_t)(ch * 32), v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = round_bf16(v[i] + bias_s[ch * 32 + i]);
+                if (p.logits_out && valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + ch * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            w4[t] = (__float_as_uint(v[u * 8 + 2 * t]) >> 16) |
+                                    (__float_as_uint(v[u * 8 + 2 * t + 1]) & 0xFFFF0000u);
+                        dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) gmax[i % NG] = fmaxf(gmax[i % NG], v[i]);
+            }
+            sort_desc<NG>(gmax);
+            float T = gmax[0];
+#pragma unroll
+            for (int g = 1; g < NG; ++g) T = (g == p.k - 1) ? gmax[g] : T;
+            // 2. candidates >= T as ordered keys
+            int n = 0;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                float v[32];
+                tmem_ld32(taddr + (uint32_t)(ch * 32), v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float zr = round_bf16(v[i] + bias_s[ch * 32 + i]);
+                    if (zr >= T) {
+                        if (n < kCandCap) cand[n * kTcBM + row] = make_key(zr, ch * 32 + i);
+                        ++n;
+                    }
+                }
+            }
+            // 3. k extractions, exact fallback if the list overflowed
+            const bool overflow = n > kCandCap;
+            if (__any_sync(0xffffffffu, overflow)) {
+                uint32_t prev = 0xFFFFFFFFu;
+                for (int r = 0; r < p.k; ++r) {
+                    uint32_t best = 0u;
+                    for (int ch = 0; ch < nchunks; ++ch) {
+                        float v[32];
+                        tmem_ld32(taddr + (uint32_t)(ch * 32), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const uint32_t key =
+                                make_key(round_bf16(v[i] + bias_s[ch * 32 + i]), ch * 32 + i);
+                            if (key < prev && key > best) best = key;
+                        }
+                    }
+                    if (overflow) sel[r * kTcBM + row] = best;
+                    prev = best;
+                }
+            }
+            if (!overflow) {
+                uint32_t prev = 0xFFFFFFFFu;
+                for (int r = 0; r < p.k; ++r) {
+                    uint32_t best = 0u;
+                    for (int j = 0; j < n; ++j) {
+                        const uint32_t c = cand[j * kTcBM + row];
+                        if (c < prev && c > best) best = c;
+                    }
+                    sel[r * kTcBM + row] = best;
+                    prev = best;
+                }
+            }
+            // softmax over the selected logits, shared slot
+            if (valid) {
+                const float vmax = key_value(sel[row]);
+                float sum = 0.0f;
+                for (int r = 0; r < p.k; ++r) sum += expf(key_value(sel[r * kTcBM + row]) - vmax);
+                int32_t *orow = p.ids + (int64_t)grow * p.width;
+                float *wrow = p.wts + (int64_t)grow * p.width;
+                for (int r = 0; r < p.k; ++r) {
+                    const uint32_t key = sel[r * kTcBM + row];
+                    orow[r] = key_id(key);
+                    wrow[r] = expf(key_value(key) - vmax) / sum;
+                }
+                if (p.S) {
+                    const float s = s_hi + s_lo;
+                    orow[p.k] = p.E;
+                    wrow[p.k] = p.scale * sigmoid_stable(s);
+                }
+            }
+        } else {
+            set_error(p.err, kErrWaitTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------------ host --
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcPlan {
+    TcParams p;
+    size_t smem;
+    int grid;
+};
+
+static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
+    if (E < 32 || E > 512 || E % 32 != 0 || k < 1 || k > 32 || k > E || H < 8 || H % 8 != 0 ||
+        H > 16384)
+        return false;
+    TcParams p{};
+    p.H = H;
+    p.E = E;
+    p.S = S;
+    p.k = k;
+    p.M = M;
+    p.width = k + S;
+    p.num_kb = (H + kTcBK - 1) / kTcBK;
+    p.n_pieces = (E + 255) / 256;
+    p.piece_n = E / p.n_pieces;
+    p.b_box_rows = (E % 256 == 0) ? 256 : (E % 128 == 0) ? 128 : (E % 64 == 0) ? 64 : 32;
+    p.n_b_boxes = E / p.b_box_rows;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)E) cols <<= 1;
+    p.tmem_cols = cols;
+    p.stage_bytes = (uint32_t)(kTcBM * kTcBK * 2 + E * kTcBK * 2);
+    p.tx_bytes = p.stage_bytes;
+    // misc: barriers and flags (256 B), bias [E] fp32, shared gate [H] bf16
+    p.misc_bias_off = 256;
+    p.misc_ws_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
+    const size_t misc = p.misc_ws_off + (S ? (size_t)H * 2 : 0);
+    const size_t budget = (size_t)kTcSmemLimit - 1024 - misc;
+    int st = (int)(budget / p.stage_bytes);
+    if (st > 8) st = 8;
+    if (st < 2) return false;
+    // the epilogue scratch (candidate list + selection) reuses the stage ring
+    if ((size_t)st * p.stage_bytes < (size_t)(kCandCap + 32) * kTcBM * 4) return false;
+    p.stages = st;
+    out->p = p;
+    out->smem = 1024 + (size_t)st * p.stage_bytes + misc;
+    out->grid = (M + kTcBM - 1) / kTcBM;
+    return true;
+}
+
+bool tc_route_supported(int H, int E, int k, int S) {
+    TcPlan plan;
+    return plan_tc(1, H, E, k, S, &plan);
+}
+
+template <int NG>
+static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const TcPlan &plan,
+                             cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_route_kernel<NG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kTcSmemLimit);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    tc_route_kernel<NG><<<plan.grid, kTcThreads, plan.smem, stream>>>(mx, mw, plan.p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
+    TcPlan plan;
+    if (!plan_tc(a.M, a.H, a.E, a.k, a.S, &plan)) return cudaErrorNotSupported;
+    TcParams &p = plan.p;
+    p.scale = a.scale;
+    p.bias = a.bias;
+    p.ws = a.ws;
+    p.ids = a.ids;
+    p.wts = a.wts;
+    p.logits_out = a.logits_out;
+    p.err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, a.x, (uint64_t)a.H, (uint64_t)a.M, (uint64_t)a.ld * 2, kTcBK, kTcBM))
+        return cudaErrorInvalidValue;
+    if (!make_map(&mw, a.w, (uint64_t)a.H, (uint64_t)a.E, (uint64_t)a.H * 2, kTcBK,
+                  (uint32_t)p.b_box_rows))
+        return cudaErrorInvalidValue;
+    return a.k <= 16 ? launch_ng<16>(mx, mw, plan, stream) : launch_ng<32>(mx, mw, plan, stream);
+}
+
+}  // namespace smr

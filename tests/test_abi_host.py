@@ -1,0 +1,173 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and exports
+every function include/smr.h declares; refusals list every reason and happen
+before any device work; workspace sizes, the tier and the capacity helpers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from moe_router_top_gb300 import _lib
+from moe_router_top_gb300._lib import AlignArgs, RouteArgs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_router_top_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "smr.h")).read()
+    return sorted(set(re.findall(r"SMR_API\s+[\w\s\*]+?\b(smr_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _header_functions()
+    assert len(declared) >= 14
+    assert sorted(_lib.EXPORTED) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_struct_layouts_match_header(lib):
+    # field order and sizes as declared in include/smr.h (LP64)
+    assert ctypes.sizeof(RouteArgs) == 7 * 4 + 4 + 8 * 8
+    assert RouteArgs.hidden.offset == 32
+    assert ctypes.sizeof(AlignArgs) == 8 + 6 * 4 + 5 * 8
+    assert AlignArgs.sorted_token_ids.offset == 32
+
+
+def test_version_and_status_strings(lib):
+    assert lib.smr_version() == 0x000100
+    assert lib.smr_status_string(0) == b"SMR_OK"
+    assert lib.smr_status_string(2) == b"SMR_ERR_UNSUPPORTED"
+
+
+def _good_route(M=4, H=4096, E=512, k=10, S=1):
+    a = RouteArgs()
+    a.M, a.H, a.E, a.topk, a.has_shared = M, H, E, k, S
+    a.shared_scale = 1.0
+    a.renormalize = 1
+    a.hidden = 0x10000
+    a.ld_hidden = H
+    a.gate_w = 0x20000
+    a.shared_w = 0x30000 if S else None
+    a.bias = None
+    a.topk_ids = 0x40000
+    a.topk_weights = 0x50000
+    return a
+
+
+def test_route_refusal_lists_every_reason(lib):
+    a = _good_route()
+    a.H = 4100          # not a multiple of 8
+    a.hidden = 0x10004  # misaligned
+    a.shared_w = None   # has_shared but NULL
+    a.topk_ids = None
+    st = lib.smr_route(ctypes.byref(a), None, 0, None)
+    assert st == _lib.SMR_ERR_INVALID_ARG
+    msg = lib.smr_last_error().decode()
+    for frag in ("H must be a multiple of 8", "hidden must be 16-byte aligned",
+                 "shared_w is NULL", "topk_ids is NULL"):
+        assert frag in msg, msg
+    assert lib.smr_last_launch_count() == 0
+
+
+def test_route_unsupported_contract(lib):
+    a = _good_route()
+    a.renormalize = 0
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
+    assert "renormalize" in lib.smr_last_error().decode()
+    a = _good_route(M=64, E=500)      # tcgen05 path needs E % 32 == 0
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
+    assert "E % 32 == 0" in lib.smr_last_error().decode()
+    a = _good_route(k=32, S=1, E=64)  # width 33 > 32
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
+
+
+def test_route_workspace_checked_before_device(lib):
+    a = _good_route()
+    need = lib.smr_route_workspace_size(ctypes.byref(a))
+    assert need == 256 + ((4 * 513 * 4 + 255) // 256) * 256
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_WORKSPACE
+    assert lib.smr_route(ctypes.byref(a), 0x100080, need, None) == _lib.SMR_ERR_WORKSPACE  # misaligned
+    assert lib.smr_route(ctypes.byref(a), 0x100000, need - 1, None) == _lib.SMR_ERR_WORKSPACE
+    big = _good_route(M=16384)
+    assert lib.smr_route_workspace_size(ctypes.byref(big)) == 256  # tcgen05 path keeps no scratch
+
+
+def test_route_m0_is_a_no_op(lib):
+    a = _good_route(M=0)
+    a.hidden = a.gate_w = a.shared_w = a.topk_ids = a.topk_weights = None
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_OK
+    assert lib.smr_last_launch_count() == 0
+
+
+def _good_align(T=4, W=11, E_al=513, A=64):
+    a = AlignArgs()
+    a.topk_ids = 0x10000
+    a.num_tokens, a.width, a.num_experts = T, W, E_al
+    a.routed_topk, a.routed_experts = W - 1, E_al - 1
+    a.block_size = A
+    cap = T * W + E_al * (max(A, 64) - 1) if A else T * W + E_al * 127
+    a.sorted_token_ids = 0x20000
+    a.sorted_cap = cap
+    a.expert_ids = 0x30000
+    a.expert_cap = cap
+    a.num_tokens_post_padded = 0x40000
+    return a
+
+
+def test_align_refusals(lib):
+    a = _good_align()
+    a.sorted_cap = 10
+    a.num_tokens_post_padded = None
+    assert lib.smr_align(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_INVALID_ARG
+    msg = lib.smr_last_error().decode()
+    assert "sorted_cap 10 < required 32363" in msg and "num_tokens_post_padded is NULL" in msg
+    a = _good_align(A=0)
+    a.routed_topk = 0
+    assert lib.smr_align(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_INVALID_ARG
+    assert "routed_topk" in lib.smr_last_error().decode()
+
+
+def test_align_workspace_sizes(lib):
+    a = _good_align(T=4)
+    assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256          # one CTA, no scratch
+    a = _good_align(T=16384, A=128)
+    ntiles = (16384 * 11 + 8191) // 8192
+    assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256 + ((ntiles * 513 * 4 + 255) // 256) * 256
+
+
+def test_route_align_consistency_checks(lib):
+    r = _good_route()
+    a = _good_align()
+    a.topk_ids = r.topk_ids
+    a.width = 10  # should be topk + S = 11
+    assert lib.smr_route_align(ctypes.byref(r), ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_INVALID_ARG
+    assert "align.width must equal" in lib.smr_last_error().decode()
+
+
+def test_tier_and_capacity_match_oracle(lib):
+    for T, k, E in [(6, 8, 128), (1024, 8, 128), (2048, 8, 128), (4, 10, 512), (16384, 10, 512),
+                    (0, 8, 128), (1, 1, 1)]:
+        assert lib.smr_select_block_size(T, k, E) == oracle.select_block_size(T, k, E)
+    for numel, E, A in [(1024, 128, 128), (1024, 128, 64), (8192, 128, 64), (44, 513, 64), (0, 1, 1)]:
+        assert lib.smr_align_capacity(numel, E, A) == oracle.align_capacity(numel, E, A)
+    assert lib.smr_select_block_size(5, 0, 8) == -1
+    assert lib.smr_align_capacity(5, 0, 8) == -1
+
+
+def test_disable_switch(monkeypatch):
+    import moe_router_top_gb300 as smr
+    monkeypatch.setenv("SMR_DISABLE", "1")
+    with pytest.raises(smr.SmrUnsupported):
+        smr.route(None, None, topk=1)

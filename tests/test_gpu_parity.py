@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle on the five
+workloads, edge cases, graph replay and workspace reuse. Needs a GB300."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from moe_router_top_gb300 import inputs
+
+from _parity import check_align, check_route, check_route_properties
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def smr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import moe_router_top_gb300 as m
+    return m
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _dev(ri):
+    x = _bf16(ri.x)
+    w = _bf16(ri.w)
+    ws = _bf16(ri.ws) if ri.ws is not None else None
+    b = torch.from_numpy(ri.bias).cuda() if ri.bias is not None else None
+    return x, w, ws, b
+
+
+def _route_align(smr, ri, A, with_logits=True):
+    x, w, ws, b = _dev(ri)
+    logits = torch.empty((ri.M, ri.E), dtype=torch.int16, device="cuda") if with_logits else None
+    out = smr.route_align(x, w, ws, b, topk=ri.topk, block_size=A, shared_scale=ri.shared_scale,
+                          logits_out=logits)
+    torch.cuda.synchronize()
+    ids, wts, srt, eids, npp = (t.cpu().numpy() for t in out)
+    lg = logits.cpu().numpy().view(np.uint16) if with_logits else None
+    return ids, wts, srt, eids, npp, lg
+
+
+def _full_check(smr, ri, A, exact=False):
+    ids, wts, srt, eids, npp, lg = _route_align(smr, ri, A)
+    rep = check_route(ri, ids, wts, lg, exact_logits=exact)
+    check_route_properties(ri, ids, wts)
+    Aeff = A if A > 0 else oracle.select_block_size(ri.M, ri.topk, ri.E)
+    al = check_align(ids, ri.num_experts_align, Aeff, srt, eids, npp)
+    return rep, al, ids
+
+
+# ------------------------------------------------------------- workloads --
+
+def test_small_verify_m4(smr):
+    ri = inputs.small_verify(4)
+    rep, al, _ = _full_check(smr, ri, 64)
+    assert smr.last_launch_count() == 1
+    print(f"small_verify M=4: {rep} npp={al.npp}")
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_tie_stress_bit_exact(smr, M):
+    """Integer inputs: fp32 accumulation is exact, so every logit, id and
+    align output must match the oracle bit for bit."""
+    ri = inputs.tie_stress(M)
+    rep, al, ids = _full_check(smr, ri, 64, exact=True)
+    assert rep.rows_ids_differ == 0
+
+
+def test_short_prefill_blocks(smr):
+    ri = inputs.short_prefill()
+    res = {}
+    for A in (64, 128, 0):
+        rep, al, ids = _full_check(smr, ri, A)
+        res[A] = al.npp
+    assert oracle.select_block_size(128, 8, 128) == 64 and res[0] == res[64]
+    print(f"short_prefill npp: A=64 {res[64]}, A=128 {res[128]}, ratio@128 {res[128] / 1024:.2f}")
+
+
+@pytest.mark.parametrize("M", list(inputs.ZIPF_TOKENS))
+def test_zipf_sweep(smr, M):
+    ri = inputs.zipf_sweep(M)
+    rep, al, ids = _full_check(smr, ri, 0)
+    A = oracle.select_block_size(M, 8, 128)
+    cnt = np.bincount(ids.ravel(), minlength=128)
+    assert al.npp == int(((cnt + A - 1) // A * A).sum())
+    print(f"zipf M={M}: A={A} npp={al.npp} touched={(cnt > 0).sum()} {rep}")
+
+
+def test_large_batch_sampled(smr):
+    """M=16384 in the launch configuration the benchmark times: oracle on
+    sampled rows (first, last tile and a random spread), invariants on all
+    rows, align bit-exact on all ids."""
+    ri = inputs.large_batch()
+    ids, wts, srt, eids, npp, lg = _route_align(smr, ri, 128)
+    rng = np.random.default_rng(99)
+    rows = np.unique(np.concatenate([np.arange(0, 130), np.arange(ri.M - 130, ri.M),
+                                     rng.choice(ri.M, 300, replace=False)]))
+    rep = check_route(ri, ids, wts, lg, rows=rows)
+    check_route_properties(ri, ids, wts)
+    check_align(ids, 513, 128, srt, eids, npp)
+    print(f"large_batch: {rep}")
+
+
+# ------------------------------------------------------------ edge cases --
+
+@pytest.mark.parametrize("M,H,E,k,S", [
+    (1, 8, 1, 1, 0),        # smallest problem
+    (16, 4096, 512, 10, 1),  # largest small-M batch
+    (5, 200, 37, 5, 1),      # H not a multiple of 64, odd E
+    (7, 16384, 64, 8, 0),    # largest H, several passes per thread
+    (2, 1024, 1024, 31, 1),  # largest E, widest row
+    (17, 256, 64, 8, 1),     # smallest tcgen05 batch
+    (130, 200, 96, 6, 1),    # two tiles, ragged tail, ragged K
+    (300, 512, 512, 16, 0),  # k = 16 threshold classes
+    (64, 128, 32, 32, 0),    # k = E, 32 classes
+    (256, 2048, 256, 1, 1),  # k = 1
+])
+def test_shapes(smr, M, H, E, k, S):
+    ri = inputs.make_route_inputs(M, H, E, k, S, seed=M * 1000 + E, shared_scale=0.75)
+    _full_check(smr, ri, 64)
+
+
+@pytest.mark.parametrize("M", [4, 40])
+def test_all_equal_logits_lowest_ids_win(smr, M):
+    ri = inputs.make_route_inputs(M, 256, 128, 8, 1, seed=3)
+    ri.w[:] = ri.w[0]  # every expert row identical: all logits tie
+    ids, wts, srt, eids, npp, lg = _route_align(smr, ri, 64)
+    assert np.all(ids[:, :8] == np.arange(8))
+    assert np.all(wts[:, :8] == np.float32(1 / 8))
+    check_route(ri, ids, wts, lg)
+
+
+def test_bias_and_strided_hidden(smr):
+    ri = inputs.make_route_inputs(40, 512, 128, 8, 1, seed=5, zipf_s=1.1)
+    x, w, ws, b = _dev(ri)
+    big = torch.zeros((40, 520), dtype=torch.bfloat16, device="cuda")
+    big[:, :512] = x
+    xs = big[:, :512]  # row stride 520
+    logits = torch.empty((40, 128), dtype=torch.int16, device="cuda")
+    ids, wts = smr.route(xs, w, ws, b, topk=8, logits_out=logits)
+    torch.cuda.synchronize()
+    check_route(ri, ids.cpu().numpy(), wts.cpu().numpy(), logits.cpu().numpy().view(np.uint16))
+
+
+def test_graph_replay_matches_eager(smr):
+    for M in (4, 300):
+        ri = inputs.make_route_inputs(M, 1024, 128, 8, 1, seed=11 + M)
+        x, w, ws, b = _dev(ri)
+        A = 64
+        wsp = smr.Workspace()
+        eager = smr.route_align(x, w, ws, b, topk=8, block_size=A, workspace=wsp)
+        torch.cuda.synchronize()
+        eager = [t.clone() for t in eager]
+        outs = [torch.empty_like(t) for t in eager]
+        for t in outs:
+            t.fill_(-5)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            smr.route_align(x, w, ws, b, topk=8, block_size=A, topk_ids=outs[0],
+                            topk_weights=outs[1], sorted_token_ids=outs[2], expert_ids=outs[3],
+                            num_tokens_post_padded=outs[4], workspace=wsp)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            smr.route_align(x, w, ws, b, topk=8, block_size=A, topk_ids=outs[0],
+                            topk_weights=outs[1], sorted_token_ids=outs[2], expert_ids=outs[3],
+                            num_tokens_post_padded=outs[4], workspace=wsp)
+        for _ in range(3):
+            for t in outs:
+                t.fill_(-5)
+            g.replay()
+            torch.cuda.synchronize()
+            n = int(eager[4].item())
+            assert torch.equal(outs[0], eager[0]) and torch.equal(outs[1], eager[1])
+            assert int(outs[4].item()) == n
+            assert torch.equal(outs[2][:n], eager[2][:n])
+            assert torch.equal(outs[3][: n // A], eager[3][: n // A])
+        assert smr.get_device_error(wsp) == 0
+
+
+def test_workspace_reuse_is_deterministic(smr):
+    ri = inputs.small_verify(8, variant=1)
+    x, w, ws, b = _dev(ri)
+    wsp = smr.Workspace()
+    first = [t.clone() for t in smr.route_align(x, w, ws, b, topk=10, block_size=64, workspace=wsp)]
+    for _ in range(5):
+        again = smr.route_align(x, w, ws, b, topk=10, block_size=64, workspace=wsp)
+        torch.cuda.synchronize()
+        n = int(first[4].item())
+        assert torch.equal(again[0], first[0]) and torch.equal(again[1], first[1])
+        assert torch.equal(again[2][:n], first[2][:n])
+    # the ticket counter is back at zero after every call
+    assert int(wsp.buf[:4].view(torch.int32).item()) == 0
+    assert smr.get_device_error(wsp) == 0
+
+
+# ----------------------------------------------------------------- align --
+
+@pytest.mark.parametrize("T,W,E_al,A,skew", [
+    (0, 11, 513, 64, None),        # empty input
+    (1, 1, 1, 1, None),
+    (4, 11, 513, 64, None),
+    (700, 11, 513, 64, 1.1),       # single CTA near its limit (7700 slots)
+    (745, 11, 513, 128, None),     # just above: two tiles
+    (16384, 11, 513, 128, 1.1),    # the large batch's shape
+    (2048, 8, 128, 128, 2.0),      # very hot experts
+    (3000, 3, 7, 200, None),       # odd block size, few experts
+    (9000, 1, 1025, 16, None),     # widest expert range
+])
+def test_align_standalone(smr, T, W, E_al, A, skew):
+    ids = inputs.random_ids(T, W, E_al, seed=T + W + A, skew=skew) if T else np.zeros((0, W), np.int32)
+    dids = torch.from_numpy(ids).cuda()
+    srt, eids, npp = smr.align(dids, E_al, A)
+    torch.cuda.synchronize()
+    check_align(ids, E_al, A, srt.cpu().numpy(), eids.cpu().numpy(), npp.cpu().numpy())
+    assert smr.last_launch_count() == (1 if T * W <= 8192 else 2)
+
+
+def test_align_bad_id_sets_error_bit(smr):
+    ids = inputs.random_ids(20, 4, 16, seed=1)
+    ids[3, 2] = 16  # out of range
+    wsp = smr.Workspace()
+    dids = torch.from_numpy(ids).cuda()
+    smr.align(dids, 16, 64, workspace=wsp)
+    assert smr.get_device_error(wsp) & smr.ERR_BAD_ID
+    smr.clear_device_error(wsp)
+    assert smr.get_device_error(wsp) == 0
