@@ -1,12 +1,17 @@
 """Comparison of the CUDA path with the oracle (shared by the GPU tests).
 
 Acceptance rules:
- * logits: the GPU's bf16-rounded routed logits equal the oracle's, except
-   where the oracle's exact logit lies within the fp32-accumulation error
-   bound of a bf16 rounding midpoint; there the GPU may take the neighbouring
-   bf16 value (one step, never more). Bound: 2 * (H + 2) * 2^-24 * sum|x*W|,
-   the worst case of any summation order of H+1 terms in fp32 with at most one
-   ulp of error per addition.
+ * logits: each GPU bf16 logit must be the bf16 rounding of some value within
+   delta of the exact sum z, i.e. lie in [bf16(z - delta), bf16(z + delta)];
+   where it differs from the oracle's bf16(z) it is counted. delta is the
+   worst-case error of the kernel's fp32 summation tree, one ulp (2^-24
+   relative) per addition on the chain, times sum|x*W| (+|bias|), doubled:
+     small-M path  : a chain of 16*ceil(H/4096) products per thread, then 13
+                     tree levels (warp butterfly + 8 warps): 16*ceil(H/4096)+16
+     tcgen05 path  : one fp32 accumulator update per K=16 instruction, so
+                     H/16 sequential additions (+32 for the in-instruction sum).
+   Near-zero logits (heavy cancellation) can therefore move several bf16
+   steps; logits near the top-k are ~1e3 ulps larger and move at most one.
  * selection: the oracle's top-k + softmax applied to the GPU's own logits
    reproduces the GPU's ids exactly and its weights within 2e-6 relative
    (absolute 4 * 2^-149 below the fp32 normal range).
@@ -36,15 +41,14 @@ def weights_close(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return np.abs(got - ref) <= np.maximum(W_RTOL * np.abs(ref), W_ATOL)
 
 
-def bf16_neighbours(v: np.ndarray):
-    """bf16 values one step below and above each bf16-valued double."""
-    f = v.astype(np.float32)
-    bits = f.view(np.uint32) >> 16
-    up = np.where(f >= 0, bits + 1, bits - 1).astype(np.uint32)
-    dn = np.where(f > 0, bits - 1, np.where(f == 0, 0x8001, bits + 1)).astype(np.uint32)
-    upv = (up << 16).view(np.float32).astype(np.float64)
-    dnv = (dn << 16).view(np.float32).astype(np.float64)
-    return dnv, upv
+def accumulation_bound(ri: inputs.RouteInputs) -> float:
+    """Relative fp32 summation bound (times sum|x*W|) of the kernel path."""
+    u = 2.0 ** -24
+    if ri.M <= 16:
+        chain = 16 * -(-ri.H // 4096) + 16
+    else:
+        chain = -(-ri.H // 16) + 32
+    return 2.0 * chain * u
 
 
 @dataclasses.dataclass
@@ -73,18 +77,18 @@ def check_route(ri: inputs.RouteInputs, ids_g: np.ndarray, w_g: np.ndarray,
         diff = zg != ref.zhat
         if diff.any():
             assert not exact_logits, f"{int(diff.sum())} logits differ on exact-arithmetic inputs"
-            H = ri.H
-            delta = 2.0 * (H + 2) * 2.0 ** -24 * ref.absdot
-            dn, up = bf16_neighbours(ref.zhat)
+            delta = accumulation_bound(ri) * ref.absdot
             t, e = np.nonzero(diff)
-            for a, b in zip(t, e):
-                g, zh, z = zg[a, b], ref.zhat[a, b], ref.z[a, b]
-                assert g == dn[a, b] or g == up[a, b], (
-                    f"row {rows[a]} expert {b}: gpu {g} vs oracle {zh} is more than one bf16 step")
-                mid = 0.5 * (g + zh)
-                assert abs(z - mid) <= delta[a, b], (
-                    f"row {rows[a]} expert {b}: exact logit {z} is {abs(z - mid):.3g} from the "
-                    f"rounding midpoint, beyond the accumulation bound {delta[a, b]:.3g}")
+            z = ref.z[t, e]
+            lo = oracle.bf16_round(z - delta[t, e])
+            hi = oracle.bf16_round(z + delta[t, e])
+            g = zg[t, e]
+            bad = (g < lo) | (g > hi)
+            if bad.any():
+                j = int(np.argmax(bad))
+                raise AssertionError(
+                    f"{int(bad.sum())} logits outside the accumulation bound; e.g. row {rows[t[j]]} "
+                    f"expert {e[j]}: gpu {g[j]} vs exact {z[j]} (allowed [{lo[j]}, {hi[j]}])")
             rep.logit_mismatch = int(diff.sum())
             row_bad = diff.any(axis=1)
             rep.rows_with_mismatch = int(row_bad.sum())
