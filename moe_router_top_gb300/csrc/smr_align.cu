@@ -6,8 +6,8 @@
 // ceil(tokens_e / A) * A. The output order inside an expert is ascending flat
 // slot index, so results are deterministic and bit-identical across runs.
 //
-//  - numel <= kAlignSingleMax: one CTA of 512 threads does count, scan,
-//    scatter and padding (one launch);
+//  - numel <= kAlignSingleMax: one CTA of 512 threads stages the ids in
+//    shared memory and does count, scan, scatter and padding (one launch);
 //  - larger inputs: align_hist_kernel writes per-tile expert counts to the
 //    workspace, then align_scatter_kernel (one CTA per tile) derives the
 //    global segment offsets from all tile counts (a short fixed-order loop),
@@ -22,27 +22,38 @@ constexpr int kAlignThreads = 512;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
 __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const AlignLaunch a) {
-    extern __shared__ int sm[];
+    extern __shared__ __align__(16) int sm[];
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
-    AlignSmem s = align_carve(sm, a.E_al);
-    align_count(a.ids, a.numel, a.E_al, s, err);
+    int *ids = sm;  // [kAlignSingleMax] staged ids
+    AlignSmem s = align_carve(sm + kAlignSingleMax, a.E_al);
+    stage_ids(ids, a.ids, a.numel);
+    align_count(ids, a.numel, a.E_al, s, err);
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
-    align_scatter(a.ids, a.numel, a.E_al, 0, s, false, a.sorted);
-    align_blocks(npp, a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids, threadIdx.x >> 5,
-                 kAlignWarps);
+    align_scatter(ids, a.numel, a.E_al, 0, s, false, a.sorted);
+    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids, threadIdx.x >> 5, kAlignWarps);
     if (threadIdx.x == 0) *a.npp = npp;
 }
 
 __global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLaunch a) {
     extern __shared__ int cnt[];
+    constexpr int kPer = kAlignTile / kAlignThreads;  // ids per thread
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
     for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
     const int beg = blockIdx.x * kAlignTile, end = min(beg + kAlignTile, a.numel);
-    for (int b = beg + warp * 32; b < end; b += kAlignThreads) {
-        const int i = b + lane;
-        int e = (i < end) ? a.ids[i] : -1;
+    // every load of the tile is issued before the first is used (addresses
+    // clamped into the tile, out-of-tile lanes masked afterwards)
+    int v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = beg + j * kAlignThreads + warp * 32 + lane;
+        v[j] = __ldg(a.ids + min(i, end - 1));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = beg + j * kAlignThreads + warp * 32 + lane;
+        int e = (i < end) ? v[j] : -1;
         if (i < end && (unsigned)e >= (unsigned)a.E_al) {
             set_error(err, kErrBadId);
             e = -1;
@@ -56,27 +67,37 @@ __global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLa
 }
 
 __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const AlignLaunch a) {
-    extern __shared__ int sm[];
+    extern __shared__ __align__(16) int sm[];
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
-    AlignSmem s = align_carve(sm, a.E_al);
+    int *ids = sm;  // [kAlignTile] this tile's ids
+    AlignSmem s = align_carve(sm + kAlignTile, a.E_al);
     const int t = blockIdx.x, ntiles = gridDim.x;
     const int beg = t * kAlignTile, n = min(beg + kAlignTile, a.numel) - beg;
-    align_count(a.ids + beg, n, a.E_al, s, err);  // per-warp starts inside this tile
+    stage_ids(ids, a.ids + beg, n);
+    align_count(ids, n, a.E_al, s, err);  // per-warp starts inside this tile
+    // global per-expert totals and this tile's offset inside each expert, from
+    // all tiles' counts (fixed order; eight loads in flight per thread)
     for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) {
         int base = 0, tot = 0;
-        for (int u = 0; u < ntiles; ++u) {
-            const int c = a.tile_counts[(int64_t)u * a.E_al + e];
-            base += (u < t) ? c : 0;
-            tot += c;
+        for (int u0 = 0; u0 < ntiles; u0 += 8) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                c[j] = (u0 + j < ntiles) ? __ldg(a.tile_counts + (int64_t)(u0 + j) * a.E_al + e) : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                base += (u0 + j < t) ? c[j] : 0;
+                tot += c[j];
+            }
         }
         s.base[e] = base;
         s.cnt[e] = tot;
     }
     __syncthreads();
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
-    align_scatter(a.ids + beg, n, a.E_al, beg, s, true, a.sorted);
-    align_blocks(npp, a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids,
-                 t * kAlignWarps + (threadIdx.x >> 5), ntiles * kAlignWarps);
+    align_scatter(ids, n, a.E_al, beg, s, true, a.sorted);
+    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids,
+               t * kAlignWarps + (threadIdx.x >> 5), ntiles * kAlignWarps);
     if (t == 0 && threadIdx.x == 0) *a.npp = npp;
 }
 
@@ -96,8 +117,8 @@ static cudaError_t set_smem(const void *kern, size_t bytes) {
 }
 
 cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream) {
-    const size_t smem = (size_t)align_smem_words(kAlignWarps, a.E_al) * 4;
-    const size_t smem_max = (size_t)align_smem_words(kAlignWarps, 1025) * 4;
+    const size_t smem = (size_t)(kAlignTile + align_smem_words(kAlignWarps, a.E_al)) * 4;
+    const size_t smem_max = (size_t)(kAlignTile + align_smem_words(kAlignWarps, 1025)) * 4;
     cudaError_t e;
     if (a.numel <= kAlignSingleMax) {
         if ((e = set_smem((const void *)align_single_kernel, smem_max)) != cudaSuccess) return e;

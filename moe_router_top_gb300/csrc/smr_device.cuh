@@ -197,19 +197,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma: K-major operand whose rows
-// are 128 bytes (64 bf16) with the 128-byte swizzle that TMA writes; rows are
-// packed, so 8-row groups are 1024 bytes apart. Fields: start address >> 4
-// (bits 0-13), leading byte offset >> 4 (16-29, unused for swizzled K-major),
-// stride byte offset >> 4 (32-45), descriptor version 1 (46-47), base offset
-// 0 (49-51, tile bases are 1024-byte aligned), layout 2 = 128B swizzle (61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// are SW bytes long (SW = 128, 64 or 32: 64, 32 or 16 bf16) and swizzled the
+// way TMA writes them with the matching swizzle mode; rows are packed, so
+// 8-row groups are 8*SW bytes apart. Fields: start address >> 4 (bits 0-13),
+// leading byte offset >> 4 (16-29, unused for swizzled K-major), stride byte
+// offset >> 4 (32-45), descriptor version 1 (46-47), base offset 0 (49-51;
+// tile bases are 1024-byte aligned), layout (61-63): 2 = 128B, 4 = 64B,
+// 6 = 32B swizzle. A K step inside the row advances the start address.
+template <int SW>
+__device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr) {
+    static_assert(SW == 128 || SW == 64 || SW == 32, "swizzle width");
+    constexpr uint64_t layout = SW == 128 ? 2 : (SW == 64 ? 4 : 6);
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)((8u * SW) >> 4) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= layout << 61;
     return d;
+}
+
+// 16-byte chunk c of row r of such a tile sits at chunk c ^ f(r): the
+// swizzle XORs address bits [4, 4+log2(SW/16)) with bits [7, ...).
+template <int SW>
+__device__ __forceinline__ int swizzled_chunk(int row, int c) {
+    return c ^ (((row * SW) >> 7) & (SW / 16 - 1));
 }
 
 // Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1),
@@ -375,26 +387,38 @@ __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_a
     }
 }
 
-// Blocks b = first, first+stride, ... < npp/A: expert_ids[b] = owner of the
-// block, sorted[p] = sentinel for the block's rows past the owner's last
-// slot. One warp per block; tot[] are the per-expert totals.
-__device__ __forceinline__ void align_blocks(int npp, int A, int E_al, const int *tot,
-                                             const AlignSmem &s, int sentinel, int32_t *sorted,
-                                             int32_t *expert_ids, int first, int stride) {
+// Padding and block owners, driven by expert: warps take 32 experts at a
+// time (warp `wfirst`, stride `wstride` over all participating warps); for
+// each touched expert e the warp writes expert_ids over e's blocks and the
+// sentinel into e's rows past its last slot. tot[] are per-expert totals.
+__device__ __forceinline__ void align_fill(int A, int E_al, const int *tot, const AlignSmem &s,
+                                           int sentinel, int32_t *sorted, int32_t *expert_ids,
+                                           int wfirst, int wstride) {
     const int lane = threadIdx.x & 31;
-    const int nblocks = npp / A;
-    for (int b = first; b < nblocks; b += stride) {
-        const int p0 = b * A;
-        int lo = 0, hi = E_al;  // largest e with off[e] <= p0 (and off[e+1] > p0)
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s.off[mid] <= p0) lo = mid; else hi = mid;
+    for (int e0 = wfirst * 32; e0 < E_al; e0 += wstride * 32) {
+        const int e = e0 + lane;
+        const int c = (e < E_al) ? tot[e] : 0;
+        uint32_t touched = __ballot_sync(0xffffffffu, c > 0);
+        while (touched) {
+            const int ee = e0 + __ffs(touched) - 1;
+            touched &= touched - 1;
+            const int o0 = s.off[ee], o1 = s.off[ee + 1], cnt = tot[ee];
+            for (int b = o0 / A + lane; b < o1 / A; b += 32) expert_ids[b] = ee;
+            for (int q = o0 + cnt + lane; q < o1; q += 32) sorted[q] = sentinel;
         }
-        const int e = lo;
-        if (lane == 0) expert_ids[b] = e;
-        const int fill0 = max(p0, s.off[e] + tot[e]);
-        for (int p = fill0 + lane; p < p0 + A; p += 32) sorted[p] = sentinel;
     }
+}
+
+// Copy n int32 ids from global memory to shared memory with 16-byte loads
+// where the source is aligned (all loads in flight before any is used).
+__device__ __forceinline__ void stage_ids(int *dst, const int32_t *src, int n) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+    const int n4 = vec ? (n >> 2) : 0;
+    const int4 *s4 = reinterpret_cast<const int4 *>(src);
+    int4 *d4 = reinterpret_cast<int4 *>(dst);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) d4[i] = __ldg(s4 + i);
+    for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(src + i);
+    __syncthreads();
 }
 
 }  // namespace smr

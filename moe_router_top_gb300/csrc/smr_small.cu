@@ -1,29 +1,34 @@
 // smr_small.cu -- single-launch route (+ align) for M <= 16 tokens.
 //
 // What it computes is the one-launch small-M router of "[AMD] One-launch
-// small-M MoE router for Qwen3.5 on gfx950", Modifications: every CTA
-// computes a few of the E+S gate rows for all M tokens with fp32
-// accumulation; the last CTA to finish (self-resetting ticket, no spin-wait)
-// rounds the routed logits to bf16, selects the top-k with the lowest id
-// winning ties, applies softmax + renormalisation, writes the shared slot
-// (E, sigmoid(s) * scale) and, when asked, runs moe_align_block_size on the
-// M*(k+S) ids it just produced ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
-// moe_align block size", Purpose) -- all in one launch.
+// small-M MoE router for Qwen3.5 on gfx950", Modifications: the E+S gate rows
+// are computed for all M tokens with fp32 accumulation across CTAs; the last
+// CTA to finish (self-resetting ticket, no spin-wait) rounds the routed logits
+// to bf16, selects the top-k with the lowest id winning ties, applies softmax +
+// renormalisation, writes the shared slot (E, sigmoid(s) * scale) and, when
+// asked, runs moe_align_block_size on the M*(k+S) ids it just produced
+// ("[ROCm][Kernel] W4A16 MoE prefill: M-aware moe_align block size",
+// Purpose) -- all in one launch.
 //
 // GB300 design:
-//  - the gate stream is HBM-bound (4 MiB at E=512, H=4096): each of the
-//    ~129 CTAs (one wave on 152 SMs) issues all of its 16-byte weight loads
-//    (ld.global.nc, no L1 allocation) before any arithmetic, so the whole
-//    matrix is in flight at once;
-//  - the tokens' hidden states go to shared memory with cp.async into
-//    thread-private slots (no CTA barrier), each x chunk is reused by all R
-//    gate rows of the CTA;
-//  - the per-thread partial dot products are reduced with a warp butterfly
-//    reduce-scatter (R*MT values, 5 shuffle stages) and a fixed-order sum
-//    over the 8 warps, so results are deterministic;
-//  - the top-k tail is warp-parallel: one warp per token, the E logits as
-//    ordered 32-bit keys spread over 32 lanes, k rounds of one redux.sync
-//    max -- instead of k serial argmax passes over the row.
+//  - the gate stream is HBM-bound (4 MiB at E=512, H=4096). CTA (g, q) owns
+//    gate rows [16g, 16g+16) and the q-th of KQ contiguous ranges of 32-wide
+//    K slices, so ~130 CTAs (one wave on the SMs) each stream ~32 KB; every
+//    thread issues all of its 16-byte loads (gate rows via ld.global.nc, no L1
+//    allocation) before the first multiply;
+//  - the dot products run on the tensor cores with mma.sync m16n8k16 (bf16 in,
+//    fp32 accumulate): 16 gate rows x 8 tokens per instruction. A sum over K
+//    does not depend on the order of K, so each thread feeds its own
+//    contiguous 8-element chunk straight from its 16-byte loads into the A and
+//    B fragments (the same K permutation on both operands), with no shared
+//    memory staging;
+//  - the 8 warps' partial sums are added in a fixed order and stored per K
+//    range; the tail adds the KQ ranges in a fixed order, so results are
+//    deterministic;
+//  - the tail is warp-parallel: one warp per token, each lane holds E/32
+//    ordered 32-bit keys sorted in registers, k rounds of one redux.sync max
+//    and a register shift pop the winner -- instead of k serial argmax
+//    passes over the row.
 #include "smr_device.cuh"
 #include "smr_launch.h"
 
@@ -31,61 +36,99 @@ namespace smr {
 
 constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kCPT = 2;  // 16-byte chunks of a row per thread per pass
+constexpr int kSliceK = 32;           // K elements per slice (two m16n8k16 steps)
+constexpr int kMaxSlicesPerWarp = 4;  // slices whose loads are in flight at once
 
 struct SmallParams {
     SmallRouteLaunch a;
-    int rows;  // E + S
+    int rows;     // E + S
+    int KQ;       // K ranges per 16-row group
+    int slices;   // ceil(H / 32)
+    int per_cta;  // slices per K range
 };
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int N>
-struct Log2 { static constexpr int value = 1 + Log2<N / 2>::value; };
-template <>
-struct Log2<1> { static constexpr int value = 0; };
-
-// Top-k of one token row in one warp. logits: fp32 [E] (read through L2);
-// writes ids/weights for slots 0..k-1 and returns the slot's id in lane j < k
-// (-1 elsewhere).
-__device__ __forceinline__ int warp_topk_row(const float *logits, const float *bias, int E, int k,
-                                             uint16_t *logits_out, int32_t *ids, float *wts) {
-    const int lane = threadIdx.x & 31;
-    const int nk = (E + 31) >> 5;
-    uint32_t key[32];
+// Sort NK keys descending in registers (bitonic network).
+template <int NK>
+__device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[NK]) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        key[i] = 0u;
+    for (int size = 2; size <= NK; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < NK; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = ((i & size) == 0);
+                    const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
+                    a[i] = desc ? hi : lo;
+                    a[j] = desc ? lo : hi;
+                }
+            }
+        }
+    }
+}
+
+// Top-k of one token row in one warp. part: fp32 partial logits laid out
+// [KQ][M][rows]; this token's first range starts at part, later ranges are
+// kq_stride apart. Writes ids and weights of slots 0..k-1 and returns the
+// slot's id in lanes j < k (-1 elsewhere).
+template <int NK>
+__device__ __forceinline__ int warp_topk_row(const float *part, int KQ, int64_t kq_stride, int E,
+                                             int k, const float *bias, uint16_t *logits_out,
+                                             int32_t *ids, float *wts) {
+    const int lane = threadIdx.x & 31;
+    float z[NK];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) z[i] = 0.0f;
+    // all partial loads of a pair of ranges are issued before any is used:
+    // addresses are clamped into the row, out-of-row lanes are masked below
+    int q = 0;
+    for (; q + 2 <= KQ; q += 2) {
+        float v0[NK], v1[NK];
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+            const int e = min(lane + 32 * i, E - 1);
+            v0[i] = __ldcg(part + q * kq_stride + e);
+            v1[i] = __ldcg(part + (q + 1) * kq_stride + e);
+        }
+#pragma unroll
+        for (int i = 0; i < NK; ++i) z[i] = (z[i] + v0[i]) + v1[i];
+    }
+    if (q < KQ) {
+#pragma unroll
+        for (int i = 0; i < NK; ++i) z[i] += __ldcg(part + q * kq_stride + min(lane + 32 * i, E - 1));
+    }
+    uint32_t key[NK];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
         const int e = lane + 32 * i;
-        if (i < nk && e < E) {
-            float z = __ldcg(logits + e);
-            if (bias) z += __ldg(bias + e);
-            const float zr = round_bf16(z);
+        key[i] = 0u;
+        if (e < E) {
+            const float zr = round_bf16(bias ? z[i] + __ldg(bias + e) : z[i]);
             key[i] = make_key(zr, e);
             if (logits_out) logits_out[e] = (uint16_t)(__float_as_uint(zr) >> 16);
         }
     }
-    uint32_t lm = 0u;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) lm = max(lm, key[i]);
+    sort_keys_desc<NK>(key);
     uint32_t mine = 0u, first = 0u;
     for (int r = 0; r < k; ++r) {
-        const uint32_t g = __reduce_max_sync(0xffffffffu, lm);
-        if (r == 0) first = g;
-        if (lane == r) mine = g;
-        if (lm == g) {  // the single lane holding the winner removes it
-            lm = 0u;
+        const uint32_t gmax = __reduce_max_sync(0xffffffffu, key[0]);
+        if (r == 0) first = gmax;
+        if (lane == r) mine = gmax;
+        if (key[0] == gmax) {  // the single lane holding the winner pops it
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if (key[i] == g) key[i] = 0u;
-                lm = max(lm, key[i]);
-            }
+            for (int i = 0; i + 1 < NK; ++i) key[i] = key[i + 1];
+            key[NK - 1] = 0u;
         }
     }
     // softmax over the selected logits (renormalised top-k)
@@ -103,120 +146,93 @@ __device__ __forceinline__ int warp_topk_row(const float *logits, const float *b
     return id;
 }
 
-template <int R, int MT>
+template <int NB>  // N blocks of 8 tokens: 1 (M <= 8) or 2 (M <= 16)
 __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     const SmallRouteLaunch &p = P.a;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
     const int rows = P.rows;
-    const int row0 = blockIdx.x * R;
-    const int nch = p.H >> 3;
-    constexpr int N = R * MT;
-
-    uint4 *xs = reinterpret_cast<uint4 *>(smem);  // [MT][kCPT][256], thread-private slots
-    float *red = reinterpret_cast<float *>(smem + MT * kCPT * kSmallThreads * 16);  // [8][N]
+    const int rg = blockIdx.x / P.KQ, kq = blockIdx.x % P.KQ;
+    const int row0 = rg * 16;
     __shared__ int s_last;
 
-    // ---- 1. gate rows x tokens: fp32 partial dot products per thread ----
-    float acc[R][MT];
+    // ---- 1. gate rows x tokens on the tensor cores ----
+    // rows past E+S and tokens past M read a clamped (valid) row; their
+    // results are never stored
+    const int ra = min(row0 + g, rows - 1), rb = min(row0 + g + 8, rows - 1);
+    const uint16_t *wa = (ra < p.E) ? p.w + (int64_t)ra * p.H : p.ws;
+    const uint16_t *wb = (rb < p.E) ? p.w + (int64_t)rb * p.H : p.ws;
+    const uint16_t *xa = p.x + (int64_t)min(g, p.M - 1) * p.ld;
+    const uint16_t *xb = p.x + (int64_t)min(g + 8, p.M - 1) * p.ld;
+    float acc[NB][4];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[r][m] = 0.0f;
+        for (int j = 0; j < 4; ++j) acc[nb][j] = 0.0f;
 
-    for (int c0 = 0; c0 < nch; c0 += kSmallThreads * kCPT) {
-        uint4 wv[R][kCPT];
+    const int s_beg = kq * P.per_cta, s_end = min(s_beg + P.per_cta, P.slices);
+    for (int s0 = s_beg + warp; s0 < s_end; s0 += kSmallWarps * kMaxSlicesPerWarp) {
+        uint4 va[kMaxSlicesPerWarp], vb[kMaxSlicesPerWarp], x0[kMaxSlicesPerWarp],
+            x1[kMaxSlicesPerWarp];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = row0 + r;
-            const uint16_t *src = (row < p.E) ? p.w + (int64_t)row * p.H : p.ws;
-#pragma unroll
-            for (int j = 0; j < kCPT; ++j) {
-                const int c = c0 + j * kSmallThreads + tid;
-                wv[r][j] = (row < rows && c < nch) ? ld_stream_v4(src + (int64_t)c * 8)
-                                                   : make_uint4(0u, 0u, 0u, 0u);
-            }
+        for (int j = 0; j < kMaxSlicesPerWarp; ++j) {
+            const int s = s0 + j * kSmallWarps;
+            const int k0 = s * kSliceK + 8 * t;
+            const int kc = min(k0, p.H - 8);  // clamped so every load stays in bounds
+            va[j] = ld_stream_v4(wa + kc);
+            vb[j] = ld_stream_v4(wb + kc);
+            x0[j] = __ldg(reinterpret_cast<const uint4 *>(xa + kc));
+            if (NB > 1) x1[j] = __ldg(reinterpret_cast<const uint4 *>(xb + kc));
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m < p.M) {
-#pragma unroll
-                for (int j = 0; j < kCPT; ++j) {
-                    const int c = c0 + j * kSmallThreads + tid;
-                    if (c < nch)
-                        cp_async16(&xs[(m * kCPT + j) * kSmallThreads + tid],
-                                   p.x + (int64_t)m * p.ld + (int64_t)c * 8);
-                }
+        for (int j = 0; j < kMaxSlicesPerWarp; ++j) {
+            const int s = s0 + j * kSmallWarps;
+            if (s >= s_end) continue;  // uniform across the warp (mma.sync is warp-wide)
+            if (s * kSliceK + 8 * t >= p.H) {  // this thread's chunk is past H: contributes 0
+                va[j] = vb[j] = x0[j] = make_uint4(0u, 0u, 0u, 0u);
+                if (NB > 1) x1[j] = x0[j];
             }
-        }
-        cp_async_wait_all();
-#pragma unroll
-        for (int j = 0; j < kCPT; ++j) {
-            const int c = c0 + j * kSmallThreads + tid;
-            if (c < nch) {
-                float wf[R][8];
-#pragma unroll
-                for (int r = 0; r < R; ++r) unpack8(wv[r][j], wf[r]);
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m < p.M) {
-                        float xf[8];
-                        unpack8(xs[(m * kCPT + j) * kSmallThreads + tid], xf);
-#pragma unroll
-                        for (int r = 0; r < R; ++r)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(wf[r][e], xf[e], acc[r][m]);
-                    }
-                }
+            // one slice = two K=16 steps over this thread's elements k0..k0+7:
+            // step 0 takes elements 0-3 (as logical k 2t,2t+1 | 2t+8,2t+9),
+            // step 1 elements 4-7; A rows g and g+8, B column = token g
+            mma_bf16_16816(acc[0], va[j].x, vb[j].x, va[j].y, vb[j].y, x0[j].x, x0[j].y);
+            mma_bf16_16816(acc[0], va[j].z, vb[j].z, va[j].w, vb[j].w, x0[j].z, x0[j].w);
+            if (NB > 1) {
+                mma_bf16_16816(acc[NB - 1], va[j].x, vb[j].x, va[j].y, vb[j].y, x1[j].x, x1[j].y);
+                mma_bf16_16816(acc[NB - 1], va[j].z, vb[j].z, va[j].w, vb[j].w, x1[j].z, x1[j].w);
             }
         }
     }
 
-    // ---- 2. reduce over the CTA: warp butterfly reduce-scatter + 8 warps ----
-    float v[N];
+    // ---- 2. sum the 8 warps in a fixed order, store this K range's partials ----
+    float *red = reinterpret_cast<float *>(smem);  // [8 warps][16 rows][16 tokens]
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int m = 0; m < MT; ++m) v[r * MT + m] = acc[r][m];
-    constexpr int LOGN = Log2<N>::value;
-    constexpr int STEPS = LOGN < 5 ? LOGN : 5;
-#pragma unroll
-    for (int s = 0; s < STEPS; ++s) {
-        const int o = 16 >> s;
-        const int half = N >> (s + 1);
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    constexpr int KEEP = (N >> STEPS) > 0 ? (N >> STEPS) : 1;  // values per lane now
-#pragma unroll
-    for (int o = 16 >> STEPS; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-    if (N >= 32) {
-#pragma unroll
-        for (int j = 0; j < KEEP; ++j) red[warp * N + lane * KEEP + j] = v[j];
-    } else if ((lane & ((32 >> STEPS) - 1)) == 0) {
-        red[warp * N + (lane >> (5 - STEPS))] = v[0];
+    for (int nb = 0; nb < NB; ++nb) {
+        const int tok = nb * 8 + 2 * t;
+        red[(warp * 16 + g) * 16 + tok] = acc[nb][0];
+        red[(warp * 16 + g) * 16 + tok + 1] = acc[nb][1];
+        red[(warp * 16 + g + 8) * 16 + tok] = acc[nb][2];
+        red[(warp * 16 + g + 8) * 16 + tok + 1] = acc[nb][3];
     }
     __syncthreads();
-    if (tid < N) {
-        float t = 0.0f;
+    {
+        const int r = tid >> 4, m = tid & 15;  // 256 threads = 16 rows x 16 tokens
+        if (m < p.M && m < NB * 8 && row0 + r < rows) {
+            float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kSmallWarps; ++w) t += red[w * N + tid];
-        const int r = tid / MT, m = tid % MT, row = row0 + r;
-        if (row < rows && m < p.M) p.scratch[(int64_t)m * rows + row] = t;
-        __threadfence();
+            for (int w = 0; w < kSmallWarps; ++w) v += red[(w * 16 + r) * 16 + m];
+            p.scratch[((int64_t)kq * p.M + m) * rows + row0 + r] = v;
+            __threadfence();
+        }
     }
     __syncthreads();
 
     // ---- 3. hand-off: the last CTA to arrive runs the tail ----
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.hdr);
     if (tid == 0) {
-        const unsigned t = atomicAdd(&hdr->ticket, 1u);
-        s_last = (t == gridDim.x - 1);
+        const unsigned tk = atomicAdd(&hdr->ticket, 1u);
+        s_last = (tk == gridDim.x - 1);
     }
     __syncthreads();
     if (!s_last) return;
@@ -225,19 +241,31 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
 
     // ---- 4. tail: top-k + softmax + shared slot, one warp per token ----
     const int width = p.k + p.S;
-    int32_t *ids_s = reinterpret_cast<int32_t *>(smem);  // [M*width], reuses x staging
+    int32_t *ids_s = reinterpret_cast<int32_t *>(smem);  // [M*width]
     int *align_smem = ids_s + kSmallMaxM * 32;
+    const int64_t kq_stride = (int64_t)p.M * rows;
+    const int nk = (p.E + 31) >> 5;
     __syncthreads();
     for (int m = warp; m < p.M; m += kSmallWarps) {
         const float *zrow = p.scratch + (int64_t)m * rows;
-        const int id = warp_topk_row(zrow, p.bias, p.E, p.k,
-                                     p.logits_out ? p.logits_out + (int64_t)m * p.E : nullptr,
-                                     p.ids + (int64_t)m * width, p.wts + (int64_t)m * width);
+        uint16_t *lrow = p.logits_out ? p.logits_out + (int64_t)m * p.E : nullptr;
+        int32_t *irow = p.ids + (int64_t)m * width;
+        float *wrow = p.wts + (int64_t)m * width;
+        int id;
+        if (nk <= 4)
+            id = warp_topk_row<4>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
+        else if (nk <= 8)
+            id = warp_topk_row<8>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
+        else if (nk <= 16)
+            id = warp_topk_row<16>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
+        else
+            id = warp_topk_row<32>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
         if (lane < p.k) ids_s[m * width + lane] = id;
         if (p.S && lane == p.k) {
-            const float s = __ldcg(zrow + p.E);
-            p.ids[(int64_t)m * width + p.k] = p.E;
-            p.wts[(int64_t)m * width + p.k] = p.scale * sigmoid_stable(s);
+            float s = 0.0f;
+            for (int q = 0; q < P.KQ; ++q) s += __ldcg(zrow + q * kq_stride + p.E);
+            irow[p.k] = p.E;
+            wrow[p.k] = p.scale * sigmoid_stable(s);
             ids_s[m * width + p.k] = p.E;
         }
     }
@@ -250,36 +278,34 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
     align_count(ids_s, numel, rows, as, &hdr->error);
     const int npp = align_offsets(as.cnt, rows, p.A, as);
     align_scatter(ids_s, numel, rows, 0, as, false, p.sorted);
-    align_blocks(npp, p.A, rows, as.cnt, as, numel, p.sorted, p.expert_ids, warp, kSmallWarps);
+    align_fill(p.A, rows, as.cnt, as, numel, p.sorted, p.expert_ids, warp, kSmallWarps);
     if (tid == 0) *p.npp = npp;
 }
 
-template <int R, int MT>
-static cudaError_t launch_rm(const SmallParams &P, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = small_route_kernel<R, MT>;
+template <int NB>
+static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             160 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    kern<<<grid, kSmallThreads, smem, stream>>>(P);
+    small_route_kernel<NB><<<grid, kSmallThreads, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
-template <int R>
-static cudaError_t launch_r(const SmallParams &P, int MT, int grid, size_t smem,
-                            cudaStream_t stream) {
-    switch (MT) {
-        case 1: return launch_rm<R, 1>(P, grid, smem, stream);
-        case 2: return launch_rm<R, 2>(P, grid, smem, stream);
-        case 4: return launch_rm<R, 4>(P, grid, smem, stream);
-        case 8: return launch_rm<R, 8>(P, grid, smem, stream);
-        default: return launch_rm<R, 16>(P, grid, smem, stream);
-    }
+int small_route_k_ranges(int E, int S, int H) {
+    // enough CTAs for one wave on ~150 SMs, at least one slice per warp
+    const int groups = (E + S + 15) / 16;
+    const int slices = (H + kSliceK - 1) / kSliceK;
+    int KQ = 150 / groups;
+    if (KQ < 1) KQ = 1;
+    const int max_kq = (slices + kSmallWarps - 1) / kSmallWarps;
+    if (KQ > max_kq) KQ = max_kq;
+    return KQ;
 }
 
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
@@ -287,18 +313,15 @@ cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
     SmallParams P;
     P.a = a;
     P.rows = a.E + a.S;
-    const int R = P.rows <= 160 ? 1 : (P.rows <= 320 ? 2 : 4);
-    int MT = 1;
-    while (MT < a.M) MT <<= 1;
-    const int grid = (P.rows + R - 1) / R;
-    const size_t stage = (size_t)MT * kCPT * kSmallThreads * 16 + (size_t)kSmallWarps * R * MT * 4;
+    P.slices = (a.H + kSliceK - 1) / kSliceK;
+    P.KQ = small_route_k_ranges(a.E, a.S, a.H);
+    P.per_cta = (P.slices + P.KQ - 1) / P.KQ;
+    const int groups = (P.rows + 15) / 16;
+    const int grid = groups * P.KQ;
+    const size_t stage = (size_t)kSmallWarps * 16 * 16 * 4;
     const size_t tail = (size_t)(kSmallMaxM * 32 + align_smem_words(kSmallWarps, P.rows)) * 4;
     const size_t smem = stage > tail ? stage : tail;
-    switch (R) {
-        case 1: return launch_r<1>(P, MT, grid, smem, stream);
-        case 2: return launch_r<2>(P, MT, grid, smem, stream);
-        default: return launch_r<4>(P, MT, grid, smem, stream);
-    }
+    return a.M <= 8 ? launch_nb<1>(P, grid, smem, stream) : launch_nb<2>(P, grid, smem, stream);
 }
 
 }  // namespace smr

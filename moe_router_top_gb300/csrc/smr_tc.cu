@@ -9,8 +9,9 @@
 // (M=16384: 2*16384*4096*513 = 68.9 GFLOP) and belongs on the tensor cores.
 //
 // One CTA per 128-token tile, 192 threads:
-//   warp 0     TMA producer: x tile [128 x 64] and the whole gate [E x 64] per
-//              k-block, 128-byte swizzle, into a ring of shared-memory stages;
+//   warp 0     TMA producer: x tile [128 x 32] and the whole gate [E x 32] per
+//              k-block, 64-byte swizzle, into a ring of shared-memory stages
+//              (5 stages of 40 KB at E=512);
 //   warp 1     allocates TMEM (E fp32 columns x 128 lanes) and issues
 //              tcgen05.mma (M=128, N<=256 per instruction, K=16) from one
 //              thread; tcgen05.commit frees each stage;
@@ -36,7 +37,8 @@
 namespace smr {
 
 constexpr int kTcBM = 128;
-constexpr int kTcBK = 64;
+constexpr int kTcBK = 32;             // k-block: 32 bf16 = 64-byte rows, 64B swizzle
+constexpr int kTcSW = kTcBK * 2;
 constexpr int kTcThreads = 192;
 constexpr int kCandCap = 32;
 constexpr int kTcSmemLimit = 232448;  // 227 KiB opt-in per CTA
@@ -176,10 +178,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const uint32_t b_base = a_base + kTcBM * kTcBK * 2;
 #pragma unroll
                 for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                    const uint64_t adesc = smem_desc_sw128(a_base + kk * 32);
+                    const uint64_t adesc = smem_desc_sw<kTcSW>(a_base + kk * 32);
                     for (int pc = 0; pc < p.n_pieces; ++pc) {
                         const uint64_t bdesc =
-                            smem_desc_sw128(b_base + (uint32_t)(pc * p.piece_n * 128) + kk * 32);
+                            smem_desc_sw<kTcSW>(b_base + (uint32_t)(pc * p.piece_n * kTcSW) + kk * 32);
                         tc_mma_bf16(tmem + (uint32_t)(pc * p.piece_n), adesc, bdesc, idesc,
                                     (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -202,13 +204,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 // warp-uniform: either every lane saw the stage or the warp stops
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag)))
                     break;
-                const uint8_t *arow = smem + (size_t)s * p.stage_bytes + row * (kTcBK * 2);
+                const uint8_t *arow = smem + (size_t)s * p.stage_bytes + row * kTcSW;
                 float part = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < kTcBK / 8; ++c) {
                     const int h = kb * kTcBK + c * 8;
                     if (h < p.H) {
-                        const uint4 xa = *reinterpret_cast<const uint4 *>(arow + ((c ^ (row & 7)) << 4));
+                        const uint4 xa =
+                            *reinterpret_cast<const uint4 *>(arow + (swizzled_chunk<kTcSW>(row, c) << 4));
                         const uint4 wa = *reinterpret_cast<const uint4 *>(ws_s + h);
                         float xf[8], wf[8];
                         unpack8(xa, xf);
@@ -364,7 +367,9 @@ static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              kTcSW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                           : (kTcSW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B),
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -6,8 +6,9 @@ Acceptance rules:
    where it differs from the oracle's bf16(z) it is counted. delta is the
    worst-case error of the kernel's fp32 summation tree, one ulp (2^-24
    relative) per addition on the chain, times sum|x*W| (+|bias|), doubled:
-     small-M path  : a chain of 16*ceil(H/4096) products per thread, then 13
-                     tree levels (warp butterfly + 8 warps): 16*ceil(H/4096)+16
+     small-M path  : per warp a chain of mma.sync K=16 steps over its share of
+                     K, then 8 warps and the K ranges added in a fixed order;
+                     bounded by ceil(H/64) + 48 additions
      tcgen05 path  : one fp32 accumulator update per K=16 instruction, so
                      H/16 sequential additions (+32 for the in-instruction sum).
    Near-zero logits (heavy cancellation) can therefore move several bf16
@@ -45,7 +46,7 @@ def accumulation_bound(ri: inputs.RouteInputs) -> float:
     """Relative fp32 summation bound (times sum|x*W|) of the kernel path."""
     u = 2.0 ** -24
     if ri.M <= 16:
-        chain = 16 * -(-ri.H // 4096) + 16
+        chain = -(-ri.H // 64) + 48
     else:
         chain = -(-ri.H // 16) + 32
     return 2.0 * chain * u
