@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const Align
     align_count(ids, a.numel, a.E_al, s, err);
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
     align_scatter(ids, a.numel, a.E_al, 0, s, false, a.sorted);
-    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids, threadIdx.x >> 5, kAlignWarps);
+    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids, threadIdx.x, blockDim.x);
     if (threadIdx.x == 0) *a.npp = npp;
 }
 
@@ -53,13 +53,10 @@ __global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLa
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int i = beg + j * kAlignThreads + warp * 32 + lane;
-        int e = (i < end) ? v[j] : -1;
-        if (i < end && (unsigned)e >= (unsigned)a.E_al) {
-            set_error(err, kErrBadId);
-            e = -1;
+        if (i < end) {
+            if ((unsigned)v[j] < (unsigned)a.E_al) atomicAdd(&cnt[v[j]], 1);
+            else set_error(err, kErrBadId);
         }
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[e], __popc(peers));
     }
     __syncthreads();
     for (int e = threadIdx.x; e < a.E_al; e += blockDim.x)
@@ -76,16 +73,17 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const Alig
     stage_ids(ids, a.ids + beg, n);
     align_count(ids, n, a.E_al, s, err);  // per-warp starts inside this tile
     // global per-expert totals and this tile's offset inside each expert, from
-    // all tiles' counts (fixed order; eight loads in flight per thread)
+    // all tiles' counts (fixed order; sixteen loads in flight per thread)
     for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) {
         int base = 0, tot = 0;
-        for (int u0 = 0; u0 < ntiles; u0 += 8) {
-            int c[8];
+        for (int u0 = 0; u0 < ntiles; u0 += 16) {
+            int c[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                c[j] = (u0 + j < ntiles) ? __ldg(a.tile_counts + (int64_t)(u0 + j) * a.E_al + e) : 0;
+            for (int j = 0; j < 16; ++j)  // clamped addresses: all 16 loads in flight
+                c[j] = __ldg(a.tile_counts + (int64_t)min(u0 + j, ntiles - 1) * a.E_al + e);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 16; ++j) {
+                c[j] = (u0 + j < ntiles) ? c[j] : 0;
                 base += (u0 + j < t) ? c[j] : 0;
                 tot += c[j];
             }
@@ -97,7 +95,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const Alig
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
     align_scatter(ids, n, a.E_al, beg, s, true, a.sorted);
     align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids,
-               t * kAlignWarps + (threadIdx.x >> 5), ntiles * kAlignWarps);
+               threadIdx.x * ntiles + t, ntiles * blockDim.x);
     if (t == 0 && threadIdx.x == 0) *a.npp = npp;
 }
 

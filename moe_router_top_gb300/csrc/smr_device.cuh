@@ -177,9 +177,10 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
-// lane (base lane + i), columns [col, col+32).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
-    uint32_t r[32];
+// lane (base lane + i), columns [col, col+32). Asynchronous: the registers
+// are valid only after tmem_wait_ld(r), which also ties them to the wait so
+// the compiler cannot read them earlier.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32"
         " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -191,9 +192,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+          "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+          "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+          "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+          "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+          "+r"(r[31])
+        :: "memory");
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma: K-major operand whose rows
@@ -244,7 +253,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
 // Stability without a sort: each warp owns a contiguous range of slots; a
 // first pass counts per (warp, expert), an exclusive prefix over warps gives
 // each warp its start inside every expert segment, and a second pass ranks
-// equal ids inside each 32-slot step with match_any + popc.
+// equal ids inside each 32-slot step with a ballot-built peer mask + popc.
 
 struct AlignSmem {
     int *wcnt;     // [nwarps][E_al] per-warp counts, then per-warp starts
@@ -275,6 +284,21 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// Lanes of the warp holding the same value as this lane, for values in
+// [0, 2048): eleven ballots, one per bit (a fixed cost, unlike a
+// data-dependent match loop). Invalid entries use 2047, never a valid id.
+__device__ __forceinline__ uint32_t peers_of(int v) {
+    uint32_t m = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 11; ++b) {
+        const bool bit = (v >> b) & 1;
+        const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+constexpr int kNoExpert = 2047;
+
 // Slots [warp*L, min((warp+1)*L, n)) belong to warp `warp`; L is a multiple of 32.
 __device__ __forceinline__ int align_warp_span(int n) {
     const int nw = blockDim.x >> 5;
@@ -294,13 +318,13 @@ __device__ __forceinline__ void align_count(const int32_t *ids, int n, int E_al,
     int *wc = s.wcnt + warp * E_al;
     for (int b = beg; b < end; b += 32) {
         const int i = b + lane;
-        int e = (i < end) ? ids[i] : -1;
+        int e = (i < end) ? ids[i] : kNoExpert;
         if (i < end && (unsigned)e >= (unsigned)E_al) {
             set_error(err, kErrBadId);
-            e = -1;
+            e = kNoExpert;
         }
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+        const uint32_t peers = peers_of(e);
+        if (e != kNoExpert && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
         __syncwarp();
     }
     __syncthreads();
@@ -374,38 +398,31 @@ __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_a
     const uint32_t lt = lanemask_lt();
     for (int b = beg; b < end; b += 32) {
         const int i = b + lane;
-        int e = (i < end) ? ids[i] : -1;
-        if ((unsigned)e >= (unsigned)E_al) e = -1;
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0) {
+        int e = (i < end) ? ids[i] : kNoExpert;
+        if ((unsigned)e >= (unsigned)E_al) e = kNoExpert;
+        const uint32_t peers = peers_of(e);
+        if (e != kNoExpert) {
             const int pos = s.off[e] + (use_base ? s.base[e] : 0) + wc[e] + __popc(peers & lt);
             sorted[pos] = flat0 + i;
         }
         __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+        if (e != kNoExpert && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
         __syncwarp();
     }
 }
 
-// Padding and block owners, driven by expert: warps take 32 experts at a
-// time (warp `wfirst`, stride `wstride` over all participating warps); for
-// each touched expert e the warp writes expert_ids over e's blocks and the
-// sentinel into e's rows past its last slot. tot[] are per-expert totals.
+// Padding and block owners, one thread per expert (experts first, first +
+// stride, ...): a touched expert e owns blocks [off[e]/A, off[e+1]/A) and its
+// rows past its last slot, [off[e] + tot[e], off[e+1]), hold the sentinel.
 __device__ __forceinline__ void align_fill(int A, int E_al, const int *tot, const AlignSmem &s,
                                            int sentinel, int32_t *sorted, int32_t *expert_ids,
-                                           int wfirst, int wstride) {
-    const int lane = threadIdx.x & 31;
-    for (int e0 = wfirst * 32; e0 < E_al; e0 += wstride * 32) {
-        const int e = e0 + lane;
-        const int c = (e < E_al) ? tot[e] : 0;
-        uint32_t touched = __ballot_sync(0xffffffffu, c > 0);
-        while (touched) {
-            const int ee = e0 + __ffs(touched) - 1;
-            touched &= touched - 1;
-            const int o0 = s.off[ee], o1 = s.off[ee + 1], cnt = tot[ee];
-            for (int b = o0 / A + lane; b < o1 / A; b += 32) expert_ids[b] = ee;
-            for (int q = o0 + cnt + lane; q < o1; q += 32) sorted[q] = sentinel;
-        }
+                                           int first, int stride) {
+    for (int e = first; e < E_al; e += stride) {
+        const int c = tot[e];
+        if (c == 0) continue;
+        const int o0 = s.off[e], o1 = s.off[e + 1];
+        for (int b = o0 / A; b < o1 / A; ++b) expert_ids[b] = e;
+        for (int q = o0 + c; q < o1; ++q) sorted[q] = sentinel;
     }
 }
 

@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
     align_count(ids_s, numel, rows, as, &hdr->error);
     const int npp = align_offsets(as.cnt, rows, p.A, as);
     align_scatter(ids_s, numel, rows, 0, as, false, p.sorted);
-    align_fill(p.A, rows, as.cnt, as, numel, p.sorted, p.expert_ids, warp, kSmallWarps);
+    align_fill(p.A, rows, as.cnt, as, numel, p.sorted, p.expert_ids, tid, kSmallThreads);
     if (tid == 0) *p.npp = npp;
 }
 

@@ -28,7 +28,8 @@
 //                3. k max-extractions over that short list (exact fallback
 //                   over all E logits if the list overflows).
 // Every mbarrier wait is bounded; on timeout the kernel sets the workspace's
-// error bit, skips its outputs, frees TMEM and returns.
+// error bit, skips its outputs, frees TMEM and returns. Warps hand off through
+// mbarriers only (stage ring, accumulator ready, epilogue scratch, TMEM free).
 #include <cudaTypedefs.h>
 
 #include "smr_device.cuh"
@@ -87,6 +88,28 @@ __device__ __forceinline__ void sort_desc(float (&a)[N]) {
     }
 }
 
+// Bounded wait that ignores the abort flag (teardown only).
+__device__ __forceinline__ bool mbar_wait_teardown(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > (1ll << 32)) return false;
+    return true;
+}
+
+// Predicated shared store (no branch): writes v to addr only if c != 0.
+__device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, uint32_t c) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %2, 0;\n @p st.shared.u32 [%0], %1;\n}"
+                 ::"r"(addr), "r"(v), "r"(c) : "memory");
+}
+
+// Candidate entry (bf16 bits of the rounded logit in the high half, expert id
+// in the low half) -> ordered selection key.
+__device__ __forceinline__ uint32_t entry_key(uint32_t entry) {
+    const uint32_t b = entry >> 16;
+    const uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+    return (ord << 16) | (0xFFFFu - (entry & 0xFFFFu));
+}
+
 template <int NG>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -98,8 +121,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     uint8_t *misc = smem + (size_t)ST * p.stage_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + ST;
-    uint64_t *accum = empty + ST;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    uint64_t *accum = empty + ST;      // MMAs of the whole K loop done
+    uint64_t *epi_sync = accum + 1;    // the 4 epilogue warps are done with the stage ring
+    uint64_t *done = epi_sync + 1;     // the 4 epilogue warps are done with TMEM
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
     uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
@@ -113,6 +138,8 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             mbar_init(smem_u32(&empty[s]), 1 + (p.S ? 4 : 0));
         }
         mbar_init(smem_u32(accum), 1);
+        mbar_init(smem_u32(epi_sync), 4);
+        mbar_init(smem_u32(done), 4);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tm_x);
@@ -162,6 +189,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer -----
         if (lane == 0) {
@@ -190,6 +218,11 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
             tc_commit(smem_u32(accum));
         }
+        __syncwarp();
+        // free TMEM once the epilogue warps have finished reading it
+        if (!mbar_wait_teardown(smem_u32(done), 0u)) set_error(p.err, kErrWaitTimeout);
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
     } else {
         // ------------------------------------------- epilogue warps 2-5 ---
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -227,24 +260,26 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
         bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
         tc_fence_after();
-        // all four epilogue warps are past the shared-dot reads of the stage
-        // ring before any of them reuses it as scratch
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag ? 1 : 0, 0) != 0;  // one decision per warp
+        // every epilogue warp is past its shared-dot reads of the stage ring
+        // before any of them reuses the ring as scratch
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(epi_sync));
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(epi_sync), 0u, abort_flag)) && ok;
+        ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
         if (ok) {
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-            const int nchunks = p.E >> 5;
-            uint32_t *cand = reinterpret_cast<uint32_t *>(smem);          // [kCandCap][128]
-            uint32_t *sel = cand + kCandCap * kTcBM;                        // [32][128]
-            // 1. class maxima and threshold
+            const int nch = p.E >> 5;
+            uint32_t *cand = reinterpret_cast<uint32_t *>(smem);  // [kCandCap][128] entries
+            uint32_t *sel = cand + kCandCap * kTcBM;               // [32][128] selected keys
+            uint32_t ra[32], rb[32];
+            // 1. rounded logits, class maxima (class = column mod NG), threshold
             float gmax[NG];
 #pragma unroll
             for (int g = 0; g < NG; ++g) gmax[g] = -INFINITY;
-            for (int ch = 0; ch < nchunks; ++ch) {
-                float v[32];
-                tmem_ld32(taddr + (uint32_t)(ch * 32), v);
+            auto phase1 = [&](uint32_t (&r)[32], int ch) {
+                float zr[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = round_bf16(v[i] + bias_s[ch * 32 + i]);
+                for (int i = 0; i < 32; ++i) zr[i] = round_bf16(__uint_as_float(r[i]) + bias_s[ch * 32 + i]);
                 if (p.logits_out && valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + ch * 32);
 #pragma unroll
@@ -252,46 +287,80 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         uint32_t w4[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t)
-                            w4[t] = (__float_as_uint(v[u * 8 + 2 * t]) >> 16) |
-                                    (__float_as_uint(v[u * 8 + 2 * t + 1]) & 0xFFFF0000u);
+                            w4[t] = (__float_as_uint(zr[u * 8 + 2 * t]) >> 16) |
+                                    (__float_as_uint(zr[u * 8 + 2 * t + 1]) & 0xFFFF0000u);
                         dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) gmax[i % NG] = fmaxf(gmax[i % NG], v[i]);
-            }
-            sort_desc<NG>(gmax);
-            float T = gmax[0];
-#pragma unroll
-            for (int g = 1; g < NG; ++g) T = (g == p.k - 1) ? gmax[g] : T;
-            // 2. candidates >= T as ordered keys
-            int n = 0;
-            for (int ch = 0; ch < nchunks; ++ch) {
-                float v[32];
-                tmem_ld32(taddr + (uint32_t)(ch * 32), v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float zr = round_bf16(v[i] + bias_s[ch * 32 + i]);
-                    if (zr >= T) {
-                        if (n < kCandCap) cand[n * kTcBM + row] = make_key(zr, ch * 32 + i);
-                        ++n;
-                    }
+                for (int i = 0; i < 32; ++i) gmax[i % NG] = fmaxf(gmax[i % NG], zr[i]);
+            };
+            // TMEM loads double-buffered: the next chunk is in flight while
+            // this one is processed
+            tmem_ld32_async(taddr, ra);
+            tmem_wait_ld(ra);
+            for (int ch = 0; ch < nch; ch += 2) {
+                const bool two = ch + 1 < nch;
+                if (two) tmem_ld32_async(taddr + (uint32_t)((ch + 1) * 32), rb);
+                phase1(ra, ch);
+                if (two) {
+                    tmem_wait_ld(rb);
+                    if (ch + 2 < nch) tmem_ld32_async(taddr + (uint32_t)((ch + 2) * 32), ra);
+                    phase1(rb, ch + 1);
+                    if (ch + 2 < nch) tmem_wait_ld(ra);
                 }
             }
-            // 3. k extractions, exact fallback if the list overflowed
-            const bool overflow = n > kCandCap;
+            // gmax sorted descending: the k-th largest is the minimum of the
+            // first k (a masked min keeps gmax in registers)
+            sort_desc<NG>(gmax);
+            float T = INFINITY;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) T = fminf(T, g < p.k ? gmax[g] : INFINITY);
+            // 2. append every logit >= T (branch-free predicated stores)
+            uint32_t n = 0;
+            const uint32_t cand_row = smem_u32(cand + row);
+            auto phase2 = [&](uint32_t (&r)[32], int ch) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float zr = round_bf16(__uint_as_float(r[i]) + bias_s[ch * 32 + i]);
+                    const uint32_t c = zr >= T ? 1u : 0u;
+                    const uint32_t slot = min(n, (uint32_t)(kCandCap - 1));
+                    st_shared_if(cand_row + slot * (kTcBM * 4),
+                                 (__float_as_uint(zr) & 0xFFFF0000u) | (uint32_t)(ch * 32 + i),
+                                 c & (n < (uint32_t)kCandCap ? 1u : 0u));
+                    n += c;
+                }
+            };
+            tmem_ld32_async(taddr, ra);
+            tmem_wait_ld(ra);
+            for (int ch = 0; ch < nch; ch += 2) {
+                const bool two = ch + 1 < nch;
+                if (two) tmem_ld32_async(taddr + (uint32_t)((ch + 1) * 32), rb);
+                phase2(ra, ch);
+                if (two) {
+                    tmem_wait_ld(rb);
+                    if (ch + 2 < nch) tmem_ld32_async(taddr + (uint32_t)((ch + 2) * 32), ra);
+                    phase2(rb, ch + 1);
+                    if (ch + 2 < nch) tmem_wait_ld(ra);
+                }
+            }
+            // 3. k extractions over the candidates; exact fallback over all E
+            //    logits for rows whose list overflowed
+            const bool overflow = n > (uint32_t)kCandCap;
+            const int nn = (int)min(n, (uint32_t)kCandCap);
+            for (int j = 0; j < nn; ++j) cand[j * kTcBM + row] = entry_key(cand[j * kTcBM + row]);
             if (__any_sync(0xffffffffu, overflow)) {
                 uint32_t prev = 0xFFFFFFFFu;
                 for (int r = 0; r < p.k; ++r) {
                     uint32_t best = 0u;
-                    for (int ch = 0; ch < nchunks; ++ch) {
-                        float v[32];
-                        tmem_ld32(taddr + (uint32_t)(ch * 32), v);
+                    for (int ch = 0; ch < nch; ++ch) {
+                        tmem_ld32_async(taddr + (uint32_t)(ch * 32), ra);
+                        tmem_wait_ld(ra);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const uint32_t key =
-                                make_key(round_bf16(v[i] + bias_s[ch * 32 + i]), ch * 32 + i);
-                            if (key < prev && key > best) best = key;
+                            const uint32_t key = make_key(
+                                round_bf16(__uint_as_float(ra[i]) + bias_s[ch * 32 + i]), ch * 32 + i);
+                            best = (key < prev && key > best) ? key : best;
                         }
                     }
                     if (overflow) sel[r * kTcBM + row] = best;
@@ -302,9 +371,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 uint32_t prev = 0xFFFFFFFFu;
                 for (int r = 0; r < p.k; ++r) {
                     uint32_t best = 0u;
-                    for (int j = 0; j < n; ++j) {
+                    for (int j = 0; j < nn; ++j) {
                         const uint32_t c = cand[j * kTcBM + row];
-                        if (c < prev && c > best) best = c;
+                        best = (c < prev && c > best) ? c : best;
                     }
                     sel[r * kTcBM + row] = best;
                     prev = best;
@@ -323,21 +392,17 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     wrow[r] = expf(key_value(key) - vmax) / sum;
                 }
                 if (p.S) {
-                    const float s = s_hi + s_lo;
+                    const float sh = s_hi + s_lo;
                     orow[p.k] = p.E;
-                    wrow[p.k] = p.scale * sigmoid_stable(s);
+                    wrow[p.k] = p.scale * sigmoid_stable(sh);
                 }
             }
         } else {
             set_error(p.err, kErrWaitTimeout);
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
+        tc_fence_before();
         __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, p.tmem_cols);
+        if (lane == 0) mbar_arrive(smem_u32(done));
     }
 }
 
@@ -400,7 +465,8 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.tmem_cols = cols;
     p.stage_bytes = (uint32_t)(kTcBM * kTcBK * 2 + E * kTcBK * 2);
     p.tx_bytes = p.stage_bytes;
-    // misc: barriers and flags (256 B), bias [E] fp32, shared gate [H] bf16
+    // misc: barriers and flags (256 B: 2*stages+3 mbarriers, TMEM slot, abort
+    // flag), bias [E] fp32, shared gate [H] bf16
     p.misc_bias_off = 256;
     p.misc_ws_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
     const size_t misc = p.misc_ws_off + (S ? (size_t)H * 2 : 0);
@@ -410,6 +476,7 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     if (st < 2) return false;
     // the epilogue scratch (candidate list + selection) reuses the stage ring
     if ((size_t)st * p.stage_bytes < (size_t)(kCandCap + 32) * kTcBM * 4) return false;
+    static_assert(8 * (2 * 8 + 3) + 8 <= 256, "barriers fit the misc header");
     p.stages = st;
     out->p = p;
     out->smem = 1024 + (size_t)st * p.stage_bytes + misc;
