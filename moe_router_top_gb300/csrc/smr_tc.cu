@@ -8,7 +8,9 @@
 // for many tokens, where the gate GEMM is a dense contraction
 // (M=16384: 2*16384*4096*513 = 68.9 GFLOP) and belongs on the tensor cores.
 //
-// One CTA per 128-token tile, 192 threads:
+// One CTA per 128-token tile, 192 threads, in clusters of C CTAs (C=8 at
+// M=16384) that share the gate: per k-block each CTA loads E/C gate rows with
+// a TMA multicast to all C, so the gate crosses L2 C times less often:
 //   warp 0     TMA producer: x tile [128 x 32] and the whole gate [E x 32] per
 //              k-block, 64-byte swizzle, into a ring of shared-memory stages
 //              (5 stages of 40 KB at E=512);
@@ -54,6 +56,7 @@ struct TcParams {
     uint16_t *logits_out;
     uint32_t *err;
     int num_kb, stages, n_pieces, piece_n, b_box_rows, n_b_boxes;
+    int cluster;  // CTAs sharing each gate k-block through TMA multicast (1 = none)
     uint32_t tmem_cols, stage_bytes, tx_bytes, misc_bias_off, misc_ws_off;
 };
 
@@ -96,10 +99,33 @@ __device__ __forceinline__ bool mbar_wait_teardown(uint32_t bar, uint32_t parity
     return true;
 }
 
-// Predicated shared store (no branch): writes v to addr only if c != 0.
+// Predicated shared store (no branch): writes v to addr only if c != 0. No
+// memory clobber, so surrounding loads can still be scheduled freely; callers
+// put one compiler barrier after their store loop.
 __device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, uint32_t c) {
     asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %2, 0;\n @p st.shared.u32 [%0], %1;\n}"
-                 ::"r"(addr), "r"(v), "r"(c) : "memory");
+                 ::"r"(addr), "r"(v), "r"(c));
+}
+
+// Descending sort of N unsigned keys (bitonic network, N a power of two).
+template <int N>
+__device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = ((i & size) == 0);
+                    const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
+                    a[i] = desc ? hi : lo;
+                    a[j] = desc ? lo : hi;
+                }
+            }
+        }
+    }
 }
 
 // Candidate entry (bf16 bits of the rounded logit in the high half, expert id
@@ -135,7 +161,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1 + (p.S ? 4 : 0));
+            // every CTA of the cluster writes into this stage (gate slices),
+            // so it is free once all of their MMAs (and the local shared-dot
+            // warps, which read the x tile) are done with it
+            mbar_init(smem_u32(&empty[s]), p.cluster + (p.S ? 4 : 0));
         }
         mbar_init(smem_u32(accum), 1);
         mbar_init(smem_u32(epi_sync), 4);
@@ -156,9 +185,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             reinterpret_cast<uint4 *>(ws_s)[c] = reinterpret_cast<const uint4 *>(p.ws)[c];
     }
     tc_fence_before();
-    __syncthreads();
+    if (p.cluster > 1)
+        cluster_sync();  // peers may signal our barriers only after they exist
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t rank = p.cluster > 1 ? cluster_ctarank() : 0u;
+    const uint16_t cmask = (uint16_t)((1u << p.cluster) - 1u);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
@@ -173,9 +207,16 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const uint32_t a_dst = smem_u32(smem + (size_t)s * p.stage_bytes);
                 tma_load_2d(a_dst, &tm_x, kb * kTcBK, m0, fb);
                 const uint32_t b_dst = a_dst + kTcBM * kTcBK * 2;
-                for (int bb = 0; bb < p.n_b_boxes; ++bb)
-                    tma_load_2d(b_dst + (uint32_t)(bb * p.b_box_rows * kTcBK * 2), &tm_w,
-                                kb * kTcBK, bb * p.b_box_rows, fb);
+                if (p.cluster > 1) {
+                    // this CTA's slice of the gate rows, to every CTA of the cluster
+                    const int r0 = (int)rank * p.b_box_rows;
+                    tma_load_2d_multicast(b_dst + (uint32_t)(r0 * kTcBK * 2), &tm_w, kb * kTcBK, r0,
+                                          fb, cmask);
+                } else {
+                    for (int bb = 0; bb < p.n_b_boxes; ++bb)
+                        tma_load_2d(b_dst + (uint32_t)(bb * p.b_box_rows * kTcBK * 2), &tm_w,
+                                    kb * kTcBK, bb * p.b_box_rows, fb);
+                }
             }
             if (kb < p.num_kb) {
                 // gave up: let the copies already issued land before exiting
@@ -214,7 +255,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                     (kb | kk) != 0 ? 1u : 0u);
                     }
                 }
-                tc_commit(smem_u32(&empty[s]));
+                if (p.cluster > 1)
+                    tc_commit_multicast(smem_u32(&empty[s]), cmask);
+                else
+                    tc_commit(smem_u32(&empty[s]));
             }
             tc_commit(smem_u32(accum));
         }
@@ -276,10 +320,19 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             float gmax[NG];
 #pragma unroll
             for (int g = 0; g < NG; ++g) gmax[g] = -INFINITY;
+            const bool has_bias = p.bias != nullptr;
+            auto rounded = [&](uint32_t (&r)[32], int ch, float (&zr)[32]) {
+                if (has_bias) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) zr[i] = round_bf16(__uint_as_float(r[i]) + bias_s[ch * 32 + i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) zr[i] = round_bf16(__uint_as_float(r[i]));
+                }
+            };
             auto phase1 = [&](uint32_t (&r)[32], int ch) {
                 float zr[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) zr[i] = round_bf16(__uint_as_float(r[i]) + bias_s[ch * 32 + i]);
+                rounded(r, ch, zr);
                 if (p.logits_out && valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + ch * 32);
 #pragma unroll
@@ -320,13 +373,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             uint32_t n = 0;
             const uint32_t cand_row = smem_u32(cand + row);
             auto phase2 = [&](uint32_t (&r)[32], int ch) {
+                float zr[32];
+                rounded(r, ch, zr);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float zr = round_bf16(__uint_as_float(r[i]) + bias_s[ch * 32 + i]);
-                    const uint32_t c = zr >= T ? 1u : 0u;
+                    const uint32_t c = zr[i] >= T ? 1u : 0u;
                     const uint32_t slot = min(n, (uint32_t)(kCandCap - 1));
                     st_shared_if(cand_row + slot * (kTcBM * 4),
-                                 (__float_as_uint(zr) & 0xFFFF0000u) | (uint32_t)(ch * 32 + i),
+                                 (__float_as_uint(zr[i]) & 0xFFFF0000u) | (uint32_t)(ch * 32 + i),
                                  c & (n < (uint32_t)kCandCap ? 1u : 0u));
                     n += c;
                 }
@@ -344,11 +398,16 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     if (ch + 2 < nch) tmem_wait_ld(ra);
                 }
             }
-            // 3. k extractions over the candidates; exact fallback over all E
-            //    logits for rows whose list overflowed
+            asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
+            // 3. the candidates as ordered keys in registers, sorted descending:
+            //    the top-k are the first k. Rows whose list overflowed take an
+            //    exact k-pass selection over all E logits instead.
             const bool overflow = n > (uint32_t)kCandCap;
-            const int nn = (int)min(n, (uint32_t)kCandCap);
-            for (int j = 0; j < nn; ++j) cand[j * kTcBM + row] = entry_key(cand[j * kTcBM + row]);
+            uint32_t key[kCandCap];
+#pragma unroll
+            for (int j = 0; j < kCandCap; ++j)
+                key[j] = (j < (int)n) ? entry_key(cand[j * kTcBM + row]) : 0u;
+            sort_keys_desc<kCandCap>(key);
             if (__any_sync(0xffffffffu, overflow)) {
                 uint32_t prev = 0xFFFFFFFFu;
                 for (int r = 0; r < p.k; ++r) {
@@ -356,40 +415,40 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int ch = 0; ch < nch; ++ch) {
                         tmem_ld32_async(taddr + (uint32_t)(ch * 32), ra);
                         tmem_wait_ld(ra);
+                        float zr[32];
+                        rounded(ra, ch, zr);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const uint32_t key = make_key(
-                                round_bf16(__uint_as_float(ra[i]) + bias_s[ch * 32 + i]), ch * 32 + i);
-                            best = (key < prev && key > best) ? key : best;
+                            const uint32_t k2 = make_key(zr[i], ch * 32 + i);
+                            best = (k2 < prev && k2 > best) ? k2 : best;
                         }
                     }
                     if (overflow) sel[r * kTcBM + row] = best;
                     prev = best;
                 }
-            }
-            if (!overflow) {
-                uint32_t prev = 0xFFFFFFFFu;
-                for (int r = 0; r < p.k; ++r) {
-                    uint32_t best = 0u;
-                    for (int j = 0; j < nn; ++j) {
-                        const uint32_t c = cand[j * kTcBM + row];
-                        best = (c < prev && c > best) ? c : best;
-                    }
-                    sel[r * kTcBM + row] = best;
-                    prev = best;
+                if (overflow) {
+#pragma unroll
+                    for (int j = 0; j < kCandCap; ++j) key[j] = (j < p.k) ? sel[j * kTcBM + row] : 0u;
                 }
             }
             // softmax over the selected logits, shared slot
             if (valid) {
-                const float vmax = key_value(sel[row]);
+                const float vmax = key_value(key[0]);
+                float ev[kCandCap];
                 float sum = 0.0f;
-                for (int r = 0; r < p.k; ++r) sum += expf(key_value(sel[r * kTcBM + row]) - vmax);
+#pragma unroll
+                for (int j = 0; j < kCandCap; ++j) {
+                    ev[j] = (j < p.k) ? expf(key_value(key[j]) - vmax) : 0.0f;
+                    sum += ev[j];
+                }
                 int32_t *orow = p.ids + (int64_t)grow * p.width;
                 float *wrow = p.wts + (int64_t)grow * p.width;
-                for (int r = 0; r < p.k; ++r) {
-                    const uint32_t key = sel[r * kTcBM + row];
-                    orow[r] = key_id(key);
-                    wrow[r] = expf(key_value(key) - vmax) / sum;
+#pragma unroll
+                for (int j = 0; j < kCandCap; ++j) {
+                    if (j < p.k) {
+                        orow[j] = key_id(key[j]);
+                        wrow[j] = ev[j] / sum;
+                    }
                 }
                 if (p.S) {
                     const float sh = s_hi + s_lo;
@@ -404,6 +463,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(done));
     }
+    // no CTA leaves while a peer may still arrive on its barriers
+    __syncwarp();
+    if (p.cluster > 1) cluster_sync();
 }
 
 // ------------------------------------------------------------------ host --
@@ -458,8 +520,21 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.num_kb = (H + kTcBK - 1) / kTcBK;
     p.n_pieces = (E + 255) / 256;
     p.piece_n = E / p.n_pieces;
-    p.b_box_rows = (E % 256 == 0) ? 256 : (E % 128 == 0) ? 128 : (E % 64 == 0) ? 64 : 32;
-    p.n_b_boxes = E / p.b_box_rows;
+    // cluster size: gate k-blocks are multicast to C CTAs (each loads E/C
+    // rows); the largest C in {8,4,2} with at least 2C row tiles and E/C a
+    // multiple of 8 (whole 8-row swizzle atoms)
+    const int tiles = (M + kTcBM - 1) / kTcBM;
+    int C = 1;
+    for (int c = 8; c >= 2; c >>= 1)
+        if (tiles >= 2 * c && (E / c) % 8 == 0 && E % c == 0) { C = c; break; }
+    p.cluster = C;
+    if (C > 1) {
+        p.b_box_rows = E / C;
+        p.n_b_boxes = 1;
+    } else {
+        p.b_box_rows = (E % 256 == 0) ? 256 : (E % 128 == 0) ? 128 : (E % 64 == 0) ? 64 : 32;
+        p.n_b_boxes = E / p.b_box_rows;
+    }
     uint32_t cols = 32;
     while (cols < (uint32_t)E) cols <<= 1;
     p.tmem_cols = cols;
@@ -480,7 +555,7 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.stages = st;
     out->p = p;
     out->smem = 1024 + (size_t)st * p.stage_bytes + misc;
-    out->grid = (M + kTcBM - 1) / kTcBM;
+    out->grid = (tiles + C - 1) / C * C;  // whole clusters; extra tiles are all padding
     return true;
 }
 
@@ -502,8 +577,19 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    tc_route_kernel<NG><<<plan.grid, kTcThreads, plan.smem, stream>>>(mx, mw, plan.p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_route_kernel<NG>, mx, mw, plan.p);
 }
 
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
