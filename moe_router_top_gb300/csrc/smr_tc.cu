@@ -8,15 +8,22 @@
 // for many tokens, where the gate GEMM is a dense contraction
 // (M=16384: 2*16384*4096*513 = 68.9 GFLOP) and belongs on the tensor cores.
 //
-// One CTA per 128-token tile, 192 threads, in clusters of C CTAs (C=8 at
-// M=16384) that share the gate: per k-block each CTA loads E/C gate rows with
-// a TMA multicast to all C, so the gate crosses L2 C times less often:
-//   warp 0     TMA producer: x tile [128 x 32] and the whole gate [E x 32] per
-//              k-block, 64-byte swizzle, into a ring of shared-memory stages
-//              (5 stages of 40 KB at E=512);
-//   warp 1     allocates TMEM (E fp32 columns x 128 lanes) and issues
-//              tcgen05.mma (M=128, N<=256 per instruction, K=16) from one
-//              thread; tcgen05.commit frees each stage;
+// CTA pairs (clusters of 2) own 256-token tiles and use the pair form of the
+// 5th-generation tensor-core MMA (tcgen05.mma.cta_group::2, M=256): each CTA
+// keeps its 128 token rows of x and HALF of every gate tile in its shared
+// memory, and the two SMs' tensor cores share the halves. An M=128 single-SM
+// MMA would need every SM to receive the whole gate tile; with it, TMA writes
+// plus MMA operand reads reach the SM's shared-memory bandwidth, while the
+// pair form halves the gate bytes per SM.
+//
+// Per CTA, 192 threads:
+//   warp 0     TMA producer: x tile [128 x 64] and this CTA's half of each
+//              N<=256 gate piece [E/2 x 64] per k-block (128-byte swizzle),
+//              into a ring of shared-memory stages; loads of both CTAs
+//              complete the leader CTA's "full" barrier;
+//   warp 1     allocates TMEM for the pair (E fp32 columns x 128 lanes per
+//              CTA); in the leader CTA one thread issues the pair MMAs and
+//              commits (multicast to both CTAs) to free each stage;
 //   warps 2-5  meanwhile compute the shared-expert logit of their row from the
 //              staged x tile (CUDA cores, fp32 per k-block, compensated sum
 //              across k-blocks); then the epilogue: thread = token row, reads
@@ -25,13 +32,13 @@
 //                1. maxima of NG column classes (c mod NG) -> threshold T =
 //                   k-th largest class maximum (at least k logits >= T, so
 //                   every top-k logit, ties included, is >= T);
-//                2. collect the logits >= T as ordered keys (about 1.5k of
-//                   them on random data) into a per-thread shared list;
-//                3. k max-extractions over that short list (exact fallback
-//                   over all E logits if the list overflows).
+//                2. append the logits >= T (about 1.5k of them on random
+//                   data) to a per-thread shared list with predicated stores;
+//                3. sort that list as ordered keys in registers (exact
+//                   fallback over all E logits if the list overflows).
 // Every mbarrier wait is bounded; on timeout the kernel sets the workspace's
-// error bit, skips its outputs, frees TMEM and returns. Warps hand off through
-// mbarriers only (stage ring, accumulator ready, epilogue scratch, TMEM free).
+// error bit, skips its outputs and still frees TMEM and leaves through the
+// cluster barriers. Warps hand off through mbarriers only.
 #include <cudaTypedefs.h>
 
 #include "smr_device.cuh"
@@ -39,8 +46,8 @@
 
 namespace smr {
 
-constexpr int kTcBM = 128;
-constexpr int kTcBK = 32;             // k-block: 32 bf16 = 64-byte rows, 64B swizzle
+constexpr int kTcBM = 128;            // token rows per CTA (256 per CTA pair)
+constexpr int kTcBK = 64;             // k-block: 64 bf16 = 128-byte rows, 128B swizzle
 constexpr int kTcSW = kTcBK * 2;
 constexpr int kTcThreads = 192;
 constexpr int kCandCap = 32;
@@ -55,9 +62,8 @@ struct TcParams {
     float *wts;
     uint16_t *logits_out;
     uint32_t *err;
-    int num_kb, stages, n_pieces, piece_n, b_box_rows, n_b_boxes;
-    int cluster;  // CTAs sharing each gate k-block through TMA multicast (1 = none)
-    uint32_t tmem_cols, stage_bytes, tx_bytes, misc_bias_off, misc_ws_off;
+    int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
+    uint32_t tmem_cols, stage_bytes, misc_bias_off, misc_ws_off;
 };
 
 // Compensated (two-sum) accumulation of k-block partial sums.
@@ -89,14 +95,6 @@ __device__ __forceinline__ void sort_desc(float (&a)[N]) {
             }
         }
     }
-}
-
-// Bounded wait that ignores the abort flag (teardown only).
-__device__ __forceinline__ bool mbar_wait_teardown(uint32_t bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > (1ll << 32)) return false;
-    return true;
 }
 
 // Predicated shared store (no branch): writes v to addr only if c != 0. No
@@ -145,38 +143,38 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                                 ~static_cast<uintptr_t>(1023));
     const int ST = p.stages;
     uint8_t *misc = smem + (size_t)ST * p.stage_bytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(misc);
-    uint64_t *empty = full + ST;
-    uint64_t *accum = empty + ST;      // MMAs of the whole K loop done
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc);  // leader: both CTAs' loads landed
+    uint64_t *empty = full + ST;       // both CTAs: the pair MMAs (and local readers) are done
+    uint64_t *a_ready = empty + ST;    // peer: the leader saw this stage full (x tile readable)
+    uint64_t *accum = a_ready + ST;    // the pair MMAs of the whole K loop are done
     uint64_t *epi_sync = accum + 1;    // the 4 epilogue warps are done with the stage ring
-    uint64_t *done = epi_sync + 1;     // the 4 epilogue warps are done with TMEM
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_sync + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
     uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * kTcBM;
+    const uint32_t rank = cluster_ctarank();  // 0 = leader of the pair, 1 = peer
+    const bool leader = rank == 0;
+    const uint16_t pair_mask = 0x3;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            // every CTA of the cluster writes into this stage (gate slices),
-            // so it is free once all of their MMAs (and the local shared-dot
-            // warps, which read the x tile) are done with it
-            mbar_init(smem_u32(&empty[s]), p.cluster + (p.S ? 4 : 0));
+            mbar_init(smem_u32(&empty[s]), 1 + (p.S ? 4 : 0));
+            mbar_init(smem_u32(&a_ready[s]), 1);
         }
         mbar_init(smem_u32(accum), 1);
         mbar_init(smem_u32(epi_sync), 4);
-        mbar_init(smem_u32(done), 4);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_w);
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
-        tmem_relinquish();
+    if (warp == 1) {  // one warp in each CTA of the pair allocates for both
+        tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);
+        tmem_relinquish_pair();
     }
     for (int i = threadIdx.x; i < p.E; i += kTcThreads) bias_s[i] = p.bias ? p.bias[i] : 0.0f;
     if (p.S) {
@@ -185,56 +183,36 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             reinterpret_cast<uint4 *>(ws_s)[c] = reinterpret_cast<const uint4 *>(p.ws)[c];
     }
     tc_fence_before();
-    if (p.cluster > 1)
-        cluster_sync();  // peers may signal our barriers only after they exist
-    else
-        __syncthreads();
+    cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t rank = p.cluster > 1 ? cluster_ctarank() : 0u;
-    const uint16_t cmask = (uint16_t)((1u << p.cluster) - 1u);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
+            const uint32_t half = (uint32_t)(p.piece_n / 2);  // gate rows per CTA per piece
             int kb = 0;
             for (; kb < p.num_kb; ++kb) {
                 const int s = kb % ST;
                 const uint32_t ph = (uint32_t)(kb / ST) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag)) break;
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, p.tx_bytes);
+                const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0u);  // leader's barrier
+                if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * p.stage_bytes);
                 const uint32_t a_dst = smem_u32(smem + (size_t)s * p.stage_bytes);
-                tma_load_2d(a_dst, &tm_x, kb * kTcBK, m0, fb);
-                const uint32_t b_dst = a_dst + kTcBM * kTcBK * 2;
-                if (p.cluster > 1) {
-                    // this CTA's slice of the gate rows, to every CTA of the cluster
-                    const int r0 = (int)rank * p.b_box_rows;
-                    tma_load_2d_multicast(b_dst + (uint32_t)(r0 * kTcBK * 2), &tm_w, kb * kTcBK, r0,
-                                          fb, cmask);
-                } else {
-                    for (int bb = 0; bb < p.n_b_boxes; ++bb)
-                        tma_load_2d(b_dst + (uint32_t)(bb * p.b_box_rows * kTcBK * 2), &tm_w,
-                                    kb * kTcBK, bb * p.b_box_rows, fb);
-                }
+                tma_load_2d_pair(a_dst, &tm_x, kb * kTcBK, m0, fb);
+                const uint32_t b_dst = a_dst + kTcBM * kTcSW;
+                for (int pc = 0; pc < p.n_pieces; ++pc)
+                    tma_load_2d_pair(b_dst + (uint32_t)pc * half * kTcSW, &tm_w, kb * kTcBK,
+                                     pc * p.piece_n + (int)(rank * half), fb);
             }
-            if (kb < p.num_kb) {
-                // gave up: let the copies already issued land before exiting
-                set_error(p.err, kErrWaitTimeout);
-                for (int j = kb - 1; j >= 0 && j >= kb - ST; --j) {
-                    const uint32_t fb = smem_u32(&full[j % ST]);
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(fb, (uint32_t)(j / ST) & 1u) &&
-                           clock64() - t0 < (1ll << 28)) {
-                    }
-                }
-            }
+            if (kb < p.num_kb) set_error(p.err, kErrWaitTimeout);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------- MMA issuer -----
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kTcBM, p.piece_n);
+        // ------------------------------------------ MMA issuer (leader) ----
+        if (leader && lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(2 * kTcBM, p.piece_n);
+            const uint32_t half = (uint32_t)(p.piece_n / 2);
             for (int kb = 0; kb < p.num_kb; ++kb) {
                 const int s = kb % ST;
                 const uint32_t ph = (uint32_t)(kb / ST) & 1u;
@@ -243,30 +221,24 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     break;
                 }
                 tc_fence_after();
+                if (p.S) mbar_arrive_remote(cluster_addr(smem_u32(&a_ready[s]), 1u));
                 const uint32_t a_base = smem_u32(smem + (size_t)s * p.stage_bytes);
-                const uint32_t b_base = a_base + kTcBM * kTcBK * 2;
+                const uint32_t b_base = a_base + kTcBM * kTcSW;
 #pragma unroll
                 for (int kk = 0; kk < kTcBK / 16; ++kk) {
                     const uint64_t adesc = smem_desc_sw<kTcSW>(a_base + kk * 32);
                     for (int pc = 0; pc < p.n_pieces; ++pc) {
                         const uint64_t bdesc =
-                            smem_desc_sw<kTcSW>(b_base + (uint32_t)(pc * p.piece_n * kTcSW) + kk * 32);
-                        tc_mma_bf16(tmem + (uint32_t)(pc * p.piece_n), adesc, bdesc, idesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                            smem_desc_sw<kTcSW>(b_base + (uint32_t)pc * half * kTcSW + kk * 32);
+                        tc_mma_bf16_pair(tmem + (uint32_t)(pc * p.piece_n), adesc, bdesc, idesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
                     }
                 }
-                if (p.cluster > 1)
-                    tc_commit_multicast(smem_u32(&empty[s]), cmask);
-                else
-                    tc_commit(smem_u32(&empty[s]));
+                tc_commit_pair(smem_u32(&empty[s]), pair_mask);
             }
-            tc_commit(smem_u32(accum));
+            tc_commit_pair(smem_u32(accum), pair_mask);
         }
         __syncwarp();
-        // free TMEM once the epilogue warps have finished reading it
-        if (!mbar_wait_teardown(smem_u32(done), 0u)) set_error(p.err, kErrWaitTimeout);
-        tc_fence_after();
-        tmem_dealloc(tmem, p.tmem_cols);
     } else {
         // ------------------------------------------- epilogue warps 2-5 ---
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -278,9 +250,12 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             for (int kb = 0; kb < p.num_kb; ++kb) {
                 const int s = kb % ST;
                 const uint32_t ph = (uint32_t)(kb / ST) & 1u;
-                // warp-uniform: either every lane saw the stage or the warp stops
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag)))
-                    break;
+                // warp-uniform: either every lane saw the stage or the warp stops.
+                // The leader's full barrier covers both CTAs' loads; the peer
+                // learns of it through a_ready, which the leader's MMA thread
+                // arrives on after its own wait.
+                const uint32_t rb = leader ? smem_u32(&full[s]) : smem_u32(&a_ready[s]);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(rb, ph, abort_flag))) break;
                 const uint8_t *arow = smem + (size_t)s * p.stage_bytes + row * kTcSW;
                 float part = 0.0f;
 #pragma unroll
@@ -461,11 +436,15 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(done));
     }
-    // no CTA leaves while a peer may still arrive on its barriers
+    // both CTAs' epilogues are done with TMEM and no barrier of either CTA
+    // can still be signalled: free the pair's TMEM, then leave
     __syncwarp();
-    if (p.cluster > 1) cluster_sync();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, p.tmem_cols);
+    }
 }
 
 // ------------------------------------------------------------------ host --
@@ -518,44 +497,32 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.M = M;
     p.width = k + S;
     p.num_kb = (H + kTcBK - 1) / kTcBK;
+    // gate pieces of at most 256 columns (one pair MMA each, N <= 256); each
+    // CTA holds half of every piece's rows (a multiple of 8: whole swizzle atoms)
     p.n_pieces = (E + 255) / 256;
     p.piece_n = E / p.n_pieces;
-    // cluster size: gate k-blocks are multicast to C CTAs (each loads E/C
-    // rows); the largest C in {8,4,2} with at least 2C row tiles and E/C a
-    // multiple of 8 (whole 8-row swizzle atoms)
-    const int tiles = (M + kTcBM - 1) / kTcBM;
-    int C = 1;
-    for (int c = 8; c >= 2; c >>= 1)
-        if (tiles >= 2 * c && (E / c) % 8 == 0 && E % c == 0) { C = c; break; }
-    p.cluster = C;
-    if (C > 1) {
-        p.b_box_rows = E / C;
-        p.n_b_boxes = 1;
-    } else {
-        p.b_box_rows = (E % 256 == 0) ? 256 : (E % 128 == 0) ? 128 : (E % 64 == 0) ? 64 : 32;
-        p.n_b_boxes = E / p.b_box_rows;
-    }
+    if (p.piece_n % 16 != 0) return false;
     uint32_t cols = 32;
     while (cols < (uint32_t)E) cols <<= 1;
     p.tmem_cols = cols;
-    p.stage_bytes = (uint32_t)(kTcBM * kTcBK * 2 + E * kTcBK * 2);
-    p.tx_bytes = p.stage_bytes;
-    // misc: barriers and flags (256 B: 2*stages+3 mbarriers, TMEM slot, abort
+    p.stage_bytes = (uint32_t)(kTcBM * kTcSW + (E / 2) * kTcSW);
+    // misc: barriers and flags (256 B: 3*stages+2 mbarriers, TMEM slot, abort
     // flag), bias [E] fp32, shared gate [H] bf16
     p.misc_bias_off = 256;
     p.misc_ws_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
     const size_t misc = p.misc_ws_off + (S ? (size_t)H * 2 : 0);
     const size_t budget = (size_t)kTcSmemLimit - 1024 - misc;
     int st = (int)(budget / p.stage_bytes);
-    if (st > 8) st = 8;
+    if (st > 6) st = 6;
     if (st < 2) return false;
+    static_assert(8 * (3 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
     // the epilogue scratch (candidate list + selection) reuses the stage ring
     if ((size_t)st * p.stage_bytes < (size_t)(kCandCap + 32) * kTcBM * 4) return false;
-    static_assert(8 * (2 * 8 + 3) + 8 <= 256, "barriers fit the misc header");
     p.stages = st;
     out->p = p;
     out->smem = 1024 + (size_t)st * p.stage_bytes + misc;
-    out->grid = (tiles + C - 1) / C * C;  // whole clusters; extra tiles are all padding
+    const int tiles = (M + kTcBM - 1) / kTcBM;
+    out->grid = (tiles + 1) / 2 * 2;  // whole CTA pairs; a missing partner tile is all padding
     return true;
 }
 
@@ -584,7 +551,7 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)plan.p.cluster;
+    attr[0].val.clusterDim.x = 2;  // CTA pairs
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -607,7 +574,7 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     if (!make_map(&mx, a.x, (uint64_t)a.H, (uint64_t)a.M, (uint64_t)a.ld * 2, kTcBK, kTcBM))
         return cudaErrorInvalidValue;
     if (!make_map(&mw, a.w, (uint64_t)a.H, (uint64_t)a.E, (uint64_t)a.H * 2, kTcBK,
-                  (uint32_t)p.b_box_rows))
+                  (uint32_t)(p.piece_n / 2)))
         return cudaErrorInvalidValue;
     return a.k <= 16 ? launch_ng<16>(mx, mw, plan, stream) : launch_ng<32>(mx, mw, plan, stream);
 }
