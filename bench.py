@@ -475,6 +475,24 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """A few route+align steps at --profile-m tokens (large-batch shapes), for
+    ncu captures of single launches on a small case."""
+    import torch
+    import moe_router_top_gb300 as smr
+    from moe_router_top_gb300 import build, inputs
+    build.build()
+    torch.cuda.set_device(0)
+    ri = inputs.large_batch(args.profile_m)
+    x, w, ws = (to_dev_bf16(a, torch) for a in (ri.x, ri.w, ri.ws))
+    wsp = smr.Workspace()
+    for _ in range(args.warmup + args.steps):
+        smr.route_align(x, w, ws, topk=K, block_size=A_LARGE, workspace=wsp)
+    torch.cuda.synchronize()
+    assert smr.get_device_error(wsp) == 0
+    print(f"profile run: {args.steps} steps at M={args.profile_m}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -485,10 +503,15 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-large", action="store_true",
                     help="only the M=4/8 small-batch timings (prints a partial line)")
+    ap.add_argument("--profile-m", type=int, default=0,
+                    help="profiling aid: run `--steps` route+align steps of the large-batch "
+                         "shapes at this many tokens and exit (no JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile_m:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_smr(args)
