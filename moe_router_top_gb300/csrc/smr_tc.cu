@@ -49,7 +49,7 @@ namespace smr {
 constexpr int kTcBM = 128;            // token rows per CTA (256 per CTA pair)
 constexpr int kTcBK = 64;             // k-block: 64 bf16 = 128-byte rows, 128B swizzle
 constexpr int kTcSW = kTcBK * 2;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 256;
 constexpr int kCandCap = 32;
 constexpr int kTcSmemLimit = 232448;  // 227 KiB opt-in per CTA
 
@@ -58,6 +58,8 @@ struct TcParams {
     float scale;
     const float *bias;
     const uint16_t *ws;
+    const uint16_t *x;  // hidden states (row stride ld), read directly by the shared-logit warps
+    int64_t ld;
     int32_t *ids;
     float *wts;
     uint16_t *logits_out;
@@ -134,6 +136,23 @@ __device__ __forceinline__ uint32_t entry_key(uint32_t entry) {
     return (ord << 16) | (0xFFFFu - (entry & 0xFFFFu));
 }
 
+// Bitonic merge of a bitonic sequence of N keys into descending order.
+template <int N>
+__device__ __forceinline__ void bitonic_merge_desc(uint32_t (&a)[N]) {
+#pragma unroll
+    for (int stride = N >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int j = i ^ stride;
+            if (j > i) {
+                const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
+                a[i] = hi;
+                a[j] = lo;
+            }
+        }
+    }
+}
+
 template <int NG>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -144,11 +163,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int ST = p.stages;
     uint8_t *misc = smem + (size_t)ST * p.stage_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);  // leader: both CTAs' loads landed
-    uint64_t *empty = full + ST;       // both CTAs: the pair MMAs (and local readers) are done
-    uint64_t *a_ready = empty + ST;    // peer: the leader saw this stage full (x tile readable)
-    uint64_t *accum = a_ready + ST;    // the pair MMAs of the whole K loop are done
-    uint64_t *epi_sync = accum + 1;    // the 4 epilogue warps are done with the stage ring
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_sync + 1);
+    uint64_t *empty = full + ST;       // both CTAs: the pair MMAs are done with the stage
+    uint64_t *accum = empty + ST;      // the pair MMAs of the whole K loop are done
+    uint64_t *half_done = accum + 1;   // the 4 warps of column half 0 posted their top-k
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(half_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
     uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
@@ -162,11 +180,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1 + (p.S ? 4 : 0));
-            mbar_init(smem_u32(&a_ready[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(accum), 1);
-        mbar_init(smem_u32(epi_sync), 4);
+        mbar_init(smem_u32(half_done), 4);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tm_x);
@@ -187,10 +204,20 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int hf = warp >> 2; // column half this warp takes in the epilogue
+    const int row = q * 32 + lane;
+    const int grow = m0 + row;
+    const bool valid = grow < p.M;
+    float s_hi = 0.0f, s_lo = 0.0f;  // shared-expert logit (warps 4-7)
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
             const uint32_t half = (uint32_t)(p.piece_n / 2);  // gate rows per CTA per piece
+            // a tile entirely past M (the padding partner of a pair) loads a
+            // valid tile instead; its results are never written
+            const int m_load = m0 < p.M ? m0 : 0;
             int kb = 0;
             for (; kb < p.num_kb; ++kb) {
                 const int s = kb % ST;
@@ -199,7 +226,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0u);  // leader's barrier
                 if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * p.stage_bytes);
                 const uint32_t a_dst = smem_u32(smem + (size_t)s * p.stage_bytes);
-                tma_load_2d_pair(a_dst, &tm_x, kb * kTcBK, m0, fb);
+                tma_load_2d_pair(a_dst, &tm_x, kb * kTcBK, m_load, fb);
                 const uint32_t b_dst = a_dst + kTcBM * kTcSW;
                 for (int pc = 0; pc < p.n_pieces; ++pc)
                     tma_load_2d_pair(b_dst + (uint32_t)pc * half * kTcSW, &tm_w, kb * kTcBK,
@@ -221,7 +248,6 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     break;
                 }
                 tc_fence_after();
-                if (p.S) mbar_arrive_remote(cluster_addr(smem_u32(&a_ready[s]), 1u));
                 const uint32_t a_base = smem_u32(smem + (size_t)s * p.stage_bytes);
                 const uint32_t b_base = a_base + kTcBM * kTcSW;
 #pragma unroll
@@ -239,204 +265,223 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc_commit_pair(smem_u32(accum), pair_mask);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------- epilogue warps 2-5 ---
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;
-        const int grow = m0 + row;
-        const bool valid = grow < p.M;
-        float s_hi = 0.0f, s_lo = 0.0f;
-        if (p.S) {
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % ST;
-                const uint32_t ph = (uint32_t)(kb / ST) & 1u;
-                // warp-uniform: either every lane saw the stage or the warp stops.
-                // The leader's full barrier covers both CTAs' loads; the peer
-                // learns of it through a_ready, which the leader's MMA thread
-                // arrives on after its own wait.
-                const uint32_t rb = leader ? smem_u32(&full[s]) : smem_u32(&a_ready[s]);
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(rb, ph, abort_flag))) break;
-                const uint8_t *arow = smem + (size_t)s * p.stage_bytes + row * kTcSW;
-                float part = 0.0f;
+    } else if (hf == 1 && p.S) {
+        // ------------- shared-expert logit, warps 4-7, from global memory ---
+        // Independent of the stage ring: each thread reads its own row of x
+        // (L2-hot, TMA streams the same tile), two k-blocks of loads in flight.
+        const uint16_t *xr = p.x + (int64_t)min(grow, p.M - 1) * p.ld;
+        const int nch = p.H >> 3;  // 16-byte chunks per row
+        constexpr int kAhead = 16;
+        uint4 buf[kAhead];
 #pragma unroll
-                for (int c = 0; c < kTcBK / 8; ++c) {
-                    const int h = kb * kTcBK + c * 8;
-                    if (h < p.H) {
-                        const uint4 xa =
-                            *reinterpret_cast<const uint4 *>(arow + (swizzled_chunk<kTcSW>(row, c) << 4));
-                        const uint4 wa = *reinterpret_cast<const uint4 *>(ws_s + h);
-                        float xf[8], wf[8];
-                        unpack8(xa, xf);
-                        unpack8(wa, wf);
+        for (int j = 0; j < kAhead; ++j) buf[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + min(j, nch - 1));
+        for (int c0 = 0; c0 < nch; c0 += kAhead / 2) {
+            float part = 0.0f;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
-                    }
+            for (int j = 0; j < kAhead / 2; ++j) {
+                const int c = c0 + j;
+                if (c < nch) {
+                    float xf[8], wf[8];
+                    unpack8(buf[j], xf);
+                    unpack8(reinterpret_cast<const uint4 *>(ws_s)[c], wf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
                 }
-                two_sum_acc(s_hi, s_lo, part);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            }
+            two_sum_acc(s_hi, s_lo, part);
+#pragma unroll
+            for (int j = 0; j < kAhead / 2; ++j) {
+                buf[j] = buf[j + kAhead / 2];
+                buf[j + kAhead / 2] =
+                    __ldg(reinterpret_cast<const uint4 *>(xr) + min(c0 + kAhead + j, nch - 1));
             }
         }
-        bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
-        tc_fence_after();
-        // every epilogue warp is past its shared-dot reads of the stage ring
-        // before any of them reuses the ring as scratch
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(epi_sync));
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(epi_sync), 0u, abort_flag)) && ok;
-        ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
-        if (ok) {
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-            const int nch = p.E >> 5;
-            uint32_t *cand = reinterpret_cast<uint32_t *>(smem);  // [kCandCap][128] entries
-            uint32_t *sel = cand + kCandCap * kTcBM;               // [32][128] selected keys
-            uint32_t ra[32], rb[32];
-            // 1. rounded logits, class maxima (class = column mod NG), threshold
-            float gmax[NG];
+    }
+
+    // ---------------------------------- epilogue: all 8 warps ----------
+    // warp (q, hf) owns TMEM lanes of quarter q (token rows q*32..q*32+31) and
+    // expert columns [hf*E/2, (hf+1)*E/2); each half finds its own exact
+    // top-k, half 1 merges both lists and writes the row.
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
+    tc_fence_after();
+    ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
+    const int ecols = p.E / 2;
+    const int c_beg = hf * ecols;
+    const int nch = ecols >> 4;  // 16-column TMEM chunks per half (E/2 is a multiple of 16)
+    uint32_t *cand = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);  // [kCandCap][128] per half
+    uint32_t *posted = reinterpret_cast<uint32_t *>(smem) + 2 * kCandCap * kTcBM;    // [32][128] half 0's top-k
+    uint32_t key[kCandCap];
+    if (ok) {
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
+        const bool has_bias = p.bias != nullptr;
+        uint32_t ra[16], rb[16];
+        auto rounded = [&](uint32_t (&r)[16], int ch, float (&zr)[16]) {
+            const int c = c_beg + ch * 16;
+            if (has_bias) {
 #pragma unroll
-            for (int g = 0; g < NG; ++g) gmax[g] = -INFINITY;
-            const bool has_bias = p.bias != nullptr;
-            auto rounded = [&](uint32_t (&r)[32], int ch, float (&zr)[32]) {
-                if (has_bias) {
+                for (int i = 0; i < 16; ++i) zr[i] = round_bf16(__uint_as_float(r[i]) + bias_s[c + i]);
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) zr[i] = round_bf16(__uint_as_float(r[i]) + bias_s[ch * 32 + i]);
-                } else {
+                for (int i = 0; i < 16; ++i) zr[i] = round_bf16(__uint_as_float(r[i]));
+            }
+        };
+        // 1. class maxima (class = column mod NG within the half), threshold
+        float gmax[NG];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) zr[i] = round_bf16(__uint_as_float(r[i]));
+        for (int g = 0; g < NG; ++g) gmax[g] = -INFINITY;
+        auto phase1 = [&](uint32_t (&r)[16], int ch) {
+            float zr[16];
+            rounded(r, ch, zr);
+            if (p.logits_out && valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + c_beg + ch * 16);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        w4[t] = (__float_as_uint(zr[u * 8 + 2 * t]) >> 16) |
+                                (__float_as_uint(zr[u * 8 + 2 * t + 1]) & 0xFFFF0000u);
+                    dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-            };
-            auto phase1 = [&](uint32_t (&r)[32], int ch) {
-                float zr[32];
-                rounded(r, ch, zr);
-                if (p.logits_out && valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + ch * 32);
+            }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint32_t w4[4];
+            for (int i = 0; i < 16; ++i) gmax[(ch * 16 + i) % NG] = fmaxf(gmax[(ch * 16 + i) % NG], zr[i]);
+        };
+        // TMEM loads double-buffered: the next chunk is in flight while this
+        // one is processed
+        tmem_ld16_async(taddr, ra);
+        tmem_wait_ld16(ra);
+        for (int ch = 0; ch < nch; ch += 2) {
+            const bool two = ch + 1 < nch;
+            if (two) tmem_ld16_async(taddr + (uint32_t)((ch + 1) * 16), rb);
+            phase1(ra, ch);
+            if (two) {
+                tmem_wait_ld16(rb);
+                if (ch + 2 < nch) tmem_ld16_async(taddr + (uint32_t)((ch + 2) * 16), ra);
+                phase1(rb, ch + 1);
+                if (ch + 2 < nch) tmem_wait_ld16(ra);
+            }
+        }
+        // gmax sorted descending: the k-th largest is the minimum of the
+        // first k (a masked min keeps gmax in registers); it bounds this
+        // half's top-k from below
+        sort_desc<NG>(gmax);
+        float T = INFINITY;
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            w4[t] = (__float_as_uint(zr[u * 8 + 2 * t]) >> 16) |
-                                    (__float_as_uint(zr[u * 8 + 2 * t + 1]) & 0xFFFF0000u);
-                        dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        for (int g = 0; g < NG; ++g) T = fminf(T, g < p.k ? gmax[g] : INFINITY);
+        // 2. append every logit >= T of this half (branch-free predicated stores)
+        uint32_t n = 0;
+        const uint32_t cand_row = smem_u32(cand + row);
+        auto phase2 = [&](uint32_t (&r)[16], int ch) {
+            float zr[16];
+            rounded(r, ch, zr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t c = zr[i] >= T ? 1u : 0u;
+                const uint32_t slot = min(n, (uint32_t)(kCandCap - 1));
+                st_shared_if(cand_row + slot * (kTcBM * 4),
+                             (__float_as_uint(zr[i]) & 0xFFFF0000u) | (uint32_t)(c_beg + ch * 16 + i),
+                             c & (n < (uint32_t)kCandCap ? 1u : 0u));
+                n += c;
+            }
+        };
+        tmem_ld16_async(taddr, ra);
+        tmem_wait_ld16(ra);
+        for (int ch = 0; ch < nch; ch += 2) {
+            const bool two = ch + 1 < nch;
+            if (two) tmem_ld16_async(taddr + (uint32_t)((ch + 1) * 16), rb);
+            phase2(ra, ch);
+            if (two) {
+                tmem_wait_ld16(rb);
+                if (ch + 2 < nch) tmem_ld16_async(taddr + (uint32_t)((ch + 2) * 16), ra);
+                phase2(rb, ch + 1);
+                if (ch + 2 < nch) tmem_wait_ld16(ra);
+            }
+        }
+        asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
+        // 3. this half's candidates as ordered keys in registers, sorted
+        //    descending. A row whose list overflowed takes an exact k-pass
+        //    selection over the half's logits instead.
+        const bool overflow = n > (uint32_t)kCandCap;
+#pragma unroll
+        for (int j = 0; j < kCandCap; ++j)
+            key[j] = (j < (int)n) ? entry_key(cand[j * kTcBM + row]) : 0u;
+        sort_keys_desc<kCandCap>(key);
+        if (__any_sync(0xffffffffu, overflow)) {
+            uint32_t prev = 0xFFFFFFFFu;
+            uint32_t picked[kCandCap];
+#pragma unroll
+            for (int j = 0; j < kCandCap; ++j) picked[j] = 0u;
+            for (int r = 0; r < p.k; ++r) {
+                uint32_t best = 0u;
+                for (int ch = 0; ch < nch; ++ch) {
+                    tmem_ld16_async(taddr + (uint32_t)(ch * 16), ra);
+                    tmem_wait_ld16(ra);
+                    float zr[16];
+                    rounded(ra, ch, zr);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t k2 = make_key(zr[i], c_beg + ch * 16 + i);
+                        best = (k2 < prev && k2 > best) ? k2 : best;
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) gmax[i % NG] = fmaxf(gmax[i % NG], zr[i]);
-            };
-            // TMEM loads double-buffered: the next chunk is in flight while
-            // this one is processed
-            tmem_ld32_async(taddr, ra);
-            tmem_wait_ld(ra);
-            for (int ch = 0; ch < nch; ch += 2) {
-                const bool two = ch + 1 < nch;
-                if (two) tmem_ld32_async(taddr + (uint32_t)((ch + 1) * 32), rb);
-                phase1(ra, ch);
-                if (two) {
-                    tmem_wait_ld(rb);
-                    if (ch + 2 < nch) tmem_ld32_async(taddr + (uint32_t)((ch + 2) * 32), ra);
-                    phase1(rb, ch + 1);
-                    if (ch + 2 < nch) tmem_wait_ld(ra);
-                }
+                for (int j = 0; j < kCandCap; ++j) picked[j] = (j == r) ? best : picked[j];
+                prev = best;
             }
-            // gmax sorted descending: the k-th largest is the minimum of the
-            // first k (a masked min keeps gmax in registers)
-            sort_desc<NG>(gmax);
-            float T = INFINITY;
+            if (overflow) {
 #pragma unroll
-            for (int g = 0; g < NG; ++g) T = fminf(T, g < p.k ? gmax[g] : INFINITY);
-            // 2. append every logit >= T (branch-free predicated stores)
-            uint32_t n = 0;
-            const uint32_t cand_row = smem_u32(cand + row);
-            auto phase2 = [&](uint32_t (&r)[32], int ch) {
-                float zr[32];
-                rounded(r, ch, zr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t c = zr[i] >= T ? 1u : 0u;
-                    const uint32_t slot = min(n, (uint32_t)(kCandCap - 1));
-                    st_shared_if(cand_row + slot * (kTcBM * 4),
-                                 (__float_as_uint(zr[i]) & 0xFFFF0000u) | (uint32_t)(ch * 32 + i),
-                                 c & (n < (uint32_t)kCandCap ? 1u : 0u));
-                    n += c;
-                }
-            };
-            tmem_ld32_async(taddr, ra);
-            tmem_wait_ld(ra);
-            for (int ch = 0; ch < nch; ch += 2) {
-                const bool two = ch + 1 < nch;
-                if (two) tmem_ld32_async(taddr + (uint32_t)((ch + 1) * 32), rb);
-                phase2(ra, ch);
-                if (two) {
-                    tmem_wait_ld(rb);
-                    if (ch + 2 < nch) tmem_ld32_async(taddr + (uint32_t)((ch + 2) * 32), ra);
-                    phase2(rb, ch + 1);
-                    if (ch + 2 < nch) tmem_wait_ld(ra);
-                }
+                for (int j = 0; j < kCandCap; ++j) key[j] = picked[j];
             }
-            asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
-            // 3. the candidates as ordered keys in registers, sorted descending:
-            //    the top-k are the first k. Rows whose list overflowed take an
-            //    exact k-pass selection over all E logits instead.
-            const bool overflow = n > (uint32_t)kCandCap;
-            uint32_t key[kCandCap];
+        }
+        if (hf == 0) {
 #pragma unroll
             for (int j = 0; j < kCandCap; ++j)
-                key[j] = (j < (int)n) ? entry_key(cand[j * kTcBM + row]) : 0u;
-            sort_keys_desc<kCandCap>(key);
-            if (__any_sync(0xffffffffu, overflow)) {
-                uint32_t prev = 0xFFFFFFFFu;
-                for (int r = 0; r < p.k; ++r) {
-                    uint32_t best = 0u;
-                    for (int ch = 0; ch < nch; ++ch) {
-                        tmem_ld32_async(taddr + (uint32_t)(ch * 32), ra);
-                        tmem_wait_ld(ra);
-                        float zr[32];
-                        rounded(ra, ch, zr);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const uint32_t k2 = make_key(zr[i], ch * 32 + i);
-                            best = (k2 < prev && k2 > best) ? k2 : best;
-                        }
-                    }
-                    if (overflow) sel[r * kTcBM + row] = best;
-                    prev = best;
-                }
-                if (overflow) {
-#pragma unroll
-                    for (int j = 0; j < kCandCap; ++j) key[j] = (j < p.k) ? sel[j * kTcBM + row] : 0u;
-                }
-            }
-            // softmax over the selected logits, shared slot
-            if (valid) {
-                const float vmax = key_value(key[0]);
-                float ev[kCandCap];
-                float sum = 0.0f;
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) {
-                    ev[j] = (j < p.k) ? expf(key_value(key[j]) - vmax) : 0.0f;
-                    sum += ev[j];
-                }
-                int32_t *orow = p.ids + (int64_t)grow * p.width;
-                float *wrow = p.wts + (int64_t)grow * p.width;
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) {
-                    if (j < p.k) {
-                        orow[j] = key_id(key[j]);
-                        wrow[j] = ev[j] / sum;
-                    }
-                }
-                if (p.S) {
-                    const float sh = s_hi + s_lo;
-                    orow[p.k] = p.E;
-                    wrow[p.k] = p.scale * sigmoid_stable(sh);
-                }
-            }
-        } else {
-            set_error(p.err, kErrWaitTimeout);
+                if (j < p.k) posted[j * kTcBM + row] = key[j];
         }
-        tc_fence_before();
-        __syncwarp();
     }
+    if (hf == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(half_done));
+    } else {
+        // ------------------------------ half 1: merge, softmax, write -----
+        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag));
+        if (ok && got && valid) {
+            // both lists sorted descending: reverse the other half's list
+            // behind this one -> bitonic sequence of 64 -> merge
+            uint32_t m[2 * kCandCap];
+#pragma unroll
+            for (int j = 0; j < kCandCap; ++j) {
+                m[j] = key[j];
+                m[2 * kCandCap - 1 - j] = (j < p.k) ? posted[j * kTcBM + row] : 0u;
+            }
+            bitonic_merge_desc<2 * kCandCap>(m);
+            const float vmax = key_value(m[0]);
+            float ev[kCandCap];
+            float sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kCandCap; ++j) {
+                ev[j] = (j < p.k) ? expf(key_value(m[j]) - vmax) : 0.0f;
+                sum += ev[j];
+            }
+            int32_t *orow = p.ids + (int64_t)grow * p.width;
+            float *wrow = p.wts + (int64_t)grow * p.width;
+#pragma unroll
+            for (int j = 0; j < kCandCap; ++j) {
+                if (j < p.k) {
+                    orow[j] = key_id(m[j]);
+                    wrow[j] = ev[j] / sum;
+                }
+            }
+            if (p.S) {
+                const float sh = s_hi + s_lo;
+                orow[p.k] = p.E;
+                wrow[p.k] = p.scale * sigmoid_stable(sh);
+            }
+        }
+        if (!(ok && got)) set_error(p.err, kErrWaitTimeout);
+    }
+    tc_fence_before();
     // both CTAs' epilogues are done with TMEM and no barrier of either CTA
     // can still be signalled: free the pair's TMEM, then leave
     __syncwarp();
@@ -506,7 +551,7 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     while (cols < (uint32_t)E) cols <<= 1;
     p.tmem_cols = cols;
     p.stage_bytes = (uint32_t)(kTcBM * kTcSW + (E / 2) * kTcSW);
-    // misc: barriers and flags (256 B: 3*stages+2 mbarriers, TMEM slot, abort
+    // misc: barriers and flags (256 B: 2*stages+2 mbarriers, TMEM slot, abort
     // flag), bias [E] fp32, shared gate [H] bf16
     p.misc_bias_off = 256;
     p.misc_ws_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
@@ -515,9 +560,9 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     int st = (int)(budget / p.stage_bytes);
     if (st > 6) st = 6;
     if (st < 2) return false;
-    static_assert(8 * (3 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
-    // the epilogue scratch (candidate list + selection) reuses the stage ring
-    if ((size_t)st * p.stage_bytes < (size_t)(kCandCap + 32) * kTcBM * 4) return false;
+    static_assert(8 * (2 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
+    // the epilogue scratch (two candidate lists + half 0's top-k) reuses the stage ring
+    if ((size_t)st * p.stage_bytes < (size_t)(2 * kCandCap + 32) * kTcBM * 4) return false;
     p.stages = st;
     out->p = p;
     out->smem = 1024 + (size_t)st * p.stage_bytes + misc;
@@ -565,6 +610,8 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     TcParams &p = plan.p;
     p.scale = a.scale;
     p.bias = a.bias;
+    p.x = a.x;
+    p.ld = a.ld;
     p.ws = a.ws;
     p.ids = a.ids;
     p.wts = a.wts;
