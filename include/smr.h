@@ -143,6 +143,25 @@ SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t
 SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_args *align,
                            void *workspace, size_t workspace_bytes, void *stream);
 
+/* Route then align for 1 <= M <= 16 in one launch, like smr_route_align, but
+ * with NO workspace argument and no allocation: for callers that cannot
+ * allocate device memory on their launch path (no device allocator is
+ * available to them, or allocation is forbidden once their memory pool is
+ * sized). The scratch is a fixed array of 256 KiB inside the library, kept
+ * by every GPU that loads the library until the process exits. (The pages
+ * have no counterpart; this is an interface convenience.)
+ *  - The first call on a device, with that device current, resolves the
+ *    array's device address and zeroes its counter; make that first call
+ *    outside any stream capture. Later calls do no set-up.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents: calls that overlap on the GPU (different streams
+ *    without ordering, or host threads) race and give wrong results.
+ *  - Problems whose scratch would exceed the array (see
+ *    smr_route_align_workspace_size) and M outside [1, 16] are refused with
+ *    SMR_ERR_UNSUPPORTED. Outputs are as for smr_route_align. */
+SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr_align_args *align,
+                                          void *stream);
+
 /* Sticky device error word of a workspace: synchronises `stream`, then copies
  * the word to *code_out (0 = no error; bit 0 = an id out of range in align,
  * bit 1 = a bounded wait inside a kernel gave up). Not for launch paths. */

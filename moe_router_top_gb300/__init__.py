@@ -18,6 +18,7 @@ from ._lib import AlignArgs, RouteArgs
 
 __all__ = [
     "SmrError", "SmrUnsupported", "Workspace", "route", "align", "route_align",
+    "route_align_static",
     "select_block_size", "align_capacity", "route_workspace_size", "align_workspace_size",
     "route_align_workspace_size", "get_device_error", "clear_device_error",
     "last_launch_count", "version",
@@ -253,6 +254,31 @@ def route_align(hidden, gate_w, shared_w=None, bias=None, *, topk: int, block_si
     need = lib.smr_route_align_workspace_size(ctypes.byref(ra), ctypes.byref(aa))
     wp, wn = _workspace(workspace, need, hidden.device)
     _check(lib.smr_route_align(ctypes.byref(ra), ctypes.byref(aa), wp, wn, _stream_ptr(stream)))
+    return (topk_ids, topk_weights) + tuple(outs)
+
+
+def route_align_static(hidden, gate_w, shared_w=None, bias=None, *, topk: int,
+                       block_size: int = 0, shared_scale: float = 1.0, renormalize: bool = True,
+                       topk_ids=None, topk_weights=None, logits_out=None, sorted_token_ids=None,
+                       expert_ids=None, num_tokens_post_padded=None, stream=None) -> Tuple:
+    """route_align for 1 <= M <= 16 without a workspace: the library's fixed
+    device scratch array is used instead, for callers that cannot allocate
+    device memory. Calls must not overlap on the GPU; the first call on a
+    device must come before any stream capture. Same outputs as route_align.
+    (Passing the outputs in avoids the allocations this wrapper otherwise
+    makes with torch for convenience.)"""
+    _disabled()
+    lib = _lib.load()
+    S = 1 if shared_w is not None else 0
+    topk_ids, topk_weights = _route_outputs(hidden, topk, S, topk_ids, topk_weights)
+    ra = _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, topk_ids,
+                     topk_weights, logits_out)
+    M, E = ra.M, ra.E
+    A = block_size if block_size > 0 else select_block_size(M, topk, E)
+    outs = _align_outputs(hidden.device, M * (topk + S), E + S, A, sorted_token_ids, expert_ids,
+                          num_tokens_post_padded)
+    aa = _align_args(topk_ids, M, topk + S, E + S, block_size, topk, E, *outs)
+    _check(lib.smr_route_align_static(ctypes.byref(ra), ctypes.byref(aa), _stream_ptr(stream)))
     return (topk_ids, topk_weights) + tuple(outs)
 
 

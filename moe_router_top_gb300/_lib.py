@@ -25,7 +25,7 @@ EXPORTED = (
     "smr_select_block_size", "smr_align_capacity", "smr_route_workspace_size",
     "smr_align_workspace_size", "smr_route_align_workspace_size", "smr_route", "smr_align",
     "smr_route_align", "smr_get_device_error", "smr_clear_device_error", "smr_status_string",
-    "smr_last_error", "smr_version", "smr_last_launch_count",
+    "smr_last_error", "smr_version", "smr_last_launch_count", "smr_route_align_static",
 )
 
 
@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH):
             "smr_last_error": ([], ctypes.c_char_p),
             "smr_version": ([], i32),
             "smr_last_launch_count": ([], i32),
+            "smr_route_align_static": ([RA, AA, P], ctypes.c_int),
         }
         for name, (argtypes, restype) in sigs.items():
             fn = getattr(lib, name)

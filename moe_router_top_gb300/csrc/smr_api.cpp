@@ -365,6 +365,45 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
     return SMR_OK;
 }
 
+SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr_align_args *align,
+                                          void *stream) {
+    g_last_launches = 0;
+    if (!route || !align) {
+        g_last_error = "smr_route_align_static: route or align args is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    Reasons r;
+    check_route(route, r);
+    const int S = route->has_shared ? 1 : 0;
+    smr_align_args al = *align;
+    al.routed_topk = route->topk;
+    al.routed_experts = route->E;
+    if (align->topk_ids != route->topk_ids) r.bad("align.topk_ids must equal route.topk_ids");
+    if (align->num_tokens != route->M) r.bad("align.num_tokens must equal route.M");
+    if (align->width != route->topk + S) r.bad("align.width must equal route.topk + has_shared");
+    if (align->num_experts != route->E + S) r.bad("align.num_experts must equal route.E + has_shared");
+    check_align(&al, r, true);
+    if (route->M < 1 || route->M > smr::kSmallMaxM)
+        r.unsup("the fixed-scratch entry point covers 1 <= M <= 16 (got M=" +
+                std::to_string(route->M) + ")");
+    if (!r.ok()) return r.finish("smr_route_align_static");
+    const size_t need = smr_route_align_workspace_size(route, &al);
+    if (need > smr::kStaticScratchBytes) {
+        r.unsup("needs " + std::to_string(need) + " bytes of scratch, above the fixed " +
+                std::to_string(smr::kStaticScratchBytes) + "-byte array");
+        return r.finish("smr_route_align_static");
+    }
+    smr_status st = check_device();
+    if (st != SMR_OK) return st;
+    void *scratch = nullptr;
+    cudaError_t e = smr::static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail("smr_route_align_static: scratch set-up", e);
+    int launches = 0;
+    st = run_route(route, scratch, static_cast<cudaStream_t>(stream), &al, &launches);
+    if (st == SMR_OK) g_last_launches = launches;
+    return st;
+}
+
 SMR_API smr_status smr_get_device_error(const void *workspace, void *stream, int32_t *code_out) {
     if (!workspace || !code_out) {
         g_last_error = "smr_get_device_error: workspace or code_out is NULL";

@@ -32,6 +32,10 @@ constexpr int kSmallMaxM = 16;
 // small_route_k_ranges(E, S, H) * M * (E + S) fp32 partial logits.
 int small_route_k_ranges(int E, int S, int H);
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream);
+// Fixed scratch in device memory (no allocation): capacity, and its device
+// address for the current device (set up on first use per device).
+constexpr size_t kStaticScratchBytes = 256 * 1024;
+cudaError_t static_scratch(void **ptr);
 
 // tcgen05 GEMM with the top-k fused into the epilogue.
 struct TcRouteLaunch {

@@ -308,6 +308,39 @@ int small_route_k_ranges(int E, int S, int H) {
     return KQ;
 }
 
+// ---- fixed device scratch for callers that cannot allocate ----------------
+//
+// Some callers cannot call cudaMalloc on their launch path at all (a host
+// that hands out no device allocator, a runtime that forbids allocation once
+// its memory pool is sized, code that must not disturb a captured allocation
+// pattern). For them the single-launch route+align can run on this
+// file-scope array instead of a caller workspace. It lives in every GPU
+// that loads the library until the process exits. Host code must not use
+// the symbol itself as a pointer (on the host it is only a stand-in), so the
+// device address is fetched once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
+
+cudaError_t static_scratch(void **ptr) {
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (addr[dev] == nullptr) {
+        // first use on this device (with it current): resolve the address and
+        // zero the hand-off counter and error word, which later calls leave
+        // at zero themselves
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (e != cudaSuccess) return e;
+        e = cudaMemset(p, 0, sizeof(WsHeader));
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
+
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
     if (a.M <= 0 || a.M > kSmallMaxM) return cudaErrorInvalidValue;
     SmallParams P;
