@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLa
         const int i = beg + j * kAlignThreads + warp * 32 + lane;
         v[j] = __ldg(a.ids + min(i, end - 1));
     }
+    __syncwarp();
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLa
             else set_error(err, kErrBadId);
         }
     }
+    __syncwarp();
     __syncthreads();
     for (int e = threadIdx.x; e < a.E_al; e += blockDim.x)
         a.tile_counts[(int64_t)blockIdx.x * a.E_al + e] = cnt[e];
@@ -91,6 +93,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const Alig
         s.base[e] = base;
         s.cnt[e] = tot;
     }
+    __syncwarp();
     __syncthreads();
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
     align_scatter(ids, n, a.E_al, beg, s, true, a.sorted);

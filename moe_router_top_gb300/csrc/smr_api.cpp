@@ -120,8 +120,7 @@ void check_route(const smr_route_args *a, Reasons &r) {
 size_t route_scratch_bytes(const smr_route_args *a) {
     if (a->M <= 0 || a->M > smr::kSmallMaxM) return 0;
     const int S = a->has_shared ? 1 : 0;
-    const size_t kq = (size_t)smr::small_route_k_ranges(a->E, S, a->H);
-    return round_up(kq * (size_t)a->M * (size_t)(a->E + S) * 4, kWsAlign);
+    return round_up((size_t)a->M * (size_t)(a->E + S) * 4, kWsAlign);
 }
 
 // --- align ------------------------------------------------------------------

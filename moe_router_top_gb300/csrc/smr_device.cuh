@@ -22,7 +22,7 @@ constexpr uint32_t kErrWaitTimeout = 2u;  // a bounded wait gave up
 // First 256 bytes of every workspace. Zeroed once by the caller; kernels
 // return the counters to zero before they exit.
 struct WsHeader {
-    uint32_t ticket;  // small route: CTAs that finished their gate rows
+    uint32_t ticket;  // small route: row groups whose gate logits are stored
     uint32_t error;   // sticky error bits (kErr*)
     uint32_t reserved[62];
 };
@@ -225,6 +225,16 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t ra
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
 }
+// 32-bit store into another CTA's shared memory (address from cluster_addr).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Acquire-release atomic add at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                  : "memory");
@@ -347,6 +357,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
 // each warp its start inside every expert segment, and a second pass ranks
 // equal ids inside each 32-slot step with a ballot-built peer mask + popc.
 
+// Convergence: a CTA barrier does not merge a warp whose lanes reached it on
+// different paths (loops with per-lane trip counts, single-lane stores), and
+// a warp that stays split replays every later instruction once per path and
+// pays a handshake at each shuffle or ballot. Every barrier after divergent
+// work is therefore preceded by __syncwarp().
 struct AlignSmem {
     int *wcnt;     // [nwarps][E_al] per-warp counts, then per-warp starts
     int *cnt;      // [E_al] counts of this CTA's slots (then reused as totals)
@@ -404,6 +419,7 @@ __device__ __forceinline__ void align_count(const int32_t *ids, int n, int E_al,
                                             const AlignSmem &s, uint32_t *err) {
     const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < nw * E_al; i += blockDim.x) s.wcnt[i] = 0;
+    __syncwarp();
     __syncthreads();
     const int L = align_warp_span(n);
     const int beg = warp * L, end = min(beg + L, n);
@@ -419,6 +435,7 @@ __device__ __forceinline__ void align_count(const int32_t *ids, int n, int E_al,
         if (e != kNoExpert && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
         __syncwarp();
     }
+    __syncwarp();
     __syncthreads();
     for (int e = threadIdx.x; e < E_al; e += blockDim.x) {
         int run = 0;
@@ -429,6 +446,7 @@ __device__ __forceinline__ void align_count(const int32_t *ids, int n, int E_al,
         }
         s.cnt[e] = run;
     }
+    __syncwarp();
     __syncthreads();
 }
 
@@ -442,6 +460,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
         if (lane >= o) x += y;
     }
     if (lane == 31) scratch[warp] = x;
+    __syncwarp();
     __syncthreads();
     if (warp == 0) {
         int t = lane < nw ? scratch[lane] : 0;
@@ -452,9 +471,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
         }
         scratch[lane] = t;
     }
+    __syncwarp();
     __syncthreads();
     const int excl = x - v + (warp > 0 ? scratch[warp - 1] : 0);
     *total = scratch[nw - 1];
+    __syncwarp();
     __syncthreads();
     return excl;
 }
@@ -467,6 +488,7 @@ __device__ __forceinline__ int align_offsets(const int *tot, int E_al, int A, co
     const int e0 = threadIdx.x * per, e1 = min(e0 + per, E_al);
     int local = 0;
     for (int e = e0; e < e1; ++e) local += (tot[e] + A - 1) / A * A;
+    __syncwarp();
     int total;
     int run = block_exclusive_scan(local, s.scratch, &total);
     for (int e = e0; e < e1; ++e) {
@@ -474,6 +496,7 @@ __device__ __forceinline__ int align_offsets(const int *tot, int E_al, int A, co
         run += (tot[e] + A - 1) / A * A;
     }
     if (threadIdx.x == 0) s.off[E_al] = total;
+    __syncwarp();
     __syncthreads();
     return total;
 }
@@ -527,6 +550,7 @@ __device__ __forceinline__ void stage_ids(int *dst, const int32_t *src, int n) {
     int4 *d4 = reinterpret_cast<int4 *>(dst);
     for (int i = threadIdx.x; i < n4; i += blockDim.x) d4[i] = __ldg(s4 + i);
     for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(src + i);
+    __syncwarp();
     __syncthreads();
 }
 

@@ -19,7 +19,7 @@ struct SmallRouteLaunch {
     int32_t *ids;
     float *wts;
     uint16_t *logits_out;
-    float *scratch;        // workspace: [K ranges][M][E+S] fp32 partial logits
+    float *scratch;        // workspace: [M][E+S] fp32 gate logits
     void *hdr;             // workspace header (WsHeader)
     // fused align (sorted == nullptr: route only)
     int A;
@@ -28,8 +28,8 @@ struct SmallRouteLaunch {
     int32_t *npp;
 };
 constexpr int kSmallMaxM = 16;
-// Number of K ranges the gate rows are split into; the scratch holds
-// small_route_k_ranges(E, S, H) * M * (E + S) fp32 partial logits.
+// Number of K ranges the gate rows are split into (the CTAs of one cluster);
+// the scratch holds M * (E + S) fp32 gate logits.
 int small_route_k_ranges(int E, int S, int H);
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream);
 // Fixed scratch in device memory (no allocation): capacity, and its device

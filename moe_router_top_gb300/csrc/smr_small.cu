@@ -22,13 +22,17 @@
 //    contiguous 8-element chunk straight from its 16-byte loads into the A and
 //    B fragments (the same K permutation on both operands), with no shared
 //    memory staging;
-//  - the 8 warps' partial sums are added in a fixed order and stored per K
-//    range; the tail adds the KQ ranges in a fixed order, so results are
-//    deterministic;
-//  - the tail is warp-parallel: one warp per token, each lane holds E/32
-//    ordered 32-bit keys sorted in registers, k rounds of one redux.sync max
-//    and a register shift pop the winner -- instead of k serial argmax
-//    passes over the row.
+//  - the KQ CTAs of a row group form a thread-block cluster: each adds its 8
+//    warps' partials in a fixed order and stores the sum into a slot in the
+//    shared memory of the cluster's first CTA (distributed shared memory),
+//    which adds the KQ slots in a fixed order after one cluster barrier and
+//    stores the group's final logits -- results are deterministic;
+//  - one acquire-release ticket per row group hands the tail to the last
+//    group (no spin-wait);
+//  - the tail is warp-parallel and straight-line: one warp per token, each
+//    lane holds E/32 ordered 32-bit keys sorted in registers, k rounds of one
+//    redux.sync max and a register shift pop the winner; the align of the
+//    few ids ranks (expert, position) keys instead of scanning all experts.
 #include "smr_device.cuh"
 #include "smr_launch.h"
 
@@ -38,6 +42,12 @@ constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSliceK = 32;           // K elements per slice (two m16n8k16 steps)
 constexpr int kMaxSlicesPerWarp = 4;  // slices whose loads are in flight at once
+constexpr int kSmallMaxCluster = 8;   // K ranges per row group = CTAs per cluster (portable size)
+constexpr int kSmallFrontWords = 4096;  // partials + cluster slots (16 KB), reused by the tail
+constexpr int kSmallMaxE = 1024;
+constexpr int kSmallBiasPerThread = kSmallMaxE / 256;
+static_assert(kSmallWarps * 256 + kSmallMaxCluster * 256 <= kSmallFrontWords, "partials + slots");
+static_assert(kSmallMaxM * 32 * 7 + 1 <= kSmallFrontWords, "tail arrays");
 
 struct SmallParams {
     SmallRouteLaunch a;
@@ -78,72 +88,153 @@ __device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[NK]) {
     }
 }
 
-// Top-k of one token row in one warp. part: fp32 partial logits laid out
-// [KQ][M][rows]; this token's first range starts at part, later ranges are
-// kq_stride apart. Writes ids and weights of slots 0..k-1 and returns the
-// slot's id in lanes j < k (-1 elsewhere).
+// Top-k of one token row in one warp, plus its shared slot. zrow: the
+// token's fp32 gate logits (E routed, then the shared one when S = 1);
+// bias_s: the routed experts' bias in shared memory (zeros without a bias).
+// Writes ids and weights of slots 0..width-1 to global memory and to
+// ids_s (the align input). The code is kept straight-line: it runs once per
+// call on whichever SM finishes last, where every taken jump into code the
+// instruction prefetcher has not reached costs a fetch from L2 or memory.
 template <int NK>
-__device__ __forceinline__ int warp_topk_row(const float *part, int KQ, int64_t kq_stride, int E,
-                                             int k, const float *bias, uint16_t *logits_out,
-                                             int32_t *ids, float *wts) {
+__device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, int k, float scale,
+                                              const float *bias_s, uint16_t *logits_out,
+                                              int32_t *ids, float *wts, int32_t *ids_s) {
     const int lane = threadIdx.x & 31;
     float z[NK];
+    // every load issued before the first use (the shared logit with them);
+    // lanes past E read a clamped (valid) element that is masked below
 #pragma unroll
-    for (int i = 0; i < NK; ++i) z[i] = 0.0f;
-    // all partial loads of a pair of ranges are issued before any is used:
-    // addresses are clamped into the row, out-of-row lanes are masked below
-    int q = 0;
-    for (; q + 2 <= KQ; q += 2) {
-        float v0[NK], v1[NK];
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-            const int e = min(lane + 32 * i, E - 1);
-            v0[i] = __ldcg(part + q * kq_stride + e);
-            v1[i] = __ldcg(part + (q + 1) * kq_stride + e);
-        }
-#pragma unroll
-        for (int i = 0; i < NK; ++i) z[i] = (z[i] + v0[i]) + v1[i];
-    }
-    if (q < KQ) {
-#pragma unroll
-        for (int i = 0; i < NK; ++i) z[i] += __ldcg(part + q * kq_stride + min(lane + 32 * i, E - 1));
-    }
+    for (int i = 0; i < NK; ++i) z[i] = __ldcg(zrow + min(lane + 32 * i, E - 1));
+    const float sv = __ldcg(zrow + E - 1 + S);
     uint32_t key[NK];
 #pragma unroll
     for (int i = 0; i < NK; ++i) {
         const int e = lane + 32 * i;
-        key[i] = 0u;
-        if (e < E) {
-            const float zr = round_bf16(bias ? z[i] + __ldg(bias + e) : z[i]);
-            key[i] = make_key(zr, e);
-            if (logits_out) logits_out[e] = (uint16_t)(__float_as_uint(zr) >> 16);
-        }
+        z[i] = round_bf16(z[i] + bias_s[min(e, E - 1)]);
+        key[i] = (e < E) ? make_key(z[i], e) : 0u;
+    }
+    if (__builtin_expect(logits_out != nullptr, 0)) {
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            if (lane + 32 * i < E) logits_out[lane + 32 * i] = (uint16_t)(__float_as_uint(z[i]) >> 16);
+        __syncwarp();
     }
     sort_keys_desc<NK>(key);
     uint32_t mine = 0u, first = 0u;
     for (int r = 0; r < k; ++r) {
         const uint32_t gmax = __reduce_max_sync(0xffffffffu, key[0]);
-        if (r == 0) first = gmax;
-        if (lane == r) mine = gmax;
-        if (key[0] == gmax) {  // the single lane holding the winner pops it
+        first = (r == 0) ? gmax : first;
+        mine = (lane == r) ? gmax : mine;
+        // the single lane holding the winner pops it (selects, no branch:
+        // the warp stays converged for the next reduction)
+        const bool win = key[0] == gmax;
 #pragma unroll
-            for (int i = 0; i + 1 < NK; ++i) key[i] = key[i + 1];
-            key[NK - 1] = 0u;
-        }
+        for (int i = 0; i + 1 < NK; ++i) key[i] = win ? key[i + 1] : key[i];
+        key[NK - 1] = win ? 0u : key[NK - 1];
     }
-    // softmax over the selected logits (renormalised top-k)
+    // softmax over the selected logits (renormalised top-k); every lane
+    // evaluates the exponential, lanes past k drop it
     const float vmax = key_value(first);
-    const float ev = (lane < k) ? expf(key_value(mine) - vmax) : 0.0f;
+    const float ex = expf(key_value(mine) - vmax);
+    const float ev = (lane < k) ? ex : 0.0f;
     float sum = ev;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    int id = -1;
-    if (lane < k) {
-        id = key_id(mine);
+    // slot `lane`: a routed pick, or the shared expert in slot k
+    const bool shared_slot = S != 0 && lane == k;
+    const int id = shared_slot ? E : key_id(mine);
+    const float wt = shared_slot ? scale * sigmoid_stable(sv) : ev / sum;
+    if (lane < k + S) {
         ids[lane] = id;
-        wts[lane] = ev / sum;
+        wts[lane] = wt;
+        ids_s[lane] = id;
     }
-    return id;
+    __syncwarp();
+}
+
+// moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
+// moe_align block size", Purpose) for the n <= 512 ids of one small batch,
+// without a histogram or scan over all experts. Each id is keyed
+// (expert << 10 | position); two passes in which every thread compares its
+// key with all n keys (shared-memory broadcasts) give, per id: its rank in
+// the stable expert order, its expert's count and first rank, whether it is
+// the expert's first occurrence, and the padded offset of its expert (the
+// padded sizes of the experts below it). The first occurrence of each expert
+// records which blocks it owns; then each warp writes whole blocks
+// (coalesced): the ids' flat positions, the sentinel n up to the block end,
+// and the block's expert.
+__device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, int32_t *sorted,
+                                           int32_t *expert_ids, int32_t *npp_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kCap = kSmallMaxM * 32;
+    const int n4 = (n + 3) & ~3;
+    uint32_t *keys = reinterpret_cast<uint32_t *>(ids);   // [n4], in place of the ids
+    uint32_t *srt = reinterpret_cast<uint32_t *>(sm);     // [n] keys in ascending order
+    int *padv = sm + kCap;        // [n4] padded size of the id's expert at its first occurrence, else 0
+    int *cntv = padv + kCap;      // [n] count of the id's expert
+    int *ltv = cntv + kCap;       // [n] ids of lower experts = the expert's first rank
+    int *offv = ltv + kCap;       // [n] padded offset of the id's expert
+    int *owner = offv + kCap;     // [nblk] first-occurrence id owning each block
+    int *s_total = owner + kCap;
+    for (int i = tid; i < n4; i += kSmallThreads)
+        keys[i] = i < n ? ((uint32_t)ids[i] << 10) | (uint32_t)i : 0xFFFFFFFFu;
+    __syncwarp();
+    __syncthreads();
+    // pass 1 (ids i = tid, tid + 256): counts against every key
+    for (int i = tid; i < n4; i += kSmallThreads) {
+        const uint32_t k = keys[i], e = k >> 10;
+        int lt = 0, eq = 0, eqb = 0;
+        for (int j = 0; j < n4; j += 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                lt += (w[u] >> 10) < e;
+                eq += (w[u] >> 10) == e;
+                eqb += ((w[u] >> 10) == e) & (w[u] < k);
+            }
+        }
+        const bool real = i < n;
+        if (real) srt[lt + eqb] = k;
+        padv[i] = (real && eqb == 0) ? (eq + A - 1) / A * A : 0;
+        cntv[i] = eq;
+        ltv[i] = lt;
+    }
+    __syncwarp();
+    __syncthreads();
+    // pass 2: padded offset of each id's expert; first occurrences claim blocks
+    for (int i = tid; i < n4; i += kSmallThreads) {
+        const uint32_t e = keys[i] >> 10;
+        int off = 0, total = 0;
+        for (int j = 0; j < n4; j += 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
+            const int4 pv = *reinterpret_cast<const int4 *>(padv + j);
+            off += ((v.x >> 10) < e ? pv.x : 0) + ((v.y >> 10) < e ? pv.y : 0) +
+                   ((v.z >> 10) < e ? pv.z : 0) + ((v.w >> 10) < e ? pv.w : 0);
+            total += pv.x + pv.y + pv.z + pv.w;
+        }
+        offv[i] = off;
+        const int pad = padv[i];
+        for (int b = off / A; b < (off + pad) / A; ++b) owner[b] = i;
+        if (i == 0) {
+            *s_total = total;
+            *npp_out = total;
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+    const int nblk = *s_total / A;
+    for (int b = warp; b < nblk; b += kSmallWarps) {
+        const int i = owner[b];
+        const int cnt = cntv[i], first = ltv[i];
+        const int local0 = b * A - offv[i];
+        if (lane == 0) expert_ids[b] = (int32_t)(keys[i] >> 10);
+        for (int u = lane; u < A; u += 32) {
+            const int local = local0 + u;
+            sorted[(int64_t)b * A + u] = local < cnt ? (int32_t)(srt[first + local] & 1023u) : n;
+        }
+        __syncwarp();
+    }
 }
 
 template <int NB>  // N blocks of 8 tokens: 1 (M <= 8) or 2 (M <= 16)
@@ -153,9 +244,21 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
     const int rows = P.rows;
-    const int rg = blockIdx.x / P.KQ, kq = blockIdx.x % P.KQ;
+    const int rg = blockIdx.x / P.KQ;         // row group
+    const int kq = (int)cluster_ctarank();    // K range = rank in the group's cluster
     const int row0 = rg * 16;
     __shared__ int s_last;
+
+    // the group leader (rank 0) keeps the routed bias for the tail: loads
+    // issued now, stored to shared memory after the gate stream
+    float bias_r[kSmallBiasPerThread];
+#pragma unroll
+    for (int j = 0; j < kSmallBiasPerThread; ++j) bias_r[j] = 0.0f;
+    if (kq == 0 && p.bias != nullptr) {
+#pragma unroll
+        for (int j = 0; j < kSmallBiasPerThread; ++j)
+            bias_r[j] = __ldg(p.bias + min(tid + j * kSmallThreads, p.E - 1));
+    }
 
     // ---- 1. gate rows x tokens on the tensor cores ----
     // rows past E+S and tokens past M read a clamped (valid) row; their
@@ -205,8 +308,14 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
         }
     }
 
-    // ---- 2. sum the 8 warps in a fixed order, store this K range's partials ----
-    float *red = reinterpret_cast<float *>(smem);  // [8 warps][16 rows][16 tokens]
+    // ---- 2. sum the 8 warps, then the cluster's K ranges, in a fixed order ----
+    // Shared memory: [0, 8 KB) the warps' partials; [8 KB, 16 KB) the group
+    // leader's slots for the cluster's K ranges (written by each CTA of the
+    // cluster into the leader's memory); the tail reuses [0, 16 KB); the
+    // routed bias sits at [16 KB, 20 KB).
+    float *red = reinterpret_cast<float *>(smem);                 // [8 warps][16 rows][16 tokens]
+    float *slots = red + kSmallWarps * 16 * 16;                   // [KQ][16 rows][16 tokens]
+    float *bias_s = reinterpret_cast<float *>(smem) + kSmallFrontWords;  // [E]
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         const int tok = nb * 8 + 2 * t;
@@ -215,86 +324,88 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
         red[(warp * 16 + g + 8) * 16 + tok] = acc[nb][2];
         red[(warp * 16 + g + 8) * 16 + tok + 1] = acc[nb][3];
     }
+    if (kq == 0) {
+#pragma unroll
+        for (int j = 0; j < kSmallBiasPerThread; ++j)
+            if (tid + j * kSmallThreads < p.E) bias_s[tid + j * kSmallThreads] = bias_r[j];
+    }
+    __syncwarp();
     __syncthreads();
     {
-        const int r = tid >> 4, m = tid & 15;  // 256 threads = 16 rows x 16 tokens
-        if (m < p.M && m < NB * 8 && row0 + r < rows) {
-            float v = 0.0f;
+        // this K range's sum over the warps -> slot kq of the group leader
+        float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kSmallWarps; ++w) v += red[(w * 16 + r) * 16 + m];
-            p.scratch[((int64_t)kq * p.M + m) * rows + row0 + r] = v;
-            __threadfence();
-        }
+        for (int w = 0; w < kSmallWarps; ++w) v += red[w * 256 + tid];  // tid = row * 16 + token
+        st_cluster_f32(cluster_addr(smem_u32(slots + kq * 256 + tid), 0u), v);
     }
+    // the cluster barrier publishes every CTA's slot to the leader; the other
+    // CTAs are done after it
+    cluster_sync();
+    if (kq != 0) return;
+    const int r16 = tid >> 4, m16 = tid & 15;  // 256 threads = 16 rows x 16 tokens
+    {
+        float v = 0.0f;
+        for (int q = 0; q < P.KQ; ++q) v += slots[q * 256 + tid];
+        if (m16 < p.M && m16 < NB * 8 && row0 + r16 < rows)
+            p.scratch[(int64_t)m16 * rows + row0 + r16] = v;
+    }
+    __syncwarp();
     __syncthreads();
 
-    // ---- 3. hand-off: the last CTA to arrive runs the tail ----
+    // ---- 3. hand-off: the last row group to arrive runs the tail ----
+    // One acquire-release increment by the ticket-taking thread: it releases
+    // the logit stores the CTA barrier ordered before it, and the last
+    // group's increment acquires every other group's.
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.hdr);
-    if (tid == 0) {
-        const unsigned tk = atomicAdd(&hdr->ticket, 1u);
-        s_last = (tk == gridDim.x - 1);
-    }
+    const unsigned groups = gridDim.x / (unsigned)P.KQ;
+    if (tid == 0) s_last = (atomic_add_acq_rel(&hdr->ticket, 1u) == groups - 1);
+    __syncwarp();
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    if (tid == 0) hdr->ticket = 0u;  // every CTA has arrived: reset for the next call
+    if (tid == 0) hdr->ticket = 0u;  // every group has arrived: reset for the next call
+    __syncwarp();  // a split warp would replay the whole tail once per path
 
     // ---- 4. tail: top-k + softmax + shared slot, one warp per token ----
     const int width = p.k + p.S;
     int32_t *ids_s = reinterpret_cast<int32_t *>(smem);  // [M*width]
-    int *align_smem = ids_s + kSmallMaxM * 32;
-    const int64_t kq_stride = (int64_t)p.M * rows;
     const int nk = (p.E + 31) >> 5;
-    __syncthreads();
     for (int m = warp; m < p.M; m += kSmallWarps) {
         const float *zrow = p.scratch + (int64_t)m * rows;
         uint16_t *lrow = p.logits_out ? p.logits_out + (int64_t)m * p.E : nullptr;
         int32_t *irow = p.ids + (int64_t)m * width;
         float *wrow = p.wts + (int64_t)m * width;
-        int id;
+        int32_t *srow = ids_s + m * width;
         if (nk <= 4)
-            id = warp_topk_row<4>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
+            warp_topk_row<4>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
         else if (nk <= 8)
-            id = warp_topk_row<8>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
+            warp_topk_row<8>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
         else if (nk <= 16)
-            id = warp_topk_row<16>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
+            warp_topk_row<16>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
         else
-            id = warp_topk_row<32>(zrow, P.KQ, kq_stride, p.E, p.k, p.bias, lrow, irow, wrow);
-        if (lane < p.k) ids_s[m * width + lane] = id;
-        if (p.S && lane == p.k) {
-            float s = 0.0f;
-            for (int q = 0; q < P.KQ; ++q) s += __ldcg(zrow + q * kq_stride + p.E);
-            irow[p.k] = p.E;
-            wrow[p.k] = p.scale * sigmoid_stable(s);
-            ids_s[m * width + p.k] = p.E;
-        }
+            warp_topk_row<32>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
     }
     if (p.sorted == nullptr) return;
 
     // ---- 5. moe_align_block_size on the M*width ids of this call ----
     __syncthreads();
-    const int numel = p.M * width;
-    AlignSmem as = align_carve(align_smem, rows);
-    align_count(ids_s, numel, rows, as, &hdr->error);
-    const int npp = align_offsets(as.cnt, rows, p.A, as);
-    align_scatter(ids_s, numel, rows, 0, as, false, p.sorted);
-    align_fill(p.A, rows, as.cnt, as, numel, p.sorted, p.expert_ids, tid, kSmallThreads);
-    if (tid == 0) *p.npp = npp;
+    align_tiny(ids_s, p.M * width, p.A, ids_s + kSmallMaxM * 32, p.sorted, p.expert_ids, p.npp);
 }
 
 template <int NB>
 static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaStream_t stream) {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    small_route_kernel<NB><<<grid, kSmallThreads, smem, stream>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kSmallThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P.KQ;  // the K ranges of one row group
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, small_route_kernel<NB>, P);
 }
 
 int small_route_k_ranges(int E, int S, int H) {
@@ -302,6 +413,7 @@ int small_route_k_ranges(int E, int S, int H) {
     const int groups = (E + S + 15) / 16;
     const int slices = (H + kSliceK - 1) / kSliceK;
     int KQ = 150 / groups;
+    if (KQ > kSmallMaxCluster) KQ = kSmallMaxCluster;
     if (KQ < 1) KQ = 1;
     const int max_kq = (slices + kSmallWarps - 1) / kSmallWarps;
     if (KQ > max_kq) KQ = max_kq;
@@ -351,9 +463,7 @@ cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
     P.per_cta = (P.slices + P.KQ - 1) / P.KQ;
     const int groups = (P.rows + 15) / 16;
     const int grid = groups * P.KQ;
-    const size_t stage = (size_t)kSmallWarps * 16 * 16 * 4;
-    const size_t tail = (size_t)(kSmallMaxM * 32 + align_smem_words(kSmallWarps, P.rows)) * 4;
-    const size_t smem = stage > tail ? stage : tail;
+    const size_t smem = (size_t)(kSmallFrontWords + kSmallMaxE) * 4;
     return a.M <= 8 ? launch_nb<1>(P, grid, smem, stream) : launch_nb<2>(P, grid, smem, stream);
 }
 

@@ -16,7 +16,7 @@
 // plus MMA operand reads reach the SM's shared-memory bandwidth, while the
 // pair form halves the gate bytes per SM.
 //
-// Per CTA, 192 threads:
+// Per CTA, 256 threads (8 warps):
 //   warp 0     TMA producer: x tile [128 x 64] and this CTA's half of each
 //              N<=256 gate piece [E/2 x 64] per k-block (128-byte swizzle),
 //              into a ring of shared-memory stages; loads of both CTAs
@@ -24,21 +24,27 @@
 //   warp 1     allocates TMEM for the pair (E fp32 columns x 128 lanes per
 //              CTA); in the leader CTA one thread issues the pair MMAs and
 //              commits (multicast to both CTAs) to free each stage;
-//   warps 2-5  meanwhile compute the shared-expert logit of their row from the
-//              staged x tile (CUDA cores, fp32 per k-block, compensated sum
-//              across k-blocks); then the epilogue: thread = token row, reads
-//              its E logits from TMEM (tcgen05.ld 32x32b), rounds them to
-//              bf16, and selects the top-k in three steps:
-//                1. maxima of NG column classes (c mod NG) -> threshold T =
-//                   k-th largest class maximum (at least k logits >= T, so
-//                   every top-k logit, ties included, is >= T);
-//                2. append the logits >= T (about 1.5k of them on random
-//                   data) to a per-thread shared list with predicated stores;
-//                3. sort that list as ordered keys in registers (exact
-//                   fallback over all E logits if the list overflows).
-// Every mbarrier wait is bounded; on timeout the kernel sets the workspace's
-// error bit, skips its outputs and still frees TMEM and leaves through the
-// cluster barriers. Warps hand off through mbarriers only.
+//   warps 4-7  meanwhile compute the shared-expert logit of their row from
+//              global memory (CUDA cores, fp32 per k-block, compensated sum
+//              across k-blocks).
+// Epilogue, all 8 warps: warp w reads TMEM lane quarter w%4 (thread = token
+// row) and column half w/4 (E/2 experts). Each half selects its own exact
+// top-k of bf16-rounded logits in three steps:
+//   1. one sweep over TMEM: add the bias, round to bf16 two at a time, keep
+//      the rounded row in the (now idle) stage ring, and take the maximum of
+//      each group of 8 consecutive columns; T = k-th largest group maximum
+//      (k groups hold a logit >= T, so every top-k logit, ties included, is
+//      >= T, and only groups whose maximum is >= T -- about k of them -- can
+//      hold one);
+//   2. append the logits >= T of those groups to a per-thread shared list
+//      with predicated stores (about 1.2k entries on random data);
+//   3. sort the list as ordered keys in registers (exact k-pass fallback over
+//      the half's rounded logits if the list overflows).
+// Half 0 posts its top-k to shared memory; half 1 merges the two sorted lists
+// (bitonic merge), applies the softmax and writes the row with its shared
+// slot. Every mbarrier wait is bounded; on timeout the kernel sets the
+// workspace's error bit, skips its outputs and still frees TMEM and leaves
+// through the cluster barriers. Warps hand off through mbarriers only.
 #include <cudaTypedefs.h>
 
 #include "smr_device.cuh"
@@ -51,6 +57,8 @@ constexpr int kTcBK = 64;             // k-block: 64 bf16 = 128-byte rows, 128B 
 constexpr int kTcSW = kTcBK * 2;
 constexpr int kTcThreads = 256;
 constexpr int kCandCap = 32;
+constexpr int kGroup = 8;             // consecutive columns per group (one 16-byte bf16 group)
+constexpr int kEpiListBytes = 3 * kCandCap * kTcBM * 4;  // two candidate lists + half 0's top-k
 constexpr int kTcSmemLimit = 232448;  // 227 KiB opt-in per CTA
 
 struct TcParams {
@@ -65,7 +73,7 @@ struct TcParams {
     uint16_t *logits_out;
     uint32_t *err;
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
-    uint32_t tmem_cols, stage_bytes, misc_bias_off, misc_ws_off;
+    uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off;
 };
 
 // Compensated (two-sum) accumulation of k-block partial sums.
@@ -108,8 +116,10 @@ __device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, uint32_t
 }
 
 // Descending sort of N unsigned keys (bitonic network, N a power of two).
-template <int N>
-__device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[N]) {
+// Only the first N entries of the array take part.
+template <int N, int CAP>
+__device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[CAP]) {
+    static_assert(N <= CAP, "prefix within the array");
 #pragma unroll
     for (int size = 2; size <= N; size <<= 1) {
 #pragma unroll
@@ -131,10 +141,49 @@ __device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[N]) {
 // Candidate entry (bf16 bits of the rounded logit in the high half, expert id
 // in the low half) -> ordered selection key.
 __device__ __forceinline__ uint32_t entry_key(uint32_t entry) {
-    const uint32_t b = entry >> 16;
+    uint32_t b = entry >> 16;
+    b = (b == 0x8000u) ? 0u : b;  // a rounded -0 ranks (and ties) as +0
     const uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
     return (ord << 16) | (0xFFFFu - (entry & 0xFFFFu));
 }
+
+// TMEM loads of CW columns (CW = 32 or 16) for one warp's 32 lanes.
+template <int CW>
+__device__ __forceinline__ void tmem_ld_async(uint32_t taddr, uint32_t (&r)[CW]) {
+    if constexpr (CW == 32) tmem_ld32_async(taddr, r); else tmem_ld16_async(taddr, r);
+}
+template <int CW>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[CW]) {
+    if constexpr (CW == 32) tmem_wait_ld(r); else tmem_wait_ld16(r);
+}
+
+// Two fp32 values rounded to bf16 (nearest-even) in one 32-bit word, lo in
+// the low half (the lower address in memory).
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// Lane-wise maximum of two bf16 pairs.
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// Row stride of the rounded-logit copy in shared memory: an odd multiple of
+// 16 bytes, so eight consecutive rows' 16-byte groups fall in distinct banks.
+__host__ __device__ constexpr uint32_t dump_row_bytes(int ecols) { return (uint32_t)ecols * 2u + 16u; }
 
 // Bitonic merge of a bitonic sequence of N keys into descending order.
 template <int N>
@@ -153,7 +202,7 @@ __device__ __forceinline__ void bitonic_merge_desc(uint32_t (&a)[N]) {
     }
 }
 
-template <int NG>
+template <int NGM, int CW>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const TcParams p) {
@@ -161,7 +210,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const int ST = p.stages;
-    uint8_t *misc = smem + (size_t)ST * p.stage_bytes;
+    uint8_t *misc = smem + p.misc_off;
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);  // leader: both CTAs' loads landed
     uint64_t *empty = full + ST;       // both CTAs: the pair MMAs are done with the stage
     uint64_t *accum = empty + ST;      // the pair MMAs of the whole K loop are done
@@ -305,135 +354,132 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
     tc_fence_after();
     ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
+    __syncwarp();  // lanes left the bounded wait on different iterations
     const int ecols = p.E / 2;
     const int c_beg = hf * ecols;
-    const int nch = ecols >> 4;  // 16-column TMEM chunks per half (E/2 is a multiple of 16)
+    const int nch = ecols / CW;       // CW-column TMEM chunks per half
+    const int ng = ecols / kGroup;    // groups of kGroup consecutive columns per half
+    // the stage ring is idle once the accumulator is complete: it holds the
+    // candidate lists, half 0's posted top-k and each half's rounded logits
     uint32_t *cand = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);  // [kCandCap][128] per half
     uint32_t *posted = reinterpret_cast<uint32_t *>(smem) + 2 * kCandCap * kTcBM;    // [32][128] half 0's top-k
+    const uint32_t rs = dump_row_bytes(ecols);
+    const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
     uint32_t key[kCandCap];
     if (ok) {
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
         const bool has_bias = p.bias != nullptr;
-        uint32_t ra[16], rb[16];
-        auto rounded = [&](uint32_t (&r)[16], int ch, float (&zr)[16]) {
-            const int c = c_beg + ch * 16;
-            if (has_bias) {
+        // 1. one sweep over this half's TMEM columns: round to bf16 (two per
+        //    32-bit word), keep the row's rounded logits in shared memory,
+        //    take the maximum of every group of kGroup columns
+        float gm[NGM];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) zr[i] = round_bf16(__uint_as_float(r[i]) + bias_s[c + i]);
-            } else {
+        for (int g = 0; g < NGM; ++g) gm[g] = -INFINITY;
+        uint32_t ra[CW], rb[CW];
+        auto process = [&](uint32_t (&r)[CW], int ch) {
+            const int c = c_beg + ch * CW;
+            uint32_t wv[CW / 2];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) zr[i] = round_bf16(__uint_as_float(r[i]));
-            }
-        };
-        // 1. class maxima (class = column mod NG within the half), threshold
-        float gmax[NG];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) gmax[g] = -INFINITY;
-        auto phase1 = [&](uint32_t (&r)[16], int ch) {
-            float zr[16];
-            rounded(r, ch, zr);
-            if (p.logits_out && valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + c_beg + ch * 16);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        w4[t] = (__float_as_uint(zr[u * 8 + 2 * t]) >> 16) |
-                                (__float_as_uint(zr[u * 8 + 2 * t + 1]) & 0xFFFF0000u);
-                    dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            for (int t = 0; t < CW / 2; ++t) {
+                float lo = __uint_as_float(r[2 * t]), hi = __uint_as_float(r[2 * t + 1]);
+                if (has_bias) {
+                    lo += bias_s[c + 2 * t];
+                    hi += bias_s[c + 2 * t + 1];
                 }
+                wv[t] = pack_bf16x2_rn(lo, hi);
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) gmax[(ch * 16 + i) % NG] = fmaxf(gmax[(ch * 16 + i) % NG], zr[i]);
+            for (int u = 0; u < CW / kGroup; ++u) {
+                const uint4 v = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+                st_shared_v4(drow + (uint32_t)((ch * (CW / kGroup) + u) * 16), v);
+                const uint32_t mx = max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
+                gm[ch * (CW / kGroup) + u] =
+                    fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+                if (p.logits_out && valid)
+                    reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + c)[u] = v;
+            }
         };
-        // TMEM loads double-buffered: the next chunk is in flight while this
-        // one is processed
-        tmem_ld16_async(taddr, ra);
-        tmem_wait_ld16(ra);
-        for (int ch = 0; ch < nch; ch += 2) {
-            const bool two = ch + 1 < nch;
-            if (two) tmem_ld16_async(taddr + (uint32_t)((ch + 1) * 16), rb);
-            phase1(ra, ch);
-            if (two) {
-                tmem_wait_ld16(rb);
-                if (ch + 2 < nch) tmem_ld16_async(taddr + (uint32_t)((ch + 2) * 16), ra);
-                phase1(rb, ch + 1);
-                if (ch + 2 < nch) tmem_wait_ld16(ra);
+        // chunks unrolled (group maxima stay in registers), the next chunk's
+        // TMEM load in flight while one is processed
+        tmem_ld_async<CW>(taddr, ra);
+        tmem_ld_wait<CW>(ra);
+#pragma unroll
+        for (int ch = 0; ch < NGM * kGroup / CW; ++ch) {
+            if (ch < nch) {
+                uint32_t (&cur)[CW] = (ch & 1) ? rb : ra;
+                uint32_t (&nxt)[CW] = (ch & 1) ? ra : rb;
+                if (ch + 1 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), nxt);
+                process(cur, ch);
+                if (ch + 1 < nch) tmem_ld_wait<CW>(nxt);
             }
         }
-        // gmax sorted descending: the k-th largest is the minimum of the
-        // first k (a masked min keeps gmax in registers); it bounds this
-        // half's top-k from below
-        sort_desc<NG>(gmax);
+        // the k-th largest group maximum T bounds this half's top-k from
+        // below (k groups hold a logit >= T); only groups whose maximum is
+        // >= T can hold a logit >= T
+        float gs[NGM];
+#pragma unroll
+        for (int g = 0; g < NGM; ++g) gs[g] = gm[g];
+        sort_desc<NGM>(gs);
         float T = INFINITY;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) T = fminf(T, g < p.k ? gmax[g] : INFINITY);
-        // 2. append every logit >= T of this half (branch-free predicated stores)
+        for (int g = 0; g < NGM; ++g) T = fminf(T, g < p.k ? gs[g] : INFINITY);
+        if (p.k > ng) T = -INFINITY;  // fewer groups than k: every logit is a candidate
+        uint32_t sel = 0;
+#pragma unroll
+        for (int g = 0; g < NGM; ++g) sel |= (g < ng && gm[g] >= T) ? (1u << g) : 0u;
+        // 2. append every logit >= T of the selected groups (about k groups)
         uint32_t n = 0;
         const uint32_t cand_row = smem_u32(cand + row);
-        auto phase2 = [&](uint32_t (&r)[16], int ch) {
-            float zr[16];
-            rounded(r, ch, zr);
+        while (__any_sync(0xffffffffu, sel != 0u)) {
+            const uint32_t act = sel != 0u ? 1u : 0u;
+            const int g = act ? __ffs(sel) - 1 : 0;
+            sel &= sel - 1u;
+            const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t c = zr[i] >= T ? 1u : 0u;
-                const uint32_t slot = min(n, (uint32_t)(kCandCap - 1));
-                st_shared_if(cand_row + slot * (kTcBM * 4),
-                             (__float_as_uint(zr[i]) & 0xFFFF0000u) | (uint32_t)(c_beg + ch * 16 + i),
+            for (int u = 0; u < kGroup; ++u) {
+                const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
+                const uint32_t c = act & (__uint_as_float(hb) >= T ? 1u : 0u);
+                st_shared_if(cand_row + min(n, (uint32_t)(kCandCap - 1)) * (kTcBM * 4),
+                             hb | (uint32_t)(c_beg + g * kGroup + u),
                              c & (n < (uint32_t)kCandCap ? 1u : 0u));
                 n += c;
-            }
-        };
-        tmem_ld16_async(taddr, ra);
-        tmem_wait_ld16(ra);
-        for (int ch = 0; ch < nch; ch += 2) {
-            const bool two = ch + 1 < nch;
-            if (two) tmem_ld16_async(taddr + (uint32_t)((ch + 1) * 16), rb);
-            phase2(ra, ch);
-            if (two) {
-                tmem_wait_ld16(rb);
-                if (ch + 2 < nch) tmem_ld16_async(taddr + (uint32_t)((ch + 2) * 16), ra);
-                phase2(rb, ch + 1);
-                if (ch + 2 < nch) tmem_wait_ld16(ra);
             }
         }
         asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
         // 3. this half's candidates as ordered keys in registers, sorted
         //    descending. A row whose list overflowed takes an exact k-pass
-        //    selection over the half's logits instead.
+        //    selection over the half's rounded logits in shared memory.
         const bool overflow = n > (uint32_t)kCandCap;
 #pragma unroll
         for (int j = 0; j < kCandCap; ++j)
             key[j] = (j < (int)n) ? entry_key(cand[j * kTcBM + row]) : 0u;
-        sort_keys_desc<kCandCap>(key);
-        if (__any_sync(0xffffffffu, overflow)) {
-            uint32_t prev = 0xFFFFFFFFu;
-            uint32_t picked[kCandCap];
+        if (__all_sync(0xffffffffu, n <= 16u))
+            sort_keys_desc<16>(key);
+        else
+            sort_keys_desc<kCandCap>(key);
+        if (overflow) {
 #pragma unroll
-            for (int j = 0; j < kCandCap; ++j) picked[j] = 0u;
+            for (int j = 0; j < kCandCap; ++j) key[j] = 0u;
+            uint32_t prev = 0xFFFFFFFFu;
             for (int r = 0; r < p.k; ++r) {
                 uint32_t best = 0u;
-                for (int ch = 0; ch < nch; ++ch) {
-                    tmem_ld16_async(taddr + (uint32_t)(ch * 16), ra);
-                    tmem_wait_ld16(ra);
-                    float zr[16];
-                    rounded(ra, ch, zr);
+                for (int g = 0; g < ng; ++g) {
+                    const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t k2 = make_key(zr[i], c_beg + ch * 16 + i);
+                    for (int u = 0; u < kGroup; ++u) {
+                        const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
+                        const uint32_t k2 = entry_key(hb | (uint32_t)(c_beg + g * kGroup + u));
                         best = (k2 < prev && k2 > best) ? k2 : best;
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < kCandCap; ++j) picked[j] = (j == r) ? best : picked[j];
+                for (int j = 0; j < kCandCap; ++j) key[j] = (j == r) ? best : key[j];
                 prev = best;
             }
-            if (overflow) {
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) key[j] = picked[j];
-            }
         }
+        __syncwarp();  // only overflowing lanes took the fallback
         if (hf == 0) {
 #pragma unroll
             for (int j = 0; j < kCandCap; ++j)
@@ -446,22 +492,38 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     } else {
         // ------------------------------ half 1: merge, softmax, write -----
         const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag));
+        __syncwarp();
         if (ok && got && valid) {
             // both lists sorted descending: reverse the other half's list
-            // behind this one -> bitonic sequence of 64 -> merge
-            uint32_t m[2 * kCandCap];
+            // behind this one -> bitonic sequence -> merge
+            uint32_t top[kCandCap];
+            if (p.k <= 16) {
+                uint32_t h[32];
 #pragma unroll
-            for (int j = 0; j < kCandCap; ++j) {
-                m[j] = key[j];
-                m[2 * kCandCap - 1 - j] = (j < p.k) ? posted[j * kTcBM + row] : 0u;
+                for (int j = 0; j < 16; ++j) {
+                    h[j] = key[j];
+                    h[31 - j] = (j < p.k) ? posted[j * kTcBM + row] : 0u;
+                }
+                bitonic_merge_desc<32>(h);
+#pragma unroll
+                for (int j = 0; j < kCandCap; ++j) top[j] = h[j];
+            } else {
+                uint32_t m[2 * kCandCap];
+#pragma unroll
+                for (int j = 0; j < kCandCap; ++j) {
+                    m[j] = key[j];
+                    m[2 * kCandCap - 1 - j] = (j < p.k) ? posted[j * kTcBM + row] : 0u;
+                }
+                bitonic_merge_desc<2 * kCandCap>(m);
+#pragma unroll
+                for (int j = 0; j < kCandCap; ++j) top[j] = m[j];
             }
-            bitonic_merge_desc<2 * kCandCap>(m);
-            const float vmax = key_value(m[0]);
+            const float vmax = key_value(top[0]);
             float ev[kCandCap];
             float sum = 0.0f;
 #pragma unroll
             for (int j = 0; j < kCandCap; ++j) {
-                ev[j] = (j < p.k) ? expf(key_value(m[j]) - vmax) : 0.0f;
+                ev[j] = (j < p.k) ? expf(key_value(top[j]) - vmax) : 0.0f;
                 sum += ev[j];
             }
             int32_t *orow = p.ids + (int64_t)grow * p.width;
@@ -469,7 +531,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
             for (int j = 0; j < kCandCap; ++j) {
                 if (j < p.k) {
-                    orow[j] = key_id(m[j]);
+                    orow[j] = key_id(top[j]);
                     wrow[j] = ev[j] / sum;
                 }
             }
@@ -561,11 +623,16 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     if (st > 6) st = 6;
     if (st < 2) return false;
     static_assert(8 * (2 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
-    // the epilogue scratch (two candidate lists + half 0's top-k) reuses the stage ring
-    if ((size_t)st * p.stage_bytes < (size_t)(2 * kCandCap + 32) * kTcBM * 4) return false;
+    // the epilogue (candidate lists, half 0's top-k, both halves' rounded
+    // logits) reuses the stage ring; the misc block follows the larger one
+    const size_t ring = (size_t)st * p.stage_bytes;
+    const size_t epi = (size_t)kEpiListBytes + 2 * (size_t)kTcBM * dump_row_bytes(E / 2);
+    const size_t front = ring > epi ? ring : epi;
+    if (1024 + front + misc > (size_t)kTcSmemLimit) return false;
     p.stages = st;
+    p.misc_off = (uint32_t)front;
     out->p = p;
-    out->smem = 1024 + (size_t)st * p.stage_bytes + misc;
+    out->smem = 1024 + front + misc;
     const int tiles = (M + kTcBM - 1) / kTcBM;
     out->grid = (tiles + 1) / 2 * 2;  // whole CTA pairs; a missing partner tile is all padding
     return true;
@@ -576,14 +643,14 @@ bool tc_route_supported(int H, int E, int k, int S) {
     return plan_tc(1, H, E, k, S, &plan);
 }
 
-template <int NG>
+template <int NGM, int CW>
 static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const TcPlan &plan,
                              cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_route_kernel<NG>,
+        cudaError_t e = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kTcSmemLimit);
         if (e != cudaSuccess) return e;
@@ -601,7 +668,7 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_route_kernel<NG>, mx, mw, plan.p);
+    return cudaLaunchKernelEx(&cfg, tc_route_kernel<NGM, CW>, mx, mw, plan.p);
 }
 
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
@@ -623,7 +690,12 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     if (!make_map(&mw, a.w, (uint64_t)a.H, (uint64_t)a.E, (uint64_t)a.H * 2, kTcBK,
                   (uint32_t)(p.piece_n / 2)))
         return cudaErrorInvalidValue;
-    return a.k <= 16 ? launch_ng<16>(mx, mw, plan, stream) : launch_ng<32>(mx, mw, plan, stream);
+    // 32-column TMEM chunks when each column half is a multiple of 32, else
+    // 16; at most 16 or 32 column groups per half
+    const bool wide = (a.E / 2) % 32 == 0;
+    if (a.E <= 256)
+        return wide ? launch_ng<16, 32>(mx, mw, plan, stream) : launch_ng<16, 16>(mx, mw, plan, stream);
+    return wide ? launch_ng<32, 32>(mx, mw, plan, stream) : launch_ng<32, 16>(mx, mw, plan, stream);
 }
 
 }  // namespace smr
