@@ -203,23 +203,18 @@ def bench_large(args, world, rank, torch, smr, inputs):
     wsp = smr.Workspace()
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
-        if ev is not None:
-            ev[1].record(stream)
-        smr.align(ids, E + S, A_LARGE, sorted_token_ids=srt, expert_ids=eids,
-                  num_tokens_post_padded=npp, workspace=wsp)
+    def step(i):
+        # one call of the public route+align entry point (the route kernel also
+        # counts the experts of its rows for the align launches behind it)
+        smr.route_align(xs[i & 1], w, ws, topk=K, block_size=A_LARGE, topk_ids=ids,
+                        topk_weights=wts, sorted_token_ids=srt, expert_ids=eids,
+                        num_tokens_post_padded=npp, workspace=wsp)
 
-    launches_per_step = 1
     for i in range(args.warmup):
         step(i)
-    launches_per_step += smr.last_launch_count()
+    launches_per_step = smr.last_launch_count()
     torch.cuda.synchronize()
 
-    route_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device())
     barrier(world)
@@ -227,11 +222,26 @@ def bench_large(args, world, rank, torch, smr, inputs):
     with sampler:
         start.record(stream)
         for i in range(args.steps):
-            step(i, route_ev[i])
+            step(i)
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     ms = start.elapsed_time(end) / args.steps
+    assert smr.get_device_error(wsp) == 0
+
+    # the route kernel alone (roofline): route-only calls on the same
+    # alternating inputs, each bracketed by CUDA events on the launch stream
+    n_route = max(3, min(args.steps, 500))
+    route_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_route)]
+    for i in range(3):
+        smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
+    torch.cuda.synchronize()
+    for i in range(n_route):
+        route_ev[i][0].record(stream)
+        smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
+        route_ev[i][1].record(stream)
+    torch.cuda.synchronize()
     route_ms = statistics.mean(a.elapsed_time(b) for a, b in route_ev)
     assert smr.get_device_error(wsp) == 0
 
@@ -393,6 +403,8 @@ def run_smr(args):
                      "traffic": traffic_from_profile(),
                      "kernel": "tc_route_kernel (gate GEMM + fused top-k epilogue)",
                      "kernel_us": res["route_ms"] * 1000.0,
+                     "kernel_timing": "route-only calls on the same alternating inputs, CUDA events "
+                                      "around each launch on its stream",
                      "peak_source": f"{src} bf16 dense (burst)"},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],

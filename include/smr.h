@@ -164,7 +164,9 @@ SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr
 
 /* Sticky device error word of a workspace: synchronises `stream`, then copies
  * the word to *code_out (0 = no error; bit 0 = an id out of range in align,
- * bit 1 = a bounded wait inside a kernel gave up). Not for launch paths. */
+ * bit 1 = a bounded wait inside a kernel gave up, bit 2 = an align output
+ * position fell outside sorted_cap / expert_cap -- possible only from a
+ * corrupted workspace -- and that write was skipped). Not for launch paths. */
 SMR_API smr_status smr_get_device_error(const void *workspace, void *stream, int32_t *code_out);
 
 /* Clears the sticky device error word (stream-ordered memset). */

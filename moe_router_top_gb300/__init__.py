@@ -26,6 +26,7 @@ __all__ = [
 
 ERR_BAD_ID = 1
 ERR_WAIT_TIMEOUT = 2
+ERR_BAD_SLOT = 4
 
 
 class SmrError(RuntimeError):

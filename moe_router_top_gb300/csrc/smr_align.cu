@@ -8,11 +8,12 @@
 //
 //  - numel <= kAlignSingleMax: one CTA of 512 threads stages the ids in
 //    shared memory and does count, scan, scatter and padding (one launch);
-//  - larger inputs: align_hist_kernel writes per-tile expert counts to the
-//    workspace, then align_scatter_kernel (one CTA per tile) derives the
-//    global segment offsets from all tile counts (a short fixed-order loop),
-//    scatters its tile and writes its share of padding rows and block expert
-//    ids (two launches, no inter-CTA waiting).
+//  - larger inputs, three launches with no inter-CTA waiting, over tiles of
+//    >= 1024 slots: per-tile expert counts; for each expert the tiles' starts
+//    inside it (a prefix over tiles) and its total; then per tile the padded
+//    expert offsets (block scan of the totals), the stable scatter of the
+//    tile's slots, and the padding rows and block owners of a share of the
+//    experts.
 #include "smr_device.cuh"
 #include "smr_launch.h"
 
@@ -23,115 +24,282 @@ constexpr int kAlignWarps = kAlignThreads / 32;
 
 __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const AlignLaunch a) {
     extern __shared__ __align__(16) int sm[];
+    griddep_wait();  // the ids come from the previous kernel
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
     int *ids = sm;  // [kAlignSingleMax] staged ids
     AlignSmem s = align_carve(sm + kAlignSingleMax, a.E_al);
     stage_ids(ids, a.ids, a.numel);
     align_count(ids, a.numel, a.E_al, s, err);
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
-    align_scatter(ids, a.numel, a.E_al, 0, s, false, a.sorted);
-    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids, threadIdx.x, blockDim.x);
+    align_scatter(ids, a.numel, a.E_al, 0, s, false, a.sorted, a.sorted_cap, err);
+    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.sorted_cap, a.expert_ids, a.expert_cap, err,
+               threadIdx.x, blockDim.x);
     if (threadIdx.x == 0) *a.npp = npp;
 }
 
-__global__ void __launch_bounds__(kAlignThreads) align_hist_kernel(const AlignLaunch a) {
+// ---- multi-CTA path: count, scan over tiles, scatter ----------------------
+
+constexpr int kTileThreads = 256;
+constexpr int kTileWarps = kTileThreads / 32;
+constexpr int kTileSub = kTileWarps * 128;  // slots per sub-chunk of the scatter
+constexpr int kMaxExpertsAl = 1025;
+static_assert(kAlignMinTile % kTileSub == 0, "tiles are whole sub-chunks");
+
+// 1. Per-tile expert counts (shared-memory histogram), four loads in flight
+//    per thread; ids outside [0, E_al) are skipped and flagged.
+__global__ void __launch_bounds__(kTileThreads) align_tile_count_kernel(const AlignLaunch a, int tile) {
     extern __shared__ int cnt[];
-    constexpr int kPer = kAlignTile / kAlignThreads;  // ids per thread
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
-    for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) cnt[e] = 0;
-    const int beg = blockIdx.x * kAlignTile, end = min(beg + kAlignTile, a.numel);
-    // every load of the tile is issued before the first is used (addresses
-    // clamped into the tile, out-of-tile lanes masked afterwards)
-    int v[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int i = beg + j * kAlignThreads + warp * 32 + lane;
-        v[j] = __ldg(a.ids + min(i, end - 1));
-    }
+    const int tid = threadIdx.x;
+    griddep_launch_dependents();
+    griddep_wait();  // the ids come from the previous kernel
+    for (int e = tid; e < a.E_al; e += kTileThreads) cnt[e] = 0;
     __syncwarp();
     __syncthreads();
+    const int beg = blockIdx.x * tile, end = min(beg + tile, a.numel);
+    for (int i0 = beg; i0 < end; i0 += 4 * kTileThreads) {
+        int v[4];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int i = beg + j * kAlignThreads + warp * 32 + lane;
-        if (i < end) {
-            if ((unsigned)v[j] < (unsigned)a.E_al) atomicAdd(&cnt[v[j]], 1);
-            else set_error(err, kErrBadId);
+        for (int j = 0; j < 4; ++j) v[j] = __ldg(a.ids + min(i0 + j * kTileThreads + tid, end - 1));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (i0 + j * kTileThreads + tid < end) {
+                if ((unsigned)v[j] < (unsigned)a.E_al) atomicAdd(&cnt[v[j]], 1);
+                else set_error(err, kErrBadId);
+            }
         }
     }
     __syncwarp();
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E_al; e += blockDim.x)
+    for (int e = tid; e < a.E_al; e += kTileThreads)
         a.tile_counts[(int64_t)blockIdx.x * a.E_al + e] = cnt[e];
 }
 
-__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const AlignLaunch a) {
+// 2. For 32 experts per CTA: every tile's start inside each expert (exclusive
+//    prefix over tiles, in tile order) and each expert's total. Thread
+//    (expert el, chunk c) adds a contiguous run of tiles; the 32 chunk sums
+//    are combined in chunk order.
+__global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch a, int ntiles) {
+    __shared__ int part[32][33];
+    const int el = threadIdx.x & 31, c = threadIdx.x >> 5;
+    griddep_launch_dependents();
+    griddep_wait();  // the tile counts come from the previous kernel
+    const int e = blockIdx.x * 32 + el;
+    const int ec = min(e, a.E_al - 1);  // clamped: every load stays in bounds
+    const int tpc = (ntiles + 31) / 32;
+    const int t0 = min(c * tpc, ntiles), t1 = min(t0 + tpc, ntiles);
+    int sum = 0;
+    for (int t = t0; t < t1; t += 16) {
+        int v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            v[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sum += (t + j < t1) ? v[j] : 0;
+    }
+    part[c][el] = sum;
+    __syncthreads();
+    int run = 0, total = 0;
+    for (int q = 0; q < 32; ++q) {
+        const int x = part[q][el];
+        run += (q < c) ? x : 0;
+        total += x;
+    }
+    for (int t = t0; t < t1; t += 16) {  // same batches of 16 loads as above
+        int v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            v[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (t + j < t1 && e < a.E_al) a.tile_base[(int64_t)(t + j) * a.E_al + e] = run;
+            run += v[j];
+        }
+    }
+    if (c == 0 && e < a.E_al) a.totals[e] = total;
+}
+
+// 3. Per tile: padded expert offsets from the totals (block scan, fixed
+//    order), then the stable scatter of the tile's slots to
+//    off[e] + (tile start in e) + rank inside the tile; each CTA also writes
+//    the padding rows and block owners of experts t, t + tiles, ... (one warp
+//    per expert, coalesced). The tile is taken in sub-chunks of 1024 slots:
+//    warp w owns slots [w*128, w*128 + 128) of a sub-chunk, four per lane,
+//    kept in registers with their peer masks between counting and scattering.
+__global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const AlignLaunch a, int tile) {
     extern __shared__ __align__(16) int sm[];
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
-    int *ids = sm;  // [kAlignTile] this tile's ids
-    AlignSmem s = align_carve(sm + kAlignTile, a.E_al);
+    const int E_al = a.E_al;
+    int *wcnt = sm;                   // [8 warps][E_al] counts, then starts
+    int *cum = wcnt + kTileWarps * E_al;  // [E_al] running start of this tile in each expert
+    int *tot = cum + E_al;            // [E_al] expert totals
+    int *off = tot + E_al;            // [E_al + 1] padded expert offsets
+    int *scratch = off + E_al + 1;    // [32]
     const int t = blockIdx.x, ntiles = gridDim.x;
-    const int beg = t * kAlignTile, n = min(beg + kAlignTile, a.numel) - beg;
-    stage_ids(ids, a.ids + beg, n);
-    align_count(ids, n, a.E_al, s, err);  // per-warp starts inside this tile
-    // global per-expert totals and this tile's offset inside each expert, from
-    // all tiles' counts (fixed order; sixteen loads in flight per thread)
-    for (int e = threadIdx.x; e < a.E_al; e += blockDim.x) {
-        int base = 0, tot = 0;
-        for (int u0 = 0; u0 < ntiles; u0 += 16) {
-            int c[16];
+    const int beg = t * tile, n = min(beg + tile, a.numel) - beg;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t lt = lanemask_lt();
+    griddep_wait();  // the tile starts and totals come from the previous kernel
+    // the first sub-chunk's ids (warp w: slots w*128 + g*32 + lane), this
+    // tile's starts and the totals: all loads issued first, one round trip
+    auto load_ids = [&](int c0, int (&e4)[4]) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)  // clamped addresses: all 16 loads in flight
-                c[j] = __ldg(a.tile_counts + (int64_t)min(u0 + j, ntiles - 1) * a.E_al + e);
+        for (int g = 0; g < 4; ++g) e4[g] = __ldg(a.ids + beg + min(c0 + warp * 128 + g * 32 + lane, n - 1));
+    };
+    int e4[4];
+    load_ids(0, e4);
+    constexpr int kPerThread = (kMaxExpertsAl + kTileThreads - 1) / kTileThreads;
+    int bse[kPerThread], tt[kPerThread];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                c[j] = (u0 + j < ntiles) ? c[j] : 0;
-                base += (u0 + j < t) ? c[j] : 0;
-                tot += c[j];
-            }
+    for (int j = 0; j < kPerThread; ++j) {
+        const int e = min(threadIdx.x + j * kTileThreads, E_al - 1);
+        bse[j] = __ldg(a.tile_base + (int64_t)t * E_al + e);
+        tt[j] = __ldg(a.totals + e);
+    }
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int e = threadIdx.x + j * kTileThreads;
+        if (e < E_al) {
+            cum[e] = bse[j];
+            tot[e] = tt[j];
         }
-        s.base[e] = base;
-        s.cnt[e] = tot;
     }
     __syncwarp();
     __syncthreads();
-    const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
-    align_scatter(ids, n, a.E_al, beg, s, true, a.sorted);
-    align_fill(a.A, a.E_al, s.cnt, s, a.numel, a.sorted, a.expert_ids,
-               threadIdx.x * ntiles + t, ntiles * blockDim.x);
+    AlignSmem s;
+    s.off = off;
+    s.scratch = scratch;
+    const int npp = align_offsets(tot, E_al, a.A, s);
+    for (int c0 = 0; c0 < n; c0 += kTileSub) {
+        // the warp's four groups of 32 slots: ids and peer masks
+        if (c0 > 0) load_ids(c0, e4);
+        uint32_t pm[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int i = c0 + warp * 128 + g * 32 + lane;
+            int e = e4[g];
+            if (i >= n) e = kNoExpert;
+            else if ((unsigned)e >= (unsigned)E_al) {
+                set_error(err, kErrBadId);
+                e = kNoExpert;
+            }
+            e4[g] = e;
+        }
+        for (int q = threadIdx.x; q < kTileWarps * E_al; q += kTileThreads) wcnt[q] = 0;
+        __syncwarp();
+        __syncthreads();
+        int *wc = wcnt + warp * E_al;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            pm[g] = peers_of(e4[g]);
+            if (e4[g] != kNoExpert && lane == __ffs(pm[g]) - 1) wc[e4[g]] += __popc(pm[g]);
+            __syncwarp();
+        }
+        __syncthreads();
+        // per expert: starts of the warps' runs (after earlier sub-chunks)
+        for (int e = threadIdx.x; e < E_al; e += kTileThreads) {
+            int run = cum[e];
+#pragma unroll
+            for (int w = 0; w < kTileWarps; ++w) {
+                const int c = wcnt[w * E_al + e];
+                wcnt[w * E_al + e] = run;
+                run += c;
+            }
+            cum[e] = run;
+        }
+        __syncwarp();
+        __syncthreads();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int e = e4[g];
+            if (e != kNoExpert)
+                st_slot(a.sorted, off[e] + wc[e] + __popc(pm[g] & lt), a.sorted_cap,
+                        beg + c0 + warp * 128 + g * 32 + lane, err);
+            __syncwarp();
+            if (e != kNoExpert && lane == __ffs(pm[g]) - 1) wc[e] += __popc(pm[g]);
+            __syncwarp();
+        }
+        __syncthreads();  // the next sub-chunk clears the counts
+    }
+    for (int e = t + warp * ntiles; e < E_al; e += kTileWarps * ntiles) {
+        const int c = tot[e];
+        if (c == 0) continue;  // warp-uniform
+        const int o0 = off[e], o1 = off[e + 1];
+        for (int b = o0 / a.A + lane; b < o1 / a.A; b += 32) st_slot(a.expert_ids, b, a.expert_cap, e, err);
+        for (int q = o0 + c + lane; q < o1; q += 32) st_slot(a.sorted, q, a.sorted_cap, a.numel, err);
+        __syncwarp();
+    }
     if (t == 0 && threadIdx.x == 0) *a.npp = npp;
 }
 
-static cudaError_t set_smem(const void *kern, size_t bytes) {
-    static bool done[3][64] = {};
+// Once per kernel and device: the dynamic shared-memory limit and the largest
+// shared-memory carveout. Every kernel of the library asks for the same
+// carveout, so consecutive launches (route, then align) do not reconfigure
+// the SMs' L1/shared split in between.
+static cudaError_t configure(const void *kern, int slot, size_t bytes) {
+    static bool done[4][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    int slot = kern == (const void *)align_single_kernel ? 0
-             : kern == (const void *)align_scatter_kernel ? 1 : 2;
     if (dev < 64 && !done[slot][dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         done[slot][dev] = true;
     }
     return cudaSuccess;
 }
 
+// A launch that may overlap the end of the previous kernel in the stream
+// (programmatic stream serialization); the kernel waits for it with
+// griddep_wait() before reading its output.
+template <typename... Args>
+static cudaError_t launch_dependent(void (*kern)(Args...), int grid, int block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream) {
-    const size_t smem = (size_t)(kAlignTile + align_smem_words(kAlignWarps, a.E_al)) * 4;
-    const size_t smem_max = (size_t)(kAlignTile + align_smem_words(kAlignWarps, 1025)) * 4;
     cudaError_t e;
     if (a.numel <= kAlignSingleMax) {
-        if ((e = set_smem((const void *)align_single_kernel, smem_max)) != cudaSuccess) return e;
-        align_single_kernel<<<1, kAlignThreads, smem, stream>>>(a);
-        return cudaGetLastError();
+        const size_t smem = (size_t)(kAlignSingleMax + align_smem_words(kAlignWarps, a.E_al)) * 4;
+        const size_t smem_max = (size_t)(kAlignSingleMax + align_smem_words(kAlignWarps, 1025)) * 4;
+        if ((e = configure((const void *)align_single_kernel, 0, smem_max)) != cudaSuccess) return e;
+        return launch_dependent(align_single_kernel, 1, kAlignThreads, smem, stream, a);
     }
-    const int ntiles = align_num_tiles(a.numel);
-    align_hist_kernel<<<ntiles, kAlignThreads, (size_t)a.E_al * 4, stream>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = set_smem((const void *)align_scatter_kernel, smem_max)) != cudaSuccess) return e;
-    align_scatter_kernel<<<ntiles, kAlignThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    int tile, ntiles;
+    if (a.counted_tile > 0) {  // counts written by the route, one tile per route CTA
+        tile = a.counted_tile;
+        ntiles = (a.numel + tile - 1) / tile;
+    } else {
+        tile = align_tile_size(a.numel);
+        ntiles = align_num_tiles(a.numel);
+        if ((e = configure((const void *)align_tile_count_kernel, 2, (size_t)kMaxExpertsAl * 4)) !=
+            cudaSuccess)
+            return e;
+        e = launch_dependent(align_tile_count_kernel, ntiles, kTileThreads, (size_t)a.E_al * 4,
+                             stream, a, tile);
+        if (e != cudaSuccess) return e;
+    }
+    if ((e = configure((const void *)align_tile_scan_kernel, 3, 0)) != cudaSuccess) return e;
+    e = launch_dependent(align_tile_scan_kernel, (a.E_al + 31) / 32, 1024, 0, stream, a, ntiles);
+    if (e != cudaSuccess) return e;
+    const size_t smem = (size_t)((kTileWarps + 3) * a.E_al + 1 + 32) * 4;
+    const size_t smem_max = (size_t)((kTileWarps + 3) * kMaxExpertsAl + 1 + 32) * 4;
+    if ((e = configure((const void *)align_tile_scatter_kernel, 1, smem_max)) != cudaSuccess) return e;
+    return launch_dependent(align_tile_scatter_kernel, ntiles, kTileThreads, smem, stream, a, tile);
 }
 
 }  // namespace smr

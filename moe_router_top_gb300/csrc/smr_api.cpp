@@ -5,8 +5,9 @@
 // Modifications, for the guarded single launch; "[ROCm][Kernel] W4A16 MoE
 // prefill: M-aware moe_align block size", Purpose, for the alignment tier):
 //   route_align, M <= 16 : 1 launch  (small route + fused align)
-//   route_align, M > 16  : 1 tcgen05 route launch + 1 or 2 align launches
-//   route        : 1 launch;  align : 1 launch (numel <= 8192) or 2.
+//   route_align, M > 16  : 1 tcgen05 route launch (which also counts the experts of
+//                          its rows when the align is multi-CTA) + 1 or 2 align launches
+//   route        : 1 launch;  align : 1 launch (numel <= 8192) or 3.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -167,7 +168,7 @@ void check_align(const smr_align_args *a, Reasons &r, bool ids_from_route) {
 size_t align_scratch_bytes(const smr_align_args *a) {
     const int64_t numel = (int64_t)a->num_tokens * a->width;
     if (numel <= smr::kAlignSingleMax) return 0;
-    return round_up((size_t)smr::align_num_tiles((int)numel) * (size_t)a->num_experts * 4, kWsAlign);
+    return round_up((size_t)smr::align_scratch_words(numel, a->num_experts) * 4, kWsAlign);
 }
 
 smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
@@ -187,8 +188,18 @@ smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
     return SMR_OK;
 }
 
+// The align behind a tcgen05 route over more than kAlignSingleMax slots takes
+// its per-tile expert counts from the route (tiles of 64 token rows).
+bool align_counted_by_route(const smr_route_args *r, int64_t numel) {
+    return r->M > smr::kSmallMaxM && numel > smr::kAlignSingleMax;
+}
+int64_t route_tiles(const smr_route_args *r) {
+    return (r->M + smr::kTcCountRows - 1) / smr::kTcCountRows;
+}
+
+// counted_tile > 0: tiles of that many slots whose counts the route writes.
 smr::AlignLaunch make_align_launch(const smr_align_args *a, const int32_t *ids, void *ws,
-                                   size_t align_off) {
+                                   size_t align_off, int counted_tile = 0) {
     smr::AlignLaunch L{};
     L.ids = ids;
     L.numel = a->num_tokens * a->width;
@@ -197,13 +208,22 @@ smr::AlignLaunch make_align_launch(const smr_align_args *a, const int32_t *ids, 
     L.sorted = a->sorted_token_ids;
     L.expert_ids = a->expert_ids;
     L.npp = a->num_tokens_post_padded;
+    L.sorted_cap = a->sorted_cap;
+    L.expert_cap = a->expert_cap;
     L.hdr = ws;
     L.tile_counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + align_off);
+    L.counted_tile = counted_tile;
+    const int64_t tiles = counted_tile > 0 ? ((int64_t)L.numel + counted_tile - 1) / counted_tile
+                                           : smr::align_num_tiles(L.numel);
+    const int64_t tw = tiles * L.E_al;
+    L.tile_base = L.tile_counts + tw;
+    L.totals = L.tile_base + tw;
     return L;
 }
 
 smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
-                     const smr_align_args *fused_align, int *launches) {
+                     const smr_align_args *fused_align, int *launches,
+                     int32_t *tile_counts = nullptr) {
     const int S = a->has_shared ? 1 : 0;
     if (a->M <= smr::kSmallMaxM) {
         smr::SmallRouteLaunch L{};
@@ -224,6 +244,8 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
             L.sorted = fused_align->sorted_token_ids;
             L.expert_ids = fused_align->expert_ids;
             L.npp = fused_align->num_tokens_post_padded;
+            L.sorted_cap = fused_align->sorted_cap;
+            L.expert_cap = fused_align->expert_cap;
         }
         cudaError_t e = smr::launch_small_route(L, stream);
         if (e != cudaSuccess) return cuda_fail("small-M route launch", e);
@@ -242,6 +264,7 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
     L.wts = a->topk_weights;
     L.logits_out = a->logits_out;
     L.hdr = ws;
+    L.tile_counts = tile_counts;
     cudaError_t e = smr::launch_tc_route(L, stream);
     if (e != cudaSuccess) return cuda_fail("tcgen05 route launch", e);
     *launches += 1;
@@ -278,6 +301,11 @@ SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const
     al.num_tokens = route->M;
     al.width = route->topk + (route->has_shared ? 1 : 0);
     al.num_experts = route->E + (route->has_shared ? 1 : 0);
+    const int64_t numel = (int64_t)al.num_tokens * al.width;
+    if (align_counted_by_route(route, numel))  // tiles of 64 route rows
+        return kHeaderBytes + route_scratch_bytes(route) +
+               round_up((size_t)smr::align_scratch_words_tiles(route_tiles(route), al.num_experts) * 4,
+                        kWsAlign);
     return kHeaderBytes + route_scratch_bytes(route) + align_scratch_bytes(&al);
 }
 
@@ -317,7 +345,7 @@ SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t
     smr::AlignLaunch L = make_align_launch(args, args->topk_ids, workspace, kHeaderBytes);
     cudaError_t e = smr::launch_align(L, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("align launch", e);
-    g_last_launches = L.numel <= smr::kAlignSingleMax ? 1 : 2;
+    g_last_launches = smr::align_launches(L.numel, false);
     return SMR_OK;
 }
 
@@ -351,15 +379,17 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
         if (st == SMR_OK) g_last_launches = launches;
         return st;
     }
+    const bool counted = align_counted_by_route(route, (int64_t)route->M * al.width);
+    smr::AlignLaunch L = make_align_launch(&al, route->topk_ids, workspace,
+                                           kHeaderBytes + route_scratch_bytes(route),
+                                           counted ? smr::kTcCountRows * al.width : 0);
     if (route->M > 0) {
-        st = run_route(route, workspace, s, nullptr, &launches);
+        st = run_route(route, workspace, s, nullptr, &launches, counted ? L.tile_counts : nullptr);
         if (st != SMR_OK) return st;
     }
-    smr::AlignLaunch L = make_align_launch(&al, route->topk_ids, workspace,
-                                           kHeaderBytes + route_scratch_bytes(route));
     cudaError_t e = smr::launch_align(L, s);
     if (e != cudaSuccess) return cuda_fail("align launch", e);
-    launches += L.numel <= smr::kAlignSingleMax ? 1 : 2;
+    launches += smr::align_launches(L.numel, counted);
     g_last_launches = launches;
     return SMR_OK;
 }

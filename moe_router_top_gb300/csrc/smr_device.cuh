@@ -18,6 +18,7 @@ namespace smr {
 // Sticky error bits in the workspace header.
 constexpr uint32_t kErrBadId = 1u;        // align saw an id outside [0, E_al)
 constexpr uint32_t kErrWaitTimeout = 2u;  // a bounded wait gave up
+constexpr uint32_t kErrBadSlot = 4u;      // an align output position fell outside its array (skipped)
 
 // First 256 bytes of every workspace. Zeroed once by the caller; kernels
 // return the counters to zero before they exit.
@@ -225,6 +226,17 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t ra
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
 }
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start before the previous kernel in the stream has
+// finished; griddep_wait() blocks until that kernel has completed and its
+// memory is visible (immediately when the launch was not programmatic), so it
+// precedes every read of the previous kernel's output. griddep_launch_dependents()
+// lets the next such kernel start now.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 32-bit store into another CTA's shared memory (address from cluster_addr).
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -406,6 +418,14 @@ __device__ __forceinline__ uint32_t peers_of(int v) {
 }
 constexpr int kNoExpert = 2047;
 
+// Align output write, checked against the caller's array length: a position
+// outside it (only possible from a corrupted workspace) is skipped and flagged
+// instead of written.
+__device__ __forceinline__ void st_slot(int32_t *arr, int64_t pos, int64_t cap, int32_t v, uint32_t *err) {
+    if ((uint64_t)pos < (uint64_t)cap) arr[pos] = v;
+    else set_error(err, kErrBadSlot);
+}
+
 // Slots [warp*L, min((warp+1)*L, n)) belong to warp `warp`; L is a multiple of 32.
 __device__ __forceinline__ int align_warp_span(int n) {
     const int nw = blockDim.x >> 5;
@@ -505,7 +525,7 @@ __device__ __forceinline__ int align_offsets(const int *tot, int E_al, int A, co
 // sorted[off[e] + base[e] + warp start + rank]. Consumes s.wcnt.
 __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_al, int flat0,
                                               const AlignSmem &s, bool use_base,
-                                              int32_t *sorted) {
+                                              int32_t *sorted, int64_t sorted_cap, uint32_t *err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = align_warp_span(n);
     const int beg = warp * L, end = min(beg + L, n);
@@ -518,7 +538,7 @@ __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_a
         const uint32_t peers = peers_of(e);
         if (e != kNoExpert) {
             const int pos = s.off[e] + (use_base ? s.base[e] : 0) + wc[e] + __popc(peers & lt);
-            sorted[pos] = flat0 + i;
+            st_slot(sorted, pos, sorted_cap, flat0 + i, err);
         }
         __syncwarp();
         if (e != kNoExpert && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
@@ -530,14 +550,15 @@ __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_a
 // stride, ...): a touched expert e owns blocks [off[e]/A, off[e+1]/A) and its
 // rows past its last slot, [off[e] + tot[e], off[e+1]), hold the sentinel.
 __device__ __forceinline__ void align_fill(int A, int E_al, const int *tot, const AlignSmem &s,
-                                           int sentinel, int32_t *sorted, int32_t *expert_ids,
+                                           int sentinel, int32_t *sorted, int64_t sorted_cap,
+                                           int32_t *expert_ids, int64_t expert_cap, uint32_t *err,
                                            int first, int stride) {
     for (int e = first; e < E_al; e += stride) {
         const int c = tot[e];
         if (c == 0) continue;
         const int o0 = s.off[e], o1 = s.off[e + 1];
-        for (int b = o0 / A; b < o1 / A; ++b) expert_ids[b] = e;
-        for (int q = o0 + c; q < o1; ++q) sorted[q] = sentinel;
+        for (int b = o0 / A; b < o1 / A; ++b) st_slot(expert_ids, b, expert_cap, e, err);
+        for (int q = o0 + c; q < o1; ++q) st_slot(sorted, q, sorted_cap, sentinel, err);
     }
 }
 

@@ -26,6 +26,7 @@ struct SmallRouteLaunch {
     int32_t *sorted;
     int32_t *expert_ids;
     int32_t *npp;
+    int64_t sorted_cap, expert_cap;  // output array lengths (every write is checked)
 };
 constexpr int kSmallMaxM = 16;
 // Number of K ranges the gate rows are split into (the CTAs of one cluster);
@@ -50,7 +51,12 @@ struct TcRouteLaunch {
     float *wts;
     uint16_t *logits_out;
     void *hdr;
+    // optional (align fused behind the route): expert counts of every
+    // kTcCountRows-row tile, [ceil(M / kTcCountRows)][E + S]
+    int32_t *tile_counts;
 };
+constexpr int kTcTileRows = 128;   // token rows per CTA of the tcgen05 route
+constexpr int kTcCountRows = 64;   // token rows per align tile counted by the route
 // Returns cudaErrorNotSupported when the shape is outside the tcgen05 path.
 bool tc_route_supported(int H, int E, int k, int S);
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream);
@@ -64,12 +70,38 @@ struct AlignLaunch {
     int32_t *sorted;
     int32_t *expert_ids;
     int32_t *npp;
+    int64_t sorted_cap, expert_cap;  // output array lengths (every write is checked)
     void *hdr;
-    int32_t *tile_counts;  // workspace for the multi-CTA path
+    // multi-CTA path (workspace): [tiles][E_al] counts, [tiles][E_al] each
+    // tile's start inside every expert, [E_al] expert totals
+    int32_t *tile_counts;
+    int32_t *tile_base;
+    int32_t *totals;
+    // > 0: the tile counts were written by the tcgen05 route (tiles of
+    // counted_tile slots); the count launch is skipped
+    int counted_tile;
 };
 constexpr int kAlignSingleMax = 8192;   // numel handled by one CTA
-constexpr int kAlignTile = 8192;        // slots per CTA in the multi-CTA path
-inline int align_num_tiles(int numel) { return (numel + kAlignTile - 1) / kAlignTile; }
+constexpr int kAlignMinTile = 1024;     // slots per CTA in the multi-CTA path, at least
+constexpr int kAlignMaxTiles = 2048;    // tiles, at most (larger inputs take larger tiles)
+inline int align_tile_size(int64_t numel) {
+    int64_t t = (numel + kAlignMaxTiles - 1) / kAlignMaxTiles;
+    if (t < kAlignMinTile) t = kAlignMinTile;
+    return (int)((t + kAlignMinTile - 1) / kAlignMinTile * kAlignMinTile);
+}
+inline int align_num_tiles(int64_t numel) {
+    const int64_t t = align_tile_size(numel);
+    return (int)((numel + t - 1) / t);
+}
+// Workspace words of the multi-CTA path over `tiles` tiles.
+inline int64_t align_scratch_words_tiles(int64_t tiles, int E_al) { return 2 * tiles * E_al + E_al; }
+inline int64_t align_scratch_words(int64_t numel, int E_al) {
+    return align_scratch_words_tiles(align_num_tiles(numel), E_al);
+}
+// Launches of launch_align for these inputs.
+inline int align_launches(int64_t numel, bool counted) {
+    return numel <= kAlignSingleMax ? 1 : (counted ? 2 : 3);
+}
 cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream);
 
 }  // namespace smr

@@ -164,7 +164,8 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
 // (coalesced): the ids' flat positions, the sentinel n up to the block end,
 // and the block's expert.
 __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, int32_t *sorted,
-                                           int32_t *expert_ids, int32_t *npp_out) {
+                                           int64_t sorted_cap, int32_t *expert_ids,
+                                           int64_t expert_cap, int32_t *npp_out, uint32_t *err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kCap = kSmallMaxM * 32;
     const int n4 = (n + 3) & ~3;
@@ -228,10 +229,11 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
         const int i = owner[b];
         const int cnt = cntv[i], first = ltv[i];
         const int local0 = b * A - offv[i];
-        if (lane == 0) expert_ids[b] = (int32_t)(keys[i] >> 10);
+        if (lane == 0) st_slot(expert_ids, b, expert_cap, (int32_t)(keys[i] >> 10), err);
         for (int u = lane; u < A; u += 32) {
             const int local = local0 + u;
-            sorted[(int64_t)b * A + u] = local < cnt ? (int32_t)(srt[first + local] & 1023u) : n;
+            st_slot(sorted, (int64_t)b * A + u, sorted_cap,
+                    local < cnt ? (int32_t)(srt[first + local] & 1023u) : n, err);
         }
         __syncwarp();
     }
@@ -388,11 +390,22 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
 
     // ---- 5. moe_align_block_size on the M*width ids of this call ----
     __syncthreads();
-    align_tiny(ids_s, p.M * width, p.A, ids_s + kSmallMaxM * 32, p.sorted, p.expert_ids, p.npp);
+    align_tiny(ids_s, p.M * width, p.A, ids_s + kSmallMaxM * 32, p.sorted, p.sorted_cap, p.expert_ids,
+               p.expert_cap, p.npp, &hdr->error);
 }
 
 template <int NB>
 static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {  // the same carveout as every other kernel of the library
+        cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB>,
+                                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kSmallThreads, 1, 1);

@@ -25,8 +25,9 @@
 //              CTA); in the leader CTA one thread issues the pair MMAs and
 //              commits (multicast to both CTAs) to free each stage;
 //   warps 4-7  meanwhile compute the shared-expert logit of their row from
-//              global memory (CUDA cores, fp32 per k-block, compensated sum
-//              across k-blocks).
+//              the x tile of each stage (CUDA cores, fp32 per k-block,
+//              compensated sum across k-blocks), read once the MMAs are done
+//              with the stage and before it is refilled.
 // Epilogue, all 8 warps: warp w reads TMEM lane quarter w%4 (thread = token
 // row) and column half w/4 (E/2 experts). Each half selects its own exact
 // top-k of bf16-rounded logits in three steps:
@@ -72,8 +73,9 @@ struct TcParams {
     float *wts;
     uint16_t *logits_out;
     uint32_t *err;
+    int32_t *tile_counts;  // optional: expert counts of each 64-row tile, [tiles][E + S]
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
-    uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off;
+    uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off;
 };
 
 // Compensated (two-sum) accumulation of k-block partial sums.
@@ -202,6 +204,63 @@ __device__ __forceinline__ void bitonic_merge_desc(uint32_t (&a)[N]) {
     }
 }
 
+// The key of rank k (1 = largest) among 32 unique keys: k rounds of taking
+// the maximum and clearing it (a short loop instead of a sorting network).
+__device__ __forceinline__ uint32_t kth_largest_key(uint32_t (&a)[kCandCap], int k) {
+    uint32_t m = 0u;
+    for (int r = 0; r < k; ++r) {
+        m = 0u;
+#pragma unroll
+        for (int i = 0; i < kCandCap; ++i) m = max(m, a[i]);
+#pragma unroll
+        for (int i = 0; i < kCandCap; ++i) a[i] = (a[i] == m) ? 0u : a[i];
+    }
+    return m;
+}
+
+// A thread's n <= kCandCap candidate entries (list column, stride kTcBM
+// words) -> its k largest keys, in order, written back to the same column.
+__device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k) {
+    uint32_t a[kCandCap];
+#pragma unroll
+    for (int j = 0; j < kCandCap; ++j) a[j] = (j < (int)n) ? entry_key(col[j * kTcBM]) : 0u;
+    for (int r = 0; r < k; ++r) {
+        uint32_t m = 0u;
+#pragma unroll
+        for (int i = 0; i < kCandCap; ++i) m = max(m, a[i]);
+#pragma unroll
+        for (int i = 0; i < kCandCap; ++i) a[i] = (a[i] == m) ? 0u : a[i];
+        col[r * kTcBM] = m;
+    }
+}
+
+// Exact fallback for a row whose candidates overflowed the list: k passes
+// over the ng groups of its rounded logits in shared memory, each taking the
+// largest key below the previous one.
+__device__ __noinline__ void topk_from_row(uint32_t drow, int ng, int c_beg, int k, uint32_t *col) {
+    uint32_t prev = 0xFFFFFFFFu;
+    for (int r = 0; r < k; ++r) {
+        uint32_t best = 0u;
+        for (int g = 0; g < ng; ++g) {
+            const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < kGroup; ++u) {
+                const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
+                const uint32_t k2 = entry_key(hb | (uint32_t)(c_beg + g * kGroup + u));
+                best = (k2 < prev && k2 > best) ? k2 : best;
+            }
+        }
+        col[r * kTcBM] = best;
+        prev = best;
+    }
+}
+
+// Optional logits output: the row's rounded logits from shared memory.
+__device__ __noinline__ void copy_row_out(uint32_t drow, uint16_t *dst, int ng) {
+    for (int g = 0; g < ng; ++g) reinterpret_cast<uint4 *>(dst)[g] = ld_shared_v4(drow + (uint32_t)(g * 16));
+}
+
 template <int NGM, int CW>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -212,12 +271,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int ST = p.stages;
     uint8_t *misc = smem + p.misc_off;
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);  // leader: both CTAs' loads landed
-    uint64_t *empty = full + ST;       // both CTAs: the pair MMAs are done with the stage
+    uint64_t *mma_done = full + ST;    // both CTAs: the pair MMAs are done with the stage
+    uint64_t *empty = mma_done + ST;   // both CTAs, with a shared gate: the shared-logit warps are too
     uint64_t *accum = empty + ST;      // the pair MMAs of the whole K loop are done
     uint64_t *half_done = accum + 1;   // the 4 warps of column half 0 posted their top-k
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(half_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
+    int *hist = reinterpret_cast<int *>(misc + p.misc_hist_off);  // [2][E + S] counts of the CTA's two 64-row tiles
     uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -229,7 +290,8 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&mma_done[s]), 1);  // the MMA commit (multicast to both CTAs)
+            mbar_init(smem_u32(&empty[s]), 4);     // the 4 shared-logit warps
         }
         mbar_init(smem_u32(accum), 1);
         mbar_init(smem_u32(half_done), 4);
@@ -242,11 +304,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);
         tmem_relinquish_pair();
     }
+    griddep_launch_dependents();  // the align launches may start; they wait for this grid
     for (int i = threadIdx.x; i < p.E; i += kTcThreads) bias_s[i] = p.bias ? p.bias[i] : 0.0f;
-    if (p.S) {
+    for (int i = threadIdx.x; i < 2 * (p.E + p.S); i += kTcThreads) hist[i] = 0;
+    if (p.S) {  // shared gate row, zero-padded to whole k-blocks
         const int nch = p.H >> 3;
-        for (int c = threadIdx.x; c < nch; c += kTcThreads)
-            reinterpret_cast<uint4 *>(ws_s)[c] = reinterpret_cast<const uint4 *>(p.ws)[c];
+        for (int c = threadIdx.x; c < p.num_kb * (kTcBK / 8); c += kTcThreads)
+            reinterpret_cast<uint4 *>(ws_s)[c] =
+                c < nch ? reinterpret_cast<const uint4 *>(p.ws)[c] : make_uint4(0u, 0u, 0u, 0u);
     }
     tc_fence_before();
     cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
@@ -271,7 +336,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             for (; kb < p.num_kb; ++kb) {
                 const int s = kb % ST;
                 const uint32_t ph = (uint32_t)(kb / ST) & 1u;
-                if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag)) break;
+                // a stage is refilled once the MMAs (and, with a shared gate,
+                // the shared-logit warps) are done with it
+                if (!mbar_wait_bounded(smem_u32(p.S ? &empty[s] : &mma_done[s]), ph ^ 1u, abort_flag)) break;
                 const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0u);  // leader's barrier
                 if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * p.stage_bytes);
                 const uint32_t a_dst = smem_u32(smem + (size_t)s * p.stage_bytes);
@@ -309,48 +376,51 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                          (kb | kk) != 0 ? 1u : 0u);
                     }
                 }
-                tc_commit_pair(smem_u32(&empty[s]), pair_mask);
+                tc_commit_pair(smem_u32(&mma_done[s]), pair_mask);
             }
             tc_commit_pair(smem_u32(accum), pair_mask);
         }
         __syncwarp();
     } else if (hf == 1 && p.S) {
-        // ------------- shared-expert logit, warps 4-7, from global memory ---
-        // Independent of the stage ring: each thread reads its own row of x
-        // (L2-hot, TMA streams the same tile), two k-blocks of loads in flight.
-        const uint16_t *xr = p.x + (int64_t)min(grow, p.M - 1) * p.ld;
-        const int nch = p.H >> 3;  // 16-byte chunks per row
-        constexpr int kAhead = 16;
-        uint4 buf[kAhead];
-#pragma unroll
-        for (int j = 0; j < kAhead; ++j) buf[j] = __ldg(reinterpret_cast<const uint4 *>(xr) + min(j, nch - 1));
-        for (int c0 = 0; c0 < nch; c0 += kAhead / 2) {
+        // ------- shared-expert logit, warps 4-7, from each stage's x tile ---
+        // once the MMAs are done with a stage (their commit reaches both
+        // CTAs) its x tile is still in place: thread = token row reads the
+        // row's 64 elements of the k-block (eight 16-byte chunks, 128-byte
+        // swizzle: chunk c sits at c ^ (row & 7)), fp32 dot per k-block,
+        // compensated sum across k-blocks; each warp then releases the stage
+        const uint32_t swz = (uint32_t)(row & 7);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            const int s = kb % ST;
+            const uint32_t ph = (uint32_t)(kb / ST) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mma_done[s]), ph, abort_flag))) {
+                set_error(p.err, kErrWaitTimeout);
+                break;
+            }
+            const uint8_t *xrow = smem + (size_t)s * p.stage_bytes + (size_t)row * kTcSW;
+            const uint4 *wsv = reinterpret_cast<const uint4 *>(ws_s) + kb * (kTcBK / 8);
             float part = 0.0f;
 #pragma unroll
-            for (int j = 0; j < kAhead / 2; ++j) {
-                const int c = c0 + j;
-                if (c < nch) {
-                    float xf[8], wf[8];
-                    unpack8(buf[j], xf);
-                    unpack8(reinterpret_cast<const uint4 *>(ws_s)[c], wf);
+            for (int c = 0; c < kTcBK / 8; ++c) {
+                float xf[8], wf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(xrow + ((c ^ swz) << 4)), xf);
+                unpack8(wsv[c], wf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
-                }
+                for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
             }
             two_sum_acc(s_hi, s_lo, part);
-#pragma unroll
-            for (int j = 0; j < kAhead / 2; ++j) {
-                buf[j] = buf[j + kAhead / 2];
-                buf[j + kAhead / 2] =
-                    __ldg(reinterpret_cast<const uint4 *>(xr) + min(c0 + kAhead + j, nch - 1));
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
+        __syncwarp();
     }
 
     // ---------------------------------- epilogue: all 8 warps ----------
     // warp (q, hf) owns TMEM lanes of quarter q (token rows q*32..q*32+31) and
     // expert columns [hf*E/2, (hf+1)*E/2); each half finds its own exact
-    // top-k, half 1 merges both lists and writes the row.
+    // top-k, half 1 merges both lists and writes the row. The epilogue runs
+    // once per CTA after other kernels have used the SM, so its instructions
+    // are fetched cold: it is written as short rolled loops (k rounds of a
+    // 32-key maximum, a pointer merge) rather than unrolled sorting networks.
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
     tc_fence_after();
     ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
@@ -359,77 +429,77 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int c_beg = hf * ecols;
     const int nch = ecols / CW;       // CW-column TMEM chunks per half
     const int ng = ecols / kGroup;    // groups of kGroup consecutive columns per half
-    // the stage ring is idle once the accumulator is complete: it holds the
-    // candidate lists, half 0's posted top-k and each half's rounded logits
-    uint32_t *cand = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);  // [kCandCap][128] per half
-    uint32_t *posted = reinterpret_cast<uint32_t *>(smem) + 2 * kCandCap * kTcBM;    // [32][128] half 0's top-k
+    // the stage ring is idle once the accumulator is complete. Per half a
+    // list column per thread ([32][128] words: group maxima, then candidates,
+    // then the half's top-k), softmax numerators of half 1, and each half's
+    // rounded logits (row stride rs)
+    uint32_t *list = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);
+    uint32_t *list0 = reinterpret_cast<uint32_t *>(smem);                 // half 0's top-k
+    float *numer = reinterpret_cast<float *>(smem) + 2 * kCandCap * kTcBM;  // [32][128]
     const uint32_t rs = dump_row_bytes(ecols);
     const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
-    uint32_t key[kCandCap];
     if (ok) {
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
-        const bool has_bias = p.bias != nullptr;
-        // 1. one sweep over this half's TMEM columns: round to bf16 (two per
-        //    32-bit word), keep the row's rounded logits in shared memory,
-        //    take the maximum of every group of kGroup columns
-        float gm[NGM];
-#pragma unroll
-        for (int g = 0; g < NGM; ++g) gm[g] = -INFINITY;
+        // 1. one sweep over this half's TMEM columns: add the bias, round to
+        //    bf16 two at a time, keep the row in shared memory and the maximum
+        //    of each group of kGroup columns in the thread's list column
         uint32_t ra[CW], rb[CW];
         auto process = [&](uint32_t (&r)[CW], int ch) {
             const int c = c_beg + ch * CW;
-            uint32_t wv[CW / 2];
-#pragma unroll
-            for (int t = 0; t < CW / 2; ++t) {
-                float lo = __uint_as_float(r[2 * t]), hi = __uint_as_float(r[2 * t + 1]);
-                if (has_bias) {
-                    lo += bias_s[c + 2 * t];
-                    hi += bias_s[c + 2 * t + 1];
-                }
-                wv[t] = pack_bf16x2_rn(lo, hi);
-            }
 #pragma unroll
             for (int u = 0; u < CW / kGroup; ++u) {
-                const uint4 v = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
-                st_shared_v4(drow + (uint32_t)((ch * (CW / kGroup) + u) * 16), v);
-                const uint32_t mx = max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
-                gm[ch * (CW / kGroup) + u] =
-                    fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
-                if (p.logits_out && valid)
-                    reinterpret_cast<uint4 *>(p.logits_out + (int64_t)grow * p.E + c)[u] = v;
+                uint32_t wv[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int i = u * kGroup + 2 * t;
+                    wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + bias_s[c + i],
+                                           __uint_as_float(r[i + 1]) + bias_s[c + i + 1]);
+                }
+                const int g = ch * (CW / kGroup) + u;
+                st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                const uint32_t mx = max_bf16x2(max_bf16x2(wv[0], wv[1]), max_bf16x2(wv[2], wv[3]));
+                list[g * kTcBM + row] = make_key(fmaxf(__uint_as_float(mx << 16),
+                                                       __uint_as_float(mx & 0xFFFF0000u)), g);
             }
         };
-        // chunks unrolled (group maxima stay in registers), the next chunk's
-        // TMEM load in flight while one is processed
         tmem_ld_async<CW>(taddr, ra);
         tmem_ld_wait<CW>(ra);
-#pragma unroll
-        for (int ch = 0; ch < NGM * kGroup / CW; ++ch) {
-            if (ch < nch) {
-                uint32_t (&cur)[CW] = (ch & 1) ? rb : ra;
-                uint32_t (&nxt)[CW] = (ch & 1) ? ra : rb;
-                if (ch + 1 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), nxt);
-                process(cur, ch);
-                if (ch + 1 < nch) tmem_ld_wait<CW>(nxt);
+        for (int ch = 0; ch < nch; ch += 2) {  // the next chunk's load in flight
+            const bool two = ch + 1 < nch;
+            if (two) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), rb);
+            process(ra, ch);
+            if (two) {
+                tmem_ld_wait<CW>(rb);
+                if (ch + 2 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 2) * CW), ra);
+                process(rb, ch + 1);
+                if (ch + 2 < nch) tmem_ld_wait<CW>(ra);
             }
         }
+        __syncwarp();
+        if (__builtin_expect(p.logits_out != nullptr, 0) && valid)
+            copy_row_out(drow, p.logits_out + (int64_t)grow * p.E + c_beg, ng);
         // the k-th largest group maximum T bounds this half's top-k from
         // below (k groups hold a logit >= T); only groups whose maximum is
         // >= T can hold a logit >= T
-        float gs[NGM];
+        uint32_t a[kCandCap];
 #pragma unroll
-        for (int g = 0; g < NGM; ++g) gs[g] = gm[g];
-        sort_desc<NGM>(gs);
-        float T = INFINITY;
-#pragma unroll
-        for (int g = 0; g < NGM; ++g) T = fminf(T, g < p.k ? gs[g] : INFINITY);
-        if (p.k > ng) T = -INFINITY;  // fewer groups than k: every logit is a candidate
+        for (int g = 0; g < kCandCap; ++g) a[g] = (g < ng) ? list[g * kTcBM + row] : 0u;
         uint32_t sel = 0;
+        float T = -INFINITY;
+        if (p.k <= ng) {
+            const uint32_t kth = kth_largest_key(a, p.k);
+            T = key_value(kth);
 #pragma unroll
-        for (int g = 0; g < NGM; ++g) sel |= (g < ng && gm[g] >= T) ? (1u << g) : 0u;
+            for (int g = 0; g < kCandCap; ++g)
+                sel |= (g < ng && key_value(list[g * kTcBM + row]) >= T) ? (1u << g) : 0u;
+        } else {
+            sel = (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);  // fewer groups than k: all
+        }
+        __syncwarp();
         // 2. append every logit >= T of the selected groups (about k groups)
+        //    to the list column, over the group maxima
         uint32_t n = 0;
-        const uint32_t cand_row = smem_u32(cand + row);
+        const uint32_t cand_row = smem_u32(list + row);
         while (__any_sync(0xffffffffu, sel != 0u)) {
             const uint32_t act = sel != 0u ? 1u : 0u;
             const int g = act ? __ffs(sel) - 1 : 0;
@@ -447,44 +517,17 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
         }
         asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
-        // 3. this half's candidates as ordered keys in registers, sorted
-        //    descending. A row whose list overflowed takes an exact k-pass
-        //    selection over the half's rounded logits in shared memory.
-        const bool overflow = n > (uint32_t)kCandCap;
-#pragma unroll
-        for (int j = 0; j < kCandCap; ++j)
-            key[j] = (j < (int)n) ? entry_key(cand[j * kTcBM + row]) : 0u;
-        if (__all_sync(0xffffffffu, n <= 16u))
-            sort_keys_desc<16>(key);
-        else
-            sort_keys_desc<kCandCap>(key);
-        if (overflow) {
-#pragma unroll
-            for (int j = 0; j < kCandCap; ++j) key[j] = 0u;
-            uint32_t prev = 0xFFFFFFFFu;
-            for (int r = 0; r < p.k; ++r) {
-                uint32_t best = 0u;
-                for (int g = 0; g < ng; ++g) {
-                    const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int u = 0; u < kGroup; ++u) {
-                        const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
-                        const uint32_t k2 = entry_key(hb | (uint32_t)(c_beg + g * kGroup + u));
-                        best = (k2 < prev && k2 > best) ? k2 : best;
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) key[j] = (j == r) ? best : key[j];
-                prev = best;
-            }
+        __syncwarp();
+        // 3. this half's top-k, in order, into the list column: k rounds of
+        //    the largest remaining candidate key. A row whose candidates
+        //    overflowed the list takes k passes over its rounded logits.
+        if (__builtin_expect(__any_sync(0xffffffffu, n > (uint32_t)kCandCap), 0)) {
+            if (n > (uint32_t)kCandCap) topk_from_row(drow, ng, c_beg, p.k, list + row);
+            else topk_from_list(list + row, n, p.k);
+        } else {
+            topk_from_list(list + row, n, p.k);
         }
-        __syncwarp();  // only overflowing lanes took the fallback
-        if (hf == 0) {
-#pragma unroll
-            for (int j = 0; j < kCandCap; ++j)
-                if (j < p.k) posted[j * kTcBM + row] = key[j];
-        }
+        __syncwarp();
     }
     if (hf == 0) {
         __syncwarp();
@@ -494,51 +537,46 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag));
         __syncwarp();
         if (ok && got && valid) {
-            // both lists sorted descending: reverse the other half's list
-            // behind this one -> bitonic sequence -> merge
-            uint32_t top[kCandCap];
-            if (p.k <= 16) {
-                uint32_t h[32];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    h[j] = key[j];
-                    h[31 - j] = (j < p.k) ? posted[j * kTcBM + row] : 0u;
-                }
-                bitonic_merge_desc<32>(h);
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) top[j] = h[j];
-            } else {
-                uint32_t m[2 * kCandCap];
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) {
-                    m[j] = key[j];
-                    m[2 * kCandCap - 1 - j] = (j < p.k) ? posted[j * kTcBM + row] : 0u;
-                }
-                bitonic_merge_desc<2 * kCandCap>(m);
-#pragma unroll
-                for (int j = 0; j < kCandCap; ++j) top[j] = m[j];
-            }
-            const float vmax = key_value(top[0]);
-            float ev[kCandCap];
-            float sum = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kCandCap; ++j) {
-                ev[j] = (j < p.k) ? expf(key_value(top[j]) - vmax) : 0.0f;
-                sum += ev[j];
-            }
             int32_t *orow = p.ids + (int64_t)grow * p.width;
             float *wrow = p.wts + (int64_t)grow * p.width;
-#pragma unroll
-            for (int j = 0; j < kCandCap; ++j) {
-                if (j < p.k) {
-                    orow[j] = key_id(top[j]);
-                    wrow[j] = ev[j] / sum;
-                }
+            int *h = hist + (row / kTcCountRows) * (p.E + p.S);
+            const bool count = p.tile_counts != nullptr;
+            // both halves' lists are sorted descending: a pointer merge of k
+            // steps gives the row's top-k; the softmax numerators go to
+            // shared memory, the ids straight out
+            int i = 0, j = 0;
+            float vmax = 0.0f, sum = 0.0f;
+            for (int r = 0; r < p.k; ++r) {
+                const uint32_t x1 = i < p.k ? list[i * kTcBM + row] : 0u;
+                const uint32_t x0 = j < p.k ? list0[j * kTcBM + row] : 0u;
+                const bool take1 = x1 > x0;
+                const uint32_t m = take1 ? x1 : x0;
+                i += take1 ? 1 : 0;
+                j += take1 ? 0 : 1;
+                vmax = (r == 0) ? key_value(m) : vmax;
+                const float ev = expf(key_value(m) - vmax);
+                sum += ev;
+                numer[r * kTcBM + row] = ev;
+                orow[r] = key_id(m);
+                if (count) atomicAdd(&h[key_id(m)], 1);
             }
+            for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] / sum;
             if (p.S) {
                 const float sh = s_hi + s_lo;
                 orow[p.k] = p.E;
                 wrow[p.k] = p.scale * sigmoid_stable(sh);
+                if (count) atomicAdd(&h[p.E], 1);
+            }
+        }
+        __syncwarp();
+        if (p.tile_counts) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the 4 warps of half 1
+            const int E_al = p.E + p.S;
+            for (int t = 0; t < kTcTileRows / kTcCountRows; ++t) {  // tiles that hold rows
+                if (m0 + t * kTcCountRows < p.M)
+                    for (int e = threadIdx.x - 128; e < E_al; e += 128)
+                        p.tile_counts[(int64_t)(blockIdx.x * (kTcTileRows / kTcCountRows) + t) * E_al + e] =
+                            hist[t * E_al + e];
             }
         }
         if (!(ok && got)) set_error(p.err, kErrWaitTimeout);
@@ -613,16 +651,18 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     while (cols < (uint32_t)E) cols <<= 1;
     p.tmem_cols = cols;
     p.stage_bytes = (uint32_t)(kTcBM * kTcSW + (E / 2) * kTcSW);
-    // misc: barriers and flags (256 B: 2*stages+2 mbarriers, TMEM slot, abort
-    // flag), bias [E] fp32, shared gate [H] bf16
+    // misc: barriers and flags (256 B: 3*stages+2 mbarriers, TMEM slot, abort
+    // flag), bias [E] fp32, expert counts [2][E+S] int32, shared gate [H, padded
+    // to whole k-blocks] bf16
     p.misc_bias_off = 256;
-    p.misc_ws_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
-    const size_t misc = p.misc_ws_off + (S ? (size_t)H * 2 : 0);
+    p.misc_hist_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
+    p.misc_ws_off = p.misc_hist_off + (uint32_t)((2 * (E + S) * 4 + 15) & ~15);
+    const size_t misc = p.misc_ws_off + (S ? (size_t)p.num_kb * kTcBK * 2 : 0);
     const size_t budget = (size_t)kTcSmemLimit - 1024 - misc;
     int st = (int)(budget / p.stage_bytes);
     if (st > 6) st = 6;
     if (st < 2) return false;
-    static_assert(8 * (2 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
+    static_assert(8 * (3 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
     // the epilogue (candidate lists, half 0's top-k, both halves' rounded
     // logits) reuses the stage ring; the misc block follows the larger one
     const size_t ring = (size_t)st * p.stage_bytes;
@@ -653,6 +693,10 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
         cudaError_t e = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kTcSmemLimit);
+        if (e == cudaSuccess)  // the same carveout as every other kernel of the library
+            e = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -684,6 +728,7 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     p.wts = a.wts;
     p.logits_out = a.logits_out;
     p.err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
+    p.tile_counts = a.tile_counts;
     CUtensorMap mx, mw;
     if (!make_map(&mx, a.x, (uint64_t)a.H, (uint64_t)a.M, (uint64_t)a.ld * 2, kTcBK, kTcBM))
         return cudaErrorInvalidValue;

@@ -143,8 +143,18 @@ def test_align_workspace_sizes(lib):
     a = _good_align(T=4)
     assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256          # one CTA, no scratch
     a = _good_align(T=16384, A=128)
-    ntiles = (16384 * 11 + 8191) // 8192
-    assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256 + ((ntiles * 513 * 4 + 255) // 256) * 256
+    # tiles of 1024 slots (at most 2048 tiles): [tiles][E_al] counts and
+    # starts, [E_al] totals
+    ntiles = (16384 * 11 + 1023) // 1024
+    words = 2 * ntiles * 513 + 513
+    assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256 + ((words * 4 + 255) // 256) * 256
+    a = _good_align(T=1 << 22, W=64, A=128)  # 2^28 slots: tiles grow to keep 2048 of them
+    tile = -(-(1 << 28) // 2048)
+    tile = -(-tile // 1024) * 1024
+    ntiles = -(-(1 << 28) // tile)
+    assert ntiles <= 2048
+    words = 2 * ntiles * 513 + 513
+    assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256 + ((words * 4 + 255) // 256) * 256
 
 
 def test_route_align_consistency_checks(lib):
