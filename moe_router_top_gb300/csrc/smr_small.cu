@@ -29,10 +29,11 @@
 //    stores the group's final logits -- results are deterministic;
 //  - one acquire-release ticket per row group hands the tail to the last
 //    group (no spin-wait);
-//  - the tail is warp-parallel and straight-line: one warp per token, each
-//    lane holds E/32 ordered 32-bit keys sorted in registers, k rounds of one
-//    redux.sync max and a register shift pop the winner; the align of the
-//    few ids ranks (expert, position) keys instead of scanning all experts.
+//  - the tail is warp-parallel and compact (it runs once per call, on a cold
+//    instruction cache): one warp per token, each lane holds E/32 ordered
+//    32-bit keys, k rounds of a lane maximum, one redux.sync max and a clear
+//    of the winner; the align of the few ids ranks (expert, position) keys
+//    instead of scanning all experts.
 #include "smr_device.cuh"
 #include "smr_launch.h"
 
@@ -67,27 +68,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Sort NK keys descending in registers (bitonic network).
-template <int NK>
-__device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[NK]) {
-#pragma unroll
-    for (int size = 2; size <= NK; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = ((i & size) == 0);
-                    const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
-                    a[i] = desc ? hi : lo;
-                    a[j] = desc ? lo : hi;
-                }
-            }
-        }
-    }
-}
-
 // Top-k of one token row in one warp, plus its shared slot. zrow: the
 // token's fp32 gate logits (E routed, then the shared one when S = 1);
 // bias_s: the routed experts' bias in shared memory (zeros without a bias).
@@ -119,18 +99,22 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
             if (lane + 32 * i < E) logits_out[lane + 32 * i] = (uint16_t)(__float_as_uint(z[i]) >> 16);
         __syncwarp();
     }
-    sort_keys_desc<NK>(key);
+    // k rounds: each lane's largest key, the warp's largest (redux), and the
+    // lane holding it clears it (keys are unique) -- selects only, so the
+    // warp stays converged, and no sorting network: the tail runs once per
+    // call on a cold instruction cache, where code size costs more than
+    // instructions
     uint32_t mine = 0u, first = 0u;
+#pragma unroll 1
     for (int r = 0; r < k; ++r) {
-        const uint32_t gmax = __reduce_max_sync(0xffffffffu, key[0]);
+        uint32_t lm = key[0];
+#pragma unroll
+        for (int i = 1; i < NK; ++i) lm = max(lm, key[i]);
+        const uint32_t gmax = __reduce_max_sync(0xffffffffu, lm);
         first = (r == 0) ? gmax : first;
         mine = (lane == r) ? gmax : mine;
-        // the single lane holding the winner pops it (selects, no branch:
-        // the warp stays converged for the next reduction)
-        const bool win = key[0] == gmax;
 #pragma unroll
-        for (int i = 0; i + 1 < NK; ++i) key[i] = win ? key[i + 1] : key[i];
-        key[NK - 1] = win ? 0u : key[NK - 1];
+        for (int i = 0; i < NK; ++i) key[i] = (key[i] == gmax) ? 0u : key[i];
     }
     // softmax over the selected logits (renormalised top-k); every lane
     // evaluates the exponential, lanes past k drop it
@@ -182,9 +166,11 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
     __syncwarp();
     __syncthreads();
     // pass 1 (ids i = tid, tid + 256): counts against every key
+#pragma unroll 1
     for (int i = tid; i < n4; i += kSmallThreads) {
         const uint32_t k = keys[i], e = k >> 10;
         int lt = 0, eq = 0, eqb = 0;
+#pragma unroll 1
         for (int j = 0; j < n4; j += 4) {
             const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -204,9 +190,11 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
     __syncwarp();
     __syncthreads();
     // pass 2: padded offset of each id's expert; first occurrences claim blocks
+#pragma unroll 1
     for (int i = tid; i < n4; i += kSmallThreads) {
         const uint32_t e = keys[i] >> 10;
         int off = 0, total = 0;
+#pragma unroll 1
         for (int j = 0; j < n4; j += 4) {
             const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
             const int4 pv = *reinterpret_cast<const int4 *>(padv + j);
@@ -216,6 +204,7 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
         }
         offv[i] = off;
         const int pad = padv[i];
+#pragma unroll 1
         for (int b = off / A; b < (off + pad) / A; ++b) owner[b] = i;
         if (i == 0) {
             *s_total = total;
@@ -225,11 +214,13 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
     __syncwarp();
     __syncthreads();
     const int nblk = *s_total / A;
+#pragma unroll 1
     for (int b = warp; b < nblk; b += kSmallWarps) {
         const int i = owner[b];
         const int cnt = cntv[i], first = ltv[i];
         const int local0 = b * A - offv[i];
         if (lane == 0) st_slot(expert_ids, b, expert_cap, (int32_t)(keys[i] >> 10), err);
+#pragma unroll 1
         for (int u = lane; u < A; u += 32) {
             const int local = local0 + u;
             st_slot(sorted, (int64_t)b * A + u, sorted_cap,
@@ -239,7 +230,10 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
     }
 }
 
-template <int NB>  // N blocks of 8 tokens: 1 (M <= 8) or 2 (M <= 16)
+// NB: blocks of 8 tokens, 1 (M <= 8) or 2 (M <= 16); NK: keys per lane in
+// the top-k, 16 (E <= 512) or 32 (E <= 1024) -- one top-k per instance, so
+// the tail's code is laid out in the order it runs
+template <int NB, int NK>
 __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     const SmallRouteLaunch &p = P.a;
@@ -370,21 +364,13 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
     // ---- 4. tail: top-k + softmax + shared slot, one warp per token ----
     const int width = p.k + p.S;
     int32_t *ids_s = reinterpret_cast<int32_t *>(smem);  // [M*width]
-    const int nk = (p.E + 31) >> 5;
     for (int m = warp; m < p.M; m += kSmallWarps) {
         const float *zrow = p.scratch + (int64_t)m * rows;
         uint16_t *lrow = p.logits_out ? p.logits_out + (int64_t)m * p.E : nullptr;
         int32_t *irow = p.ids + (int64_t)m * width;
         float *wrow = p.wts + (int64_t)m * width;
         int32_t *srow = ids_s + m * width;
-        if (nk <= 4)
-            warp_topk_row<4>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
-        else if (nk <= 8)
-            warp_topk_row<8>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
-        else if (nk <= 16)
-            warp_topk_row<16>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
-        else
-            warp_topk_row<32>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
+        warp_topk_row<NK>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
     }
     if (p.sorted == nullptr) return;
 
@@ -394,13 +380,13 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
                p.expert_cap, p.npp, &hdr->error);
 }
 
-template <int NB>
+template <int NB, int NK>
 static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {  // the same carveout as every other kernel of the library
-        cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB>,
+        cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB, NK>,
                                              cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -418,7 +404,7 @@ static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaSt
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, small_route_kernel<NB>, P);
+    return cudaLaunchKernelEx(&cfg, small_route_kernel<NB, NK>, P);
 }
 
 int small_route_k_ranges(int E, int S, int H) {
@@ -477,7 +463,9 @@ cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
     const int groups = (P.rows + 15) / 16;
     const int grid = groups * P.KQ;
     const size_t smem = (size_t)(kSmallFrontWords + kSmallMaxE) * 4;
-    return a.M <= 8 ? launch_nb<1>(P, grid, smem, stream) : launch_nb<2>(P, grid, smem, stream);
+    if (a.E <= 512)
+        return a.M <= 8 ? launch_nb<1, 16>(P, grid, smem, stream) : launch_nb<2, 16>(P, grid, smem, stream);
+    return a.M <= 8 ? launch_nb<1, 32>(P, grid, smem, stream) : launch_nb<2, 32>(P, grid, smem, stream);
 }
 
 }  // namespace smr

@@ -208,6 +208,7 @@ __device__ __forceinline__ void bitonic_merge_desc(uint32_t (&a)[N]) {
 // the maximum and clearing it (a short loop instead of a sorting network).
 __device__ __forceinline__ uint32_t kth_largest_key(uint32_t (&a)[kCandCap], int k) {
     uint32_t m = 0u;
+#pragma unroll 1
     for (int r = 0; r < k; ++r) {
         m = 0u;
 #pragma unroll
@@ -224,6 +225,7 @@ __device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k)
     uint32_t a[kCandCap];
 #pragma unroll
     for (int j = 0; j < kCandCap; ++j) a[j] = (j < (int)n) ? entry_key(col[j * kTcBM]) : 0u;
+#pragma unroll 1
     for (int r = 0; r < k; ++r) {
         uint32_t m = 0u;
 #pragma unroll
@@ -500,6 +502,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         //    to the list column, over the group maxima
         uint32_t n = 0;
         const uint32_t cand_row = smem_u32(list + row);
+#pragma unroll 1
         while (__any_sync(0xffffffffu, sel != 0u)) {
             const uint32_t act = sel != 0u ? 1u : 0u;
             const int g = act ? __ffs(sel) - 1 : 0;
@@ -546,6 +549,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // shared memory, the ids straight out
             int i = 0, j = 0;
             float vmax = 0.0f, sum = 0.0f;
+#pragma unroll 1
             for (int r = 0; r < p.k; ++r) {
                 const uint32_t x1 = i < p.k ? list[i * kTcBM + row] : 0u;
                 const uint32_t x0 = j < p.k ? list0[j * kTcBM + row] : 0u;
@@ -560,6 +564,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 orow[r] = key_id(m);
                 if (count) atomicAdd(&h[key_id(m)], 1);
             }
+#pragma unroll 1
             for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] / sum;
             if (p.S) {
                 const float sh = s_hi + s_lo;
