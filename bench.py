@@ -170,8 +170,8 @@ def traffic_from_profile():
         return None
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
+        if ": " in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(": ", 1)
             vals[k.strip()] = v.strip().strip("`")
     if vals.get("smr_tc.cu sha256[:16]") != sha:
         return None

@@ -181,3 +181,20 @@ def test_disable_switch(monkeypatch):
     monkeypatch.setenv("SMR_DISABLE", "1")
     with pytest.raises(smr.SmrUnsupported):
         smr.route(None, None, topk=1)
+
+
+def test_route_profile_summary_parses():
+    """The committed ncu summary of the route kernel carries the source hash
+    and DRAM bytes per launch that bench.py reports as roofline traffic."""
+    import hashlib
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "profiles", "tc_route_kernel_large_batch.md")).read()
+    sha = re.search(r"- smr_tc\.cu sha256\[:16\]: `([0-9a-f]{16})`", text)
+    dram = re.search(r"- dram bytes per launch: (\d+)", text)
+    assert sha and dram
+    import bench
+    src = os.path.join(root, "moe_router_top_gb300", "csrc", "smr_tc.cu")
+    current = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    expect = int(dram.group(1)) if sha.group(1) == current else None
+    assert bench.traffic_from_profile() == expect
