@@ -204,34 +204,51 @@ __device__ __forceinline__ void bitonic_merge_desc(uint32_t (&a)[N]) {
     }
 }
 
-// The key of rank k (1 = largest) among 32 unique keys: k rounds of taking
-// the maximum and clearing it (a short loop instead of a sorting network).
-__device__ __forceinline__ uint32_t kth_largest_key(uint32_t (&a)[kCandCap], int k) {
-    uint32_t m = 0u;
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        m = 0u;
-#pragma unroll
-        for (int i = 0; i < kCandCap; ++i) m = max(m, a[i]);
-#pragma unroll
-        for (int i = 0; i < kCandCap; ++i) a[i] = (a[i] == m) ? 0u : a[i];
-    }
-    return m;
+// bf16 pair -> ordered unsigned 16-bit keys (numeric order as unsigned order).
+__device__ __forceinline__ uint32_t ordered_bf16x2(uint32_t x) {
+    const uint32_t neg = (x >> 15) & 0x00010001u;  // sign bit of each half
+    return x ^ ((neg * 0xFFFFu) | 0x80008000u);
+}
+// Ordered 16-bit key -> the bf16 value as a float.
+__device__ __forceinline__ float ordered16_value(uint32_t o) {
+    const uint32_t b = (o & 0x8000u) ? (o & 0x7FFFu) : (~o & 0xFFFFu);
+    return __uint_as_float(b << 16);
 }
 
-// A thread's n <= kCandCap candidate entries (list column, stride kTcBM
-// words) -> its k largest keys, in order, written back to the same column.
-__device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k) {
-    uint32_t a[kCandCap];
+// A value of rank <= k among the 32 ordered 16-bit keys packed in pw (0 =
+// empty): k rounds of taking the maximum and clearing every half equal to it.
+// Equal keys leave together, so the result is at most the k-th largest; it
+// stays a valid lower bound for "at least k keys are >= it".
+__device__ __forceinline__ uint32_t kth_largest_packed(uint32_t (&pw)[kCandCap / 2], int k) {
+    uint32_t last = 0u;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        uint32_t m2 = pw[0];
 #pragma unroll
-    for (int j = 0; j < kCandCap; ++j) a[j] = (j < (int)n) ? entry_key(col[j * kTcBM]) : 0u;
+        for (int i = 1; i < kCandCap / 2; ++i) m2 = __vmaxu2(m2, pw[i]);
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        last = m ? m : last;
+        const uint32_t ms = m | (m << 16);
+#pragma unroll
+        for (int i = 0; i < kCandCap / 2; ++i) pw[i] &= ~__vcmpeq2(pw[i], ms);
+    }
+    return last;
+}
+
+// A thread's n <= SLOTS candidate entries (list column, stride kTcBM words)
+// -> its k largest keys, in order, written back to the same column.
+template <int SLOTS>
+__device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k) {
+    uint32_t a[SLOTS];
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) a[j] = (j < (int)n) ? entry_key(col[j * kTcBM]) : 0u;
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
         uint32_t m = 0u;
 #pragma unroll
-        for (int i = 0; i < kCandCap; ++i) m = max(m, a[i]);
+        for (int i = 0; i < SLOTS; ++i) m = max(m, a[i]);
 #pragma unroll
-        for (int i = 0; i < kCandCap; ++i) a[i] = (a[i] == m) ? 0u : a[i];
+        for (int i = 0; i < SLOTS; ++i) a[i] = (a[i] == m) ? 0u : a[i];
         col[r * kTcBM] = m;
     }
 }
@@ -446,22 +463,35 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         //    bf16 two at a time, keep the row in shared memory and the maximum
         //    of each group of kGroup columns in the thread's list column
         uint32_t ra[CW], rb[CW];
+        const bool has_bias = p.bias != nullptr;
         auto process = [&](uint32_t (&r)[CW], int ch) {
             const int c = c_beg + ch * CW;
+            uint32_t pair = 0u;  // ordered 16-bit maxima of two consecutive groups
 #pragma unroll
             for (int u = 0; u < CW / kGroup; ++u) {
+                float b[kGroup];
+#pragma unroll
+                for (int t = 0; t < kGroup; ++t) b[t] = 0.0f;
+                if (has_bias) {
+                    const float4 b0 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup);
+                    const float4 b1 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup + 4);
+                    b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                    b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+                }
                 uint32_t wv[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int i = u * kGroup + 2 * t;
-                    wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + bias_s[c + i],
-                                           __uint_as_float(r[i + 1]) + bias_s[c + i + 1]);
+                    wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + b[2 * t],
+                                           __uint_as_float(r[i + 1]) + b[2 * t + 1]);
                 }
                 const int g = ch * (CW / kGroup) + u;
                 st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                const uint32_t mx = max_bf16x2(max_bf16x2(wv[0], wv[1]), max_bf16x2(wv[2], wv[3]));
-                list[g * kTcBM + row] = make_key(fmaxf(__uint_as_float(mx << 16),
-                                                       __uint_as_float(mx & 0xFFFF0000u)), g);
+                const uint32_t mx = __vmaxu2(__vmaxu2(ordered_bf16x2(wv[0]), ordered_bf16x2(wv[1])),
+                                             __vmaxu2(ordered_bf16x2(wv[2]), ordered_bf16x2(wv[3])));
+                const uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
+                pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
+                if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
             }
         };
         tmem_ld_async<CW>(taddr, ra);
@@ -482,18 +512,23 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             copy_row_out(drow, p.logits_out + (int64_t)grow * p.E + c_beg, ng);
         // the k-th largest group maximum T bounds this half's top-k from
         // below (k groups hold a logit >= T); only groups whose maximum is
-        // >= T can hold a logit >= T
-        uint32_t a[kCandCap];
-#pragma unroll
-        for (int g = 0; g < kCandCap; ++g) a[g] = (g < ng) ? list[g * kTcBM + row] : 0u;
+        // >= T can hold a logit >= T. Group maxima are ordered 16-bit keys,
+        // two per word, so each of the k rounds works on 16 registers.
         uint32_t sel = 0;
         float T = -INFINITY;
         if (p.k <= ng) {
-            const uint32_t kth = kth_largest_key(a, p.k);
-            T = key_value(kth);
+            uint32_t pw[kCandCap / 2], po[kCandCap / 2];
 #pragma unroll
-            for (int g = 0; g < kCandCap; ++g)
-                sel |= (g < ng && key_value(list[g * kTcBM + row]) >= T) ? (1u << g) : 0u;
+            for (int i = 0; i < kCandCap / 2; ++i) po[i] = pw[i] = (2 * i < ng) ? list[i * kTcBM + row] : 0u;
+            const uint32_t t16 = kth_largest_packed(pw, p.k);
+            T = ordered16_value(t16);
+            const uint32_t ts = t16 | (t16 << 16);
+#pragma unroll
+            for (int i = 0; i < kCandCap / 2; ++i) {
+                const uint32_t ge = __vcmpgeu2(po[i], ts);
+                sel |= ((ge & 1u) << (2 * i)) | (((ge >> 16) & 1u) << (2 * i + 1));
+            }
+            sel &= (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);
         } else {
             sel = (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);  // fewer groups than k: all
         }
@@ -524,11 +559,13 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // 3. this half's top-k, in order, into the list column: k rounds of
         //    the largest remaining candidate key. A row whose candidates
         //    overflowed the list takes k passes over its rounded logits.
-        if (__builtin_expect(__any_sync(0xffffffffu, n > (uint32_t)kCandCap), 0)) {
+        if (__all_sync(0xffffffffu, n <= 16u)) {
+            topk_from_list<16>(list + row, n, p.k);  // the common case (~0.3% of rows exceed 16)
+        } else if (__builtin_expect(__any_sync(0xffffffffu, n > (uint32_t)kCandCap), 0)) {
             if (n > (uint32_t)kCandCap) topk_from_row(drow, ng, c_beg, p.k, list + row);
-            else topk_from_list(list + row, n, p.k);
+            else topk_from_list<kCandCap>(list + row, n, p.k);
         } else {
-            topk_from_list(list + row, n, p.k);
+            topk_from_list<kCandCap>(list + row, n, p.k);
         }
         __syncwarp();
     }
@@ -562,15 +599,27 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 sum += ev;
                 numer[r * kTcBM + row] = ev;
                 orow[r] = key_id(m);
-                if (count) atomicAdd(&h[key_id(m)], 1);
             }
-#pragma unroll 1
-            for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] / sum;
-            if (p.S) {
+            const float inv = 1.0f / sum;  // one division; each weight within 1.5 ulp of ev / sum
+#pragma unroll 4
+            for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] * inv;
+            if (count) {
+                // the row's experts, for the align behind the route: the top-k
+                // are the first i entries of this half's list and the first j
+                // of half 0's. All keys are loaded before the first atomic, so
+                // the atomics issue back to back (off the merge's chain).
+                uint32_t ks[kCandCap];
+#pragma unroll
+                for (int r = 0; r < kCandCap; ++r)
+                    ks[r] = (r < p.k) ? (r < i ? list[r * kTcBM + row] : list0[(r - i) * kTcBM + row]) : 0u;
+#pragma unroll
+                for (int r = 0; r < kCandCap; ++r)
+                    if (r < p.k) atomicAdd(&h[key_id(ks[r])], 1);
+            }
+            if (p.S) {  // (its count is the tile's number of rows, set below)
                 const float sh = s_hi + s_lo;
                 orow[p.k] = p.E;
                 wrow[p.k] = p.scale * sigmoid_stable(sh);
-                if (count) atomicAdd(&h[p.E], 1);
             }
         }
         __syncwarp();
@@ -578,10 +627,13 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             asm volatile("bar.sync 1, 128;" ::: "memory");  // the 4 warps of half 1
             const int E_al = p.E + p.S;
             for (int t = 0; t < kTcTileRows / kTcCountRows; ++t) {  // tiles that hold rows
-                if (m0 + t * kTcCountRows < p.M)
+                const int r0 = m0 + t * kTcCountRows;
+                if (r0 < p.M) {
+                    const int rows_t = min(kTcCountRows, p.M - r0);  // every row has one shared slot
                     for (int e = threadIdx.x - 128; e < E_al; e += 128)
                         p.tile_counts[(int64_t)(blockIdx.x * (kTcTileRows / kTcCountRows) + t) * E_al + e] =
-                            hist[t * E_al + e];
+                            (e == p.E) ? rows_t : hist[t * E_al + e];
+                }
             }
         }
         if (!(ok && got)) set_error(p.err, kErrWaitTimeout);

@@ -129,6 +129,20 @@ def test_shapes(smr, M, H, E, k, S):
     _full_check(smr, ri, 64)
 
 
+@pytest.mark.parametrize("M,H,E,k,S,zipf", [
+    (1000, 1024, 512, 10, 1, None),  # 11000 slots: the route counts 16 tiles, the last 40 rows
+    (777, 512, 256, 12, 0, 1.1),     # odd CTA count (7 tiles in 4 pairs), ragged tile, bias
+    (2049, 256, 128, 8, 1, None),    # 33 count tiles, last one a single row
+])
+def test_route_align_counts_from_route(smr, M, H, E, k, S, zipf):
+    """route_align above one CTA's align: the tcgen05 route writes each
+    64-row tile's expert counts and the align scans and scatters from them."""
+    ri = inputs.make_route_inputs(M, H, E, k, S, seed=M + E, zipf_s=zipf)
+    assert M * (k + S) > 8192
+    _full_check(smr, ri, 128)
+    assert smr.last_launch_count() == 3  # route + tile scan + tile scatter
+
+
 @pytest.mark.parametrize("M", [4, 40])
 def test_all_equal_logits_lowest_ids_win(smr, M):
     ri = inputs.make_route_inputs(M, 256, 128, 8, 1, seed=3)
