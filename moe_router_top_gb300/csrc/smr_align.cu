@@ -88,14 +88,22 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
     const int ec = min(e, a.E_al - 1);  // clamped: every load stays in bounds
     const int tpc = (ntiles + 31) / 32;
     const int t0 = min(c * tpc, ntiles), t1 = min(t0 + tpc, ntiles);
+    // one batch of 16 loads covers a chunk of up to 16 tiles (up to 512
+    // tiles); its values stay in registers for the second pass
+    int v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        v[j] = __ldg(a.tile_counts + (int64_t)min(t0 + j, ntiles - 1) * a.E_al + ec);
     int sum = 0;
-    for (int t = t0; t < t1; t += 16) {
-        int v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sum += (t0 + j < t1) ? v[j] : 0;
+    for (int t = t0 + 16; t < t1; t += 16) {  // longer chunks (more than 512 tiles)
+        int w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            v[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
+            w[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) sum += (t + j < t1) ? v[j] : 0;
+        for (int j = 0; j < 16; ++j) sum += (t + j < t1) ? w[j] : 0;
     }
     part[c][el] = sum;
     __syncthreads();
@@ -105,15 +113,20 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
         run += (q < c) ? x : 0;
         total += x;
     }
-    for (int t = t0; t < t1; t += 16) {  // same batches of 16 loads as above
-        int v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (t0 + j < t1 && e < a.E_al) a.tile_base[(int64_t)(t0 + j) * a.E_al + e] = run;
+        run += (t0 + j < t1) ? v[j] : 0;
+    }
+    for (int t = t0 + 16; t < t1; t += 16) {
+        int w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            v[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
+            w[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             if (t + j < t1 && e < a.E_al) a.tile_base[(int64_t)(t + j) * a.E_al + e] = run;
-            run += v[j];
+            run += (t + j < t1) ? w[j] : 0;
         }
     }
     if (c == 0 && e < a.E_al) a.totals[e] = total;
