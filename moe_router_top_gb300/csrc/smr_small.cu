@@ -48,7 +48,7 @@ constexpr int kSmallFrontWords = 4096;  // partials + cluster slots (16 KB), reu
 constexpr int kSmallMaxE = 1024;
 constexpr int kSmallBiasPerThread = kSmallMaxE / 256;
 static_assert(kSmallWarps * 256 + kSmallMaxCluster * 256 <= kSmallFrontWords, "partials + slots");
-static_assert(kSmallMaxM * 32 * 7 + 1 <= kSmallFrontWords, "tail arrays");
+static_assert(kSmallMaxM * 32 * 6 + 1 <= kSmallFrontWords, "tail arrays");
 
 struct SmallParams {
     SmallRouteLaunch a;
@@ -71,14 +71,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // Top-k of one token row in one warp, plus its shared slot. zrow: the
 // token's fp32 gate logits (E routed, then the shared one when S = 1);
 // bias_s: the routed experts' bias in shared memory (zeros without a bias).
-// Writes ids and weights of slots 0..width-1 to global memory and to
-// ids_s (the align input). The code is kept straight-line: it runs once per
+// Writes ids and weights of slots 0..width-1 to global memory and the
+// align's (expert << 10 | flat slot) keys to keys_s. The code is kept straight-line: it runs once per
 // call on whichever SM finishes last, where every taken jump into code the
 // instruction prefetcher has not reached costs a fetch from L2 or memory.
 template <int NK>
 __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, int k, float scale,
                                               const float *bias_s, uint16_t *logits_out,
-                                              int32_t *ids, float *wts, int32_t *ids_s) {
+                                              int32_t *ids, float *wts, uint32_t *keys_s, int flat0) {
     const int lane = threadIdx.x & 31;
     float z[NK];
     // every load issued before the first use (the shared logit with them);
@@ -131,46 +131,42 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
     if (lane < k + S) {
         ids[lane] = id;
         wts[lane] = wt;
-        ids_s[lane] = id;
+        keys_s[lane] = ((uint32_t)id << 10) | (uint32_t)(flat0 + lane);  // the align's key
     }
     __syncwarp();
 }
 
 // moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
 // moe_align block size", Purpose) for the n <= 512 ids of one small batch,
-// without a histogram or scan over all experts. Each id is keyed
-// (expert << 10 | position); two passes in which every thread compares its
-// key with all n keys (shared-memory broadcasts) give, per id: its rank in
-// the stable expert order, its expert's count and first rank, whether it is
-// the expert's first occurrence, and the padded offset of its expert (the
-// padded sizes of the experts below it). The first occurrence of each expert
-// records which blocks it owns; then each warp writes whole blocks
-// (coalesced): the ids' flat positions, the sentinel n up to the block end,
-// and the block's expert.
-__device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, int32_t *sorted,
+// without a histogram or scan over all experts. keys[i] = (expert << 10) | i
+// (written by the top-k; keys[n, n4) = ~0). Two passes in which every thread
+// compares its key with all n keys (shared-memory broadcasts, four loads in
+// flight) give, per id: its rank in the stable expert order, its expert's
+// count and first rank, whether it is the expert's first occurrence, and the
+// padded offset of its expert. The first occurrence of each expert describes
+// its blocks (expert, first sorted position, ids in the block); then each warp
+// writes whole blocks (coalesced): the ids' flat positions, the sentinel n up
+// to the block end, and the block's expert.
+__device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, int *sm, int32_t *sorted,
                                            int64_t sorted_cap, int32_t *expert_ids,
                                            int64_t expert_cap, int32_t *npp_out, uint32_t *err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kCap = kSmallMaxM * 32;
     const int n4 = (n + 3) & ~3;
-    uint32_t *keys = reinterpret_cast<uint32_t *>(ids);   // [n4], in place of the ids
     uint32_t *srt = reinterpret_cast<uint32_t *>(sm);     // [n] keys in ascending order
-    int *padv = sm + kCap;        // [n4] padded size of the id's expert at its first occurrence, else 0
-    int *cntv = padv + kCap;      // [n] count of the id's expert
-    int *ltv = cntv + kCap;       // [n] ids of lower experts = the expert's first rank
-    int *offv = ltv + kCap;       // [n] padded offset of the id's expert
-    int *owner = offv + kCap;     // [nblk] first-occurrence id owning each block
-    int *s_total = owner + kCap;
-    for (int i = tid; i < n4; i += kSmallThreads)
-        keys[i] = i < n ? ((uint32_t)ids[i] << 10) | (uint32_t)i : 0xFFFFFFFFu;
-    __syncwarp();
-    __syncthreads();
+    int *padv = sm + kCap;                               // [n4] padded size at a first occurrence, else 0
+    int *cntv = padv + kCap;                             // [n] count of the id's expert
+    int *ltv = cntv + kCap;                              // [n] the expert's first sorted rank
+    // [nblk] per block: expert (11 bits) | first sorted position << 11 (10
+    // bits) | ids in the block << 21 (<= 512)
+    uint32_t *binfo = reinterpret_cast<uint32_t *>(ltv + kCap);
+    int *s_total = reinterpret_cast<int *>(binfo + kCap);
     // pass 1 (ids i = tid, tid + 256): counts against every key
 #pragma unroll 1
     for (int i = tid; i < n4; i += kSmallThreads) {
         const uint32_t k = keys[i], e = k >> 10;
         int lt = 0, eq = 0, eqb = 0;
-#pragma unroll 1
+#pragma unroll 4
         for (int j = 0; j < n4; j += 4) {
             const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -189,12 +185,13 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
     }
     __syncwarp();
     __syncthreads();
-    // pass 2: padded offset of each id's expert; first occurrences claim blocks
+    // pass 2: padded offset of each id's expert; first occurrences describe
+    // their blocks
 #pragma unroll 1
     for (int i = tid; i < n4; i += kSmallThreads) {
         const uint32_t e = keys[i] >> 10;
         int off = 0, total = 0;
-#pragma unroll 1
+#pragma unroll 4
         for (int j = 0; j < n4; j += 4) {
             const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
             const int4 pv = *reinterpret_cast<const int4 *>(padv + j);
@@ -202,10 +199,11 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
                    ((v.z >> 10) < e ? pv.z : 0) + ((v.w >> 10) < e ? pv.w : 0);
             total += pv.x + pv.y + pv.z + pv.w;
         }
-        offv[i] = off;
-        const int pad = padv[i];
+        const int pad = padv[i], cnt = cntv[i], first = ltv[i];
+        const int b0 = off / A;
 #pragma unroll 1
-        for (int b = off / A; b < (off + pad) / A; ++b) owner[b] = i;
+        for (int u = 0; u * A < pad; ++u)
+            binfo[b0 + u] = e | ((uint32_t)(first + u * A) << 11) | ((uint32_t)min(A, cnt - u * A) << 21);
         if (i == 0) {
             *s_total = total;
             *npp_out = total;
@@ -216,16 +214,12 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
     const int nblk = *s_total / A;
 #pragma unroll 1
     for (int b = warp; b < nblk; b += kSmallWarps) {
-        const int i = owner[b];
-        const int cnt = cntv[i], first = ltv[i];
-        const int local0 = b * A - offv[i];
-        if (lane == 0) st_slot(expert_ids, b, expert_cap, (int32_t)(keys[i] >> 10), err);
-#pragma unroll 1
-        for (int u = lane; u < A; u += 32) {
-            const int local = local0 + u;
-            st_slot(sorted, (int64_t)b * A + u, sorted_cap,
-                    local < cnt ? (int32_t)(srt[first + local] & 1023u) : n, err);
-        }
+        const uint32_t bi = binfo[b];
+        const int be = (int)(bi & 2047u), bp = (int)((bi >> 11) & 1023u), bc = (int)(bi >> 21);
+        if (lane == 0) st_slot(expert_ids, b, expert_cap, be, err);
+#pragma unroll 2
+        for (int u = lane; u < A; u += 32)
+            st_slot(sorted, (int64_t)b * A + u, sorted_cap, u < bc ? (int32_t)(srt[bp + u] & 1023u) : n, err);
         __syncwarp();
     }
 }
@@ -234,7 +228,7 @@ __device__ __forceinline__ void align_tiny(int32_t *ids, int n, int A, int *sm, 
 // the top-k, 16 (E <= 512) or 32 (E <= 1024) -- one top-k per instance, so
 // the tail's code is laid out in the order it runs
 template <int NB, int NK>
-__global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallParams P) {
+__global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const SmallParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     const SmallRouteLaunch &p = P.a;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -363,21 +357,23 @@ __global__ void __launch_bounds__(kSmallThreads) small_route_kernel(const SmallP
 
     // ---- 4. tail: top-k + softmax + shared slot, one warp per token ----
     const int width = p.k + p.S;
-    int32_t *ids_s = reinterpret_cast<int32_t *>(smem);  // [M*width]
+    const int n = p.M * width, n4 = (n + 3) & ~3;
+    uint32_t *keys_s = reinterpret_cast<uint32_t *>(smem);  // [n4] the align's keys
     for (int m = warp; m < p.M; m += kSmallWarps) {
         const float *zrow = p.scratch + (int64_t)m * rows;
         uint16_t *lrow = p.logits_out ? p.logits_out + (int64_t)m * p.E : nullptr;
         int32_t *irow = p.ids + (int64_t)m * width;
         float *wrow = p.wts + (int64_t)m * width;
-        int32_t *srow = ids_s + m * width;
-        warp_topk_row<NK>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, srow);
+        warp_topk_row<NK>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, keys_s + m * width, m * width);
     }
     if (p.sorted == nullptr) return;
+    if (tid < n4 - n) keys_s[n + tid] = 0xFFFFFFFFu;  // padding keys sort last and match nothing
 
     // ---- 5. moe_align_block_size on the M*width ids of this call ----
+    __syncwarp();
     __syncthreads();
-    align_tiny(ids_s, p.M * width, p.A, ids_s + kSmallMaxM * 32, p.sorted, p.sorted_cap, p.expert_ids,
-               p.expert_cap, p.npp, &hdr->error);
+    align_tiny(keys_s, n, p.A, reinterpret_cast<int *>(keys_s + kSmallMaxM * 32), p.sorted, p.sorted_cap,
+               p.expert_ids, p.expert_cap, p.npp, &hdr->error);
 }
 
 template <int NB, int NK>
