@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
     s.off = off;
     s.scratch = scratch;
     const int npp = align_offsets(tot, E_al, a.A, s);
+    uint32_t bad = 0;
     for (int c0 = 0; c0 < n; c0 += kTileSub) {
         // the warp's four groups of 32 slots: ids and peer masks
         if (c0 > 0) load_ids(c0, e4);
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
             const int e = e4[g];
             if (e != kNoExpert)
                 st_slot(a.sorted, off[e] + wc[e] + __popc(pm[g] & lt), a.sorted_cap,
-                        beg + c0 + warp * 128 + g * 32 + lane, err);
+                        beg + c0 + warp * 128 + g * 32 + lane, bad);
             __syncwarp();
             if (e != kNoExpert && lane == __ffs(pm[g]) - 1) wc[e] += __popc(pm[g]);
             __syncwarp();
@@ -238,10 +239,11 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
         const int c = tot[e];
         if (c == 0) continue;  // warp-uniform
         const int o0 = off[e], o1 = off[e + 1];
-        for (int b = o0 / a.A + lane; b < o1 / a.A; b += 32) st_slot(a.expert_ids, b, a.expert_cap, e, err);
-        for (int q = o0 + c + lane; q < o1; q += 32) st_slot(a.sorted, q, a.sorted_cap, a.numel, err);
+        for (int b = o0 / a.A + lane; b < o1 / a.A; b += 32) st_slot(a.expert_ids, b, a.expert_cap, e, bad);
+        for (int q = o0 + c + lane; q < o1; q += 32) st_slot(a.sorted, q, a.sorted_cap, a.numel, bad);
         __syncwarp();
     }
+    report_bad_slots(bad, err);
     if (t == 0 && threadIdx.x == 0) *a.npp = npp;
 }
 

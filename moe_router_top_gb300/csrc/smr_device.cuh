@@ -419,11 +419,18 @@ __device__ __forceinline__ uint32_t peers_of(int v) {
 constexpr int kNoExpert = 2047;
 
 // Align output write, checked against the caller's array length: a position
-// outside it (only possible from a corrupted workspace) is skipped and flagged
-// instead of written.
-__device__ __forceinline__ void st_slot(int32_t *arr, int64_t pos, int64_t cap, int32_t v, uint32_t *err) {
-    if ((uint64_t)pos < (uint64_t)cap) arr[pos] = v;
-    else set_error(err, kErrBadSlot);
+// outside it (only possible from a corrupted workspace) is skipped and noted
+// in `bad` (a predicated store, no branch); the caller reports bad once.
+__device__ __forceinline__ void st_slot(int32_t *arr, int64_t pos, int64_t cap, int32_t v, uint32_t &bad) {
+    const uint32_t ok = (uint64_t)pos < (uint64_t)cap ? 1u : 0u;
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.global.b32 [%0], %1;\n}"
+                 ::"l"(arr + (ok ? pos : 0)), "r"(v), "r"(ok));
+    bad |= ok ^ 1u;
+}
+// Reports the bad-slot flag of a thread (rarely taken; the warp reconverges).
+__device__ __forceinline__ void report_bad_slots(uint32_t bad, uint32_t *err) {
+    if (bad) set_error(err, kErrBadSlot);
+    __syncwarp();
 }
 
 // Slots [warp*L, min((warp+1)*L, n)) belong to warp `warp`; L is a multiple of 32.
@@ -531,6 +538,7 @@ __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_a
     const int beg = warp * L, end = min(beg + L, n);
     int *wc = s.wcnt + warp * E_al;
     const uint32_t lt = lanemask_lt();
+    uint32_t bad = 0;
     for (int b = beg; b < end; b += 32) {
         const int i = b + lane;
         int e = (i < end) ? ids[i] : kNoExpert;
@@ -538,12 +546,13 @@ __device__ __forceinline__ void align_scatter(const int32_t *ids, int n, int E_a
         const uint32_t peers = peers_of(e);
         if (e != kNoExpert) {
             const int pos = s.off[e] + (use_base ? s.base[e] : 0) + wc[e] + __popc(peers & lt);
-            st_slot(sorted, pos, sorted_cap, flat0 + i, err);
+            st_slot(sorted, pos, sorted_cap, flat0 + i, bad);
         }
         __syncwarp();
         if (e != kNoExpert && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
         __syncwarp();
     }
+    report_bad_slots(bad, err);
 }
 
 // Padding and block owners, one thread per expert (experts first, first +
@@ -553,13 +562,16 @@ __device__ __forceinline__ void align_fill(int A, int E_al, const int *tot, cons
                                            int sentinel, int32_t *sorted, int64_t sorted_cap,
                                            int32_t *expert_ids, int64_t expert_cap, uint32_t *err,
                                            int first, int stride) {
+    uint32_t bad = 0;
     for (int e = first; e < E_al; e += stride) {
         const int c = tot[e];
         if (c == 0) continue;
         const int o0 = s.off[e], o1 = s.off[e + 1];
-        for (int b = o0 / A; b < o1 / A; ++b) st_slot(expert_ids, b, expert_cap, e, err);
-        for (int q = o0 + c; q < o1; ++q) st_slot(sorted, q, sorted_cap, sentinel, err);
+        for (int b = o0 / A; b < o1 / A; ++b) st_slot(expert_ids, b, expert_cap, e, bad);
+        for (int q = o0 + c; q < o1; ++q) st_slot(sorted, q, sorted_cap, sentinel, bad);
     }
+    __syncwarp();
+    report_bad_slots(bad, err);
 }
 
 // Copy n int32 ids from global memory to shared memory with 16-byte loads

@@ -139,18 +139,95 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
 // moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
 // moe_align block size", Purpose) for the n <= 512 ids of one small batch,
 // without a histogram or scan over all experts. keys[i] = (expert << 10) | i
-// (written by the top-k; keys[n, n4) = ~0). Two passes in which every thread
-// compares its key with all n keys (shared-memory broadcasts, four loads in
-// flight) give, per id: its rank in the stable expert order, its expert's
-// count and first rank, whether it is the expert's first occurrence, and the
-// padded offset of its expert. The first occurrence of each expert describes
-// its blocks (expert, first sorted position, ids in the block); then each warp
-// writes whole blocks (coalesced): the ids' flat positions, the sentinel n up
-// to the block end, and the block's expert.
+// (written by the top-k; keys[n, n4) = ~0). Two passes compare each id's key
+// with all n keys (shared-memory broadcasts; G = 8, 4, 2 or 1 consecutive
+// lanes share one id's scan and add their counts with shuffles) and give per
+// id: its rank in the stable expert order, its expert's count and first
+// rank, whether it is the expert's first occurrence, and the padded offset of
+// its expert. The first occurrence of each expert describes its blocks; then
+// each warp writes whole blocks (coalesced): the ids' flat positions, the
+// sentinel n up to the block end, and the block's expert.
+template <int G>
+__device__ __forceinline__ void align_tiny_passes(const uint32_t *keys, int n, int n4, int A, uint32_t *srt,
+                                                  int *padv, int *cntv, int *ltv, uint32_t *binfo,
+                                                  int *s_total, int32_t *npp_out) {
+    const int tid = threadIdx.x, sub = tid % G;
+    const int nv = n4 / 4;  // 4-key vectors
+    // pass 1: each id's counts against every key
+#pragma unroll 1
+    for (int i0 = 0; i0 < n4; i0 += kSmallThreads / G) {  // the same trip count in every lane
+        const int i = i0 + tid / G;
+        const bool act = i < n4;
+        const uint32_t k = act ? keys[i] : 0u, e = k >> 10;
+        int lt = 0, eq = 0, eqb = 0;
+#pragma unroll 4
+        for (int j = sub; j < nv; j += G) {
+            const uint4 v = reinterpret_cast<const uint4 *>(keys)[j];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                lt += (w[u] >> 10) < e;
+                eq += (w[u] >> 10) == e;
+                eqb += ((w[u] >> 10) == e) & (w[u] < k);
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+            lt += __shfl_xor_sync(0xffffffffu, lt, o);
+            eq += __shfl_xor_sync(0xffffffffu, eq, o);
+            eqb += __shfl_xor_sync(0xffffffffu, eqb, o);
+        }
+        if (act && sub == 0) {
+            const bool real = i < n;
+            if (real) srt[lt + eqb] = k;
+            padv[i] = (real && eqb == 0) ? (eq + A - 1) / A * A : 0;
+            cntv[i] = eq;
+            ltv[i] = lt;
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    // pass 2: padded offset of each id's expert; first occurrences describe
+    // their blocks
+#pragma unroll 1
+    for (int i0 = 0; i0 < n4; i0 += kSmallThreads / G) {
+        const int i = i0 + tid / G;
+        const bool act = i < n4;
+        const uint32_t e = act ? keys[i] >> 10 : 0u;
+        int off = 0, total = 0;
+#pragma unroll 4
+        for (int j = sub; j < nv; j += G) {
+            const uint4 v = reinterpret_cast<const uint4 *>(keys)[j];
+            const int4 pv = reinterpret_cast<const int4 *>(padv)[j];
+            off += ((v.x >> 10) < e ? pv.x : 0) + ((v.y >> 10) < e ? pv.y : 0) +
+                   ((v.z >> 10) < e ? pv.z : 0) + ((v.w >> 10) < e ? pv.w : 0);
+            total += pv.x + pv.y + pv.z + pv.w;
+        }
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+            off += __shfl_xor_sync(0xffffffffu, off, o);
+            total += __shfl_xor_sync(0xffffffffu, total, o);
+        }
+        if (act && sub == 0) {
+            const int pad = padv[i], cnt = cntv[i], first = ltv[i];
+            const int b0 = off / A;
+#pragma unroll 1
+            for (int u = 0; u * A < pad; ++u)
+                binfo[b0 + u] = e | ((uint32_t)(first + u * A) << 11) | ((uint32_t)min(A, cnt - u * A) << 21);
+            if (i == 0) {
+                *s_total = total;
+                *npp_out = total;
+            }
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+}
+
 __device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, int *sm, int32_t *sorted,
                                            int64_t sorted_cap, int32_t *expert_ids,
                                            int64_t expert_cap, int32_t *npp_out, uint32_t *err) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kCap = kSmallMaxM * 32;
     const int n4 = (n + 3) & ~3;
     uint32_t *srt = reinterpret_cast<uint32_t *>(sm);     // [n] keys in ascending order
@@ -161,67 +238,27 @@ __device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, i
     // bits) | ids in the block << 21 (<= 512)
     uint32_t *binfo = reinterpret_cast<uint32_t *>(ltv + kCap);
     int *s_total = reinterpret_cast<int *>(binfo + kCap);
-    // pass 1 (ids i = tid, tid + 256): counts against every key
-#pragma unroll 1
-    for (int i = tid; i < n4; i += kSmallThreads) {
-        const uint32_t k = keys[i], e = k >> 10;
-        int lt = 0, eq = 0, eqb = 0;
-#pragma unroll 4
-        for (int j = 0; j < n4; j += 4) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                lt += (w[u] >> 10) < e;
-                eq += (w[u] >> 10) == e;
-                eqb += ((w[u] >> 10) == e) & (w[u] < k);
-            }
-        }
-        const bool real = i < n;
-        if (real) srt[lt + eqb] = k;
-        padv[i] = (real && eqb == 0) ? (eq + A - 1) / A * A : 0;
-        cntv[i] = eq;
-        ltv[i] = lt;
-    }
-    __syncwarp();
-    __syncthreads();
-    // pass 2: padded offset of each id's expert; first occurrences describe
-    // their blocks
-#pragma unroll 1
-    for (int i = tid; i < n4; i += kSmallThreads) {
-        const uint32_t e = keys[i] >> 10;
-        int off = 0, total = 0;
-#pragma unroll 4
-        for (int j = 0; j < n4; j += 4) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(keys + j);
-            const int4 pv = *reinterpret_cast<const int4 *>(padv + j);
-            off += ((v.x >> 10) < e ? pv.x : 0) + ((v.y >> 10) < e ? pv.y : 0) +
-                   ((v.z >> 10) < e ? pv.z : 0) + ((v.w >> 10) < e ? pv.w : 0);
-            total += pv.x + pv.y + pv.z + pv.w;
-        }
-        const int pad = padv[i], cnt = cntv[i], first = ltv[i];
-        const int b0 = off / A;
-#pragma unroll 1
-        for (int u = 0; u * A < pad; ++u)
-            binfo[b0 + u] = e | ((uint32_t)(first + u * A) << 11) | ((uint32_t)min(A, cnt - u * A) << 21);
-        if (i == 0) {
-            *s_total = total;
-            *npp_out = total;
-        }
-    }
-    __syncwarp();
-    __syncthreads();
+    if (n4 <= kSmallThreads / 8)
+        align_tiny_passes<8>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
+    else if (n4 <= kSmallThreads / 4)
+        align_tiny_passes<4>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
+    else if (n4 <= kSmallThreads / 2)
+        align_tiny_passes<2>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
+    else
+        align_tiny_passes<1>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
     const int nblk = *s_total / A;
+    uint32_t bad = 0;
 #pragma unroll 1
     for (int b = warp; b < nblk; b += kSmallWarps) {
         const uint32_t bi = binfo[b];
         const int be = (int)(bi & 2047u), bp = (int)((bi >> 11) & 1023u), bc = (int)(bi >> 21);
-        if (lane == 0) st_slot(expert_ids, b, expert_cap, be, err);
+        st_slot(expert_ids, lane == 0 ? b : -1, expert_cap, be, bad);  // lane 0 only (-1 is skipped)
+        bad &= lane == 0 ? 1u : 0u;
 #pragma unroll 2
         for (int u = lane; u < A; u += 32)
-            st_slot(sorted, (int64_t)b * A + u, sorted_cap, u < bc ? (int32_t)(srt[bp + u] & 1023u) : n, err);
-        __syncwarp();
+            st_slot(sorted, (int64_t)b * A + u, sorted_cap, u < bc ? (int32_t)(srt[bp + u] & 1023u) : n, bad);
     }
+    report_bad_slots(bad, err);
 }
 
 // NB: blocks of 8 tokens, 1 (M <= 8) or 2 (M <= 16); NK: keys per lane in
