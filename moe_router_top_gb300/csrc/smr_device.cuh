@@ -427,6 +427,15 @@ __device__ __forceinline__ void st_slot(int32_t *arr, int64_t pos, int64_t cap, 
                  ::"l"(arr + (ok ? pos : 0)), "r"(v), "r"(ok));
     bad |= ok ^ 1u;
 }
+// Four consecutive slots [pos, pos + 4) in one 16-byte store (arr + pos must
+// be 16-byte aligned); all four are skipped and noted in `bad` unless the
+// last is below cap.
+__device__ __forceinline__ void st_slot4(int32_t *arr, int64_t pos, int64_t cap, int4 v, uint32_t &bad) {
+    const uint32_t ok = (uint64_t)pos + 3u < (uint64_t)cap ? 1u : 0u;
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %5, 0;\n @q st.global.v4.b32 [%0], {%1, %2, %3, %4};\n}"
+                 ::"l"(arr + (ok ? pos : 0)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(ok));
+    bad |= ok ^ 1u;
+}
 // Reports the bad-slot flag of a thread (rarely taken; the warp reconverges).
 __device__ __forceinline__ void report_bad_slots(uint32_t bad, uint32_t *err) {
     if (bad) set_error(err, kErrBadSlot);

@@ -86,6 +86,10 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
 #pragma unroll
     for (int i = 0; i < NK; ++i) z[i] = __ldcg(zrow + min(lane + 32 * i, E - 1));
     const float sv = __ldcg(zrow + E - 1 + S);
+    // a scheduling fence: without it the compiler interleaves the loads with
+    // the key building below and their latencies add up (measured: 4.7 us
+    // instead of 2.0 us for one token's top-k)
+    __syncwarp();
     uint32_t key[NK];
 #pragma unroll
     for (int i = 0; i < NK; ++i) {
@@ -107,10 +111,14 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
     uint32_t mine = 0u, first = 0u;
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
-        uint32_t lm = key[0];
+        uint32_t lm[NK / 2];  // a tree: depth log2(NK) instead of a chain of NK - 1
 #pragma unroll
-        for (int i = 1; i < NK; ++i) lm = max(lm, key[i]);
-        const uint32_t gmax = __reduce_max_sync(0xffffffffu, lm);
+        for (int i = 0; i < NK / 2; ++i) lm[i] = max(key[i], key[i + NK / 2]);
+#pragma unroll
+        for (int h = NK / 4; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) lm[i] = max(lm[i], lm[i + h]);
+        const uint32_t gmax = __reduce_max_sync(0xffffffffu, lm[0]);
         first = (r == 0) ? gmax : first;
         mine = (lane == r) ? gmax : mine;
 #pragma unroll
@@ -246,17 +254,29 @@ __device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, i
         align_tiny_passes<2>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
     else
         align_tiny_passes<1>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
-    const int nblk = *s_total / A;
+    // the blocks' experts, then every slot of sorted_token_ids: the slots of
+    // all blocks form one flat range that the CTA writes 4 slots per thread
+    // and step (16-byte stores when A is a multiple of 4 and the array is
+    // 16-byte aligned); slot u of block b holds the u-th id of its expert's
+    // run in the block, or the sentinel n past the run
+    const int npp = *s_total, nblk = npp / A;
     uint32_t bad = 0;
+    for (int b = threadIdx.x; b < nblk; b += kSmallThreads)
+        st_slot(expert_ids, b, expert_cap, (int)(binfo[b] & 2047u), bad);
+    const bool vec = (A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0;
+    const int step = vec ? 4 : 1;
 #pragma unroll 1
-    for (int b = warp; b < nblk; b += kSmallWarps) {
+    for (int q = threadIdx.x * step; q < npp; q += kSmallThreads * step) {
+        const int b = q / A, u = q - b * A;
         const uint32_t bi = binfo[b];
-        const int be = (int)(bi & 2047u), bp = (int)((bi >> 11) & 1023u), bc = (int)(bi >> 21);
-        st_slot(expert_ids, lane == 0 ? b : -1, expert_cap, be, bad);  // lane 0 only (-1 is skipped)
-        bad &= lane == 0 ? 1u : 0u;
-#pragma unroll 2
-        for (int u = lane; u < A; u += 32)
-            st_slot(sorted, (int64_t)b * A + u, sorted_cap, u < bc ? (int32_t)(srt[bp + u] & 1023u) : n, bad);
+        const int bp = (int)((bi >> 11) & 1023u) + u, bc = (int)(bi >> 21) - u;
+        int v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = j < bc ? (int)(srt[bp + min(j, bc - 1)] & 1023u) : n;
+        if (vec)
+            st_slot4(sorted, q, sorted_cap, make_int4(v[0], v[1], v[2], v[3]), bad);
+        else
+            st_slot(sorted, q, sorted_cap, v[0], bad);
     }
     report_bad_slots(bad, err);
 }
