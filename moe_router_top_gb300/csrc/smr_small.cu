@@ -48,7 +48,8 @@ constexpr int kSmallFrontWords = 4096;  // partials + cluster slots (16 KB), reu
 constexpr int kSmallMaxE = 1024;
 constexpr int kSmallBiasPerThread = kSmallMaxE / 256;
 static_assert(kSmallWarps * 256 + kSmallMaxCluster * 256 <= kSmallFrontWords, "partials + slots");
-static_assert(kSmallMaxM * 32 * 6 + 1 <= kSmallFrontWords, "tail arrays");
+static_assert(kSmallMaxM * 32 * 3 + 32 <= kSmallFrontWords, "tail arrays");
+static_assert(kSmallMaxM * 32 <= 2 * kSmallThreads, "two ranks per thread in the align");
 
 struct SmallParams {
     SmallRouteLaunch a;
@@ -147,136 +148,162 @@ __device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, i
 // moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
 // moe_align block size", Purpose) for the n <= 512 ids of one small batch,
 // without a histogram or scan over all experts. keys[i] = (expert << 10) | i
-// (written by the top-k; keys[n, n4) = ~0). Two passes compare each id's key
-// with all n keys (shared-memory broadcasts; G = 8, 4, 2 or 1 consecutive
-// lanes share one id's scan and add their counts with shuffles) and give per
-// id: its rank in the stable expert order, its expert's count and first
-// rank, whether it is the expert's first occurrence, and the padded offset of
-// its expert. The first occurrence of each expert describes its blocks; then
-// each warp writes whole blocks (coalesced): the ids' flat positions, the
-// sentinel n up to the block end, and the block's expert.
+// (written by the top-k; keys[n, n4) = ~0) are unique, and their ascending
+// order is the stable expert order the alignment lists ids in, so:
+//  1. each id's rank = the number of keys below its key (G = 8, 4, 2 or 1
+//     consecutive lanes share one id's count and add it with shuffles), and
+//     the sorted keys go to srt[rank];
+//  2. every thread takes H ranks (r = tid, tid + 256): a rank starts an
+//     expert's run when its expert differs from the previous rank's; the run
+//     ends at the next start (ballots of the starts, one 32-bit word per 32
+//     ranks); a start carries its run's padded size ceil(cnt / A) * A, whose
+//     exclusive prefix over ranks (warp scans plus the totals of the earlier
+//     words) is the run's offset in sorted_token_ids; the start writes its
+//     blocks' records;
+//  3. the CTA writes every slot of the blocks as one flat range, 4 slots per
+//     thread and step.
+// A single warp's instruction stream, not the amount of work, bounds this at
+// these sizes, so every step is spread over all warps.
 template <int G>
-__device__ __forceinline__ void align_tiny_passes(const uint32_t *keys, int n, int n4, int A, uint32_t *srt,
-                                                  int *padv, int *cntv, int *ltv, uint32_t *binfo,
-                                                  int *s_total, int32_t *npp_out) {
-    const int tid = threadIdx.x, sub = tid % G;
-    const int nv = n4 / 4;  // 4-key vectors
-    // pass 1: each id's counts against every key
+__device__ __forceinline__ void align_tiny_rank(const uint32_t *keys, int n, int n4, uint32_t *srt) {
+    const int tid = threadIdx.x, sub = tid % G, nv = n4 / 4;
 #pragma unroll 1
-    for (int i0 = 0; i0 < n4; i0 += kSmallThreads / G) {  // the same trip count in every lane
+    for (int i0 = 0; i0 < n4; i0 += kSmallThreads / G) {  // one pass when G >= 2
         const int i = i0 + tid / G;
-        const bool act = i < n4;
-        const uint32_t k = act ? keys[i] : 0u, e = k >> 10;
-        int lt = 0, eq = 0, eqb = 0;
+        const uint32_t k = keys[min(i, n4 - 1)];
+        int r = 0;
 #pragma unroll 4
         for (int j = sub; j < nv; j += G) {
             const uint4 v = reinterpret_cast<const uint4 *>(keys)[j];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                lt += (w[u] >> 10) < e;
-                eq += (w[u] >> 10) == e;
-                eqb += ((w[u] >> 10) == e) & (w[u] < k);
-            }
+            r += (v.x < k) + (v.y < k) + (v.z < k) + (v.w < k);
         }
 #pragma unroll
-        for (int o = 1; o < G; o <<= 1) {
-            lt += __shfl_xor_sync(0xffffffffu, lt, o);
-            eq += __shfl_xor_sync(0xffffffffu, eq, o);
-            eqb += __shfl_xor_sync(0xffffffffu, eqb, o);
-        }
-        if (act && sub == 0) {
-            const bool real = i < n;
-            if (real) srt[lt + eqb] = k;
-            padv[i] = (real && eqb == 0) ? (eq + A - 1) / A * A : 0;
-            cntv[i] = eq;
-            ltv[i] = lt;
-        }
+        for (int o = 1; o < G; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (i < n && sub == 0) srt[r] = k;
         __syncwarp();
     }
-    __syncthreads();
-    // pass 2: padded offset of each id's expert; first occurrences describe
-    // their blocks
-#pragma unroll 1
-    for (int i0 = 0; i0 < n4; i0 += kSmallThreads / G) {
-        const int i = i0 + tid / G;
-        const bool act = i < n4;
-        const uint32_t e = act ? keys[i] >> 10 : 0u;
-        int off = 0, total = 0;
-#pragma unroll 4
-        for (int j = sub; j < nv; j += G) {
-            const uint4 v = reinterpret_cast<const uint4 *>(keys)[j];
-            const int4 pv = reinterpret_cast<const int4 *>(padv)[j];
-            off += ((v.x >> 10) < e ? pv.x : 0) + ((v.y >> 10) < e ? pv.y : 0) +
-                   ((v.z >> 10) < e ? pv.z : 0) + ((v.w >> 10) < e ? pv.w : 0);
-            total += pv.x + pv.y + pv.z + pv.w;
-        }
-#pragma unroll
-        for (int o = 1; o < G; o <<= 1) {
-            off += __shfl_xor_sync(0xffffffffu, off, o);
-            total += __shfl_xor_sync(0xffffffffu, total, o);
-        }
-        if (act && sub == 0) {
-            const int pad = padv[i], cnt = cntv[i], first = ltv[i];
-            const int b0 = off / A;
-#pragma unroll 1
-            for (int u = 0; u * A < pad; ++u)
-                binfo[b0 + u] = e | ((uint32_t)(first + u * A) << 11) | ((uint32_t)min(A, cnt - u * A) << 21);
-            if (i == 0) {
-                *s_total = total;
-                *npp_out = total;
-            }
-        }
-        __syncwarp();
-    }
-    __syncthreads();
 }
 
-__device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, int *sm, int32_t *sorted,
+template <int H>
+__device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, uint32_t *sm, int32_t *sorted,
                                            int64_t sorted_cap, int32_t *expert_ids,
                                            int64_t expert_cap, int32_t *npp_out, uint32_t *err) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kCap = kSmallMaxM * 32;
+    constexpr int NW = kSmallWarps * H;  // 32-rank words
     const int n4 = (n + 3) & ~3;
-    uint32_t *srt = reinterpret_cast<uint32_t *>(sm);     // [n] keys in ascending order
-    int *padv = sm + kCap;                               // [n4] padded size at a first occurrence, else 0
-    int *cntv = padv + kCap;                             // [n] count of the id's expert
-    int *ltv = cntv + kCap;                              // [n] the expert's first sorted rank
+    uint32_t *srt = sm;                   // [n] keys by rank
     // [nblk] per block: expert (11 bits) | first sorted position << 11 (10
     // bits) | ids in the block << 21 (<= 512)
-    uint32_t *binfo = reinterpret_cast<uint32_t *>(ltv + kCap);
-    int *s_total = reinterpret_cast<int *>(binfo + kCap);
+    uint32_t *binfo = sm + kCap;
+    uint32_t *starts = binfo + kCap;                      // [NW] ballots of the run starts
+    int *wtot = reinterpret_cast<int *>(starts + 16);     // [NW] padded sizes per word
     if (n4 <= kSmallThreads / 8)
-        align_tiny_passes<8>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
+        align_tiny_rank<8>(keys, n, n4, srt);
     else if (n4 <= kSmallThreads / 4)
-        align_tiny_passes<4>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
+        align_tiny_rank<4>(keys, n, n4, srt);
     else if (n4 <= kSmallThreads / 2)
-        align_tiny_passes<2>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
+        align_tiny_rank<2>(keys, n, n4, srt);
     else
-        align_tiny_passes<1>(keys, n, n4, A, srt, padv, cntv, ltv, binfo, s_total, npp_out);
-    // the blocks' experts, then every slot of sorted_token_ids: the slots of
-    // all blocks form one flat range that the CTA writes 4 slots per thread
-    // and step (16-byte stores when A is a multiple of 4 and the array is
-    // 16-byte aligned); slot u of block b holds the u-th id of its expert's
-    // run in the block, or the sentinel n past the run
-    const int npp = *s_total, nblk = npp / A;
-    uint32_t bad = 0;
-    for (int b = threadIdx.x; b < nblk; b += kSmallThreads)
-        st_slot(expert_ids, b, expert_cap, (int)(binfo[b] & 2047u), bad);
-    const bool vec = (A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0;
-    const int step = vec ? 4 : 1;
-#pragma unroll 1
-    for (int q = threadIdx.x * step; q < npp; q += kSmallThreads * step) {
-        const int b = q / A, u = q - b * A;
-        const uint32_t bi = binfo[b];
-        const int bp = (int)((bi >> 11) & 1023u) + u, bc = (int)(bi >> 21) - u;
-        int v[4];
+        align_tiny_rank<1>(keys, n, n4, srt);
+    __syncthreads();
+    const bool pow2 = (A & (A - 1)) == 0;
+    const int lgA = __ffs(A) - 1;
+    const int nw = (n + 31) >> 5;  // words holding ranks
+    uint32_t s[H];
+    bool f[H];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = j < bc ? (int)(srt[bp + min(j, bc - 1)] & 1023u) : n;
-        if (vec)
+    for (int h = 0; h < H; ++h) {
+        const int r = tid + h * kSmallThreads;
+        s[h] = srt[min(r, n - 1)];
+        const uint32_t prev = srt[max(min(r, n - 1) - 1, 0)];
+        f[h] = r < n && (r == 0 || (s[h] >> 10) != (prev >> 10));
+        const uint32_t m = __ballot_sync(0xffffffffu, f[h]);
+        if (lane == 0) starts[warp + h * kSmallWarps] = m;
+    }
+    __syncthreads();
+    uint32_t mk[NW];
+#pragma unroll
+    for (int w = 0; w < NW; w += 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(starts + w);
+        mk[w] = v.x; mk[w + 1] = v.y; mk[w + 2] = v.z; mk[w + 3] = v.w;
+    }
+    int pad[H], cnt[H], inc[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int wd = warp + h * kSmallWarps, r = tid + h * kSmallThreads;
+        // the next run start after rank r: a later bit of this word, else the
+        // first start of a later word, else n
+        const uint32_t later = lane == 31 ? 0u : starts[wd] & ~((2u << lane) - 1u);
+        int nxt = n;
+#pragma unroll
+        for (int w = NW - 1; w >= 0; --w)
+            nxt = (w > wd && w < nw && mk[w] != 0u) ? w * 32 + __ffs(mk[w]) - 1 : nxt;
+        nxt = later ? wd * 32 + __ffs(later) - 1 : nxt;
+        cnt[h] = nxt - r;
+        pad[h] = f[h] ? (pow2 ? ((cnt[h] + A - 1) >> lgA) << lgA : (cnt[h] + A - 1) / A * A) : 0;
+        inc[h] = pad[h];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc[h], o);
+            inc[h] += lane >= o ? v : 0;
+        }
+        if (lane == 31) wtot[wd] = inc[h];
+    }
+    __syncthreads();
+    int wt[NW];
+#pragma unroll
+    for (int w = 0; w < NW; w += 4) {
+        const int4 v = *reinterpret_cast<const int4 *>(wtot + w);
+        wt[w] = v.x; wt[w + 1] = v.y; wt[w + 2] = v.z; wt[w + 3] = v.w;
+    }
+    int npp = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) npp += (w < nw) ? wt[w] : 0;
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int wd = warp + h * kSmallWarps;
+        int off = inc[h] - pad[h];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) off += (w < wd) ? wt[w] : 0;
+        if (pad[h]) {
+            const int r = tid + h * kSmallThreads;
+            const uint32_t e = s[h] >> 10;
+            const int b0 = pow2 ? off >> lgA : off / A;
+            binfo[b0] = e | ((uint32_t)r << 11) | ((uint32_t)min(A, cnt[h]) << 21);
+            for (int u = 1; u * A < pad[h]; ++u)  // an expert with more than A ids
+                binfo[b0 + u] = e | ((uint32_t)(r + u * A) << 11) | ((uint32_t)min(A, cnt[h] - u * A) << 21);
+        }
+    }
+    if (tid == 0) *npp_out = npp;
+    __syncthreads();
+    // the blocks' experts, then every slot of sorted_token_ids: slot u of
+    // block b holds the u-th id of its expert's run in the block, or the
+    // sentinel n past the run (16-byte stores when A is a multiple of 4 and
+    // the array is 16-byte aligned)
+    const int nblk = pow2 ? npp >> lgA : npp / A;
+    uint32_t bad = 0;
+    for (int b = tid; b < nblk; b += kSmallThreads)
+        st_slot(expert_ids, b, expert_cap, (int)(binfo[b] & 2047u), bad);
+    if ((A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0) {
+#pragma unroll 2
+        for (int q = tid * 4; q < npp; q += kSmallThreads * 4) {
+            const int b = pow2 ? q >> lgA : q / A, u = q - b * A;
+            const uint32_t bi = binfo[b];
+            const int bp = (int)((bi >> 11) & 1023u) + u, bc = (int)(bi >> 21) - u;
+            int v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = j < bc ? (int)(srt[bp + min(j, bc - 1)] & 1023u) : n;
             st_slot4(sorted, q, sorted_cap, make_int4(v[0], v[1], v[2], v[3]), bad);
-        else
-            st_slot(sorted, q, sorted_cap, v[0], bad);
+        }
+    } else {
+        for (int q = tid; q < npp; q += kSmallThreads) {
+            const int b = q / A, u = q - b * A;
+            const uint32_t bi = binfo[b];
+            const int bc = (int)(bi >> 21);
+            st_slot(sorted, q, sorted_cap,
+                    u < bc ? (int)(srt[(int)((bi >> 11) & 1023u) + min(u, bc - 1)] & 1023u) : n, bad);
+        }
     }
     report_bad_slots(bad, err);
 }
@@ -429,8 +456,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     // ---- 5. moe_align_block_size on the M*width ids of this call ----
     __syncwarp();
     __syncthreads();
-    align_tiny(keys_s, n, p.A, reinterpret_cast<int *>(keys_s + kSmallMaxM * 32), p.sorted, p.sorted_cap,
-               p.expert_ids, p.expert_cap, p.npp, &hdr->error);
+    if (n <= kSmallThreads)
+        align_tiny<1>(keys_s, n, p.A, keys_s + kSmallMaxM * 32, p.sorted, p.sorted_cap, p.expert_ids,
+                      p.expert_cap, p.npp, &hdr->error);
+    else
+        align_tiny<2>(keys_s, n, p.A, keys_s + kSmallMaxM * 32, p.sorted, p.sorted_cap, p.expert_ids,
+                      p.expert_cap, p.npp, &hdr->error);
 }
 
 template <int NB, int NK>
