@@ -13,7 +13,11 @@
 //    inside it (a prefix over tiles) and its total; then per tile the padded
 //    expert offsets (block scan of the totals), the stable scatter of the
 //    tile's slots, and the padding rows and block owners of a share of the
-//    experts.
+//    experts;
+//  - behind the tcgen05 route the counts come from the route's epilogue (one
+//    tile per 64 token rows), and the scatter ranks a slot among its
+//    expert's slots by the tile rows that hold the expert (each row holds an
+//    expert at most once).
 #include "smr_device.cuh"
 #include "smr_launch.h"
 
@@ -247,12 +251,95 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
     if (t == 0 && threadIdx.x == 0) *a.npp = npp;
 }
 
+// 3'. Behind the tcgen05 route, whose tiles are kTcCountRows token rows of
+//    `width` slots with distinct experts in each row: the rank of a slot
+//    among its expert's slots in the tile is the number of earlier rows of
+//    the tile that hold the expert, read from a per-expert 64-bit mask of
+//    rows (shared-memory atomicOr). Then as above: padded offsets, the
+//    scatter to off[e] + (tile start in e) + rank, and the padding rows and
+//    block owners of a share of the experts.
+constexpr int kRowsMaxSlots = 8;  // slots per thread: kTcCountRows * 32 / kTileThreads
+static_assert(kTcCountRows == 64, "two mask words per expert");
+static_assert(kTcCountRows * 32 <= kRowsMaxSlots * kTileThreads, "a tile of width 32");
+__global__ void __launch_bounds__(kTileThreads) align_rows_scatter_kernel(const AlignLaunch a, int width) {
+    extern __shared__ __align__(16) int sm[];
+    uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
+    const int E_al = a.E_al, tid = threadIdx.x;
+    uint32_t *mask = reinterpret_cast<uint32_t *>(sm);  // [E_al][2] the tile's rows holding each expert
+    int *base = sm + 2 * E_al;                          // [E_al] this tile's start inside each expert
+    int *tot = base + E_al;                             // [E_al] expert totals
+    int *off = tot + E_al;                              // [E_al + 1] padded expert offsets
+    int *scratch = off + E_al + 1;                      // [32]
+    const int t = blockIdx.x, ntiles = gridDim.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = kTcCountRows * width;
+    const int beg = t * tile, n = min(beg + tile, a.numel) - beg;
+    griddep_wait();  // the tile starts and totals come from the previous kernel
+    int ev[kRowsMaxSlots];
+#pragma unroll
+    for (int j = 0; j < kRowsMaxSlots; ++j) ev[j] = __ldg(a.ids + beg + min(tid + j * kTileThreads, n - 1));
+    constexpr int kPerThread = (kMaxExpertsAl + kTileThreads - 1) / kTileThreads;
+    int bse[kPerThread], tt[kPerThread];
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int e = min(tid + j * kTileThreads, E_al - 1);
+        bse[j] = __ldg(a.tile_base + (int64_t)t * E_al + e);
+        tt[j] = __ldg(a.totals + e);
+    }
+    for (int q = tid; q < 2 * E_al; q += kTileThreads) mask[q] = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int e = tid + j * kTileThreads;
+        if (e < E_al) {
+            base[e] = bse[j];
+            tot[e] = tt[j];
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+    int rw[kRowsMaxSlots];  // the slot's row in the tile, or -1
+#pragma unroll
+    for (int j = 0; j < kRowsMaxSlots; ++j) {
+        const int i = tid + j * kTileThreads;
+        const bool in = i < n, ok = in && (unsigned)ev[j] < (unsigned)E_al;
+        if (in && !ok) set_error(err, kErrBadId);
+        rw[j] = ok ? i / width : -1;
+        if (ok) atomicOr(&mask[2 * ev[j] + (rw[j] >> 5)], 1u << (rw[j] & 31));
+    }
+    __syncwarp();
+    AlignSmem s;
+    s.off = off;
+    s.scratch = scratch;
+    const int npp = align_offsets(tot, E_al, a.A, s);  // ends with a CTA barrier: the masks are complete
+    uint32_t bad = 0;
+#pragma unroll
+    for (int j = 0; j < kRowsMaxSlots; ++j) {
+        if (rw[j] >= 0) {
+            const int e = ev[j], r = rw[j];
+            const uint32_t m0 = mask[2 * e], m1 = mask[2 * e + 1];
+            const int rank = r < 32 ? __popc(m0 & ((1u << r) - 1u))
+                                    : __popc(m0) + __popc(m1 & ((1u << (r - 32)) - 1u));
+            st_slot(a.sorted, off[e] + base[e] + rank, a.sorted_cap, beg + tid + j * kTileThreads, bad);
+        }
+    }
+    __syncwarp();
+    for (int e = t + warp * ntiles; e < E_al; e += kTileWarps * ntiles) {
+        const int c = tot[e];
+        if (c == 0) continue;  // warp-uniform
+        const int o0 = off[e], o1 = off[e + 1];
+        for (int b = o0 / a.A + lane; b < o1 / a.A; b += 32) st_slot(a.expert_ids, b, a.expert_cap, e, bad);
+        for (int q = o0 + c + lane; q < o1; q += 32) st_slot(a.sorted, q, a.sorted_cap, a.numel, bad);
+        __syncwarp();
+    }
+    report_bad_slots(bad, err);
+    if (t == 0 && tid == 0) *a.npp = npp;
+}
+
 // Once per kernel and device: the dynamic shared-memory limit and the largest
 // shared-memory carveout. Every kernel of the library asks for the same
 // carveout, so consecutive launches (route, then align) do not reconfigure
 // the SMs' L1/shared split in between.
 static cudaError_t configure(const void *kern, int slot, size_t bytes) {
-    static bool done[4][64] = {};
+    static bool done[5][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !done[slot][dev]) {
@@ -311,6 +398,13 @@ cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream) {
     if ((e = configure((const void *)align_tile_scan_kernel, 3, 0)) != cudaSuccess) return e;
     e = launch_dependent(align_tile_scan_kernel, (a.E_al + 31) / 32, 1024, 0, stream, a, ntiles);
     if (e != cudaSuccess) return e;
+    if (a.counted_tile > 0) {  // route tiles: kTcCountRows rows of counted_tile / kTcCountRows slots
+        const size_t smem = (size_t)(5 * a.E_al + 1 + 32) * 4;
+        const size_t smem_max = (size_t)(5 * kMaxExpertsAl + 1 + 32) * 4;
+        if ((e = configure((const void *)align_rows_scatter_kernel, 4, smem_max)) != cudaSuccess) return e;
+        return launch_dependent(align_rows_scatter_kernel, ntiles, kTileThreads, smem, stream, a,
+                                a.counted_tile / kTcCountRows);
+    }
     const size_t smem = (size_t)((kTileWarps + 3) * a.E_al + 1 + 32) * 4;
     const size_t smem_max = (size_t)((kTileWarps + 3) * kMaxExpertsAl + 1 + 32) * 4;
     if ((e = configure((const void *)align_tile_scatter_kernel, 1, smem_max)) != cudaSuccess) return e;
