@@ -81,8 +81,9 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_count_kernel(const Al
 
 // 2. For 32 experts per CTA: every tile's start inside each expert (exclusive
 //    prefix over tiles, in tile order) and each expert's total. Thread
-//    (expert el, chunk c) adds a contiguous run of tiles; the 32 chunk sums
-//    are combined in chunk order.
+//    (expert el, chunk c) adds a contiguous run of tiles (coalesced over the
+//    experts); the 32 chunk sums of an expert are then scanned by one warp
+//    (lane = chunk) with shuffles.
 __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch a, int ntiles) {
     __shared__ int part[32][33];
     const int el = threadIdx.x & 31, c = threadIdx.x >> 5;
@@ -111,12 +112,23 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
     }
     part[c][el] = sum;
     __syncthreads();
-    int run = 0, total = 0;
-    for (int q = 0; q < 32; ++q) {
-        const int x = part[q][el];
-        run += (q < c) ? x : 0;
-        total += x;
+    {
+        // warp w scans expert w's column over the 32 chunks (lane = chunk):
+        // exclusive prefix in place, the total in the extra column
+        const int w = c, q = el;  // this thread's role in the transposed scan
+        const int x = part[q][w];
+        int inc = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            inc += q >= o ? y : 0;
+        }
+        part[q][w] = inc - x;
+        if (q == 31) part[w][32] = inc;
     }
+    __syncthreads();
+    int run = part[c][el];
+    const int total = part[el][32];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         if (t0 + j < t1 && e < a.E_al) a.tile_base[(int64_t)(t0 + j) * a.E_al + e] = run;
