@@ -237,7 +237,7 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
         L.ids = a->topk_ids;
         L.wts = a->topk_weights;
         L.logits_out = a->logits_out;
-        L.scratch = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kHeaderBytes);
+        L.scratch = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kHeaderBytes);
         L.hdr = ws;
         if (fused_align) {
             L.A = effective_block_size(fused_align);

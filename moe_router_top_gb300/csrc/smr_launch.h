@@ -19,7 +19,7 @@ struct SmallRouteLaunch {
     int32_t *ids;
     float *wts;
     uint16_t *logits_out;
-    float *scratch;        // workspace: [M][E+S] fp32 gate logits
+    uint32_t *scratch;     // workspace: [M][E] selection keys of the routed logits (<= M*(E+S) words)
     void *hdr;             // workspace header (WsHeader)
     // fused align (sorted == nullptr: route only)
     int A;
@@ -30,7 +30,7 @@ struct SmallRouteLaunch {
 };
 constexpr int kSmallMaxM = 16;
 // Number of K ranges the gate rows are split into (the CTAs of one cluster);
-// the scratch holds M * (E + S) fp32 gate logits.
+// the scratch holds the M * E selection keys of the routed logits (sized M * (E + S) words).
 int small_route_k_ranges(int E, int S, int H);
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream);
 // Fixed scratch in device memory (no allocation): capacity, and its device

@@ -46,14 +46,23 @@ constexpr int kMaxSlicesPerWarp = 4;  // slices whose loads are in flight at onc
 constexpr int kSmallMaxCluster = 8;   // K ranges per row group = CTAs per cluster (portable size)
 constexpr int kSmallFrontWords = 4096;  // partials + cluster slots (16 KB), reused by the tail
 constexpr int kSmallMaxE = 1024;
-constexpr int kSmallBiasPerThread = kSmallMaxE / 256;
+// The tail's arrays after the front words: the tokens of each expert (bit m
+// for token m, E + S <= 1025 words) and the touched-expert bitmap.
+constexpr int kSmallMaskWords = 1028;
+constexpr int kSmallBitWords = 36;
+constexpr int kSmallSmemWords = kSmallFrontWords + kSmallMaskWords + kSmallBitWords;
+static_assert(kSmallMaxE + 1 <= kSmallMaskWords && (kSmallMaxE + 32) / 32 <= kSmallBitWords, "mask arrays");
+static_assert(kSmallMaxM <= 32, "one bit per token");
 static_assert(kSmallWarps * 256 + kSmallMaxCluster * 256 <= kSmallFrontWords, "partials + slots");
-static_assert(kSmallMaxM * 32 * 3 + 32 <= kSmallFrontWords, "tail arrays");
+constexpr int kSmallCandWords = 3072;  // the top-k's per-warp candidate lists, past the align's arrays
+static_assert(kSmallMaxM * 32 * 3 + 32 <= kSmallCandWords, "tail arrays");
+static_assert(kSmallCandWords + kSmallWarps * 32 <= kSmallFrontWords, "candidate lists");
 static_assert(kSmallMaxM * 32 <= 2 * kSmallThreads, "two ranks per thread in the align");
 
 struct SmallParams {
     SmallRouteLaunch a;
     int rows;     // E + S
+    int mask_align;  // fused align with A >= M: one block per touched expert
     int KQ;       // K ranges per 16-row group
     int slices;   // ceil(H / 32)
     int per_cta;  // slices per K range
@@ -69,80 +78,207 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Top-k of one token row in one warp, plus its shared slot. zrow: the
-// token's fp32 gate logits (E routed, then the shared one when S = 1);
-// bias_s: the routed experts' bias in shared memory (zeros without a bias).
-// Writes ids and weights of slots 0..width-1 to global memory and the
-// align's (expert << 10 | flat slot) keys to keys_s. The code is kept straight-line: it runs once per
-// call on whichever SM finishes last, where every taken jump into code the
-// instruction prefetcher has not reached costs a fetch from L2 or memory.
+// Top-k of one token row in one warp. krow: the token's E selection keys
+// (the bf16-rounded logit and the expert id, see make_key), written by the
+// row groups; cand_s: 32 words of shared memory owned by this warp.
+// Writes ids and weights of the routed slots 0..k-1 to global memory (the
+// shared slot k was written by its row group) and the align's
+// (expert << 10 | flat slot) keys of all k + S slots to keys_s; with tmask,
+// also marks token m in the routed experts' token masks and the
+// touched-expert bitmap tbits.
+//
+// Selection by threshold instead of k serial maxima: T = the k-th largest of
+// the 32 lane maxima is a lower bound of the k-th largest key (the k lanes
+// whose maxima reach T hold k distinct keys >= T), so the top-k are among
+// the keys >= T. Those (usually k + a few) are compacted into cand_s by
+// ballots, each one ranked against the others in one shuffle pass, and
+// stored at its rank. When more than 32 keys reach T (the largest logits
+// concentrated in a few lanes), k exact rounds of a warp maximum take over.
 template <int NK>
-__device__ __forceinline__ void warp_topk_row(const float *zrow, int E, int S, int k, float scale,
-                                              const float *bias_s, uint16_t *logits_out,
-                                              int32_t *ids, float *wts, uint32_t *keys_s, int flat0) {
+__device__ __forceinline__ void warp_topk_row(const uint32_t *krow, int E, int S, int k, int32_t *ids,
+                                              float *wts, uint32_t *keys_s, int flat0, uint32_t *cand_s,
+                                              uint32_t *tmask, uint32_t *tbits, int m) {
     const int lane = threadIdx.x & 31;
-    float z[NK];
-    // every load issued before the first use (the shared logit with them);
-    // lanes past E read a clamped (valid) element that is masked below
-#pragma unroll
-    for (int i = 0; i < NK; ++i) z[i] = __ldcg(zrow + min(lane + 32 * i, E - 1));
-    const float sv = __ldcg(zrow + E - 1 + S);
-    // a scheduling fence: without it the compiler interleaves the loads with
-    // the key building below and their latencies add up (measured: 4.7 us
-    // instead of 2.0 us for one token's top-k)
-    __syncwarp();
     uint32_t key[NK];
+    // every load issued before the first use; lanes past E read a clamped
+    // (valid) element that is masked below
+#pragma unroll
+    for (int i = 0; i < NK; ++i) key[i] = __ldcg(krow + min(lane + 32 * i, E - 1));
+    // a scheduling fence: keeps the loads in one batch ahead of their uses
+    // (interleaved with them, their latencies were measured to add up)
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < NK; ++i) key[i] = (lane + 32 * i < E) ? key[i] : 0u;
+    // this lane's largest key (a tree: depth log2(NK))
+    uint32_t lm[NK / 2];
+#pragma unroll
+    for (int i = 0; i < NK / 2; ++i) lm[i] = max(key[i], key[i + NK / 2]);
+#pragma unroll
+    for (int h = NK / 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) lm[i] = max(lm[i], lm[i + h]);
+    const uint32_t lmax = lm[0];
+    // T: the lane maximum with exactly k - 1 larger ones. Valid keys are
+    // unique and nonzero; a lane without a valid key holds 0 and ranks at or
+    // past min(E, 32) >= k, so exactly one lane matches.
+    int rl = 0;
+#pragma unroll
+    for (int d = 1; d < 32; ++d) rl += __shfl_xor_sync(0xffffffffu, lmax, d) > lmax;
+    const uint32_t T = __shfl_sync(0xffffffffu, lmax, __ffs(__ballot_sync(0xffffffffu, rl == k - 1)) - 1);
+    uint32_t bal[NK];
+    int tot = 0;
 #pragma unroll
     for (int i = 0; i < NK; ++i) {
-        const int e = lane + 32 * i;
-        z[i] = round_bf16(z[i] + bias_s[min(e, E - 1)]);
-        key[i] = (e < E) ? make_key(z[i], e) : 0u;
+        bal[i] = __ballot_sync(0xffffffffu, key[i] >= T);
+        tot += __popc(bal[i]);
     }
-    if (__builtin_expect(logits_out != nullptr, 0)) {
+    uint32_t mine, first;
+    if (tot <= 32) {  // warp-uniform
+        // compact the candidates, in (i, lane) order, into cand_s[0, tot)
+        const uint32_t lt = lanemask_lt();
+        int base = 0;
 #pragma unroll
-        for (int i = 0; i < NK; ++i)
-            if (lane + 32 * i < E) logits_out[lane + 32 * i] = (uint16_t)(__float_as_uint(z[i]) >> 16);
+        for (int i = 0; i < NK; ++i) {
+            if (key[i] >= T) cand_s[base + __popc(bal[i] & lt)] = key[i];
+            base += __popc(bal[i]);
+        }
         __syncwarp();
-    }
-    // k rounds: each lane's largest key, the warp's largest (redux), and the
-    // lane holding it clears it (keys are unique) -- selects only, so the
-    // warp stays converged, and no sorting network: the tail runs once per
-    // call on a cold instruction cache, where code size costs more than
-    // instructions
-    uint32_t mine = 0u, first = 0u;
+        const uint32_t c = lane < tot ? cand_s[lane] : 0u;
+        int r = 0;  // candidates above this one (0 never counts: valid keys are nonzero)
+#pragma unroll
+        for (int d = 1; d < 32; ++d) r += __shfl_xor_sync(0xffffffffu, c, d) > c;
+        __syncwarp();
+        if (lane < tot && r < k) cand_s[r] = c;  // slot r of the row
+        __syncwarp();
+        mine = cand_s[lane];  // meaningful for lanes < k
+        first = cand_s[0];
+        __syncwarp();
+    } else {
+        // k rounds: each lane's largest key, the warp's largest (redux), and
+        // the lane holding it clears it (keys are unique)
+        mine = 0u;
+        first = 0u;
 #pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        uint32_t lm[NK / 2];  // a tree: depth log2(NK) instead of a chain of NK - 1
+        for (int r = 0; r < k; ++r) {
+            uint32_t m2[NK / 2];
 #pragma unroll
-        for (int i = 0; i < NK / 2; ++i) lm[i] = max(key[i], key[i + NK / 2]);
+            for (int i = 0; i < NK / 2; ++i) m2[i] = max(key[i], key[i + NK / 2]);
 #pragma unroll
-        for (int h = NK / 4; h >= 1; h >>= 1)
+            for (int h = NK / 4; h >= 1; h >>= 1)
 #pragma unroll
-            for (int i = 0; i < h; ++i) lm[i] = max(lm[i], lm[i + h]);
-        const uint32_t gmax = __reduce_max_sync(0xffffffffu, lm[0]);
-        first = (r == 0) ? gmax : first;
-        mine = (lane == r) ? gmax : mine;
+                for (int i = 0; i < h; ++i) m2[i] = max(m2[i], m2[i + h]);
+            const uint32_t gmax = __reduce_max_sync(0xffffffffu, m2[0]);
+            first = (r == 0) ? gmax : first;
+            mine = (lane == r) ? gmax : mine;
 #pragma unroll
-        for (int i = 0; i < NK; ++i) key[i] = (key[i] == gmax) ? 0u : key[i];
+            for (int i = 0; i < NK; ++i) key[i] = (key[i] == gmax) ? 0u : key[i];
+        }
     }
     // softmax over the selected logits (renormalised top-k); every lane
-    // evaluates the exponential, lanes past k drop it
+    // evaluates the exponential, lanes past k drop it. The weight is the
+    // exponential times the correctly rounded reciprocal of the sum (two
+    // roundings, within 1.5 ulp of the quotient).
     const float vmax = key_value(first);
     const float ex = expf(key_value(mine) - vmax);
     const float ev = (lane < k) ? ex : 0.0f;
     float sum = ev;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    // slot `lane`: a routed pick, or the shared expert in slot k
-    const bool shared_slot = S != 0 && lane == k;
-    const int id = shared_slot ? E : key_id(mine);
-    const float wt = shared_slot ? scale * sigmoid_stable(sv) : ev / sum;
-    if (lane < k + S) {
+    const float inv = __frcp_rn(sum);
+    if (lane < k) {
+        const int id = key_id(mine);
         ids[lane] = id;
-        wts[lane] = wt;
+        wts[lane] = ev * inv;
         keys_s[lane] = ((uint32_t)id << 10) | (uint32_t)(flat0 + lane);  // the align's key
+        if (tmask != nullptr) {
+            atomicOr(tmask + id, 1u << m);
+            atomicOr(tbits + (id >> 5), 1u << (id & 31));
+        }
+    } else if (S != 0 && lane == k) {
+        keys_s[lane] = ((uint32_t)E << 10) | (uint32_t)(flat0 + lane);
     }
     __syncwarp();
+}
+
+// moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
+// moe_align block size", Purpose) for a small batch whose every expert fits
+// one block (A >= M: an expert receives at most one id per token), from
+// the per-expert token masks and the touched-expert bitmap the top-k filled:
+//  - an expert's block is the number of touched experts below it (a prefix
+//    of the bitmap words' popcounts, then a popcount within the word);
+//  - an id's place in its block is the number of earlier tokens in its
+//    expert's mask (ids of one expert come one per token, so this is the
+//    ascending flat order the alignment lists them in);
+//  - npp = A * touched experts; every slot of a block past its count holds
+//    the sentinel n = M * width.
+// Three CTA barriers and no ranking pass: the tail is bound by one warp's
+// dependent instruction stream, not by the amount of work.
+__device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int width, int E_al, int A,
+                                            const uint32_t *tmask, const uint32_t *tbits, int *wpre,
+                                            int *blkcnt, int32_t *sorted, int64_t sorted_cap,
+                                            int32_t *expert_ids, int64_t expert_cap, int32_t *npp_out,
+                                            uint32_t *err) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwd = (E_al + 31) >> 5;  // bitmap words, <= 33
+    if (warp == 0) {
+        const int c = lane < nwd ? __popc(tbits[lane]) : 0;
+        int inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            inc += lane >= o ? v : 0;
+        }
+        wpre[lane] = inc - c;
+        if (lane == 31) wpre[32] = inc;  // blocks before word 32 (E + S = 1025 only)
+    }
+    __syncwarp();
+    __syncthreads();
+    const int n = M * width;
+    uint32_t bad = 0;
+#pragma unroll 1
+    for (int m = warp; m < M; m += kSmallWarps) {
+        if (lane < width) {
+            const int i = m * width + lane;
+            const int e = (int)(keys_s[i] >> 10);
+            const uint32_t tm = tmask[e];
+            const int j = __popc(tm & ((1u << m) - 1u));
+            const int b = wpre[e >> 5] + __popc(tbits[e >> 5] & ((1u << (e & 31)) - 1u));
+            st_slot(sorted, (int64_t)b * A + j, sorted_cap, i, bad);
+            if (j == 0) {
+                blkcnt[b] = __popc(tm);
+                st_slot(expert_ids, b, expert_cap, e, bad);
+            }
+        }
+        __syncwarp();
+    }
+    const int nblk = wpre[32] + (nwd > 32 ? __popc(tbits[32]) : 0);
+    const int npp = nblk * A;
+    if (tid == 0) *npp_out = npp;
+    __syncwarp();
+    __syncthreads();
+    // the padding: slots j >= the block's count (16-byte stores when A is a
+    // multiple of 4, so that four slots never straddle two blocks, and the
+    // array is 16-byte aligned)
+    const bool pow2 = (A & (A - 1)) == 0;
+    const int lgA = __ffs(A) - 1;
+    if ((A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0) {
+#pragma unroll 1
+        for (int q = tid * 4; q < npp; q += kSmallThreads * 4) {
+            const int b = pow2 ? q >> lgA : q / A, j = q - b * A, c = blkcnt[b];
+            if (j >= c) {
+                st_slot4(sorted, q, sorted_cap, make_int4(n, n, n, n), bad);
+            } else if (j + 4 > c) {
+                for (int u = c - j; u < 4; ++u) st_slot(sorted, q + u, sorted_cap, n, bad);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int q = tid; q < npp; q += kSmallThreads) {
+            const int b = q / A, j = q - b * A;
+            if (j >= blkcnt[b]) st_slot(sorted, q, sorted_cap, n, bad);
+        }
+    }
+    report_bad_slots(bad, err);
 }
 
 // moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill: M-aware
@@ -323,15 +459,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     const int row0 = rg * 16;
     __shared__ int s_last;
 
-    // the group leader (rank 0) keeps the routed bias for the tail: loads
-    // issued now, stored to shared memory after the gate stream
-    float bias_r[kSmallBiasPerThread];
-#pragma unroll
-    for (int j = 0; j < kSmallBiasPerThread; ++j) bias_r[j] = 0.0f;
-    if (kq == 0 && p.bias != nullptr) {
-#pragma unroll
-        for (int j = 0; j < kSmallBiasPerThread; ++j)
-            bias_r[j] = __ldg(p.bias + min(tid + j * kSmallThreads, p.E - 1));
+    // the group leader (rank 0) finishes the group's logits with thread
+    // (row r16, token m16): the routed bias of its row is loaded now; and
+    // clears the tail's token masks and bitmap (any leader may run the tail)
+    const int r16 = tid >> 4, m16 = tid & 15;  // 256 threads = 16 rows x 16 tokens
+    uint32_t *tmask = reinterpret_cast<uint32_t *>(smem) + kSmallFrontWords;  // [E + S]
+    uint32_t *tbits = tmask + kSmallMaskWords;                                 // [ceil((E + S) / 32)]
+    float bias_v = 0.0f;
+    if (kq == 0) {
+        if (p.bias != nullptr && row0 + r16 < p.E) bias_v = __ldg(p.bias + row0 + r16);
+        if (P.mask_align) {
+            for (int i = tid; i < rows; i += kSmallThreads) tmask[i] = 0u;
+            if (tid < kSmallBitWords) tbits[tid] = 0u;
+        }
     }
 
     // ---- 1. gate rows x tokens on the tensor cores ----
@@ -386,10 +526,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     // Shared memory: [0, 8 KB) the warps' partials; [8 KB, 16 KB) the group
     // leader's slots for the cluster's K ranges (written by each CTA of the
     // cluster into the leader's memory); the tail reuses [0, 16 KB); the
-    // routed bias sits at [16 KB, 20 KB).
+    // tail's token masks and bitmap follow at 16 KB.
     float *red = reinterpret_cast<float *>(smem);                 // [8 warps][16 rows][16 tokens]
     float *slots = red + kSmallWarps * 16 * 16;                   // [KQ][16 rows][16 tokens]
-    float *bias_s = reinterpret_cast<float *>(smem) + kSmallFrontWords;  // [E]
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         const int tok = nb * 8 + 2 * t;
@@ -397,11 +536,6 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         red[(warp * 16 + g) * 16 + tok + 1] = acc[nb][1];
         red[(warp * 16 + g + 8) * 16 + tok] = acc[nb][2];
         red[(warp * 16 + g + 8) * 16 + tok + 1] = acc[nb][3];
-    }
-    if (kq == 0) {
-#pragma unroll
-        for (int j = 0; j < kSmallBiasPerThread; ++j)
-            if (tid + j * kSmallThreads < p.E) bias_s[tid + j * kSmallThreads] = bias_r[j];
     }
     __syncwarp();
     __syncthreads();
@@ -416,12 +550,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     // CTAs are done after it
     cluster_sync();
     if (kq != 0) return;
-    const int r16 = tid >> 4, m16 = tid & 15;  // 256 threads = 16 rows x 16 tokens
     {
+        // the group's final logits: a routed one becomes its selection key
+        // (bias added in fp32, then rounded to bf16); the shared expert's
+        // slot k = (E, scale * sigmoid(s)) is final here, s not rounded
         float v = 0.0f;
         for (int q = 0; q < P.KQ; ++q) v += slots[q * 256 + tid];
-        if (m16 < p.M && m16 < NB * 8 && row0 + r16 < rows)
-            p.scratch[(int64_t)m16 * rows + row0 + r16] = v;
+        const int row = row0 + r16;
+        if (m16 < p.M && m16 < NB * 8 && row < rows) {
+            if (row < p.E) {
+                const float zr = round_bf16(v + bias_v);
+                p.scratch[(int64_t)m16 * p.E + row] = make_key(zr, row);
+                if (p.logits_out != nullptr)
+                    p.logits_out[(int64_t)m16 * p.E + row] = (uint16_t)(__float_as_uint(zr) >> 16);
+            } else {
+                p.ids[(int64_t)m16 * (p.k + 1) + p.k] = p.E;
+                p.wts[(int64_t)m16 * (p.k + 1) + p.k] = p.scale * sigmoid_stable(v);
+            }
+        }
     }
     __syncwarp();
     __syncthreads();
@@ -439,21 +585,32 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     if (tid == 0) hdr->ticket = 0u;  // every group has arrived: reset for the next call
     __syncwarp();  // a split warp would replay the whole tail once per path
 
-    // ---- 4. tail: top-k + softmax + shared slot, one warp per token ----
+    // ---- 4. tail: top-k + softmax, one warp per token ----
     const int width = p.k + p.S;
     const int n = p.M * width, n4 = (n + 3) & ~3;
     uint32_t *keys_s = reinterpret_cast<uint32_t *>(smem);  // [n4] the align's keys
-    for (int m = warp; m < p.M; m += kSmallWarps) {
-        const float *zrow = p.scratch + (int64_t)m * rows;
-        uint16_t *lrow = p.logits_out ? p.logits_out + (int64_t)m * p.E : nullptr;
-        int32_t *irow = p.ids + (int64_t)m * width;
-        float *wrow = p.wts + (int64_t)m * width;
-        warp_topk_row<NK>(zrow, p.E, p.S, p.k, p.scale, bias_s, lrow, irow, wrow, keys_s + m * width, m * width);
+    uint32_t *cand_s = keys_s + kSmallCandWords;               // [8 warps][32] top-k candidates
+    if (P.mask_align && p.S != 0 && tid == 0) {  // the shared expert: every token
+        tmask[p.E] = (p.M == 32) ? 0xFFFFFFFFu : (1u << p.M) - 1u;
+        atomicOr(tbits + (p.E >> 5), 1u << (p.E & 31));
     }
+    for (int m = warp; m < p.M; m += kSmallWarps)
+        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, p.E, p.S, p.k, p.ids + (int64_t)m * width,
+                          p.wts + (int64_t)m * width, keys_s + m * width, m * width, cand_s + warp * 32,
+                          P.mask_align ? tmask : nullptr, tbits, m);
     if (p.sorted == nullptr) return;
-    if (tid < n4 - n) keys_s[n + tid] = 0xFFFFFFFFu;  // padding keys sort last and match nothing
 
     // ---- 5. moe_align_block_size on the M*width ids of this call ----
+    __syncwarp();
+    __syncthreads();
+    if (P.mask_align) {
+        int *blkcnt = reinterpret_cast<int *>(keys_s + kSmallMaxM * 32);  // [<= n] ids per block
+        int *wpre = blkcnt + kSmallMaxM * 32;                              // [33] blocks before each word
+        align_masks(keys_s, p.M, width, rows, p.A, tmask, tbits, wpre, blkcnt, p.sorted, p.sorted_cap,
+                    p.expert_ids, p.expert_cap, p.npp, &hdr->error);
+        return;
+    }
+    if (tid < n4 - n) keys_s[n + tid] = 0xFFFFFFFFu;  // padding keys sort last and match nothing
     __syncwarp();
     __syncthreads();
     if (n <= kSmallThreads)
@@ -543,10 +700,11 @@ cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
     P.rows = a.E + a.S;
     P.slices = (a.H + kSliceK - 1) / kSliceK;
     P.KQ = small_route_k_ranges(a.E, a.S, a.H);
+    P.mask_align = (a.sorted != nullptr && a.A >= a.M) ? 1 : 0;
     P.per_cta = (P.slices + P.KQ - 1) / P.KQ;
     const int groups = (P.rows + 15) / 16;
     const int grid = groups * P.KQ;
-    const size_t smem = (size_t)(kSmallFrontWords + kSmallMaxE) * 4;
+    const size_t smem = (size_t)kSmallSmemWords * 4;
     if (a.E <= 512)
         return a.M <= 8 ? launch_nb<1, 16>(P, grid, smem, stream) : launch_nb<2, 16>(P, grid, smem, stream);
     return a.M <= 8 ? launch_nb<1, 32>(P, grid, smem, stream) : launch_nb<2, 32>(P, grid, smem, stream);

@@ -153,6 +153,18 @@ def test_all_equal_logits_lowest_ids_win(smr, M):
     check_route(ri, ids, wts, lg)
 
 
+@pytest.mark.parametrize("M,E,k", [(4, 512, 10), (13, 1024, 31), (300, 512, 10)])
+def test_top_logits_in_few_lanes(smr, M, E, k):
+    """The largest logits all sit in experts e with e % 32 < 3 (a bias of
+    +8 on them), so far more than 32 keys reach the k-th largest maximum of
+    32 interleaved lanes: the selections' exact fallbacks must give the
+    oracle's answer."""
+    ri = inputs.make_route_inputs(M, 512, E, k, 1, seed=21 + M)
+    ri.bias = np.where(np.arange(E) % 32 < 3, 8.0, 0.0).astype(np.float32)
+    rep, al, ids = _full_check(smr, ri, 64)
+    assert np.all(ids[:, :k] % 32 < 3)
+
+
 def test_bias_and_strided_hidden(smr):
     ri = inputs.make_route_inputs(40, 512, 128, 8, 1, seed=5, zipf_s=1.1)
     x, w, ws, b = _dev(ri)
