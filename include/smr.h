@@ -32,10 +32,11 @@
  *    everything else takes the existing path).
  *  - Workspace: a caller-owned device buffer of at least the size the
  *    matching *_workspace_size() returns, 256-byte aligned, ZEROED ONCE by
- *    the caller before its first use (cudaMemsetAsync). The library leaves
- *    its counters at zero after every call, so the buffer can be reused by
- *    later calls and graph replays without clearing. Calls that share a
- *    workspace must not run concurrently.
+ *    the caller before its first use (cudaMemsetAsync). Every call leaves
+ *    the buffer ready for the next one (counters back at zero, a call tag
+ *    that only advances), so it can be reused by later calls and graph
+ *    replays without clearing. Calls that share a workspace must not run
+ *    concurrently.
  *  - Inputs must be finite. NaN or Inf in hidden states, gate weights or
  *    bias give unspecified (but in-bounds) results.
  */
@@ -151,8 +152,9 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
  * by every GPU that loads the library until the process exits. (The pages
  * have no counterpart; this is an interface convenience.)
  *  - The first call on a device, with that device current, resolves the
- *    array's device address and zeroes its counter; make that first call
- *    outside any stream capture. Later calls do no set-up.
+ *    array's device address and clears the array (then synchronises the
+ *    device); make that first call outside any stream capture. Later calls
+ *    do no set-up.
  *  - Every call on a device shares the one array, which keeps the last
  *    call's contents: calls that overlap on the GPU (different streams
  *    without ordering, or host threads) race and give wrong results.

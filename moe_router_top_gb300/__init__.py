@@ -81,9 +81,10 @@ def _stream_ptr(stream) -> Optional[int]:
 class Workspace:
     """A zero-initialised device buffer that grows on demand.
 
-    The library keeps its counters at zero between calls, so a workspace is
-    zeroed once (on allocation) and can be reused by later calls and CUDA
-    graph replays. Calls sharing one workspace must not overlap on the GPU.
+    The library leaves a workspace ready for its next call (counters back at
+    zero, a call tag that only advances), so a workspace is zeroed once (on
+    allocation) and can be reused by later calls and CUDA graph replays.
+    Calls sharing one workspace must not overlap on the GPU.
     """
 
     def __init__(self, nbytes: int = 0, device=None):

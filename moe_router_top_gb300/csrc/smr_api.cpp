@@ -120,8 +120,7 @@ void check_route(const smr_route_args *a, Reasons &r) {
 
 size_t route_scratch_bytes(const smr_route_args *a) {
     if (a->M <= 0 || a->M > smr::kSmallMaxM) return 0;
-    const int S = a->has_shared ? 1 : 0;
-    return round_up((size_t)a->M * (size_t)(a->E + S) * 4, kWsAlign);
+    return round_up((size_t)a->M * (size_t)a->E * 8, kWsAlign);  // tagged selection keys
 }
 
 // --- align ------------------------------------------------------------------
@@ -237,7 +236,7 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
         L.ids = a->topk_ids;
         L.wts = a->topk_weights;
         L.logits_out = a->logits_out;
-        L.scratch = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kHeaderBytes);
+        L.scratch = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + kHeaderBytes);
         L.hdr = ws;
         if (fused_align) {
             L.A = effective_block_size(fused_align);

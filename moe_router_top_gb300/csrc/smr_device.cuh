@@ -23,9 +23,10 @@ constexpr uint32_t kErrBadSlot = 4u;      // an align output position fell outsi
 // First 256 bytes of every workspace. Zeroed once by the caller; kernels
 // return the counters to zero before they exit.
 struct WsHeader {
-    uint32_t ticket;  // small route: row groups whose gate logits are stored
+    uint32_t ticket;  // reserved (zero)
     uint32_t error;   // sticky error bits (kErr*)
-    uint32_t reserved[62];
+    uint32_t epoch;   // small route: tag of the last completed call (top bit set once used)
+    uint32_t reserved[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -242,6 +243,16 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 // Acquire-release atomic add at GPU scope; returns the old value.
+// Relaxed 64-bit accesses at GPU scope (naturally aligned: single-copy
+// atomic, so a reader sees either the old or the new word whole).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

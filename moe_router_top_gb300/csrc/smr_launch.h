@@ -19,7 +19,7 @@ struct SmallRouteLaunch {
     int32_t *ids;
     float *wts;
     uint16_t *logits_out;
-    uint32_t *scratch;     // workspace: [M][E] selection keys of the routed logits (<= M*(E+S) words)
+    unsigned long long *scratch;  // workspace: [M][E] tagged selection keys of the routed logits
     void *hdr;             // workspace header (WsHeader)
     // fused align (sorted == nullptr: route only)
     int A;
@@ -30,7 +30,8 @@ struct SmallRouteLaunch {
 };
 constexpr int kSmallMaxM = 16;
 // Number of K ranges the gate rows are split into (the CTAs of one cluster);
-// the scratch holds the M * E selection keys of the routed logits (sized M * (E + S) words).
+// the scratch holds the M * E tagged selection keys of the routed logits
+// (8 bytes each).
 int small_route_k_ranges(int E, int S, int H);
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream);
 // Fixed scratch in device memory (no allocation): capacity, and its device

@@ -2,10 +2,10 @@
 //
 // What it computes is the one-launch small-M router of "[AMD] One-launch
 // small-M MoE router for Qwen3.5 on gfx950", Modifications: the E+S gate rows
-// are computed for all M tokens with fp32 accumulation across CTAs; the last
-// CTA to finish (self-resetting ticket, no spin-wait) rounds the routed logits
-// to bf16, selects the top-k with the lowest id winning ties, applies softmax +
-// renormalisation, writes the shared slot (E, sigmoid(s) * scale) and, when
+// are computed for all M tokens with fp32 accumulation across CTAs; the routed
+// logits are rounded to bf16; one CTA then selects the top-k with the lowest
+// id winning ties, applies softmax + renormalisation, writes the shared
+// slot (E, sigmoid(s) * scale) and, when
 // asked, runs moe_align_block_size on the M*(k+S) ids it just produced
 // ("[ROCm][Kernel] W4A16 MoE prefill: M-aware moe_align block size",
 // Purpose) -- all in one launch.
@@ -27,13 +27,15 @@
 //    shared memory of the cluster's first CTA (distributed shared memory),
 //    which adds the KQ slots in a fixed order after one cluster barrier and
 //    stores the group's final logits -- results are deterministic;
-//  - one acquire-release ticket per row group hands the tail to the last
-//    group (no spin-wait);
-//  - the tail is warp-parallel and compact (it runs once per call, on a cold
-//    instruction cache): one warp per token, each lane holds E/32 ordered
-//    32-bit keys, k rounds of a lane maximum, one redux.sync max and a clear
-//    of the winner; the align of the few ids ranks (expert, position) keys
-//    instead of scanning all experts.
+//  - each group leader rounds its logits, stores them as ordered 32-bit
+//    selection keys tagged with the call's epoch in one 64-bit word, and
+//    writes the shared expert's slot itself; the leader of the last group
+//    runs the tail, loading every key word until it carries this call's tag
+//    (bounded; no fence, counter or atomic on the hand-off);
+//  - the tail is warp-parallel and compact (it runs once per call): one warp
+//    per token ranks the keys at or above the k-th largest lane maximum;
+//    the align of the few ids places them from per-expert token masks (one
+//    block per expert when A >= M) or ranks (expert, position) keys.
 #include "smr_device.cuh"
 #include "smr_launch.h"
 
@@ -54,6 +56,9 @@ constexpr int kSmallSmemWords = kSmallFrontWords + kSmallMaskWords + kSmallBitWo
 static_assert(kSmallMaxE + 1 <= kSmallMaskWords && (kSmallMaxE + 32) / 32 <= kSmallBitWords, "mask arrays");
 static_assert(kSmallMaxM <= 32, "one bit per token");
 static_assert(kSmallWarps * 256 + kSmallMaxCluster * 256 <= kSmallFrontWords, "partials + slots");
+// Reloads of a key word that still holds an older tag before the tail gives
+// up (each one waits for an L2 round trip: well above a second in all).
+constexpr int kSmallPollLimit = 1 << 22;
 constexpr int kSmallCandWords = 3072;  // the top-k's per-warp candidate lists, past the align's arrays
 static_assert(kSmallMaxM * 32 * 3 + 32 <= kSmallCandWords, "tail arrays");
 static_assert(kSmallCandWords + kSmallWarps * 32 <= kSmallFrontWords, "candidate lists");
@@ -79,8 +84,9 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 // Top-k of one token row in one warp. krow: the token's E selection keys
-// (the bf16-rounded logit and the expert id, see make_key), written by the
-// row groups; cand_s: 32 words of shared memory owned by this warp.
+// (the bf16-rounded logit and the expert id, see make_key) in the low half
+// of words whose high half is the call's tag, written by the row groups;
+// cand_s: 32 words of shared memory owned by this warp.
 // Writes ids and weights of the routed slots 0..k-1 to global memory (the
 // shared slot k was written by its row group) and the align's
 // (expert << 10 | flat slot) keys of all k + S slots to keys_s; with tmask,
@@ -95,20 +101,35 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // stored at its rank. When more than 32 keys reach T (the largest logits
 // concentrated in a few lanes), k exact rounds of a warp maximum take over.
 template <int NK>
-__device__ __forceinline__ void warp_topk_row(const uint32_t *krow, int E, int S, int k, int32_t *ids,
-                                              float *wts, uint32_t *keys_s, int flat0, uint32_t *cand_s,
-                                              uint32_t *tmask, uint32_t *tbits, int m) {
+__device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, uint32_t tag, int E, int S,
+                                              int k, int32_t *ids, float *wts, uint32_t *keys_s, int flat0,
+                                              uint32_t *cand_s, uint32_t *tmask, uint32_t *tbits, int m,
+                                              uint32_t *err) {
     const int lane = threadIdx.x & 31;
-    uint32_t key[NK];
     // every load issued before the first use; lanes past E read a clamped
-    // (valid) element that is masked below
+    // (valid) element that is masked below. A word carries this call's tag
+    // once its row group has stored it: the words still holding an older
+    // tag are loaded again, a bounded number of times.
+    unsigned long long v[NK];
 #pragma unroll
-    for (int i = 0; i < NK; ++i) key[i] = __ldcg(krow + min(lane + 32 * i, E - 1));
-    // a scheduling fence: keeps the loads in one batch ahead of their uses
-    // (interleaved with them, their latencies were measured to add up)
-    __syncwarp();
+    for (int i = 0; i < NK; ++i) v[i] = ld_relaxed_u64(krow + min(lane + 32 * i, E - 1));
+#pragma unroll 1
+    for (int tries = 0;; ++tries) {
+        bool ok = true;
 #pragma unroll
-    for (int i = 0; i < NK; ++i) key[i] = (lane + 32 * i < E) ? key[i] : 0u;
+        for (int i = 0; i < NK; ++i) ok = ok && (uint32_t)(v[i] >> 32) == tag;
+        if (__all_sync(0xffffffffu, ok)) break;
+        if (tries == kSmallPollLimit) {  // warp-uniform: the outputs of this call are not valid
+            if (lane == 0) set_error(err, kErrWaitTimeout);
+            break;
+        }
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            if ((uint32_t)(v[i] >> 32) != tag) v[i] = ld_relaxed_u64(krow + min(lane + 32 * i, E - 1));
+    }
+    uint32_t key[NK];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) key[i] = (lane + 32 * i < E) ? (uint32_t)v[i] : 0u;
     // this lane's largest key (a tree: depth log2(NK))
     uint32_t lm[NK / 2];
 #pragma unroll
@@ -457,18 +478,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     const int rg = blockIdx.x / P.KQ;         // row group
     const int kq = (int)cluster_ctarank();    // K range = rank in the group's cluster
     const int row0 = rg * 16;
-    __shared__ int s_last;
 
     // the group leader (rank 0) finishes the group's logits with thread
-    // (row r16, token m16): the routed bias of its row is loaded now; and
-    // clears the tail's token masks and bitmap (any leader may run the tail)
+    // (row r16, token m16): the routed bias of its row is loaded now; the
+    // tail CTA clears its token masks and bitmap
     const int r16 = tid >> 4, m16 = tid & 15;  // 256 threads = 16 rows x 16 tokens
     uint32_t *tmask = reinterpret_cast<uint32_t *>(smem) + kSmallFrontWords;  // [E + S]
     uint32_t *tbits = tmask + kSmallMaskWords;                                 // [ceil((E + S) / 32)]
+    // this call's tag: a 31-bit call count with the top bit set, so that it
+    // never equals a cleared word (0) or a nonnegative int32 the align leaves
+    // in a shared workspace; the leader of the last row group runs the tail
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.hdr);
+    const bool tail_cta = kq == 0 && rg == (int)(gridDim.x / (unsigned)P.KQ) - 1;
     float bias_v = 0.0f;
+    uint32_t tag = 0u;
     if (kq == 0) {
+        tag = ((__ldcg(&hdr->epoch) + 1u) & 0x7FFFFFFFu) | 0x80000000u;
         if (p.bias != nullptr && row0 + r16 < p.E) bias_v = __ldg(p.bias + row0 + r16);
-        if (P.mask_align) {
+        if (tail_cta && P.mask_align) {
             for (int i = tid; i < rows; i += kSmallThreads) tmask[i] = 0u;
             if (tid < kSmallBitWords) tbits[tid] = 0u;
         }
@@ -560,7 +587,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         if (m16 < p.M && m16 < NB * 8 && row < rows) {
             if (row < p.E) {
                 const float zr = round_bf16(v + bias_v);
-                p.scratch[(int64_t)m16 * p.E + row] = make_key(zr, row);
+                st_relaxed_u64(p.scratch + (int64_t)m16 * p.E + row,
+                               ((unsigned long long)tag << 32) | make_key(zr, row));
                 if (p.logits_out != nullptr)
                     p.logits_out[(int64_t)m16 * p.E + row] = (uint16_t)(__float_as_uint(zr) >> 16);
             } else {
@@ -572,17 +600,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     __syncwarp();
     __syncthreads();
 
-    // ---- 3. hand-off: the last row group to arrive runs the tail ----
-    // One acquire-release increment by the ticket-taking thread: it releases
-    // the logit stores the CTA barrier ordered before it, and the last
-    // group's increment acquires every other group's.
-    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.hdr);
-    const unsigned groups = gridDim.x / (unsigned)P.KQ;
-    if (tid == 0) s_last = (atomic_add_acq_rel(&hdr->ticket, 1u) == groups - 1);
-    __syncwarp();
-    __syncthreads();
-    if (!s_last) return;
-    if (tid == 0) hdr->ticket = 0u;  // every group has arrived: reset for the next call
+    // ---- 3. hand-off: the tail CTA collects the tagged keys ----
+    // No fence and no counter: every key word carries the call's tag, so
+    // the tail loads each word until it holds this call's tag (the other
+    // groups' CTAs have all been launched alongside; they only need SMs).
+    if (!tail_cta) return;
     __syncwarp();  // a split warp would replay the whole tail once per path
 
     // ---- 4. tail: top-k + softmax, one warp per token ----
@@ -595,9 +617,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         atomicOr(tbits + (p.E >> 5), 1u << (p.E & 31));
     }
     for (int m = warp; m < p.M; m += kSmallWarps)
-        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, p.E, p.S, p.k, p.ids + (int64_t)m * width,
+        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, tag, p.E, p.S, p.k, p.ids + (int64_t)m * width,
                           p.wts + (int64_t)m * width, keys_s + m * width, m * width, cand_s + warp * 32,
-                          P.mask_align ? tmask : nullptr, tbits, m);
+                          P.mask_align ? tmask : nullptr, tbits, m, &hdr->error);
+    if (tid == 0) hdr->epoch = tag;  // read by the next call's CTAs (after this launch ends)
     if (p.sorted == nullptr) return;
 
     // ---- 5. moe_align_block_size on the M*width ids of this call ----
@@ -680,12 +703,13 @@ cudaError_t static_scratch(void **ptr) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (addr[dev] == nullptr) {
         // first use on this device (with it current): resolve the address and
-        // zero the hand-off counter and error word, which later calls leave
-        // at zero themselves
+        // clear the whole array (header and tagged key words), as a caller
+        // clears a workspace before its first use
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_route_scratch);
         if (e != cudaSuccess) return e;
-        e = cudaMemset(p, 0, sizeof(WsHeader));
+        e = cudaMemset(p, 0, kStaticScratchBytes);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();  // cleared before any stream's first launch
         if (e != cudaSuccess) return e;
         addr[dev] = p;
     }

@@ -96,7 +96,7 @@ def test_route_unsupported_contract(lib):
 def test_route_workspace_checked_before_device(lib):
     a = _good_route()
     need = lib.smr_route_workspace_size(ctypes.byref(a))
-    assert need == 256 + ((4 * 513 * 4 + 255) // 256) * 256  # header + [M][E+S] fp32 logits
+    assert need == 256 + ((4 * 512 * 8 + 255) // 256) * 256  # header + [M][E] tagged 8-byte keys
     assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_WORKSPACE
     assert lib.smr_route(ctypes.byref(a), 0x100080, need, None) == _lib.SMR_ERR_WORKSPACE  # misaligned
     assert lib.smr_route(ctypes.byref(a), 0x100000, need - 1, None) == _lib.SMR_ERR_WORKSPACE

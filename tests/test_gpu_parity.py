@@ -165,6 +165,17 @@ def test_top_logits_in_few_lanes(smr, M, E, k):
     assert np.all(ids[:, :k] % 32 < 3)
 
 
+@pytest.mark.parametrize("M,A", [(16, 8), (9, 5), (16, 16), (16, 17), (3, 3), (1, 1), (12, 2)])
+def test_small_batch_block_sizes(smr, M, A):
+    """Single-launch route+align with block sizes around M on a 64-expert
+    gate (experts shared by several tokens): A >= M places each id from the
+    per-expert token masks (one block per expert), A < M ranks the ids
+    (experts, the shared one first of all, span several blocks)."""
+    ri = inputs.make_route_inputs(M, 512, 64, 8, 1, seed=31 + M * 7 + A)
+    rep, al, ids = _full_check(smr, ri, A)
+    assert smr.last_launch_count() == 1
+
+
 def test_bias_and_strided_hidden(smr):
     ri = inputs.make_route_inputs(40, 512, 128, 8, 1, seed=5, zipf_s=1.1)
     x, w, ws, b = _dev(ri)
@@ -225,8 +236,10 @@ def test_workspace_reuse_is_deterministic(smr):
         n = int(first[4].item())
         assert torch.equal(again[0], first[0]) and torch.equal(again[1], first[1])
         assert torch.equal(again[2][:n], first[2][:n])
-    # the ticket counter is back at zero after every call
-    assert int(wsp.buf[:4].view(torch.int32).item()) == 0
+    # the small route's call tag advanced once per call: 6 calls on a fresh
+    # workspace (top bit set on every tag)
+    tag = int(wsp.buf[8:12].view(torch.int32).item()) & 0xFFFFFFFF
+    assert tag == 0x80000000 | 6
     assert smr.get_device_error(wsp) == 0
 
 
