@@ -52,7 +52,11 @@ constexpr int kSmallMaxE = 1024;
 // for token m, E + S <= 1025 words) and the touched-expert bitmap.
 constexpr int kSmallMaskWords = 1028;
 constexpr int kSmallBitWords = 36;
-constexpr int kSmallSmemWords = kSmallFrontWords + kSmallMaskWords + kSmallBitWords;
+// sorted_token_ids staged for one bulk copy (64 KB: npp <= 16384).
+constexpr int kSmallSortedWords = 16384;
+constexpr int kSmallSmemWords = kSmallFrontWords + kSmallMaskWords + kSmallBitWords + kSmallSortedWords;
+static_assert(((kSmallFrontWords + kSmallMaskWords + kSmallBitWords) * 4) % 16 == 0, "16-byte aligned staging");
+static_assert(kSmallBitWords % 4 == 0, "bitmap read as uint4");
 static_assert(kSmallMaxE + 1 <= kSmallMaskWords && (kSmallMaxE + 32) / 32 <= kSmallBitWords, "mask arrays");
 static_assert(kSmallMaxM <= 32, "one bit per token");
 static_assert(kSmallWarps * 256 + kSmallMaxCluster * 256 <= kSmallFrontWords, "partials + slots");
@@ -225,46 +229,58 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
 // moe_align block size", Purpose) for a small batch whose every expert fits
 // one block (A >= M: an expert receives at most one id per token), from
 // the per-expert token masks and the touched-expert bitmap the top-k filled:
-//  - an expert's block is the number of touched experts below it (a prefix
-//    of the bitmap words' popcounts, then a popcount within the word);
+//  - an expert's block is the number of touched experts below it (every
+//    thread adds the popcounts of the bitmap words it needs: <= 36 words);
 //  - an id's place in its block is the number of earlier tokens in its
 //    expert's mask (ids of one expert come one per token, so this is the
 //    ascending flat order the alignment lists them in);
 //  - npp = A * touched experts; every slot of a block past its count holds
 //    the sentinel n = M * width.
-// Three CTA barriers and no ranking pass: the tail is bound by one warp's
-// dependent instruction stream, not by the amount of work.
-__device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int width, int E_al, int A,
-                                            const uint32_t *tmask, const uint32_t *tbits, int *wpre,
-                                            int *blkcnt, int32_t *sorted, int64_t sorted_cap,
+// The stores of one SM are the bound here (about 7 bytes per clock for
+// scattered and 16-byte stores alike), so sorted_token_ids[0, npp) is built
+// in shared memory -- sentinels, then the ids -- and written by one bulk
+// copy (cp.async.bulk) when it fits sbuf and A is a multiple of 4; otherwise
+// the ids and the padding are stored directly.
+__device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int width, int A,
+                                            const uint32_t *tmask, const uint32_t *tbits, int *blkcnt,
+                                            uint32_t *sbuf, int32_t *sorted, int64_t sorted_cap,
                                             int32_t *expert_ids, int64_t expert_cap, int32_t *npp_out,
                                             uint32_t *err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwd = (E_al + 31) >> 5;  // bitmap words, <= 33
-    if (warp == 0) {
-        const int c = lane < nwd ? __popc(tbits[lane]) : 0;
-        int inc = c;
+    uint32_t bw[kSmallBitWords];  // the touched-expert bitmap (zero past E + S)
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, inc, o);
-            inc += lane >= o ? v : 0;
-        }
-        wpre[lane] = inc - c;
-        if (lane == 31) wpre[32] = inc;  // blocks before word 32 (E + S = 1025 only)
+    for (int w = 0; w < kSmallBitWords; w += 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(tbits + w);
+        bw[w] = v.x; bw[w + 1] = v.y; bw[w + 2] = v.z; bw[w + 3] = v.w;
     }
-    __syncwarp();
-    __syncthreads();
+    int nblk = 0;
+#pragma unroll
+    for (int w = 0; w < kSmallBitWords; ++w) nblk += __popc(bw[w]);
     const int n = M * width;
+    const int npp = nblk * A;
+    if (tid == 0) *npp_out = npp;
+    const bool bulk = (A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0 &&
+                      npp <= kSmallSortedWords && (int64_t)npp <= sorted_cap;
     uint32_t bad = 0;
+    if (bulk) {
+#pragma unroll 1
+        for (int q = tid * 4; q < npp; q += kSmallThreads * 4)
+            *reinterpret_cast<uint4 *>(sbuf + q) = make_uint4(n, n, n, n);
+        __syncthreads();
+    }
 #pragma unroll 1
     for (int m = warp; m < M; m += kSmallWarps) {
         if (lane < width) {
             const int i = m * width + lane;
-            const int e = (int)(keys_s[i] >> 10);
+            const int e = (int)(keys_s[i] >> 10), we = e >> 5;
             const uint32_t tm = tmask[e];
             const int j = __popc(tm & ((1u << m) - 1u));
-            const int b = wpre[e >> 5] + __popc(tbits[e >> 5] & ((1u << (e & 31)) - 1u));
-            st_slot(sorted, (int64_t)b * A + j, sorted_cap, i, bad);
+            int b = 0;
+#pragma unroll
+            for (int w = 0; w < kSmallBitWords; ++w) b += (w < we) ? __popc(bw[w]) : 0;
+            b += __popc(tbits[we] & ((1u << (e & 31)) - 1u));
+            if (bulk) sbuf[b * A + j] = (uint32_t)i;
+            else st_slot(sorted, (int64_t)b * A + j, sorted_cap, i, bad);
             if (j == 0) {
                 blkcnt[b] = __popc(tm);
                 st_slot(expert_ids, b, expert_cap, e, bad);
@@ -272,14 +288,25 @@ __device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int w
         }
         __syncwarp();
     }
-    const int nblk = wpre[32] + (nwd > 32 ? __popc(tbits[32]) : 0);
-    const int npp = nblk * A;
-    if (tid == 0) *npp_out = npp;
+    if (bulk) {
+        // the generic-proxy writes of sbuf become visible to the bulk copy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (tid == 0 && npp > 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                         ::"l"(sorted), "r"(smem_u32(sbuf)), "r"(npp * 4) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            // the CTA's shared memory must outlive the copy's reads of it
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+        report_bad_slots(bad, err);
+        return;
+    }
     __syncwarp();
     __syncthreads();
-    // the padding: slots j >= the block's count (16-byte stores when A is a
-    // multiple of 4, so that four slots never straddle two blocks, and the
-    // array is 16-byte aligned)
+    // direct padding stores: slots j >= the block's count (16-byte stores
+    // when A is a multiple of 4, so that four slots never straddle two
+    // blocks, and the array is 16-byte aligned)
     const bool pow2 = (A & (A - 1)) == 0;
     const int lgA = __ffs(A) - 1;
     if ((A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0) {
@@ -628,8 +655,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     __syncthreads();
     if (P.mask_align) {
         int *blkcnt = reinterpret_cast<int *>(keys_s + kSmallMaxM * 32);  // [<= n] ids per block
-        int *wpre = blkcnt + kSmallMaxM * 32;                              // [33] blocks before each word
-        align_masks(keys_s, p.M, width, rows, p.A, tmask, tbits, wpre, blkcnt, p.sorted, p.sorted_cap,
+        uint32_t *sbuf = tbits + kSmallBitWords;                           // [kSmallSortedWords]
+        align_masks(keys_s, p.M, width, p.A, tmask, tbits, blkcnt, sbuf, p.sorted, p.sorted_cap,
                     p.expert_ids, p.expert_cap, p.npp, &hdr->error);
         return;
     }
@@ -653,6 +680,9 @@ static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaSt
         cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB, NK>,
                                              cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(small_route_kernel<NB, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
