@@ -40,7 +40,7 @@ METRIC = ("µs per route+align call at M=4/8 and routed tokens/s at M=16K; "
 M_LARGE, H, E, K, S, A_LARGE = 16384, 4096, 512, 10, 1, 128
 WORKLOAD = ("large_batch: M=16384 tokens, H=4096, E=512 routed + 1 shared gate, "
             "top-10 softmax+renormalize + shared slot, route + align at A=128")
-ORACLE_SAMPLE_ROWS = 1024      # cpu_baseline: rows of the large batch (~10-30 s)
+ORACLE_SAMPLE_ROWS = 4096      # cpu_baseline: rows of the large batch (~10-30 s)
 REFERENCE_BUDGET_S = 90.0      # --impl reference: whole run, warm-up included
 
 
