@@ -443,7 +443,9 @@ def run_smr(args):
                                            "peak_gbs": hbm_gbs, "frac": t_roof / r["us_per_call"],
                                            "peak_source": src},
                               "timing": f"CUDA graph of 100 calls over {r['ring_copies']} gate/hidden "
-                                        f"copies (> 2x L2), median of 20 replays"}
+                                        f"copies (> 2x L2), median of 20 replays; a call may launch "
+                                        f"during the previous call's tail (programmatic dependent "
+                                        f"launch) and stream its gate before waiting for it"}
         line["small_m"] = small
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline_large()

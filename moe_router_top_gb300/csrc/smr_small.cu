@@ -507,25 +507,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     const int row0 = rg * 16;
 
     // the group leader (rank 0) finishes the group's logits with thread
-    // (row r16, token m16): the routed bias of its row is loaded now; the
-    // tail CTA clears its token masks and bitmap
+    // (row r16, token m16); the tail CTA clears its token masks and bitmap
     const int r16 = tid >> 4, m16 = tid & 15;  // 256 threads = 16 rows x 16 tokens
     uint32_t *tmask = reinterpret_cast<uint32_t *>(smem) + kSmallFrontWords;  // [E + S]
     uint32_t *tbits = tmask + kSmallMaskWords;                                 // [ceil((E + S) / 32)]
-    // this call's tag: a 31-bit call count with the top bit set, so that it
-    // never equals a cleared word (0) or a nonnegative int32 the align leaves
-    // in a shared workspace; the leader of the last row group runs the tail
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.hdr);
     const bool tail_cta = kq == 0 && rg == (int)(gridDim.x / (unsigned)P.KQ) - 1;
-    float bias_v = 0.0f;
-    uint32_t tag = 0u;
-    if (kq == 0) {
-        tag = ((__ldcg(&hdr->epoch) + 1u) & 0x7FFFFFFFu) | 0x80000000u;
-        if (p.bias != nullptr && row0 + r16 < p.E) bias_v = __ldg(p.bias + row0 + r16);
-        if (tail_cta && P.mask_align) {
-            for (int i = tid; i < rows; i += kSmallThreads) tmask[i] = 0u;
-            if (tid < kSmallBitWords) tbits[tid] = 0u;
-        }
+    if (kq == 0 && tail_cta && P.mask_align) {
+        for (int i = tid; i < rows; i += kSmallThreads) tmask[i] = 0u;
+        if (tid < kSmallBitWords) tbits[tid] = 0u;
     }
 
     // ---- 1. gate rows x tokens on the tensor cores ----
@@ -543,18 +533,30 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         for (int j = 0; j < 4; ++j) acc[nb][j] = 0.0f;
 
     const int s_beg = kq * P.per_cta, s_end = min(s_beg + P.per_cta, P.slices);
+    bool waited = false;
     for (int s0 = s_beg + warp; s0 < s_end; s0 += kSmallWarps * kMaxSlicesPerWarp) {
         uint4 va[kMaxSlicesPerWarp], vb[kMaxSlicesPerWarp], x0[kMaxSlicesPerWarp],
             x1[kMaxSlicesPerWarp];
 #pragma unroll
         for (int j = 0; j < kMaxSlicesPerWarp; ++j) {
             const int s = s0 + j * kSmallWarps;
-            const int k0 = s * kSliceK + 8 * t;
-            const int kc = min(k0, p.H - 8);  // clamped so every load stays in bounds
+            const int kc = min(s * kSliceK + 8 * t, p.H - 8);  // clamped so every load stays in bounds
             va[j] = ld_stream_v4(wa + kc);
             vb[j] = ld_stream_v4(wb + kc);
-            x0[j] = __ldg(reinterpret_cast<const uint4 *>(xa + kc));
-            if (NB > 1) x1[j] = __ldg(reinterpret_cast<const uint4 *>(xb + kc));
+        }
+        // The gate weights are the layer's parameters; the hidden states may
+        // come from the previous kernel in the stream: the first batch of gate
+        // loads is in flight before waiting for that kernel to complete.
+        if (!waited) {
+            griddep_wait();
+            waited = true;
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxSlicesPerWarp; ++j) {
+            const int s = s0 + j * kSmallWarps;
+            const int kc = min(s * kSliceK + 8 * t, p.H - 8);
+            x0[j] = __ldcg(reinterpret_cast<const uint4 *>(xa + kc));
+            if (NB > 1) x1[j] = __ldcg(reinterpret_cast<const uint4 *>(xb + kc));
         }
 #pragma unroll
         for (int j = 0; j < kMaxSlicesPerWarp; ++j) {
@@ -574,6 +576,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
                 mma_bf16_16816(acc[NB - 1], va[j].z, vb[j].z, va[j].w, vb[j].w, x1[j].z, x1[j].w);
             }
         }
+    }
+
+    // everything below reads or writes data the previous kernel may use
+    // (bias, workspace, outputs): after its completion (a warp without
+    // slices has not waited yet)
+    griddep_wait();
+    // this call's tag: a 31-bit call count with the top bit set, so that it
+    // never equals a cleared word (0) or a nonnegative int32 the align leaves
+    // in a shared workspace; the leader of the last row group runs the tail
+    float bias_v = 0.0f;
+    uint32_t tag = 0u;
+    if (kq == 0) {
+        tag = ((__ldcg(&hdr->epoch) + 1u) & 0x7FFFFFFFu) | 0x80000000u;
+        if (p.bias != nullptr && row0 + r16 < p.E) bias_v = __ldcg(p.bias + row0 + r16);
     }
 
     // ---- 2. sum the 8 warps, then the cluster's K ranges, in a fixed order ----
@@ -632,6 +648,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     // the tail loads each word until it holds this call's tag (the other
     // groups' CTAs have all been launched alongside; they only need SMs).
     if (!tail_cta) return;
+    // every other CTA has finished its gate stream (or exited): the next
+    // kernel in the stream may launch now (programmatic dependent launch) and
+    // stream its own weights during this tail; whatever it reads from this
+    // kernel it reads after its own wait
+    griddep_launch_dependents();
     __syncwarp();  // a split warp would replay the whole tail once per path
 
     // ---- 4. tail: top-k + softmax, one warp per token ----
@@ -691,13 +712,18 @@ static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaSt
     cfg.blockDim = dim3(kSmallThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)P.KQ;  // the K ranges of one row group
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start before the previous kernel in the stream completes (it waits
+    // for that kernel before reading the hidden states or touching the
+    // workspace and outputs)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, small_route_kernel<NB, NK>, P);
 }
 

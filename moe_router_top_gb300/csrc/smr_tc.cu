@@ -487,9 +487,12 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 const int g = ch * (CW / kGroup) + u;
                 st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                const uint32_t mx = __vmaxu2(__vmaxu2(ordered_bf16x2(wv[0]), ordered_bf16x2(wv[1])),
-                                             __vmaxu2(ordered_bf16x2(wv[2]), ordered_bf16x2(wv[3])));
-                const uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
+                // the group's maximum: bf16 pair maxima, then one conversion to
+                // ordered keys; a -0 maximum counts as +0 (equal values)
+                const uint32_t bm = max_bf16x2(max_bf16x2(wv[0], wv[1]), max_bf16x2(wv[2], wv[3]));
+                const uint32_t mx = ordered_bf16x2(bm);
+                uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
+                gmax16 = (gmax16 == 0x7FFFu) ? 0x8000u : gmax16;
                 pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
                 if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
             }

@@ -243,6 +243,33 @@ def test_workspace_reuse_is_deterministic(smr):
     assert smr.get_device_error(wsp) == 0
 
 
+def test_back_to_back_small_calls_share_a_workspace(smr):
+    """Consecutive single-launch calls on one stream and one workspace: each
+    call may launch while the previous one's tail still runs (it streams its
+    gate weights, then waits for that call before touching the workspace or
+    the hidden states). Every call must give the result of an isolated call."""
+    cases = [inputs.make_route_inputs(M, 1024, 256, 8, 1, seed=60 + M) for M in (4, 9, 1, 16)]
+    dev = [_dev(ri) for ri in cases]
+    ref = []
+    for (x, w, ws, b) in dev:
+        out = smr.route_align(x, w, ws, b, topk=8, block_size=64, workspace=smr.Workspace())
+        torch.cuda.synchronize()
+        ref.append([t.clone() for t in out])
+    wsp = smr.Workspace()
+    got = []
+    for i in range(12):
+        x, w, ws, b = dev[i % 4]
+        got.append(smr.route_align(x, w, ws, b, topk=8, block_size=64, workspace=wsp))
+    torch.cuda.synchronize()
+    for i, out in enumerate(got):
+        r = ref[i % 4]
+        n = int(r[4].item())
+        assert torch.equal(out[0], r[0]) and torch.equal(out[1], r[1])
+        assert int(out[4].item()) == n
+        assert torch.equal(out[2][:n], r[2][:n]) and torch.equal(out[3][: n // 64], r[3][: n // 64])
+    assert smr.get_device_error(wsp) == 0
+
+
 # ----------------------------------------------------------------- align --
 
 @pytest.mark.parametrize("T,W,E_al,A,skew", [
