@@ -250,19 +250,29 @@ def bench_large(args, world, rank, torch, smr, inputs):
     assert smr.get_device_error(wsp) == 0
 
     # the route kernel alone (roofline): route-only calls on the same
-    # alternating inputs, each bracketed by CUDA events on the launch stream
-    n_route = max(3, min(args.steps, 500))
+    # alternating inputs, replayed from a CUDA graph of RG launches (so host
+    # submission never shows in the interval), CUDA events on the replay
+    # stream around each replay; per launch = replay time / RG
+    RG = 20
+    with torch.cuda.stream(cap_stream):
+        for i in range(3):
+            smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
+    torch.cuda.synchronize()
+    rgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rgraph, stream=cap_stream):
+        for i in range(RG):
+            smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
+    rgraph.replay()
+    torch.cuda.synchronize()
+    n_rep = max(3, min(args.steps // RG, 25))
     route_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(n_route)]
-    for i in range(3):
-        smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
+                for _ in range(n_rep)]
+    for a, b in route_ev:
+        a.record(stream)
+        rgraph.replay()
+        b.record(stream)
     torch.cuda.synchronize()
-    for i in range(n_route):
-        route_ev[i][0].record(stream)
-        smr.route(xs[i & 1], w, ws, topk=K, topk_ids=ids, topk_weights=wts, workspace=wsp)
-        route_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    route_ms = statistics.mean(a.elapsed_time(b) for a, b in route_ev)
+    route_ms = statistics.median(a.elapsed_time(b) for a, b in route_ev) / RG
     assert smr.get_device_error(wsp) == 0
 
     # e2e: hidden states from pinned host memory, outputs back to the host
@@ -424,8 +434,9 @@ def run_smr(args):
                      "traffic": traffic_from_profile(),
                      "kernel": "tc_route_kernel (gate GEMM + fused top-k epilogue)",
                      "kernel_us": res["route_ms"] * 1000.0,
-                     "kernel_timing": "route-only calls on the same alternating inputs, CUDA events "
-                                      "around each launch on its stream",
+                     "kernel_timing": "route-only launches on the same alternating inputs, replayed "
+                                      "from a CUDA graph of 20; CUDA events on the stream around "
+                                      "each replay (median) / 20, inter-launch gaps included",
                      "peak_source": f"{src} bf16 dense (burst)"},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],

@@ -28,6 +28,7 @@ constexpr int kAlignWarps = kAlignThreads / 32;
 
 __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const AlignLaunch a) {
     extern __shared__ __align__(16) int sm[];
+    griddep_launch_dependents();  // the next kernel may launch; it waits for this grid
     griddep_wait();  // the ids come from the previous kernel
     uint32_t *err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
     int *ids = sm;  // [kAlignSingleMax] staged ids
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_count_kernel(const Al
     for (int i0 = beg; i0 < end; i0 += 4 * kTileThreads) {
         int v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = __ldg(a.ids + min(i0 + j * kTileThreads + tid, end - 1));
+        for (int j = 0; j < 4; ++j) v[j] = __ldcg(a.ids + min(i0 + j * kTileThreads + tid, end - 1));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (i0 + j * kTileThreads + tid < end) {
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
     int v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-        v[j] = __ldg(a.tile_counts + (int64_t)min(t0 + j, ntiles - 1) * a.E_al + ec);
+        v[j] = __ldcg(a.tile_counts + (int64_t)min(t0 + j, ntiles - 1) * a.E_al + ec);
     int sum = 0;
 #pragma unroll
     for (int j = 0; j < 16; ++j) sum += (t0 + j < t1) ? v[j] : 0;
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
         int w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            w[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
+            w[j] = __ldcg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
 #pragma unroll
         for (int j = 0; j < 16; ++j) sum += (t + j < t1) ? w[j] : 0;
     }
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
         int w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            w[j] = __ldg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
+            w[j] = __ldcg(a.tile_counts + (int64_t)min(t + j, ntiles - 1) * a.E_al + ec);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             if (t + j < t1 && e < a.E_al) a.tile_base[(int64_t)(t + j) * a.E_al + e] = run;
@@ -168,12 +169,13 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
     const int beg = t * tile, n = min(beg + tile, a.numel) - beg;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lt = lanemask_lt();
+    griddep_launch_dependents();  // the next kernel may launch; it waits for this grid
     griddep_wait();  // the tile starts and totals come from the previous kernel
     // the first sub-chunk's ids (warp w: slots w*128 + g*32 + lane), this
     // tile's starts and the totals: all loads issued first, one round trip
     auto load_ids = [&](int c0, int (&e4)[4]) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) e4[g] = __ldg(a.ids + beg + min(c0 + warp * 128 + g * 32 + lane, n - 1));
+        for (int g = 0; g < 4; ++g) e4[g] = __ldcg(a.ids + beg + min(c0 + warp * 128 + g * 32 + lane, n - 1));
     };
     int e4[4];
     load_ids(0, e4);
@@ -182,8 +184,8 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
         const int e = min(threadIdx.x + j * kTileThreads, E_al - 1);
-        bse[j] = __ldg(a.tile_base + (int64_t)t * E_al + e);
-        tt[j] = __ldg(a.totals + e);
+        bse[j] = __ldcg(a.tile_base + (int64_t)t * E_al + e);
+        tt[j] = __ldcg(a.totals + e);
     }
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
@@ -285,17 +287,18 @@ __global__ void __launch_bounds__(kTileThreads) align_rows_scatter_kernel(const 
     const int t = blockIdx.x, ntiles = gridDim.x, warp = tid >> 5, lane = tid & 31;
     const int tile = kTcCountRows * width;
     const int beg = t * tile, n = min(beg + tile, a.numel) - beg;
+    griddep_launch_dependents();  // the next kernel may launch; it waits for this grid
     griddep_wait();  // the tile starts and totals come from the previous kernel
     int ev[kRowsMaxSlots];
 #pragma unroll
-    for (int j = 0; j < kRowsMaxSlots; ++j) ev[j] = __ldg(a.ids + beg + min(tid + j * kTileThreads, n - 1));
+    for (int j = 0; j < kRowsMaxSlots; ++j) ev[j] = __ldcg(a.ids + beg + min(tid + j * kTileThreads, n - 1));
     constexpr int kPerThread = (kMaxExpertsAl + kTileThreads - 1) / kTileThreads;
     int bse[kPerThread], tt[kPerThread];
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
         const int e = min(tid + j * kTileThreads, E_al - 1);
-        bse[j] = __ldg(a.tile_base + (int64_t)t * E_al + e);
-        tt[j] = __ldg(a.totals + e);
+        bse[j] = __ldcg(a.tile_base + (int64_t)t * E_al + e);
+        tt[j] = __ldcg(a.totals + e);
     }
     for (int q = tid; q < 2 * E_al; q += kTileThreads) mask[q] = 0u;
 #pragma unroll

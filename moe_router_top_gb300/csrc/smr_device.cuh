@@ -160,6 +160,13 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync(), for work placed between them.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -601,8 +608,8 @@ __device__ __forceinline__ void stage_ids(int *dst, const int32_t *src, int n) {
     const int n4 = vec ? (n >> 2) : 0;
     const int4 *s4 = reinterpret_cast<const int4 *>(src);
     int4 *d4 = reinterpret_cast<int4 *>(dst);
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) d4[i] = __ldg(s4 + i);
-    for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(src + i);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) d4[i] = __ldcg(s4 + i);
+    for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(src + i);
     __syncwarp();
     __syncthreads();
 }

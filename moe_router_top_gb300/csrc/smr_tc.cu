@@ -324,16 +324,22 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         tmem_relinquish_pair();
     }
     griddep_launch_dependents();  // the align launches may start; they wait for this grid
-    for (int i = threadIdx.x; i < p.E; i += kTcThreads) bias_s[i] = p.bias ? p.bias[i] : 0.0f;
-    for (int i = threadIdx.x; i < 2 * (p.E + p.S); i += kTcThreads) hist[i] = 0;
-    if (p.S) {  // shared gate row, zero-padded to whole k-blocks
+    // barriers initialised and TMEM allocated in this CTA; the producer and
+    // the MMA issuer start once the peer is there too, while the other warps
+    // stage what only later steps read (overlapping the first loads)
+    tc_fence_before();
+    cluster_arrive();
+    if (warp == 2 || warp == 3) {  // bias and expert counts, read in the epilogue
+        for (int i = threadIdx.x - 64; i < p.E; i += 64) bias_s[i] = p.bias ? p.bias[i] : 0.0f;
+        for (int i = threadIdx.x - 64; i < 2 * (p.E + p.S); i += 64) hist[i] = 0;
+    } else if (warp >= 4 && p.S) {  // shared gate row, zero-padded to whole k-blocks
         const int nch = p.H >> 3;
-        for (int c = threadIdx.x; c < p.num_kb * (kTcBK / 8); c += kTcThreads)
+        for (int c = threadIdx.x - 128; c < p.num_kb * (kTcBK / 8); c += 128)
             reinterpret_cast<uint4 *>(ws_s)[c] =
                 c < nch ? reinterpret_cast<const uint4 *>(p.ws)[c] : make_uint4(0u, 0u, 0u, 0u);
+        asm volatile("bar.sync 2, 128;" ::: "memory");  // the 4 shared-logit warps read all of it
     }
-    tc_fence_before();
-    cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
+    cluster_wait();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -351,21 +357,38 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // a tile entirely past M (the padding partner of a pair) loads a
             // valid tile instead; its results are never written
             const int m_load = m0 < p.M ? m0 : 0;
+            // the gate pieces of the first stages (layer parameters) are
+            // requested before waiting for the previous kernel in the stream
+            // (programmatic dependent launch), the hidden states after it
+            const int pre = min(ST, p.num_kb);
+            for (int kb = 0; kb < pre; ++kb) {
+                const uint32_t fb = cluster_addr(smem_u32(&full[kb]), 0u);  // leader's barrier
+                if (leader) mbar_arrive_expect_tx(smem_u32(&full[kb]), 2u * p.stage_bytes);
+                const uint32_t b_dst = smem_u32(smem + (size_t)kb * p.stage_bytes) + kTcBM * kTcSW;
+                for (int pc = 0; pc < p.n_pieces; ++pc)
+                    tma_load_2d_pair(b_dst + (uint32_t)pc * half * kTcSW, &tm_w, kb * kTcBK,
+                                     pc * p.piece_n + (int)(rank * half), fb);
+            }
+            griddep_wait();
             int kb = 0;
             for (; kb < p.num_kb; ++kb) {
                 const int s = kb % ST;
                 const uint32_t ph = (uint32_t)(kb / ST) & 1u;
-                // a stage is refilled once the MMAs (and, with a shared gate,
-                // the shared-logit warps) are done with it
-                if (!mbar_wait_bounded(smem_u32(p.S ? &empty[s] : &mma_done[s]), ph ^ 1u, abort_flag)) break;
                 const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0u);  // leader's barrier
-                if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * p.stage_bytes);
                 const uint32_t a_dst = smem_u32(smem + (size_t)s * p.stage_bytes);
+                if (kb >= pre) {
+                    // a stage is refilled once the MMAs (and, with a shared
+                    // gate, the shared-logit warps) are done with it
+                    if (!mbar_wait_bounded(smem_u32(p.S ? &empty[s] : &mma_done[s]), ph ^ 1u, abort_flag)) break;
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * p.stage_bytes);
+                }
                 tma_load_2d_pair(a_dst, &tm_x, kb * kTcBK, m_load, fb);
-                const uint32_t b_dst = a_dst + kTcBM * kTcSW;
-                for (int pc = 0; pc < p.n_pieces; ++pc)
-                    tma_load_2d_pair(b_dst + (uint32_t)pc * half * kTcSW, &tm_w, kb * kTcBK,
-                                     pc * p.piece_n + (int)(rank * half), fb);
+                if (kb >= pre) {
+                    const uint32_t b_dst = a_dst + kTcBM * kTcSW;
+                    for (int pc = 0; pc < p.n_pieces; ++pc)
+                        tma_load_2d_pair(b_dst + (uint32_t)pc * half * kTcSW, &tm_w, kb * kTcBK,
+                                         pc * p.piece_n + (int)(rank * half), fb);
+                }
             }
             if (kb < p.num_kb) set_error(p.err, kErrWaitTimeout);
         }
@@ -440,6 +463,8 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     // once per CTA after other kernels have used the SM, so its instructions
     // are fetched cold: it is written as short rolled loops (k rounds of a
     // 32-key maximum, a pointer merge) rather than unrolled sorting networks.
+    griddep_wait();   // outputs and counts are written only after the previous kernel completed
+    __syncthreads();  // the bias and count staging of warps 2-3 is visible to every warp
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
     tc_fence_after();
     ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
@@ -765,13 +790,17 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;  // CTA pairs
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start before the previous kernel in the stream completes (it waits
+    // for that kernel before loading hidden states or writing anything)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, tc_route_kernel<NGM, CW>, mx, mw, plan.p);
 }
 
