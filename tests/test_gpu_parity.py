@@ -293,6 +293,43 @@ def test_align_standalone(smr, T, W, E_al, A, skew):
     assert smr.last_launch_count() == (1 if T * W <= 8192 else 3)
 
 
+def test_align_reused_workspace_back_to_back(smr):
+    """Consecutive multi-tile aligns on one workspace and stream, alternating
+    two id sets: each kernel may launch before its predecessor finishes, so
+    what another kernel writes must be read through L2, never from a stale
+    line of an earlier call on the same SM. Every result matches the oracle."""
+    sets = [inputs.random_ids(60000, 11, 513, seed=s, skew=1.1) for s in (5, 6)]
+    dids = [torch.from_numpy(i).cuda() for i in sets]
+    wsp = smr.Workspace()
+    outs = [smr.align(dids[i % 2], 513, 128, workspace=wsp) for i in range(6)]
+    torch.cuda.synchronize()
+    for i, (srt, eids, npp) in enumerate(outs):
+        check_align(sets[i % 2], 513, 128, srt.cpu().numpy(), eids.cpu().numpy(), npp.cpu().numpy())
+    assert smr.get_device_error(wsp) == 0
+
+
+def test_route_align_reused_workspace_back_to_back(smr):
+    """tcgen05 route + two-launch align, four calls on one workspace and
+    stream with alternating inputs: each matches an isolated call."""
+    cases = [inputs.make_route_inputs(2049, 512, 256, 8, 1, seed=s) for s in (71, 72)]
+    dev = [_dev(ri) for ri in cases]
+    ref = []
+    for (x, w, ws, b) in dev:
+        out = smr.route_align(x, w, ws, b, topk=8, block_size=128, workspace=smr.Workspace())
+        torch.cuda.synchronize()
+        ref.append([t.clone() for t in out])
+    wsp = smr.Workspace()
+    got = [smr.route_align(*dev[i % 2], topk=8, block_size=128, workspace=wsp) for i in range(4)]
+    torch.cuda.synchronize()
+    for i, out in enumerate(got):
+        r = ref[i % 2]
+        n = int(r[4].item())
+        assert torch.equal(out[0], r[0]) and torch.equal(out[1], r[1])
+        assert int(out[4].item()) == n
+        assert torch.equal(out[2][:n], r[2][:n]) and torch.equal(out[3][: n // 128], r[3][: n // 128])
+    assert smr.get_device_error(wsp) == 0
+
+
 def test_align_bad_id_sets_error_bit(smr):
     ids = inputs.random_ids(20, 4, 16, seed=1)
     ids[3, 2] = 16  # out of range
