@@ -238,9 +238,11 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
 //    the sentinel n = M * width.
 // The stores of one SM are the bound here (about 7 bytes per clock for
 // scattered and 16-byte stores alike), so sorted_token_ids[0, npp) is built
-// in shared memory -- sentinels, then the ids -- and written by one bulk
-// copy (cp.async.bulk) when it fits sbuf and A is a multiple of 4; otherwise
-// the ids and the padding are stored directly.
+// in shared memory and written by one bulk copy (cp.async.bulk) when it fits
+// sbuf and A is a multiple of 4; otherwise the ids and the padding are stored
+// directly. sbuf holds the sentinel over [0, min(kSmallSortedWords,
+// A * min(E + S, n))) on entry (filled at the kernel's start), which covers
+// any npp: the ids are placed into it.
 __device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int width, int A,
                                             const uint32_t *tmask, const uint32_t *tbits, int *blkcnt,
                                             uint32_t *sbuf, int32_t *sorted, int64_t sorted_cap,
@@ -262,12 +264,6 @@ __device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int w
     const bool bulk = (A & 3) == 0 && (reinterpret_cast<uintptr_t>(sorted) & 15u) == 0 &&
                       npp <= kSmallSortedWords && (int64_t)npp <= sorted_cap;
     uint32_t bad = 0;
-    if (bulk) {
-#pragma unroll 1
-        for (int q = tid * 4; q < npp; q += kSmallThreads * 4)
-            *reinterpret_cast<uint4 *>(sbuf + q) = make_uint4(n, n, n, n);
-        __syncthreads();
-    }
 #pragma unroll 1
     for (int m = warp; m < M; m += kSmallWarps) {
         if (lane < width) {
@@ -516,6 +512,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     if (kq == 0 && tail_cta && P.mask_align) {
         for (int i = tid; i < rows; i += kSmallThreads) tmask[i] = 0u;
         if (tid < kSmallBitWords) tbits[tid] = 0u;
+        // the staged sorted_token_ids start as the sentinel n = M * (k + S),
+        // over the largest range the align can use: A * min(E + S, n) slots
+        const int n = p.M * (p.k + p.S);
+        const int fill = (int)min((int64_t)kSmallSortedWords, (int64_t)p.A * min(rows, n));
+        uint4 *sb4 = reinterpret_cast<uint4 *>(tbits + kSmallBitWords);
+        for (int q = tid; q < (fill + 3) / 4; q += kSmallThreads) sb4[q] = make_uint4(n, n, n, n);
     }
 
     // ---- 1. gate rows x tokens on the tensor cores ----
