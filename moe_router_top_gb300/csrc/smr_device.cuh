@@ -249,7 +249,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-// Acquire-release atomic add at GPU scope; returns the old value.
 // Relaxed 64-bit accesses at GPU scope (naturally aligned: single-copy
 // atomic, so a reader sees either the old or the new word whole).
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
@@ -260,10 +259,13 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t *p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+// 32-bit store into another CTA's shared memory that completes 4 bytes of
+// the transaction count of an mbarrier there (both addresses from
+// cluster_addr); no fence and no cluster barrier: the receiver waits on its
+// mbarrier.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 ::"r"(addr), "r"(__float_as_uint(v)), "r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)

@@ -509,6 +509,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     uint32_t *tbits = tmask + kSmallMaskWords;                                 // [ceil((E + S) / 32)]
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.hdr);
     const bool tail_cta = kq == 0 && rg == (int)(gridDim.x / (unsigned)P.KQ) - 1;
+    // the group leader's barrier for the other K ranges' partial sums: set
+    // up now, expecting their bytes; every CTA of the cluster arrives at the
+    // cluster barrier here and waits on it only before its remote stores
+    __shared__ __align__(8) uint64_t s_red_bar;
+    __shared__ int s_red_abort;
+    if (kq == 0 && tid == 0) {
+        s_red_abort = 0;
+        mbar_init(smem_u32(&s_red_bar), 1);
+        mbar_fence_init();
+        mbar_arrive_expect_tx(smem_u32(&s_red_bar), (uint32_t)(P.KQ - 1) * 256u * 4u);
+    }
+    __syncwarp();
+    cluster_arrive();
     if (kq == 0 && tail_cta && P.mask_align) {
         for (int i = tid; i < rows; i += kSmallThreads) tmask[i] = 0u;
         if (tid < kSmallBitWords) tbits[tid] = 0u;
@@ -612,16 +625,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     __syncwarp();
     __syncthreads();
     {
-        // this K range's sum over the warps -> slot kq of the group leader
+        // this K range's sum over the warps -> slot kq of the group leader:
+        // the leader keeps its own; the others send theirs with st.async,
+        // which completes bytes on the leader's barrier, and are done
         float v = 0.0f;
 #pragma unroll
         for (int w = 0; w < kSmallWarps; ++w) v += red[w * 256 + tid];  // tid = row * 16 + token
-        st_cluster_f32(cluster_addr(smem_u32(slots + kq * 256 + tid), 0u), v);
+        cluster_wait();  // the leader's barrier is initialised
+        if (kq != 0) {
+            st_async_cluster_f32(cluster_addr(smem_u32(slots + kq * 256 + tid), 0u), v,
+                                 cluster_addr(smem_u32(&s_red_bar), 0u));
+            return;
+        }
+        slots[tid] = v;  // read back by this thread only
     }
-    // the cluster barrier publishes every CTA's slot to the leader; the other
-    // CTAs are done after it
-    cluster_sync();
-    if (kq != 0) return;
+    // the other K ranges' slots have landed (bounded wait; on timeout the
+    // error bit is set and the sums are not valid)
+    if (!mbar_wait_bounded(smem_u32(&s_red_bar), 0u, &s_red_abort) && tid == 0)
+        set_error(&hdr->error, kErrWaitTimeout);
     {
         // the group's final logits: a routed one becomes its selection key
         // (bias added in fp32, then rounded to bf16); the shared expert's
