@@ -229,8 +229,9 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
 // moe_align block size", Purpose) for a small batch whose every expert fits
 // one block (A >= M: an expert receives at most one id per token), from
 // the per-expert token masks and the touched-expert bitmap the top-k filled:
-//  - an expert's block is the number of touched experts below it (every
-//    thread adds the popcounts of the bitmap words it needs: <= 36 words);
+//  - an expert's block is the number of touched experts below it (warp 0
+//    scans the popcounts of the <= 36 bitmap words; then one popcount
+//    within the expert's word);
 //  - an id's place in its block is the number of earlier tokens in its
 //    expert's mask (ids of one expert come one per token, so this is the
 //    ascending flat order the alignment lists them in);
@@ -244,20 +245,35 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
 // A * min(E + S, n))) on entry (filled at the kernel's start), which covers
 // any npp: the ids are placed into it.
 __device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int width, int A,
-                                            const uint32_t *tmask, const uint32_t *tbits, int *blkcnt,
+                                            const uint32_t *tmask, const uint32_t *tbits, int *wpre, int *blkcnt,
                                             uint32_t *sbuf, int32_t *sorted, int64_t sorted_cap,
                                             int32_t *expert_ids, int64_t expert_cap, int32_t *npp_out,
                                             uint32_t *err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t bw[kSmallBitWords];  // the touched-expert bitmap (zero past E + S)
+    // warp 0: touched experts before each bitmap word (an exclusive scan of
+    // the words' popcounts; words 32-35 are summed by lane 31) and in all
+    if (warp == 0) {
+        const int c = __popc(tbits[lane]);
+        int inc = c;
 #pragma unroll
-    for (int w = 0; w < kSmallBitWords; w += 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(tbits + w);
-        bw[w] = v.x; bw[w + 1] = v.y; bw[w + 2] = v.z; bw[w + 3] = v.w;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            inc += lane >= o ? v : 0;
+        }
+        wpre[lane] = inc - c;
+        if (lane == 31) {
+            int run = inc;
+#pragma unroll
+            for (int w = 32; w < kSmallBitWords; ++w) {
+                wpre[w] = run;
+                run += __popc(tbits[w]);
+            }
+            wpre[kSmallBitWords] = run;
+        }
     }
-    int nblk = 0;
-#pragma unroll
-    for (int w = 0; w < kSmallBitWords; ++w) nblk += __popc(bw[w]);
+    __syncwarp();
+    __syncthreads();
+    const int nblk = wpre[kSmallBitWords];
     const int n = M * width;
     const int npp = nblk * A;
     if (tid == 0) *npp_out = npp;
@@ -271,10 +287,7 @@ __device__ __forceinline__ void align_masks(const uint32_t *keys_s, int M, int w
             const int e = (int)(keys_s[i] >> 10), we = e >> 5;
             const uint32_t tm = tmask[e];
             const int j = __popc(tm & ((1u << m) - 1u));
-            int b = 0;
-#pragma unroll
-            for (int w = 0; w < kSmallBitWords; ++w) b += (w < we) ? __popc(bw[w]) : 0;
-            b += __popc(tbits[we] & ((1u << (e & 31)) - 1u));
+            const int b = wpre[we] + __popc(tbits[we] & ((1u << (e & 31)) - 1u));
             if (bulk) sbuf[b * A + j] = (uint32_t)i;
             else st_slot(sorted, (int64_t)b * A + j, sorted_cap, i, bad);
             if (j == 0) {
@@ -699,8 +712,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     __syncthreads();
     if (P.mask_align) {
         int *blkcnt = reinterpret_cast<int *>(keys_s + kSmallMaxM * 32);  // [<= n] ids per block
+        int *wpre = blkcnt + kSmallMaxM * 32;                              // [37] blocks before each word
         uint32_t *sbuf = tbits + kSmallBitWords;                           // [kSmallSortedWords]
-        align_masks(keys_s, p.M, width, p.A, tmask, tbits, blkcnt, sbuf, p.sorted, p.sorted_cap,
+        align_masks(keys_s, p.M, width, p.A, tmask, tbits, wpre, blkcnt, sbuf, p.sorted, p.sorted_cap,
                     p.expert_ids, p.expert_cap, p.npp, &hdr->error);
         return;
     }
