@@ -80,17 +80,21 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_count_kernel(const Al
         a.tile_counts[(int64_t)blockIdx.x * a.E_al + e] = cnt[e];
 }
 
-// 2. For 32 experts per CTA: every tile's start inside each expert (exclusive
-//    prefix over tiles, in tile order) and each expert's total. Thread
-//    (expert el, chunk c) adds a contiguous run of tiles (coalesced over the
-//    experts); the 32 chunk sums of an expert are then scanned by one warp
-//    (lane = chunk) with shuffles.
-__global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch a, int ntiles) {
-    __shared__ int part[32][33];
-    const int el = threadIdx.x & 31, c = threadIdx.x >> 5;
+// 2. For EPB experts per CTA: every tile's start inside each expert
+//    (exclusive prefix over tiles, in tile order) and each expert's total.
+//    Thread (expert el, chunk c) adds a contiguous run of tiles; the 32
+//    chunk sums of an expert are then scanned by one warp (lane = chunk)
+//    with shuffles. Few experts per CTA spread the tile-start stores (256
+//    tiles x 513 experts: 525 KB at the large batch) over many SMs: one SM
+//    stores only a few bytes per clock.
+template <int EPB>
+__global__ void __launch_bounds__(EPB * 32) align_tile_scan_kernel(const AlignLaunch a, int ntiles) {
+    __shared__ int part[32][EPB + 1];
+    __shared__ int tot_s[EPB];
+    const int el = threadIdx.x % EPB, c = threadIdx.x / EPB;
     griddep_launch_dependents();
     griddep_wait();  // the tile counts come from the previous kernel
-    const int e = blockIdx.x * 32 + el;
+    const int e = blockIdx.x * EPB + el;
     const int ec = min(e, a.E_al - 1);  // clamped: every load stays in bounds
     const int tpc = (ntiles + 31) / 32;
     const int t0 = min(c * tpc, ntiles), t1 = min(t0 + tpc, ntiles);
@@ -115,8 +119,8 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
     __syncthreads();
     {
         // warp w scans expert w's column over the 32 chunks (lane = chunk):
-        // exclusive prefix in place, the total in the extra column
-        const int w = c, q = el;  // this thread's role in the transposed scan
+        // exclusive prefix in place, the total aside
+        const int w = threadIdx.x >> 5, q = threadIdx.x & 31;
         const int x = part[q][w];
         int inc = x;
 #pragma unroll
@@ -125,11 +129,11 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
             inc += q >= o ? y : 0;
         }
         part[q][w] = inc - x;
-        if (q == 31) part[w][32] = inc;
+        if (q == 31) tot_s[w] = inc;
     }
     __syncthreads();
     int run = part[c][el];
-    const int total = part[el][32];
+    const int total = tot_s[el];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         if (t0 + j < t1 && e < a.E_al) a.tile_base[(int64_t)(t0 + j) * a.E_al + e] = run;
@@ -148,6 +152,7 @@ __global__ void __launch_bounds__(1024) align_tile_scan_kernel(const AlignLaunch
     }
     if (c == 0 && e < a.E_al) a.totals[e] = total;
 }
+constexpr int kScanExperts = 8;  // experts per scan CTA (256 threads)
 
 // 3. Per tile: padded expert offsets from the totals (block scan, fixed
 //    order), then the stable scatter of the tile's slots to
@@ -410,8 +415,9 @@ cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream) {
                              stream, a, tile);
         if (e != cudaSuccess) return e;
     }
-    if ((e = configure((const void *)align_tile_scan_kernel, 3, 0)) != cudaSuccess) return e;
-    e = launch_dependent(align_tile_scan_kernel, (a.E_al + 31) / 32, 1024, 0, stream, a, ntiles);
+    if ((e = configure((const void *)align_tile_scan_kernel<kScanExperts>, 3, 0)) != cudaSuccess) return e;
+    e = launch_dependent(align_tile_scan_kernel<kScanExperts>, (a.E_al + kScanExperts - 1) / kScanExperts,
+                         kScanExperts * 32, 0, stream, a, ntiles);
     if (e != cudaSuccess) return e;
     if (a.counted_tile > 0) {  // route tiles: kTcCountRows rows of counted_tile / kTcCountRows slots
         const size_t smem = (size_t)(5 * a.E_al + 1 + 32) * 4;
