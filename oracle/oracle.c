@@ -16,7 +16,8 @@
  *     fp64-then-bf16 reference).
  *  2. the routed logits are rounded to bf16 (round to nearest even) straight
  *     from the double, with no intermediate fp32 rounding. Same page,
- *     Modifications ("rounds the routed logits to bf16") and Accuracy Tests.
+ *     Modifications (the routed logits, and only those, go through a bf16
+ *     rounding before the selection) and Accuracy Tests.
  *  3. top-k over the rounded logits; equal values go to the lowest expert id,
  *     and slots are ordered by (value desc, id asc), the order k successive
  *     argmax passes produce. Same page, Motivation and Modifications.
