@@ -37,6 +37,15 @@
  *    that only advances), so it can be reused by later calls and graph
  *    replays without clearing. Calls that share a workspace must not run
  *    concurrently.
+ *  - Kernels are launched with programmatic stream serialization: a launch
+ *    may start while the preceding kernel on the stream is finishing. It
+ *    reads hidden states, ids and the workspace, and writes every output,
+ *    only after that kernel has completed (griddepcontrol.wait), and it lets
+ *    the next kernel launch early (a next kernel that is not launched
+ *    programmatically waits for its completion as usual). The layer's
+ *    parameters -- gate_w, shared_w and bias -- may be read before the
+ *    preceding kernel has finished: they must not be written by the kernel
+ *    immediately preceding a call on the same stream.
  *  - Inputs must be finite. NaN or Inf in hidden states, gate weights or
  *    bias give unspecified (but in-bounds) results.
  */
