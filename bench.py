@@ -312,8 +312,46 @@ def bench_large(args, world, rank, torch, smr, inputs):
         e2e_step()
     e2.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = s2.elapsed_time(e2) / n_e2e
-    return {"ms": ms, "route_ms": route_ms, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+    e2e_serial_ms = s2.elapsed_time(e2) / n_e2e
+
+    # e2e as a serving loop runs it: step i+1's hidden states cross the host
+    # link (copy stream) while step i routes (compute stream); two device
+    # buffers, events order every reuse. Every step's host->device copy and
+    # its outputs' device->host copy are inside the timed region.
+    copy_s = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    for ev in consumed:
+        ev.record(stream)
+
+    def e2e_pipelined(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(copy_s):
+                copy_s.wait_event(consumed[b])  # step i-2 is done with buffer b
+                xs[b].copy_(hx, non_blocking=True)
+                copied[b].record(copy_s)
+            stream.wait_event(copied[b])
+            step(b)
+            consumed[b].record(stream)
+            h_ids.copy_(ids, non_blocking=True)
+            h_wts.copy_(wts, non_blocking=True)
+            h_srt.copy_(srt, non_blocking=True)
+            h_eids.copy_(eids, non_blocking=True)
+            h_npp.copy_(npp, non_blocking=True)
+
+    e2e_pipelined(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s3.record(stream)
+    e2e_pipelined(n_e2e)
+    stream.wait_stream(copy_s)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s3.elapsed_time(e3) / n_e2e
+    return {"ms": ms, "route_ms": route_ms, "e2e_ms": e2e_ms, "e2e_serial_ms": e2e_serial_ms,
+            "h2d": h2d, "d2h": d2h,
             "launches_per_step": launches_per_step, "clocks": sampler.summary(), "ri": ri,
             "ids": ids, "M": M}
 
@@ -415,6 +453,7 @@ def run_smr(args):
     res = bench_large(args, world, rank, torch, smr, inputs)
     ms = max_over_ranks(world, res["ms"])
     e2e_ms = max_over_ranks(world, res["e2e_ms"])
+    e2e_serial_ms = max_over_ranks(world, res["e2e_serial_ms"])
     flops = 2.0 * M_LARGE * H * (E + S)
     achieved = flops / (res["route_ms"] * 1e-3) / 1e12
     line = {
@@ -435,7 +474,12 @@ def run_smr(args):
                    "l2": "inputs larger than L2: two alternating 134 MB hidden-state buffers",
                    "timing": "route_align steps replayed from a CUDA graph of 50 steps"},
         "e2e": {"value": replica_throughput(world, M_LARGE, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "timing": "route_align through the public API; each step's hidden states copied "
+                          "from pinned host memory and all its outputs copied back, inside the "
+                          "timed region; the next step's copy overlaps this step's routing "
+                          "(two device buffers, a copy stream)",
+                "serial_value": replica_throughput(world, M_LARGE, e2e_serial_ms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_tflops,
                      "unit": "TFLOP/s", "frac": achieved / tc_tflops,
                      "traffic": traffic_from_profile(),
