@@ -132,24 +132,35 @@ SMR_API size_t smr_route_workspace_size(const smr_route_args *args);
 SMR_API size_t smr_align_workspace_size(const smr_align_args *args);
 SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const smr_align_args *align);
 
-/* Route only. One kernel launch for M <= 16 (gate rows split across CTAs,
- * last CTA does top-k); for M > 16 one tcgen05 GEMM launch with the top-k
- * fused into its epilogue, which requires E % 32 == 0 and 32 <= E <= 512
- * (other E with M > 16 are refused with SMR_ERR_UNSUPPORTED).
- * M == 0 launches nothing. */
+/* Route only: the gate GEMM, bf16 rounding, top-k with the lowest id winning
+ * ties, softmax renormalised over the selected and the shared slot
+ * ("[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950",
+ * Modifications). One kernel launch for M <= 16: the gate rows are split
+ * across CTAs, and one CTA selects after collecting the row groups'
+ * tagged selection keys from the workspace. For M > 16, one tcgen05 GEMM
+ * launch with the top-k fused into its epilogue, which requires
+ * E % 32 == 0 and 32 <= E <= 512 (other E with M > 16 are refused with
+ * SMR_ERR_UNSUPPORTED). M == 0 launches nothing. Refusals (SMR_ERR_*) are
+ * returned before any launch; a failed launch returns SMR_ERR_CUDA. */
 SMR_API smr_status smr_route(const smr_route_args *args, void *workspace, size_t workspace_bytes,
                      void *stream);
 
-/* Align only: reads topk_ids, writes sorted_token_ids, expert_ids and
- * num_tokens_post_padded. An id outside [0, num_experts) is skipped and sets
- * the sticky device error word (see smr_get_device_error). */
+/* Align only: moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill:
+ * M-aware moe_align block size (1.6x TTFT)", Purpose). Reads topk_ids,
+ * writes sorted_token_ids, expert_ids and num_tokens_post_padded. One launch
+ * for num_tokens * width <= 8192, else three (tile counts, tile starts,
+ * scatter). An id outside [0, num_experts) is skipped and sets the sticky
+ * device error word (see smr_get_device_error). */
 SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t workspace_bytes,
                      void *stream);
 
-/* Route then align on the route's output. align->topk_ids must equal
+/* Route then align on the route's output (the two passages above, in the
+ * order the pages' serving paths run them). align->topk_ids must equal
  * route->topk_ids, align->num_tokens == route->M, align->width == topk + S,
  * align->num_experts == E + S; routed_topk/routed_experts are taken from the
- * route. For M <= 16 both run in ONE launch. */
+ * route. For M <= 16 both run in ONE launch; for larger M the tcgen05 route
+ * also writes each 64-row tile's expert counts and two align launches
+ * follow (one when the ids fit a single align CTA). */
 SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_args *align,
                            void *workspace, size_t workspace_bytes, void *stream);
 
