@@ -20,10 +20,11 @@ constexpr uint32_t kErrBadId = 1u;        // align saw an id outside [0, E_al)
 constexpr uint32_t kErrWaitTimeout = 2u;  // a bounded wait gave up
 constexpr uint32_t kErrBadSlot = 4u;      // an align output position fell outside its array (skipped)
 
-// First 256 bytes of every workspace. Zeroed once by the caller; kernels
-// return the counters to zero before they exit.
+// First 256 bytes of every workspace. Zeroed once by the caller; afterwards
+// only the error word (set on errors, cleared by the caller) and the small
+// route's call tag (advanced by every small-M call) change.
 struct WsHeader {
-    uint32_t ticket;  // reserved (zero)
+    uint32_t unused;  // zero
     uint32_t error;   // sticky error bits (kErr*)
     uint32_t epoch;   // small route: tag of the last completed call (top bit set once used)
     uint32_t reserved[61];

@@ -7,7 +7,8 @@
 
 namespace smr {
 
-// Gate rows split across CTAs, last CTA (ticket) does top-k [+ align].
+// Gate rows split across CTAs; the last row group's leader collects the tagged
+// selection keys and does the top-k [+ align].
 struct SmallRouteLaunch {
     const uint16_t *x;
     int64_t ld;
