@@ -41,7 +41,9 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # ORACLE_LIB: another build of oracle.c (the pins' mutation test
+            # points it at copies with a planted mistake)
+            lib = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
             P = ctypes.c_void_p
             i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
             lib.oracle_bf16_from_double.argtypes = [f64]
