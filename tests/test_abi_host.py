@@ -198,3 +198,66 @@ def test_route_profile_summary_parses():
     current = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     expect = int(dram.group(1)) if sha.group(1) == current else None
     assert bench.traffic_from_profile() == expect
+
+
+def _set(obj, **kw):
+    for k, v in kw.items():
+        setattr(obj, k, v)
+    return obj
+
+
+@pytest.mark.parametrize("change,status,fragment", [
+    (dict(M=-1), _lib.SMR_ERR_INVALID_ARG, "M must be >= 0"),
+    (dict(H=16392), _lib.SMR_ERR_INVALID_ARG, "H must be a multiple of 8 in [8, 16384]"),
+    (dict(E=1025), _lib.SMR_ERR_INVALID_ARG, "E must be in [1, 1024]"),
+    (dict(has_shared=2), _lib.SMR_ERR_INVALID_ARG, "has_shared must be 0 or 1"),
+    (dict(topk=0), _lib.SMR_ERR_INVALID_ARG, "topk must be in [1, E]"),
+    (dict(shared_scale=float("inf")), _lib.SMR_ERR_INVALID_ARG, "shared_scale must be finite"),
+    (dict(ld_hidden=4100), _lib.SMR_ERR_INVALID_ARG, "ld_hidden must be >= H and a multiple of 8"),
+    (dict(gate_w=0x20008), _lib.SMR_ERR_INVALID_ARG, "gate_w must be 16-byte aligned"),
+    (dict(has_shared=0, topk=10), _lib.SMR_ERR_INVALID_ARG, "shared_w must be NULL when has_shared == 0"),
+    (dict(bias=0x60002), _lib.SMR_ERR_INVALID_ARG, "bias must be 4-byte aligned"),
+    (dict(topk_weights=0x50002), _lib.SMR_ERR_INVALID_ARG, "topk_weights must be 4-byte aligned"),
+    (dict(logits_out=0x70008), _lib.SMR_ERR_INVALID_ARG, "logits_out must be 16-byte aligned"),
+    (dict(M=32, E=1024), _lib.SMR_ERR_UNSUPPORTED, "32 <= E <= 512"),
+])
+def test_route_refuses_each_bad_argument(lib, change, status, fragment):
+    """Every malformed route argument is refused before any launch, with its
+    own reason in smr_last_error()."""
+    a = _set(_good_route(), **change)
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == status
+    assert fragment in lib.smr_last_error().decode()
+    assert lib.smr_last_launch_count() == 0
+
+
+@pytest.mark.parametrize("change,status,fragment", [
+    (dict(num_tokens=-1), _lib.SMR_ERR_INVALID_ARG, "num_tokens must be >= 0"),
+    (dict(width=0), _lib.SMR_ERR_INVALID_ARG, "width must be >= 1"),
+    (dict(num_experts=1026), _lib.SMR_ERR_INVALID_ARG, "num_experts must be in [1, 1025]"),
+    (dict(block_size=4097), _lib.SMR_ERR_INVALID_ARG, "block_size must be 0 (M-aware tier) or in [1, 4096]"),
+    (dict(topk_ids=0x10002), _lib.SMR_ERR_INVALID_ARG, "topk_ids must be 4-byte aligned"),
+    (dict(sorted_token_ids=None), _lib.SMR_ERR_INVALID_ARG, "sorted_token_ids is NULL"),
+    (dict(expert_ids=None), _lib.SMR_ERR_INVALID_ARG, "expert_ids is NULL"),
+    (dict(expert_cap=3), _lib.SMR_ERR_INVALID_ARG, "expert_cap 3 < required"),
+    (dict(num_tokens=1 << 25, width=64, sorted_cap=1 << 32, expert_cap=1 << 32),
+     _lib.SMR_ERR_UNSUPPORTED, "num_tokens * width must be <= 2^30"),
+])
+def test_align_refuses_each_bad_argument(lib, change, status, fragment):
+    a = _set(_good_align(), **change)
+    assert lib.smr_align(ctypes.byref(a), None, 0, None) == status
+    assert fragment in lib.smr_last_error().decode()
+    assert lib.smr_last_launch_count() == 0
+
+
+def test_static_entry_refuses_before_device_work(lib):
+    """The no-allocation entry point checks its contract on the host, before
+    it looks up its device array: M outside [1, 16] and scratch above the
+    fixed array are refused."""
+    r = _good_route(M=17, E=64)
+    a = _set(_good_align(T=17, W=11, E_al=65), topk_ids=r.topk_ids)
+    assert lib.smr_route_align_static(ctypes.byref(r), ctypes.byref(a), None) == _lib.SMR_ERR_UNSUPPORTED
+    assert "1 <= M <= 16" in lib.smr_last_error().decode()
+    r = _good_route(M=16, E=1024, k=10)  # 16 x 1024 tagged keys = 128 KiB: fits
+    a = _set(_good_align(T=16, W=11, E_al=1025), topk_ids=r.topk_ids, width=11)
+    need = lib.smr_route_align_workspace_size(ctypes.byref(r), ctypes.byref(a))
+    assert need <= 256 * 1024
