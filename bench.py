@@ -38,10 +38,18 @@ sys.path.insert(0, ROOT)
 METRIC = ("µs per route+align call at M=4/8 and routed tokens/s at M=16K; "
           "% of roofline")
 M_LARGE, H, E, K, S, A_LARGE = 16384, 4096, 512, 10, 1, 128
+GRAPH_STEPS = 50               # route_align steps per captured CUDA graph (at most)
 WORKLOAD = ("large_batch: M=16384 tokens, H=4096, E=512 routed + 1 shared gate, "
             "top-10 softmax+renormalize + shared slot, route + align at A=128")
-ORACLE_SAMPLE_ROWS = 4096      # cpu_baseline: rows of the large batch (~10-30 s)
+ORACLE_SAMPLE_ROWS = 1024      # cpu_baseline, single-threaded leg: rows of the large batch
 REFERENCE_BUDGET_S = 90.0      # --impl reference: whole run, warm-up included
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def peaks():
@@ -224,7 +232,7 @@ def bench_large(args, world, rank, torch, smr, inputs):
 
     # the timed steps run as replays of a CUDA graph of G steps (as a serving
     # loop would), plus any remainder eagerly: exactly args.steps steps
-    G = min(args.steps, 50)
+    G = min(args.steps, GRAPH_STEPS)
     cap_stream = torch.cuda.Stream()
     cap_stream.wait_stream(stream)
     with torch.cuda.stream(cap_stream):
@@ -351,7 +359,7 @@ def bench_large(args, world, rank, torch, smr, inputs):
     torch.cuda.synchronize()
     e2e_ms = s3.elapsed_time(e3) / n_e2e
     return {"ms": ms, "route_ms": route_ms, "e2e_ms": e2e_ms, "e2e_serial_ms": e2e_serial_ms,
-            "h2d": h2d, "d2h": d2h,
+            "h2d": h2d, "d2h": d2h, "graph_steps": G, "replays": replays, "eager_steps": rest,
             "launches_per_step": launches_per_step, "clocks": sampler.summary(), "ri": ri,
             "ids": ids, "M": M}
 
@@ -422,18 +430,47 @@ def bench_small(torch, smr, inputs, M, l2_bytes, reps=20, calls=100):
 
 
 def cpu_baseline_large():
+    """The C oracle on the large batch: all 16384 rows split over every host
+    core (median of 3 runs), and single-threaded on the first
+    ORACLE_SAMPLE_ROWS rows."""
     import numpy as np
     import oracle
     from moe_router_top_gb300 import inputs
     ri = inputs.large_batch()
-    rows = np.arange(ORACLE_SAMPLE_ROWS)
-    t0 = time.perf_counter()
-    r = oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0, rows=rows)
-    oracle.align(r.ids, E + S, A_LARGE)
-    dt = time.perf_counter() - t0
-    return {"value": ORACLE_SAMPLE_ROWS / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {ORACLE_SAMPLE_ROWS} of the 16384 rows of the large batch, "
-                      f"route + align, single-threaded C oracle ({dt:.1f} s)"}
+    cores = host_cores()
+
+    def run(rows, threads):
+        t0 = time.perf_counter()
+        r = oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0, rows=rows, threads=threads)
+        oracle.align(r.ids, E + S, A_LARGE)
+        return time.perf_counter() - t0
+
+    all_rows = np.arange(ri.M)
+    mt = sorted(run(all_rows, cores) for _ in range(3))
+    st = run(np.arange(ORACLE_SAMPLE_ROWS), 1)
+    return {"value": ri.M / mt[1], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"all {ri.M} rows of the large batch, route + align, C oracle with the rows "
+                      f"split over {cores} host threads; median of 3 runs "
+                      f"({', '.join(f'{t:.2f}' for t in mt)} s)",
+            "single_thread": {"value": ORACLE_SAMPLE_ROWS / st, "unit": "tokens/s", "cores": 1,
+                              "sample": f"first {ORACLE_SAMPLE_ROWS} rows, one thread ({st:.2f} s)"}}
+
+
+def cpu_baseline_small(M):
+    """The C oracle's route + align of one small_verify call (median of 3)."""
+    import oracle
+    from moe_router_top_gb300 import inputs
+    ri = inputs.small_verify(M)
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        r = oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0)
+        oracle.align(r.ids, E + S, 64)
+        times.append(time.perf_counter() - t0)
+    times.sort()
+    return {"value": times[1] * 1e6, "unit": "us per call", "cores": 1, "kind": "oracle",
+            "sample": f"one M={M} route + align call (the whole workload), single-threaded C oracle, "
+                      f"median of 3"}
 
 
 def run_smr(args):
@@ -472,7 +509,9 @@ def run_smr(args):
         "config": {"workload": WORKLOAD, "M": M_LARGE, "H": H, "E": E, "shared": S, "topk": K,
                    "block_size": A_LARGE, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2: two alternating 134 MB hidden-state buffers",
-                   "timing": "route_align steps replayed from a CUDA graph of 50 steps"},
+                   "timing": (f"route_align steps: {res['replays']} replay(s) of a CUDA graph of "
+                              f"{res['graph_steps']} steps" +
+                              (f" + {res['eager_steps']} eager steps" if res["eager_steps"] else ""))},
         "e2e": {"value": replica_throughput(world, M_LARGE, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "timing": "route_align through the public API; each step's hidden states copied "
@@ -508,6 +547,8 @@ def run_smr(args):
                                         f"copies (> 2x L2), median of 20 replays; a call may launch "
                                         f"during the previous call's tail (programmatic dependent "
                                         f"launch) and stream its gate before waiting for it"}
+            if not args.no_cpu:
+                small[f"M{M}"]["cpu_baseline"] = cpu_baseline_small(M)
         line["small_m"] = small
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline_large()
@@ -530,14 +571,16 @@ def run_reference(args):
     from moe_router_top_gb300 import inputs
     oracle.build()
     ri = inputs.large_batch()
+    cores = host_cores()
     t0 = time.perf_counter()
-    oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0, rows=np.arange(2))
-    per_row = (time.perf_counter() - t0) / 2
-    rows_per_step = int(max(1, min(64, REFERENCE_BUDGET_S / ((args.steps + args.warmup) * per_row))))
+    oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0, rows=np.arange(2 * cores), threads=cores)
+    per_row = (time.perf_counter() - t0) / (2 * cores)
+    rows_per_step = int(max(cores, min(64 * cores,
+                                       REFERENCE_BUDGET_S / ((args.steps + args.warmup) * per_row))))
 
     def step(i):
         rows = (np.arange(rows_per_step) + i * rows_per_step) % ri.M
-        r = oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0, rows=rows)
+        r = oracle.route(ri.x, ri.w, ri.ws, None, K, 1.0, rows=rows, threads=cores)
         oracle.align(r.ids, E + S, A_LARGE)
 
     for i in range(args.warmup):
@@ -563,9 +606,10 @@ def run_reference(args):
         "data": "synthetic (seeded N(0,1) hidden states, N(0,0.02) gate weights)",
         "config": {"workload": WORKLOAD, "M": M_LARGE, "H": H, "E": E, "shared": S, "topk": K,
                    "block_size": A_LARGE, "parallelism": "host cores, rank 0 only"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows_per_step} rows of the large batch per step, "
-                                   "route + align, single-threaded C oracle"},
+                                   f"route + align, C oracle with the rows split over {cores} "
+                                   f"host threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -194,6 +194,32 @@ SMR_API smr_status smr_get_device_error(const void *workspace, void *stream, int
 /* Clears the sticky device error word (stream-ordered memset). */
 SMR_API smr_status smr_clear_device_error(void *workspace, void *stream);
 
+/* The sticky device error word of smr_route_align_static's fixed scratch
+ * array on the current device (same bits and synchronisation as
+ * smr_get_device_error), and its clear. The first use on a device sets the
+ * array up like the first smr_route_align_static call does. Not for launch
+ * paths. */
+SMR_API smr_status smr_get_static_device_error(void *stream, int32_t *code_out);
+SMR_API smr_status smr_clear_static_device_error(void *stream);
+
+/* TEST HOOK -- failure injection without a GPU fault (vLLM #60833
+ * "--monokernel decode", Details: bounded waits that set a sticky failed word
+ * instead of hanging). Process-wide; affects launches made after the call.
+ *   SMR_STALL_SMALL_TAIL: the small-M tail waits for a call tag that no row
+ *     group writes, giving up after `limit` reloads of its key words;
+ *   SMR_STALL_TC_MERGE: the tcgen05 route's merge of its two column halves
+ *     waits on a barrier nothing arrives on, giving up after `limit` SM
+ *     cycles (no copy is in flight there).
+ * The wait runs out, bit 1 of the workspace's sticky error word is set, the
+ * kernel returns (the tcgen05 route skips its outputs; the small-M tail goes
+ * on with the keys it holds) and later calls are unaffected.
+ * SMR_STALL_NONE (limit ignored) switches the hook off. Returns
+ * SMR_ERR_INVALID_ARG for another site or a limit < 1. */
+#define SMR_STALL_NONE 0
+#define SMR_STALL_SMALL_TAIL 1
+#define SMR_STALL_TC_MERGE 2
+SMR_API smr_status smr_test_force_wait_timeout(int32_t site, int64_t limit);
+
 /* Static string for a status; thread-local text of the last refusal (every
  * reason, "; "-separated) or CUDA error on this thread, "" if none. */
 SMR_API const char *smr_status_string(smr_status status);

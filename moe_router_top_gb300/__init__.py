@@ -21,6 +21,7 @@ __all__ = [
     "route_align_static",
     "select_block_size", "align_capacity", "route_workspace_size", "align_workspace_size",
     "route_align_workspace_size", "get_device_error", "clear_device_error",
+    "get_static_device_error", "clear_static_device_error", "test_force_wait_timeout",
     "last_launch_count", "version",
 ]
 
@@ -318,6 +319,29 @@ def clear_device_error(workspace, stream=None) -> None:
     lib = _lib.load()
     ptr = workspace.ptr if isinstance(workspace, Workspace) else workspace.data_ptr()
     _check(lib.smr_clear_device_error(ptr, _stream_ptr(stream)))
+
+
+def get_static_device_error(stream=None) -> int:
+    """Sticky error bits of route_align_static's fixed scratch array on the
+    current device (synchronises the stream)."""
+    code = ctypes.c_int32(0)
+    _check(_lib.load().smr_get_static_device_error(_stream_ptr(stream), ctypes.byref(code)))
+    return code.value
+
+
+def clear_static_device_error(stream=None) -> None:
+    _check(_lib.load().smr_clear_static_device_error(_stream_ptr(stream)))
+
+
+STALL_NONE = _lib.SMR_STALL_NONE
+STALL_SMALL_TAIL = _lib.SMR_STALL_SMALL_TAIL
+STALL_TC_MERGE = _lib.SMR_STALL_TC_MERGE
+
+
+def test_force_wait_timeout(site: int, limit: int = 1) -> None:
+    """Test hook: make one bounded wait of later launches run out (see
+    smr_test_force_wait_timeout in include/smr.h); STALL_NONE switches it off."""
+    _check(_lib.load().smr_test_force_wait_timeout(int(site), int(limit)))
 
 
 def last_launch_count() -> int:

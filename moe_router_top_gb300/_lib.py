@@ -26,7 +26,12 @@ EXPORTED = (
     "smr_align_workspace_size", "smr_route_align_workspace_size", "smr_route", "smr_align",
     "smr_route_align", "smr_get_device_error", "smr_clear_device_error", "smr_status_string",
     "smr_last_error", "smr_version", "smr_last_launch_count", "smr_route_align_static",
+    "smr_get_static_device_error", "smr_clear_static_device_error", "smr_test_force_wait_timeout",
 )
+
+SMR_STALL_NONE = 0
+SMR_STALL_SMALL_TAIL = 1
+SMR_STALL_TC_MERGE = 2
 
 
 class RouteArgs(ctypes.Structure):
@@ -84,6 +89,9 @@ def load(path: str = LIB_PATH):
             "smr_version": ([], i32),
             "smr_last_launch_count": ([], i32),
             "smr_route_align_static": ([RA, AA, P], ctypes.c_int),
+            "smr_get_static_device_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
+            "smr_clear_static_device_error": ([P], ctypes.c_int),
+            "smr_test_force_wait_timeout": ([i32, i64], ctypes.c_int),
         }
         for name, (argtypes, restype) in sigs.items():
             fn = getattr(lib, name)

@@ -359,19 +359,14 @@ __global__ void __launch_bounds__(kTileThreads) align_rows_scatter_kernel(const 
 // carveout, so consecutive launches (route, then align) do not reconfigure
 // the SMs' L1/shared split in between.
 static cudaError_t configure(const void *kern, int slot, size_t bytes) {
-    static bool done[5][64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !done[slot][dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+    static std::atomic<bool> done[5][kMaxDevices];
+    return once_per_device(done[slot], [kern, bytes](int) {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        done[slot][dev] = true;
-    }
-    return cudaSuccess;
+        return r;
+    });
 }
 
 // A launch that may overlap the end of the previous kernel in the stream

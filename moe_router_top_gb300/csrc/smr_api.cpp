@@ -10,6 +10,7 @@
 //   route        : 1 launch;  align : 1 launch (numel <= 8192) or 3.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -55,7 +56,7 @@ smr_status cuda_fail(const char *what, cudaError_t e) {
 
 // The kernels are built for sm_103a only.
 smr_status check_device() {
-    static int cached[64] = {};  // 0 unknown, 1 ok, 2 bad
+    static std::atomic<int> cached[smr::kMaxDevices];  // 0 unknown, 1 ok, 2 bad
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -63,12 +64,12 @@ smr_status check_device() {
         g_last_error = std::string("no current CUDA device: ") + cudaGetErrorString(e);
         return SMR_ERR_DEVICE;
     }
-    if (dev < 64 && cached[dev] == 1) return SMR_OK;
+    if (dev < smr::kMaxDevices && cached[dev].load(std::memory_order_relaxed) == 1) return SMR_OK;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     const bool ok = (major == 10 && minor == 3);
-    if (dev < 64) cached[dev] = ok ? 1 : 2;
+    if (dev < smr::kMaxDevices) cached[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
     if (!ok) {
         g_last_error = "device " + std::to_string(dev) + " is sm_" + std::to_string(major) +
                        std::to_string(minor) + "; this library is built for sm_103a (GB300)";
@@ -76,6 +77,10 @@ smr_status check_device() {
     }
     return SMR_OK;
 }
+
+// Failure-injection hook (smr_test_force_wait_timeout), process-wide.
+std::atomic<int> g_stall_site{smr::kStallNone};
+std::atomic<long long> g_stall_limit{0};
 
 // --- route ------------------------------------------------------------------
 
@@ -246,6 +251,9 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
             L.sorted_cap = fused_align->sorted_cap;
             L.expert_cap = fused_align->expert_cap;
         }
+        const smr::StallHook hook = smr::stall_hook();
+        L.stall = hook.site == smr::kStallSmallTail;
+        L.stall_limit = L.stall ? hook.limit : 0;
         cudaError_t e = smr::launch_small_route(L, stream);
         if (e != cudaSuccess) return cuda_fail("small-M route launch", e);
         *launches += 1;
@@ -264,6 +272,9 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
     L.logits_out = a->logits_out;
     L.hdr = ws;
     L.tile_counts = tile_counts;
+    const smr::StallHook hook = smr::stall_hook();
+    L.stall = hook.site == smr::kStallTcMerge;
+    L.stall_limit = L.stall ? hook.limit : 0;
     cudaError_t e = smr::launch_tc_route(L, stream);
     if (e != cudaSuccess) return cuda_fail("tcgen05 route launch", e);
     *launches += 1;
@@ -271,6 +282,12 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
 }
 
 }  // namespace
+
+namespace smr {
+StallHook stall_hook() {
+    return StallHook{g_stall_site.load(std::memory_order_relaxed), g_stall_limit.load(std::memory_order_relaxed)};
+}
+}  // namespace smr
 
 extern "C" {
 
@@ -454,6 +471,38 @@ SMR_API smr_status smr_clear_device_error(void *workspace, void *stream) {
     cudaError_t e = cudaMemsetAsync(static_cast<uint8_t *>(workspace) + 4, 0, 4,
                                     static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("smr_clear_device_error", e);
+    return SMR_OK;
+}
+
+SMR_API smr_status smr_get_static_device_error(void *stream, int32_t *code_out) {
+    if (!code_out) {
+        g_last_error = "smr_get_static_device_error: code_out is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    smr_status st = check_device();
+    if (st != SMR_OK) return st;
+    void *scratch = nullptr;
+    cudaError_t e = smr::static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail("smr_get_static_device_error: scratch set-up", e);
+    return smr_get_device_error(scratch, stream, code_out);
+}
+
+SMR_API smr_status smr_clear_static_device_error(void *stream) {
+    smr_status st = check_device();
+    if (st != SMR_OK) return st;
+    void *scratch = nullptr;
+    cudaError_t e = smr::static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail("smr_clear_static_device_error: scratch set-up", e);
+    return smr_clear_device_error(scratch, stream);
+}
+
+SMR_API smr_status smr_test_force_wait_timeout(int32_t site, int64_t limit) {
+    if (site < SMR_STALL_NONE || site > SMR_STALL_TC_MERGE || (site != SMR_STALL_NONE && limit < 1)) {
+        g_last_error = "smr_test_force_wait_timeout: site must be 0, 1 or 2 and limit >= 1 when set";
+        return SMR_ERR_INVALID_ARG;
+    }
+    g_stall_limit.store(site == SMR_STALL_NONE ? 0 : limit, std::memory_order_relaxed);
+    g_stall_site.store(site, std::memory_order_relaxed);
     return SMR_OK;
 }
 

@@ -116,16 +116,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^32 SM cycles (about 2 s at the maximum
-// clock) or as soon as *abort becomes non-zero; on giving up it sets *abort.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int *abort) {
+// Bounded wait: gives up after `limit` SM cycles (by default 2^32, about 2 s
+// at the maximum clock) or as soon as *abort becomes non-zero; on giving up
+// it sets *abort.
+constexpr long long kWaitCycles = 1ll << 32;
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                  long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > (1ll << 32)) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             return false;
         }
@@ -134,22 +136,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // ----------------------------------------------------------------- TMA ---
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-// Same, delivered to the same shared-memory offset (and completing the
-// mbarrier at the same offset) in every CTA of the cluster set in cta_mask.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, int x,
-                                                      int y, uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar), "h"(cta_mask) : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -174,17 +160,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 
 // ------------------------------------------------------------- tcgen05 ---
 
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 ::"r"(dst_smem), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -246,10 +221,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// 32-bit store into another CTA's shared memory (address from cluster_addr).
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 // Relaxed 64-bit accesses at GPU scope (naturally aligned: single-copy
 // atomic, so a reader sees either the old or the new word whole).
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
@@ -267,30 +238,6 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned l
 __device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                  ::"r"(addr), "r"(__float_as_uint(v)), "r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-                 : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation, one CTA.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-// Arrive on an mbarrier once all previously issued MMAs of this thread finish.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(bar) : "memory");
-}
-// Same, arriving on the mbarrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(cta_mask) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
@@ -359,13 +306,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr) {
     d |= (uint64_t)1 << 46;
     d |= layout << 61;
     return d;
-}
-
-// 16-byte chunk c of row r of such a tile sits at chunk c ^ f(r): the
-// swizzle XORs address bits [4, 4+log2(SW/16)) with bits [7, ...).
-template <int SW>
-__device__ __forceinline__ int swizzled_chunk(int row, int c) {
-    return c ^ (((row * SW) >> 7) & (SW / 16 - 1));
 }
 
 // Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1),

@@ -5,7 +5,42 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace smr {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device one-time set-up (kernel attributes, the fixed scratch array):
+// set_up(dev) runs with `dev` current the first time a caller reaches it on
+// that device, exactly once even when host threads race (a mutex guards the
+// first calls; later calls see the flag without locking). A failure is
+// returned and the set-up is tried again by the next call.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<bool> (&done)[kMaxDevices], F &&set_up) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = set_up(dev);
+    if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+    return e;
+}
+
+// Failure-injection hook for tests (smr_test_force_wait_timeout): which
+// bounded wait is made to wait for something nothing provides, and its
+// limit. Read once per launch into the kernel parameters.
+enum StallSite : int { kStallNone = 0, kStallSmallTail = 1, kStallTcMerge = 2 };
+struct StallHook {
+    int site;
+    long long limit;
+};
+StallHook stall_hook();
 
 // Gate rows split across CTAs; the last row group's leader collects the tagged
 // selection keys and does the top-k [+ align].
@@ -28,6 +63,10 @@ struct SmallRouteLaunch {
     int32_t *expert_ids;
     int32_t *npp;
     int64_t sorted_cap, expert_cap;  // output array lengths (every write is checked)
+    // failure-injection test hook: the tail polls for a tag no row group
+    // writes, giving up after stall_limit reloads
+    int stall;
+    long long stall_limit;
 };
 constexpr int kSmallMaxM = 16;
 // Number of K ranges the gate rows are split into (the CTAs of one cluster);
@@ -36,7 +75,7 @@ constexpr int kSmallMaxM = 16;
 int small_route_k_ranges(int E, int S, int H);
 cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream);
 // Fixed scratch in device memory (no allocation): capacity, and its device
-// address for the current device (set up on first use per device).
+// address for the current device (set up on first use per device, thread-safe).
 constexpr size_t kStaticScratchBytes = 256 * 1024;
 cudaError_t static_scratch(void **ptr);
 
@@ -56,6 +95,10 @@ struct TcRouteLaunch {
     // optional (align fused behind the route): expert counts of every
     // kTcCountRows-row tile, [ceil(M / kTcCountRows)][E + S]
     int32_t *tile_counts;
+    // failure-injection test hook: the merge of the two column halves waits
+    // on a barrier nothing arrives on, giving up after stall_limit SM cycles
+    int stall;
+    long long stall_limit;
 };
 constexpr int kTcTileRows = 128;   // token rows per CTA of the tcgen05 route
 constexpr int kTcCountRows = 64;   // token rows per align tile counted by the route

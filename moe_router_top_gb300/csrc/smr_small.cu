@@ -89,7 +89,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 
 // Top-k of one token row in one warp. krow: the token's E selection keys
 // (the bf16-rounded logit and the expert id, see make_key) in the low half
-// of words whose high half is the call's tag, written by the row groups;
+// of words whose high half is the call's tag, written by the row groups
+// (want: the tag to wait for, at most poll_limit reloads);
 // cand_s: 32 words of shared memory owned by this warp.
 // Writes ids and weights of the routed slots 0..k-1 to global memory (the
 // shared slot k was written by its row group) and the align's
@@ -105,31 +106,33 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // stored at its rank. When more than 32 keys reach T (the largest logits
 // concentrated in a few lanes), k exact rounds of a warp maximum take over.
 template <int NK>
-__device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, uint32_t tag, int E, int S,
+__device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, uint32_t want,
+                                              long long poll_limit, int E, int S,
                                               int k, int32_t *ids, float *wts, uint32_t *keys_s, int flat0,
                                               uint32_t *cand_s, uint32_t *tmask, uint32_t *tbits, int m,
                                               uint32_t *err) {
     const int lane = threadIdx.x & 31;
     // every load issued before the first use; lanes past E read a clamped
     // (valid) element that is masked below. A word carries this call's tag
-    // once its row group has stored it: the words still holding an older
-    // tag are loaded again, a bounded number of times.
+    // once its row group has stored it: the words still holding another tag
+    // than `want` (this call's tag; another one only under the failure-
+    // injection hook) are loaded again, at most poll_limit times.
     unsigned long long v[NK];
 #pragma unroll
     for (int i = 0; i < NK; ++i) v[i] = ld_relaxed_u64(krow + min(lane + 32 * i, E - 1));
 #pragma unroll 1
-    for (int tries = 0;; ++tries) {
+    for (long long tries = 0;; ++tries) {
         bool ok = true;
 #pragma unroll
-        for (int i = 0; i < NK; ++i) ok = ok && (uint32_t)(v[i] >> 32) == tag;
+        for (int i = 0; i < NK; ++i) ok = ok && (uint32_t)(v[i] >> 32) == want;
         if (__all_sync(0xffffffffu, ok)) break;
-        if (tries == kSmallPollLimit) {  // warp-uniform: the outputs of this call are not valid
+        if (tries >= poll_limit) {  // warp-uniform: the outputs of this call are not valid
             if (lane == 0) set_error(err, kErrWaitTimeout);
             break;
         }
 #pragma unroll
         for (int i = 0; i < NK; ++i)
-            if ((uint32_t)(v[i] >> 32) != tag) v[i] = ld_relaxed_u64(krow + min(lane + 32 * i, E - 1));
+            if ((uint32_t)(v[i] >> 32) != want) v[i] = ld_relaxed_u64(krow + min(lane + 32 * i, E - 1));
     }
     uint32_t key[NK];
 #pragma unroll
@@ -700,8 +703,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         tmask[p.E] = (p.M == 32) ? 0xFFFFFFFFu : (1u << p.M) - 1u;
         atomicOr(tbits + (p.E >> 5), 1u << (p.E & 31));
     }
+    // the tag the tail waits for: this call's, or under the failure-
+    // injection hook one that no row group writes (the wait then runs out
+    // after the hook's limit, sets the error bit and the tail goes on with
+    // the words it holds)
+    const uint32_t want = p.stall ? (tag + 1u) | 0x80000000u : tag;
+    const long long poll_limit = p.stall ? p.stall_limit : kSmallPollLimit;
     for (int m = warp; m < p.M; m += kSmallWarps)
-        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, tag, p.E, p.S, p.k, p.ids + (int64_t)m * width,
+        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, want, poll_limit, p.E, p.S, p.k,
+                          p.ids + (int64_t)m * width,
                           p.wts + (int64_t)m * width, keys_s + m * width, m * width, cand_s + warp * 32,
                           P.mask_align ? tmask : nullptr, tbits, m, &hdr->error);
     if (tid == 0) hdr->epoch = tag;  // read by the next call's CTAs (after this launch ends)
@@ -731,19 +741,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
 
 template <int NB, int NK>
 static cudaError_t launch_nb(const SmallParams &P, int grid, size_t smem, cudaStream_t stream) {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {  // the same carveout as every other kernel of the library
-        cudaError_t e = cudaFuncSetAttribute(small_route_kernel<NB, NK>,
+    static std::atomic<bool> configured[kMaxDevices];
+    cudaError_t e = once_per_device(configured, [smem](int) {
+        // the same carveout as every other kernel of the library
+        cudaError_t r = cudaFuncSetAttribute(small_route_kernel<NB, NK>,
                                              cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(small_route_kernel<NB, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(small_route_kernel<NB, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kSmallThreads, 1, 1);
@@ -789,24 +798,24 @@ int small_route_k_ranges(int E, int S, int H) {
 static __device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
 
 cudaError_t static_scratch(void **ptr) {
-    static void *addr[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (addr[dev] == nullptr) {
-        // first use on this device (with it current): resolve the address and
-        // clear the whole array (header and tagged key words), as a caller
-        // clears a workspace before its first use
+    static std::atomic<bool> ready[kMaxDevices];
+    static std::atomic<void *> addr[kMaxDevices];
+    // first use on a device (with it current), once even when host threads
+    // race: resolve the address and clear the whole array (header and tagged
+    // key words), as a caller clears a workspace before its first use
+    cudaError_t e = once_per_device(ready, [](int dev) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_route_scratch);
-        if (e != cudaSuccess) return e;
-        e = cudaMemset(p, 0, kStaticScratchBytes);
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();  // cleared before any stream's first launch
-        if (e != cudaSuccess) return e;
-        addr[dev] = p;
-    }
-    *ptr = addr[dev];
+        cudaError_t r = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (r != cudaSuccess) return r;
+        r = cudaMemset(p, 0, kStaticScratchBytes);
+        if (r == cudaSuccess) r = cudaDeviceSynchronize();  // cleared before any stream's first launch
+        if (r == cudaSuccess) addr[dev].store(p, std::memory_order_relaxed);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    *ptr = addr[dev].load(std::memory_order_relaxed);
     return cudaSuccess;
 }
 
@@ -814,6 +823,7 @@ cudaError_t launch_small_route(const SmallRouteLaunch &a, cudaStream_t stream) {
     if (a.M <= 0 || a.M > kSmallMaxM) return cudaErrorInvalidValue;
     SmallParams P;
     P.a = a;
+    if (P.a.stall_limit <= 0) P.a.stall_limit = kSmallPollLimit;
     P.rows = a.E + a.S;
     P.slices = (a.H + kSliceK - 1) / kSliceK;
     P.KQ = small_route_k_ranges(a.E, a.S, a.H);

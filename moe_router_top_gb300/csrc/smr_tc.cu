@@ -74,6 +74,8 @@ struct TcParams {
     uint16_t *logits_out;
     uint32_t *err;
     int32_t *tile_counts;  // optional: expert counts of each 64-row tile, [tiles][E + S]
+    int stall;             // failure-injection hook: the half merge waits on a barrier
+    long long stall_limit; // nothing arrives on, for at most stall_limit SM cycles
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
     uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off;
 };
@@ -599,10 +601,13 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     }
     if (hf == 0) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(half_done));
+        // (under the failure-injection hook half 0 does not post: the merge's
+        // wait then runs out, which sets the error bit and skips the outputs)
+        if (lane == 0 && !p.stall) mbar_arrive(smem_u32(half_done));
     } else {
         // ------------------------------ half 1: merge, softmax, write -----
-        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag));
+        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag,
+                                                                   p.stall ? p.stall_limit : kWaitCycles));
         __syncwarp();
         if (ok && got && valid) {
             int32_t *orow = p.ids + (int64_t)grow * p.width;
@@ -680,17 +685,17 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 // ------------------------------------------------------------------ host --
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once (a function-local static is initialised exactly once,
+    // also when host threads race)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    }();
     return fn;
 }
 
@@ -771,20 +776,18 @@ bool tc_route_supported(int H, int E, int k, int S) {
 template <int NGM, int CW>
 static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const TcPlan &plan,
                              cudaStream_t stream) {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
+    static std::atomic<bool> configured[kMaxDevices];
+    cudaError_t e = once_per_device(configured, [](int) {
+        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kTcSmemLimit);
-        if (e == cudaSuccess)  // the same carveout as every other kernel of the library
-            e = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
+        if (r == cudaSuccess)  // the same carveout as every other kernel of the library
+            r = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -818,6 +821,8 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     p.logits_out = a.logits_out;
     p.err = &reinterpret_cast<WsHeader *>(a.hdr)->error;
     p.tile_counts = a.tile_counts;
+    p.stall = a.stall;
+    p.stall_limit = a.stall_limit > 0 ? a.stall_limit : kWaitCycles;
     CUtensorMap mx, mw;
     if (!make_map(&mx, a.x, (uint64_t)a.H, (uint64_t)a.M, (uint64_t)a.ld * 2, kTcBK, kTcBM))
         return cudaErrorInvalidValue;

@@ -30,7 +30,7 @@ def build(force: bool = False) -> str:
     os.makedirs(_OUT_DIR, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
                                "-fno-fast-math", "-ffp-contract=off",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
@@ -59,6 +59,10 @@ def _load():
             lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, f32, P, i64, P, P, P,
                                          P, P, P, P, P, P]
             lib.oracle_route.restype = None
+            lib.oracle_route_threads.argtypes = [i32] + lib.oracle_route.argtypes
+            lib.oracle_route_threads.restype = i32
+            lib.oracle_bf16_round_array.argtypes = [i64, P, P]
+            lib.oracle_bf16_round_array.restype = None
             lib.oracle_select_block_size.argtypes = [i32, i32, i32]
             lib.oracle_select_block_size.restype = i32
             lib.oracle_align_capacity.argtypes = [i64, i32, i32]
@@ -89,10 +93,9 @@ def bf16_to_double(b: int) -> float:
 
 def bf16_round(values: np.ndarray) -> np.ndarray:
     """Round each double to bf16 (RNE), returned as doubles."""
-    lib = _load()
-    flat = np.asarray(values, dtype=np.float64).ravel()
-    out = np.array([lib.oracle_bf16_to_double(lib.oracle_bf16_from_double(float(v)))
-                    for v in flat], dtype=np.float64)
+    flat = np.ascontiguousarray(np.asarray(values, dtype=np.float64).ravel())
+    out = np.empty_like(flat)
+    _load().oracle_bf16_round_array(flat.shape[0], _ptr(flat), _ptr(out))
     return out.reshape(np.shape(values))
 
 
@@ -140,8 +143,11 @@ class RouteResult:
 
 
 def route(x: np.ndarray, w: np.ndarray, ws: Optional[np.ndarray], bias: Optional[np.ndarray],
-          topk: int, scale: float = 1.0, rows: Optional[np.ndarray] = None) -> RouteResult:
-    """Full oracle route. ``rows`` restricts it to a subset of token rows."""
+          topk: int, scale: float = 1.0, rows: Optional[np.ndarray] = None,
+          threads: int = 1) -> RouteResult:
+    """Full oracle route. ``rows`` restricts it to a subset of token rows;
+    ``threads`` > 1 splits the rows over that many host threads (same
+    results, rows are independent)."""
     x = _c(x, np.uint16)
     if rows is not None:
         x = np.ascontiguousarray(x[np.asarray(rows)])
@@ -158,9 +164,12 @@ def route(x: np.ndarray, w: np.ndarray, ws: Optional[np.ndarray], bias: Optional
     z = np.empty((M, E), dtype=np.float64)
     ad = np.empty((M, E), dtype=np.float64)
     s = np.zeros(M, dtype=np.float64)
-    _load().oracle_route(M, H, E, topk, S, float(scale), _ptr(x), H, _ptr(w), _ptr(ws),
-                         _ptr(bias), _ptr(ids), _ptr(wt), _ptr(zhat), _ptr(z), _ptr(ad),
-                         _ptr(s))
+    args = (M, H, E, topk, S, float(scale), _ptr(x), H, _ptr(w), _ptr(ws), _ptr(bias),
+            _ptr(ids), _ptr(wt), _ptr(zhat), _ptr(z), _ptr(ad), _ptr(s))
+    if threads > 1:
+        _load().oracle_route_threads(int(threads), *args)
+    else:
+        _load().oracle_route(*args)
     return RouteResult(ids, wt, zhat, z, ad, s)
 
 

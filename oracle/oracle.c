@@ -38,6 +38,7 @@
  *     Scope and safety (2048+ tokens keep the large tier).
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -76,6 +77,13 @@ ORACLE_API double oracle_bf16_to_double(uint16_t b)
     float f;
     memcpy(&f, &bits, 4);
     return (double)f;
+}
+
+/* out[i] = in[i] rounded to bf16 (as above), as a double. */
+ORACLE_API void oracle_bf16_round_array(int64_t n, const double *in, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_to_double(oracle_bf16_from_double(in[i]));
 }
 
 /* --------------------------------------------------------- gate GEMM --- */
@@ -177,6 +185,67 @@ ORACLE_API void oracle_route(int M, int H, int E, int k, int has_shared, float s
     free(z);
     free(zh);
     free(ad);
+}
+
+/* The same route with the token rows split into nthreads contiguous blocks,
+ * one thread each. Every row is computed by oracle_route exactly as in a
+ * single call (rows are independent), so the results are identical; the
+ * threads only shorten the wall time. Returns 0, or -1 if a thread could
+ * not be started (its rows are then computed on the calling thread). */
+typedef struct {
+    int M, H, E, k, has_shared;
+    float scale;
+    const uint16_t *x;
+    int64_t ld_x;
+    const uint16_t *W, *Ws;
+    const float *bias;
+    int32_t *ids;
+    float *w;
+    double *zhat_out, *z_out, *absdot_out, *s_out;
+} route_job;
+
+static void *route_job_run(void *arg)
+{
+    route_job *j = (route_job *)arg;
+    oracle_route(j->M, j->H, j->E, j->k, j->has_shared, j->scale, j->x, j->ld_x, j->W, j->Ws,
+                 j->bias, j->ids, j->w, j->zhat_out, j->z_out, j->absdot_out, j->s_out);
+    return NULL;
+}
+
+ORACLE_API int oracle_route_threads(int nthreads, int M, int H, int E, int k, int has_shared,
+                                    float scale, const uint16_t *x, int64_t ld_x,
+                                    const uint16_t *W, const uint16_t *Ws, const float *bias,
+                                    int32_t *ids, float *w, double *zhat_out, double *z_out,
+                                    double *absdot_out, double *s_out)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = M > 0 ? M : 1;
+    int width = k + (has_shared ? 1 : 0);
+    route_job *jobs = (route_job *)calloc((size_t)nthreads, sizeof(route_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    int *started = (int *)calloc((size_t)nthreads, sizeof(int));
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        int r0 = (int)((int64_t)M * i / nthreads), r1 = (int)((int64_t)M * (i + 1) / nthreads);
+        route_job *j = &jobs[i];
+        j->M = r1 - r0; j->H = H; j->E = E; j->k = k; j->has_shared = has_shared; j->scale = scale;
+        j->x = x + (int64_t)r0 * ld_x; j->ld_x = ld_x; j->W = W; j->Ws = Ws; j->bias = bias;
+        j->ids = ids + (int64_t)r0 * width; j->w = w + (int64_t)r0 * width;
+        j->zhat_out = zhat_out ? zhat_out + (int64_t)r0 * E : NULL;
+        j->z_out = z_out ? z_out + (int64_t)r0 * E : NULL;
+        j->absdot_out = absdot_out ? absdot_out + (int64_t)r0 * E : NULL;
+        j->s_out = s_out ? s_out + r0 : NULL;
+        started[i] = pthread_create(&th[i], NULL, route_job_run, j) == 0;
+        if (!started[i]) rc = -1;
+    }
+    for (int i = 0; i < nthreads; ++i) {
+        if (started[i]) pthread_join(th[i], NULL);
+        else route_job_run(&jobs[i]);
+    }
+    free(jobs);
+    free(th);
+    free(started);
+    return rc;
 }
 
 /* ------------------------------------------------------------- align --- */

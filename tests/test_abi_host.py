@@ -261,3 +261,14 @@ def test_static_entry_refuses_before_device_work(lib):
     a = _set(_good_align(T=16, W=11, E_al=1025), topk_ids=r.topk_ids, width=11)
     need = lib.smr_route_align_workspace_size(ctypes.byref(r), ctypes.byref(a))
     assert need <= 256 * 1024
+
+
+def test_failure_hook_and_static_error_refusals(lib):
+    """The failure-injection hook takes only its sites and a positive limit;
+    switching it off always succeeds. The fixed array's error getter refuses
+    a NULL output before touching any device."""
+    assert lib.smr_test_force_wait_timeout(7, 1) == _lib.SMR_ERR_INVALID_ARG
+    assert "site must be" in lib.smr_last_error().decode()
+    assert lib.smr_test_force_wait_timeout(_lib.SMR_STALL_TC_MERGE, 0) == _lib.SMR_ERR_INVALID_ARG
+    assert lib.smr_test_force_wait_timeout(_lib.SMR_STALL_NONE, 0) == _lib.SMR_OK
+    assert lib.smr_get_static_device_error(None, None) == _lib.SMR_ERR_INVALID_ARG

@@ -1,5 +1,12 @@
 """GPU parity: the CUDA path (through the C ABI) against the oracle on the five
-workloads, edge cases, graph replay and workspace reuse. Needs a GB300."""
+workloads, edge cases, graph replay and workspace reuse. Needs a GB300.
+
+The workloads are checked twice: as the benchmark calls route_align (no
+logits output, the benchmark's block sizes and a reused workspace), and with
+the optional logits output, whose every value is then checked against the
+accumulation bound. Each comparison's counts (exact, rounding-flip, boundary
+and near-midpoint rows) are appended to $SMR_PARITY_LOG when it is set.
+"""
 from __future__ import annotations
 
 import numpy as np
@@ -8,7 +15,7 @@ import pytest
 import oracle
 from moe_router_top_gb300 import inputs
 
-from _parity import check_align, check_route, check_route_properties
+from _parity import check_align, check_route, check_route_properties, record
 
 pytestmark = pytest.mark.gpu
 
@@ -37,77 +44,109 @@ def _dev(ri):
     return x, w, ws, b
 
 
-def _route_align(smr, ri, A, with_logits=True):
+def _route_align(smr, ri, A, with_logits=True, workspace=None):
     x, w, ws, b = _dev(ri)
     logits = torch.empty((ri.M, ri.E), dtype=torch.int16, device="cuda") if with_logits else None
     out = smr.route_align(x, w, ws, b, topk=ri.topk, block_size=A, shared_scale=ri.shared_scale,
-                          logits_out=logits)
+                          logits_out=logits, workspace=workspace)
     torch.cuda.synchronize()
     ids, wts, srt, eids, npp = (t.cpu().numpy() for t in out)
     lg = logits.cpu().numpy().view(np.uint16) if with_logits else None
     return ids, wts, srt, eids, npp, lg
 
 
-def _full_check(smr, ri, A, exact=False):
-    ids, wts, srt, eids, npp, lg = _route_align(smr, ri, A)
+def _full_check(smr, ri, A, exact=False, with_logits=True, name=None):
+    ids, wts, srt, eids, npp, lg = _route_align(smr, ri, A, with_logits=with_logits)
     rep = check_route(ri, ids, wts, lg, exact_logits=exact)
     check_route_properties(ri, ids, wts)
     Aeff = A if A > 0 else oracle.select_block_size(ri.M, ri.topk, ri.E)
     al = check_align(ids, ri.num_experts_align, Aeff, srt, eids, npp)
+    if name:
+        record(name, rep, logits_out=with_logits, npp=al.npp, block_size=Aeff)
     return rep, al, ids
 
 
 # ------------------------------------------------------------- workloads --
 
-def test_small_verify_m4(smr):
-    ri = inputs.small_verify(4)
-    rep, al, _ = _full_check(smr, ri, 64)
+@pytest.mark.parametrize("with_logits", [False, True], ids=["bench_call", "logits_out"])
+@pytest.mark.parametrize("M", [4, 8])
+def test_small_verify(smr, M, with_logits):
+    """M=4 (and 8), as bench.py times it: one single-launch route_align with
+    A=64 (and the same with the logits output)."""
+    ri = inputs.small_verify(M)
+    rep, al, _ = _full_check(smr, ri, 64, with_logits=with_logits,
+                             name=f"small_verify_M{M}" + ("_logits" if with_logits else ""))
     assert smr.last_launch_count() == 1
-    print(f"small_verify M=4: {rep} npp={al.npp}")
+    print(f"small_verify M={M}: {rep} npp={al.npp}")
 
 
+@pytest.mark.parametrize("with_logits", [False, True], ids=["bench_call", "logits_out"])
 @pytest.mark.parametrize("M", [1, 3, 8])
-def test_tie_stress_bit_exact(smr, M):
+def test_tie_stress_bit_exact(smr, M, with_logits):
     """Integer inputs: fp32 accumulation is exact, so every logit, id and
     align output must match the oracle bit for bit."""
     ri = inputs.tie_stress(M)
-    rep, al, ids = _full_check(smr, ri, 64, exact=True)
-    assert rep.rows_ids_differ == 0
+    rep, al, ids = _full_check(smr, ri, 64, exact=True, with_logits=with_logits,
+                               name=f"tie_stress_M{M}" + ("_logits" if with_logits else ""))
+    assert rep.exact_rows == rep.rows
 
 
-def test_short_prefill_blocks(smr):
+@pytest.mark.parametrize("with_logits", [False, True], ids=["bench_call", "logits_out"])
+def test_short_prefill_blocks(smr, with_logits):
     ri = inputs.short_prefill()
     res = {}
     for A in (64, 128, 0):
-        rep, al, ids = _full_check(smr, ri, A)
+        rep, al, ids = _full_check(smr, ri, A, with_logits=with_logits,
+                                   name=f"short_prefill_A{A}" + ("_logits" if with_logits else ""))
         res[A] = al.npp
     assert oracle.select_block_size(128, 8, 128) == 64 and res[0] == res[64]
     print(f"short_prefill npp: A=64 {res[64]}, A=128 {res[128]}, ratio@128 {res[128] / 1024:.2f}")
 
 
+@pytest.mark.parametrize("with_logits", [False, True], ids=["bench_call", "logits_out"])
 @pytest.mark.parametrize("M", list(inputs.ZIPF_TOKENS))
-def test_zipf_sweep(smr, M):
+def test_zipf_sweep(smr, M, with_logits):
     ri = inputs.zipf_sweep(M)
-    rep, al, ids = _full_check(smr, ri, 0)
+    rep, al, ids = _full_check(smr, ri, 0, with_logits=with_logits,
+                               name=f"zipf_M{M}" + ("_logits" if with_logits else ""))
     A = oracle.select_block_size(M, 8, 128)
     cnt = np.bincount(ids.ravel(), minlength=128)
     assert al.npp == int(((cnt + A - 1) // A * A).sum())
     print(f"zipf M={M}: A={A} npp={al.npp} touched={(cnt > 0).sum()} {rep}")
 
 
-def test_large_batch_sampled(smr):
-    """M=16384 in the launch configuration the benchmark times: oracle on
-    sampled rows (first, last tile and a random spread), invariants on all
-    rows, align bit-exact on all ids."""
+def test_large_batch_bench_call_all_rows(smr):
+    """M=16384 exactly as bench.py calls it (route_align, A=128, no logits
+    output, a reused workspace, second call on it): EVERY row against the
+    oracle (row-parallel on the host cores), invariants on all rows, align
+    bit-exact on all ids."""
+    ri = inputs.large_batch()
+    wsp = smr.Workspace()
+    _route_align(smr, ri, 128, with_logits=False, workspace=wsp)
+    ids, wts, srt, eids, npp, _ = _route_align(smr, ri, 128, with_logits=False, workspace=wsp)
+    assert smr.get_device_error(wsp) == 0
+    rep = check_route(ri, ids, wts, None)
+    check_route_properties(ri, ids, wts)
+    al = check_align(ids, 513, 128, srt, eids, npp)
+    record("large_batch_M16384", rep, logits_out=False, npp=al.npp, block_size=128)
+    print(f"large_batch: {rep}")
+
+
+def test_large_batch_logits_every_tile(smr):
+    """M=16384 with the logits output: every logit of two rows of each
+    64-row tile (and the first and last tile whole) inside the accumulation
+    bound, selection on them exact."""
     ri = inputs.large_batch()
     ids, wts, srt, eids, npp, lg = _route_align(smr, ri, 128)
     rng = np.random.default_rng(99)
-    rows = np.unique(np.concatenate([np.arange(0, 130), np.arange(ri.M - 130, ri.M),
-                                     rng.choice(ri.M, 300, replace=False)]))
+    tiles = np.arange(0, ri.M, 64)
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(ri.M - 64, ri.M),
+                                     tiles + rng.integers(0, 64, tiles.size),
+                                     tiles + rng.integers(0, 64, tiles.size)]))
     rep = check_route(ri, ids, wts, lg, rows=rows)
-    check_route_properties(ri, ids, wts)
     check_align(ids, 513, 128, srt, eids, npp)
-    print(f"large_batch: {rep}")
+    record("large_batch_M16384_logits_sampled", rep, logits_out=True, npp=int(npp[0]), block_size=128)
+    print(f"large_batch (logits, sampled): {rep}")
 
 
 # ------------------------------------------------------------ edge cases --

@@ -27,9 +27,65 @@ def case():
 
 def test_oracle_outputs_pass(case):
     ri, (ids, w, bits) = case
-    rep = check_route(ri, ids, w, bits)
+    for lg in (bits, None):  # with and without the GPU's logits
+        rep = check_route(ri, ids, w, lg)
+        assert rep.exact_rows == rep.rows and rep.rounding_rows == 0 and rep.logit_mismatch == 0
     check_route_properties(ri, ids, w)
-    assert rep.rows_ids_differ == 0 and rep.logit_mismatch == 0
+
+
+def _flip_case(ri, monkeypatch, rel):
+    """Widen the admissible band (accumulation_bound -> rel) so that logits of
+    the oracle's top-k have two admissible roundings; returns a row, a
+    selected expert whose logit can round the other way, and that value."""
+    import _parity
+    monkeypatch.setattr(_parity, "accumulation_bound", lambda _ri: rel)
+    ref = oracle.route(ri.x, ri.w, ri.ws, ri.bias, ri.topk, ri.shared_scale)
+    lo = oracle.bf16_round(ref.z - rel * ref.absdot)
+    hi = oracle.bf16_round(ref.z + rel * ref.absdot)
+    for t in range(ri.M):
+        for e in ref.ids[t, :ri.topk]:
+            if lo[t, e] != hi[t, e]:
+                alt = hi[t, e] if ref.zhat[t, e] == lo[t, e] else lo[t, e]
+                return ref, t, int(e), alt
+    raise AssertionError("no selected logit near a rounding boundary")
+
+
+def test_admissible_rounding_flip_is_accepted_and_counted(case, monkeypatch):
+    """A result that the oracle's selection produces on an admissible
+    rounding of one selected logit is accepted as a rounding row, with and
+    without the GPU's logits; an unexplained one is not."""
+    ri, (ids0, w0, bits0) = case
+    ref, t, e, alt = _flip_case(ri, monkeypatch, 2.0 ** -13)
+    z = ref.zhat[t].copy()
+    z[e] = alt
+    sid, sw = oracle.select(z, ri.topk)
+    ids, w, bits = ids0.copy(), w0.copy(), bits0.copy()
+    ids[t, :ri.topk], w[t, :ri.topk] = sid, sw
+    bits[t, e] = oracle.bf16_from_double(alt)
+    for lg in (bits, None):
+        rep = check_route(ri, ids, w, lg)
+        assert rep.rounding_rows == 1 and rep.exact_rows == ri.M - 1
+    w[t, 0] *= 1 + 1e-5  # no admissible rounding gives this weight
+    with pytest.raises(AssertionError):
+        check_route(ri, ids, w, None)
+
+
+def test_expert_change_off_the_boundary_is_rejected(case):
+    """A different expert SET is accepted only on boundary rows (the oracle's
+    k-th and (k+1)-th logits within 1 ulp), whatever else would explain it."""
+    ri, (ids0, w0, bits0) = case
+    ref = oracle.route(ri.x, ri.w, ri.ws, ri.bias, ri.topk, ri.shared_scale)
+    k = ri.topk
+    zs = -np.sort(-ref.zhat, axis=1)
+    t = int(np.argmax(zs[:, k - 1] - zs[:, k]))  # the row farthest from a boundary tie
+    z = ref.zhat[t].copy()
+    out = int(np.argsort(-z, kind="stable")[k])  # the (k+1)-th expert enters the top-k
+    z[out] = zs[t, 0] + 1.0
+    sid, sw = oracle.select(z, k)
+    ids, w = ids0.copy(), w0.copy()
+    ids[t, :k], w[t, :k] = sid, sw
+    with pytest.raises(AssertionError, match="off the k-th boundary"):
+        check_route(ri, ids, w, None)
 
 
 @pytest.mark.parametrize("mistake", [
@@ -60,6 +116,9 @@ def test_route_rules_reject(case, mistake):
         bits[5, e] = bits[5, e] + 2 if bits[5, e] < 0x8000 else bits[5, e] - 2
     with pytest.raises(AssertionError):
         check_route(ri, ids, w, bits)
+    if mistake != "logit two bf16 steps away":  # the same mistake without the GPU's logits
+        with pytest.raises(AssertionError):
+            check_route(ri, ids, w, None)
 
 
 @pytest.fixture(scope="module")

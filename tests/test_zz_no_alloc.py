@@ -14,7 +14,7 @@ import pytest
 
 from moe_router_top_gb300 import inputs
 
-from _parity import weights_close
+from _parity import check_align, check_route, weights_close
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,14 @@ def test_static_scratch_matches_workspace_path(smr, ri):
         assert int(npp[0]) == n
         assert np.array_equal(srt[:n], ref[2][:n])
         assert np.array_equal(eids[: n // A], ref[3][: n // A])
+        # and against the oracle itself
+        check_route(ri, ids, wts, None)
+        check_align(ids, ri.num_experts_align, A, srt, eids, npp)
     assert smr.last_launch_count() == 1
+    # the fixed array's sticky error word is readable and clear
+    assert smr.get_static_device_error() == 0
+    smr.clear_static_device_error()
+    assert smr.get_static_device_error() == 0
 
 
 def test_static_scratch_refuses_large_batches(smr):
