@@ -51,6 +51,7 @@ W_ATOL = 4 * 2.0 ** -149
 MAX_ROUNDING_FRACTION = 0.02
 MIN_ROUNDING_ROWS = 2
 MAX_COMBOS = 1 << 14
+MAX_STEPS = 4
 
 
 def weights_close(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
@@ -94,13 +95,13 @@ def bf16_next_up(v: float) -> float:
     return _val(b + 1) if v > 0 else (0.0 if b == 0x8001 else _val(b - 1))
 
 
-def bf16_values_between(lo: float, hi: float) -> List[float]:
-    out, v = [], lo
-    while v <= hi:
-        out.append(v)
-        if len(out) > 64:
-            raise AssertionError(f"admissible interval [{lo}, {hi}] spans more than 64 bf16 values")
-        v = bf16_next_up(v)
+def bf16_values_near(v: float, lo: float, hi: float, steps: int) -> List[float]:
+    """The bf16 values of [lo, hi] other than v, at most `steps` bf16 steps
+    from v, nearest first."""
+    out, up, down = [], v, v
+    for _ in range(steps):
+        up, down = bf16_next_up(up), bf16_next_down(down)
+        out += [u for u in (up, down) if lo <= u <= hi]
     return out
 
 
@@ -120,25 +121,44 @@ class RouteReport:
         return dataclasses.asdict(self)
 
 
-def _explained(zhat_row, lo_row, hi_row, k, ids_row, w_row) -> bool:
+def _explained(zhat_row, lo_row, hi_row, k, ids_row, w_row, oracle_ids) -> bool:
     """Does the oracle's selection on some admissible choice of this row's
-    logits reproduce (ids_row, w_row)? Only logits that can reach the top-k
-    (admissible maximum >= the k-th largest admissible minimum) matter. The
-    choices are tried by the number of logits that differ from the oracle's
-    rounding (one, then two, ...), at most MAX_COMBOS selections in all."""
-    kth_lo = np.partition(lo_row, -k)[-k]
-    amb = np.nonzero((hi_row >= kth_lo) & (lo_row != hi_row))[0]
-    others = {int(e): [v for v in bf16_values_between(lo_row[e], hi_row[e]) if v != zhat_row[e]]
-              for e in amb}
+    logits reproduce (ids_row, w_row)? Only the logits of experts that either
+    selection holds can make a difference (any other expert stays out of the
+    GPU's top-k at the oracle's value). Each of those may take an admissible
+    value up to MAX_STEPS bf16 steps from the oracle's rounding, or from the
+    value the GPU's weights imply for it; the choices are tried by the number
+    of logits changed (one, then two, ...), at most MAX_COMBOS selections in
+    all. An explanation found is admissible by construction (every value lies
+    in its band), so the limits only bound the search."""
+    cand = sorted(set(ids_row.tolist()) | set(oracle_ids.tolist()))
+    others = {}
+    for e in cand:
+        vals = []
+        # where a logit sums terms that nearly cancel, its admissible band
+        # spans many bf16 steps; the GPU's weights then imply its value: for
+        # e in slot j and another expert r in slot i, w_j / w_i =
+        # exp(z_e - z_r), with z_r taken at the oracle's rounding
+        if e in ids_row.tolist() and len(ids_row) > 1:
+            j = ids_row.tolist().index(e)
+            i = 1 if j == 0 else 0
+            if w_row[j] > 0 and w_row[i] > 0:
+                implied = float(oracle.bf16_round(np.array(
+                    [zhat_row[ids_row[i]] + np.log(float(w_row[j]) / float(w_row[i]))]))[0])
+                vals += [implied] + bf16_values_near(implied, lo_row[e], hi_row[e], MAX_STEPS)
+        vals += bf16_values_near(zhat_row[e], lo_row[e], hi_row[e], MAX_STEPS)
+        seen = set()
+        others[e] = [v for v in vals if lo_row[e] <= v <= hi_row[e] and v != zhat_row[e]
+                     and not (v in seen or seen.add(v))]
+    amb = [e for e in cand if others[e]]
     tried = 0
     z = zhat_row.copy()
     for r in range(1, len(amb) + 1):
-        for subset in itertools.combinations(amb.tolist(), r):
+        for subset in itertools.combinations(amb, r):
             for combo in itertools.product(*(others[e] for e in subset)):
                 tried += 1
                 if tried > MAX_COMBOS:
-                    raise AssertionError(f"{len(amb)} ambiguous logits; no explanation within "
-                                         f"{MAX_COMBOS} admissible choices")
+                    return False
                 z[list(subset)] = combo
                 sid, sw = oracle.select(z, k)
                 z[list(subset)] = zhat_row[list(subset)]
@@ -212,7 +232,7 @@ def check_route(ri: inputs.RouteInputs, ids_g: np.ndarray, w_g: np.ndarray,
         f"k-th boundary")
     for i in np.nonzero(~exact)[0]:
         if logits_g is None:  # with logits_out the GPU's own logits explained it above
-            assert _explained(ref.zhat[i], lo[i], hi[i], k, ids_g[i, :k], w_g[i, :k]), (
+            assert _explained(ref.zhat[i], lo[i], hi[i], k, ids_g[i, :k], w_g[i, :k], ref.ids[i, :k]), (
                 f"row {rows[i]}: ids {ids_g[i, :k]} / weights differ from the oracle's "
                 f"{ref.ids[i, :k]} and no admissible rounding of its logits explains them")
     rep.rounding_rows = int((~exact).sum())
