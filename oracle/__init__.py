@@ -52,11 +52,11 @@ def _load():
             lib.oracle_bf16_to_double.restype = f64
             lib.oracle_gate_logits.argtypes = [i32, i32, i32, P, i64, P, P, P, P]
             lib.oracle_gate_logits.restype = None
-            lib.oracle_select.argtypes = [i32, i32, P, P, P]
+            lib.oracle_select.argtypes = [i32, i32, i32, P, P, P]
             lib.oracle_select.restype = None
             lib.oracle_shared_weight.argtypes = [f64, f32]
             lib.oracle_shared_weight.restype = f32
-            lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, f32, P, i64, P, P, P,
+            lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, f32, i32, i32, P, i64, P, P, P,
                                          P, P, P, P, P, P]
             lib.oracle_route.restype = None
             lib.oracle_route_threads.argtypes = [i32] + lib.oracle_route.argtypes
@@ -69,6 +69,8 @@ def _load():
             lib.oracle_align_capacity.restype = i64
             lib.oracle_align.argtypes = [P, i64, i32, i32, P, i64, P, i64, P]
             lib.oracle_align.restype = i32
+            lib.oracle_align_eplb.argtypes = [P, i64, i32, i32, P, P, i32, i32, i32, P, i64, P, i64, P]
+            lib.oracle_align_eplb.restype = i32
             _lib = lib
     return _lib
 
@@ -114,22 +116,23 @@ def gate_logits(x: np.ndarray, w: np.ndarray, bias: Optional[np.ndarray] = None)
     return z, ad
 
 
-def select(zhat_row: np.ndarray, k: int):
-    """Top-k (value desc, id asc) and renormalised softmax of one row."""
+def select(zhat_row: np.ndarray, k: int, renormalize: bool = True):
+    """Top-k (value desc, id asc) and softmax weights of one row
+    (renormalised over the top-k, or the full softmax's at the top-k)."""
     z = _c(zhat_row, np.float64)
     ids = np.empty(k, dtype=np.int32)
     w = np.empty(k, dtype=np.float32)
-    _load().oracle_select(z.shape[0], k, _ptr(z), _ptr(ids), _ptr(w))
+    _load().oracle_select(z.shape[0], k, 1 if renormalize else 0, _ptr(z), _ptr(ids), _ptr(w))
     return ids, w
 
 
-def select_rows(zhat: np.ndarray, k: int):
+def select_rows(zhat: np.ndarray, k: int, renormalize: bool = True):
     zhat = _c(zhat, np.float64)
     M = zhat.shape[0]
     ids = np.empty((M, k), dtype=np.int32)
     w = np.empty((M, k), dtype=np.float32)
     for t in range(M):
-        ids[t], w[t] = select(zhat[t], k)
+        ids[t], w[t] = select(zhat[t], k, renormalize)
     return ids, w
 
 
@@ -144,10 +147,11 @@ class RouteResult:
 
 def route(x: np.ndarray, w: np.ndarray, ws: Optional[np.ndarray], bias: Optional[np.ndarray],
           topk: int, scale: float = 1.0, rows: Optional[np.ndarray] = None,
-          threads: int = 1) -> RouteResult:
+          threads: int = 1, renormalize: bool = True, shared_bf16: bool = False) -> RouteResult:
     """Full oracle route. ``rows`` restricts it to a subset of token rows;
     ``threads`` > 1 splits the rows over that many host threads (same
-    results, rows are independent)."""
+    results, rows are independent). ``renormalize`` and ``shared_bf16``:
+    see oracle_route in oracle.c."""
     x = _c(x, np.uint16)
     if rows is not None:
         x = np.ascontiguousarray(x[np.asarray(rows)])
@@ -164,7 +168,8 @@ def route(x: np.ndarray, w: np.ndarray, ws: Optional[np.ndarray], bias: Optional
     z = np.empty((M, E), dtype=np.float64)
     ad = np.empty((M, E), dtype=np.float64)
     s = np.zeros(M, dtype=np.float64)
-    args = (M, H, E, topk, S, float(scale), _ptr(x), H, _ptr(w), _ptr(ws), _ptr(bias),
+    args = (M, H, E, topk, S, float(scale), 1 if renormalize else 0, 1 if shared_bf16 else 0,
+            _ptr(x), H, _ptr(w), _ptr(ws), _ptr(bias),
             _ptr(ids), _ptr(wt), _ptr(zhat), _ptr(z), _ptr(ad), _ptr(s))
     if threads > 1:
         _load().oracle_route_threads(int(threads), *args)
@@ -200,5 +205,29 @@ def align(ids: np.ndarray, num_experts: int, A: int) -> AlignResult:
                               _ptr(expert_ids), expert_ids.shape[0], _ptr(npp))
     if rc != 0:
         raise ValueError("oracle_align: id out of range or capacity too small")
+    n = int(npp[0])
+    return AlignResult(sorted_ids[:n].copy(), expert_ids[: n // A].copy(), n)
+
+
+def align_eplb(ids: np.ndarray, num_experts: int, eplb_map: np.ndarray, eplb_count: np.ndarray,
+               num_physical: int, A: int) -> AlignResult:
+    """moe_align_block_size behind the EPLB logical->physical remap (see
+    oracle_align_eplb in oracle.c). ids [num_tokens, width]; eplb_map
+    [num_experts, max_replicas]; eplb_count [num_experts]."""
+    ids = np.asarray(ids, dtype=np.int32)
+    width = ids.shape[1] if ids.ndim == 2 else 1
+    flat = np.ascontiguousarray(ids.ravel())
+    mp = np.ascontiguousarray(eplb_map, dtype=np.int32)
+    cnt = np.ascontiguousarray(eplb_count, dtype=np.int32)
+    numel = flat.shape[0]
+    cap = align_capacity(numel, num_physical, A)
+    sorted_ids = np.full(max(cap, 1), -7, dtype=np.int32)
+    expert_ids = np.full(max((cap + A - 1) // A, 1), -7, dtype=np.int32)
+    npp = np.zeros(1, dtype=np.int32)
+    rc = _load().oracle_align_eplb(_ptr(flat), numel, width, num_experts, _ptr(mp), _ptr(cnt),
+                                   mp.shape[1], num_physical, A, _ptr(sorted_ids), cap,
+                                   _ptr(expert_ids), expert_ids.shape[0], _ptr(npp))
+    if rc != 0:
+        raise ValueError("oracle_align_eplb: id, replica count or physical id out of range")
     n = int(npp[0])
     return AlignResult(sorted_ids[:n].copy(), expert_ids[: n // A].copy(), n)

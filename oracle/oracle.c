@@ -128,16 +128,25 @@ static int by_value_then_id(const void *pa, const void *pb)
 }
 
 /* One token row: zhat[E] are the bf16-rounded logits (as doubles). Writes
- * ids[k] (slot order: value desc, id asc) and w[k] = softmax over the
- * selected logits, computed in double and rounded once to fp32. */
-ORACLE_API void oracle_select(int E, int k, const double *zhat, int32_t *ids, float *w)
+ * ids[k] (slot order: value desc, id asc) and w[k], computed in double and
+ * rounded once to fp32:
+ *   renormalize = 1: the softmax over the E experts renormalised over the k
+ *     selected, i.e. a softmax over the selected logits (the full
+ *     denominator cancels);
+ *   renormalize = 0: the softmax over the E experts itself, read at the k
+ *     selected ids (weights sum to less than 1 when k < E) -- the
+ *     "unnormalized top-k weights" a guard of vLLM #60833 ("--monokernel
+ *     decode", Details, Refusals) refuses, and the renormalize flag of the
+ *     _router_triton_kernel of sglang #41133 (Motivation) turned off. */
+ORACLE_API void oracle_select(int E, int k, int renormalize, const double *zhat, int32_t *ids, float *w)
 {
     scored *s = (scored *)malloc(sizeof(scored) * (size_t)E);
     for (int e = 0; e < E; ++e) { s[e].v = zhat[e]; s[e].id = e; }
     qsort(s, (size_t)E, sizeof(scored), by_value_then_id);
     double zmax = s[0].v;
     double denom = 0.0;
-    for (int i = 0; i < k; ++i) denom += exp(s[i].v - zmax);
+    int nden = renormalize ? k : E;
+    for (int i = 0; i < nden; ++i) denom += exp(s[i].v - zmax);
     for (int i = 0; i < k; ++i) {
         ids[i] = s[i].id;
         w[i] = (float)(exp(s[i].v - zmax) / denom);
@@ -153,8 +162,13 @@ ORACLE_API float oracle_shared_weight(double s, float scale)
 
 /* Full route for M rows. Outputs ids/w are [M, k+S] row-major. Optional:
  * zhat_out [M,E] (rounded logits as doubles), z_out [M,E] (unrounded),
- * absdot_out [M,E], s_out [M] (shared logit). */
+ * absdot_out [M,E], s_out [M] (shared logit, unrounded). renormalize: see
+ * oracle_select. shared_bf16 = 1 rounds the shared logit to bf16 before the
+ * sigmoid (the shared gate as a bf16 dot product, "Netra Kernel ...",
+ * Reusing routing work instead of recomputing it); 0 keeps it unrounded
+ * (only the routed logits are rounded, sglang #41133, Modifications). */
 ORACLE_API void oracle_route(int M, int H, int E, int k, int has_shared, float scale,
+                             int renormalize, int shared_bf16,
                              const uint16_t *x, int64_t ld_x, const uint16_t *W,
                              const uint16_t *Ws, const float *bias,
                              int32_t *ids, float *w,
@@ -170,12 +184,13 @@ ORACLE_API void oracle_route(int M, int H, int E, int k, int has_shared, float s
         oracle_gate_logits(1, H, E, xt, ld_x, W, bias, z, ad);
         for (int e = 0; e < E; ++e)
             zh[e] = oracle_bf16_to_double(oracle_bf16_from_double(z[e]));
-        oracle_select(E, k, zh, ids + (int64_t)t * width, w + (int64_t)t * width);
+        oracle_select(E, k, renormalize, zh, ids + (int64_t)t * width, w + (int64_t)t * width);
         if (has_shared) {
             double s;
             oracle_gate_logits(1, H, 1, xt, ld_x, Ws, NULL, &s, NULL);
+            double sr = shared_bf16 ? oracle_bf16_to_double(oracle_bf16_from_double(s)) : s;
             ids[(int64_t)t * width + k] = E;
-            w[(int64_t)t * width + k] = oracle_shared_weight(s, scale);
+            w[(int64_t)t * width + k] = oracle_shared_weight(sr, scale);
             if (s_out) s_out[t] = s;
         }
         if (zhat_out) memcpy(zhat_out + (int64_t)t * E, zh, sizeof(double) * (size_t)E);
@@ -195,6 +210,7 @@ ORACLE_API void oracle_route(int M, int H, int E, int k, int has_shared, float s
 typedef struct {
     int M, H, E, k, has_shared;
     float scale;
+    int renormalize, shared_bf16;
     const uint16_t *x;
     int64_t ld_x;
     const uint16_t *W, *Ws;
@@ -207,13 +223,15 @@ typedef struct {
 static void *route_job_run(void *arg)
 {
     route_job *j = (route_job *)arg;
-    oracle_route(j->M, j->H, j->E, j->k, j->has_shared, j->scale, j->x, j->ld_x, j->W, j->Ws,
+    oracle_route(j->M, j->H, j->E, j->k, j->has_shared, j->scale, j->renormalize, j->shared_bf16,
+                 j->x, j->ld_x, j->W, j->Ws,
                  j->bias, j->ids, j->w, j->zhat_out, j->z_out, j->absdot_out, j->s_out);
     return NULL;
 }
 
 ORACLE_API int oracle_route_threads(int nthreads, int M, int H, int E, int k, int has_shared,
-                                    float scale, const uint16_t *x, int64_t ld_x,
+                                    float scale, int renormalize, int shared_bf16,
+                                    const uint16_t *x, int64_t ld_x,
                                     const uint16_t *W, const uint16_t *Ws, const float *bias,
                                     int32_t *ids, float *w, double *zhat_out, double *z_out,
                                     double *absdot_out, double *s_out)
@@ -229,6 +247,7 @@ ORACLE_API int oracle_route_threads(int nthreads, int M, int H, int E, int k, in
         int r0 = (int)((int64_t)M * i / nthreads), r1 = (int)((int64_t)M * (i + 1) / nthreads);
         route_job *j = &jobs[i];
         j->M = r1 - r0; j->H = H; j->E = E; j->k = k; j->has_shared = has_shared; j->scale = scale;
+        j->renormalize = renormalize; j->shared_bf16 = shared_bf16;
         j->x = x + (int64_t)r0 * ld_x; j->ld_x = ld_x; j->W = W; j->Ws = Ws; j->bias = bias;
         j->ids = ids + (int64_t)r0 * width; j->w = w + (int64_t)r0 * width;
         j->zhat_out = zhat_out ? zhat_out + (int64_t)r0 * E : NULL;
@@ -298,5 +317,38 @@ done:
     free(cnt);
     free(off);
     free(cur);
+    return rc;
+}
+
+/* moe_align_block_size behind an expert-parallel load-balancing (EPLB)
+ * logical->physical remap, which the pages' guards refuse (sglang #41133,
+ * Modifications: "no EPLB remap"; vLLM #60833, Details, Refusals) and do not
+ * define; the reading taken here: logical expert e is held by count[e]
+ * physical replicas, listed in map[e * max_replicas + r], r < count[e]; the
+ * slot (t, s) of token t = i / width goes to replica r = t mod count[e], so a
+ * token's slots of one expert meet on one replica and consecutive tokens
+ * take its replicas in turn. The physical ids are then aligned exactly as
+ * above over num_physical experts (ids, padding and block owners are
+ * physical; the flat slot indices stored are unchanged). Returns 0, or -1 on
+ * an id, count or physical id out of range or a capacity too small. */
+ORACLE_API int oracle_align_eplb(const int32_t *ids, int64_t numel, int width, int num_experts,
+                                 const int32_t *map, const int32_t *count, int max_replicas,
+                                 int num_physical, int A, int32_t *sorted, int64_t sorted_cap,
+                                 int32_t *expert_ids, int64_t expert_cap, int32_t *npp_out)
+{
+    int32_t *phys = (int32_t *)malloc(sizeof(int32_t) * (size_t)(numel > 0 ? numel : 1));
+    int rc = 0;
+    for (int64_t i = 0; i < numel; ++i) {
+        int e = ids[i];
+        if (e < 0 || e >= num_experts || count[e] < 1 || count[e] > max_replicas) { rc = -1; break; }
+        int64_t t = i / width;
+        int p = map[(int64_t)e * max_replicas + (int)(t % count[e])];
+        if (p < 0 || p >= num_physical) { rc = -1; break; }
+        phys[i] = p;
+    }
+    if (rc == 0)
+        rc = oracle_align(phys, numel, num_physical, A, sorted, sorted_cap, expert_ids, expert_cap,
+                          npp_out);
+    free(phys);
     return rc;
 }

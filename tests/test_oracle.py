@@ -401,3 +401,99 @@ def test_npp_table_ratio_is_npp_over_routed_rows():
         # averages of per-layer multiples of A, never below one block per touched expert
         assert int(npp64) * 4 % 64 == 0 and int(npp128) * 4 % 128 == 0
         assert int(npp128) >= int(touched) * 128 and int(npp64) >= int(touched) * 64
+
+
+# ------------------------------------------------------- routing variants ---
+
+def test_select_without_renormalisation_is_the_full_softmax_at_the_top_k():
+    """renormalize = 0: the weights are scipy's softmax over all E logits,
+    read at the selected ids (same ids as with renormalisation)."""
+    rng = np.random.default_rng(41)
+    for E, k in ((64, 8), (513, 10), (7, 3)):
+        z = oracle.bf16_round(rng.normal(0, 2, E))
+        ids, w = oracle.select(z, k, renormalize=False)
+        ids1, w1 = oracle.select(z, k)
+        assert np.array_equal(ids, ids1)
+        ref = scipy.special.softmax(z)[ids]
+        assert np.allclose(w, ref.astype(np.float32), rtol=1.2e-7, atol=0)
+        assert float(w.astype(np.float64).sum()) < 1.0
+        # renormalising the unrenormalised weights gives the renormalised ones
+        assert np.allclose(w / w.astype(np.float64).sum(), w1, rtol=1e-6)
+
+
+def test_select_without_renormalisation_k_equals_e():
+    z = oracle.bf16_round(np.random.default_rng(42).normal(0, 1, 16))
+    ids0, w0 = oracle.select(z, 16, renormalize=False)
+    ids1, w1 = oracle.select(z, 16)
+    assert np.array_equal(ids0, ids1) and np.array_equal(w0, w1)
+
+
+def test_route_without_renormalisation():
+    ri = inputs.make_route_inputs(5, 256, 64, 6, 1, seed=43)
+    r0 = oracle.route(ri.x, ri.w, ri.ws, None, 6, renormalize=False)
+    r1 = oracle.route(ri.x, ri.w, ri.ws, None, 6)
+    assert np.array_equal(r0.ids, r1.ids)
+    for t in range(5):
+        ref = scipy.special.softmax(r0.zhat[t])[r0.ids[t, :6]]
+        assert np.allclose(r0.w[t, :6], ref.astype(np.float32), rtol=1.2e-7, atol=0)
+    assert np.array_equal(r0.w[:, 6], r1.w[:, 6])  # the shared slot is unaffected
+
+
+def test_route_shared_logit_rounded_to_bf16():
+    """shared_bf16: a shared logit of exactly 1 + 2^-9 rounds to 1.0 first, so
+    the weight is expit(1.0) rather than expit(1 + 2^-9); without the flag it
+    is the latter. Routed outputs do not change."""
+    H, E = 8, 4
+    x = inputs.f32_to_bf16_bits(np.array([[1, 1, 0, 0, 0, 0, 0, 0]], np.float32))
+    ws = inputs.f32_to_bf16_bits(np.array([[1, 2.0 ** -9, 0, 0, 0, 0, 0, 0]], np.float32))
+    w = inputs.f32_to_bf16_bits(np.eye(E, H, dtype=np.float32))
+    r1 = oracle.route(x, w, ws, None, 2, 2.0, shared_bf16=True)
+    r0 = oracle.route(x, w, ws, None, 2, 2.0)
+    assert r1.s[0] == 1.0 + 2.0 ** -9
+    assert r1.w[0, 2] == np.float32(2.0 * scipy.special.expit(1.0))
+    assert r0.w[0, 2] == np.float32(2.0 * scipy.special.expit(1.0 + 2.0 ** -9))
+    assert r0.w[0, 2] != r1.w[0, 2]
+    assert np.array_equal(r0.ids, r1.ids) and np.array_equal(r0.w[:, :2], r1.w[:, :2])
+
+
+def test_align_eplb_identity_map_is_plain_align():
+    ids = inputs.random_ids(300, 9, 65, seed=44, skew=1.1)
+    mp = np.arange(65, dtype=np.int32)[:, None]
+    got = oracle.align_eplb(ids, 65, mp, np.ones(65, np.int32), 65, 16)
+    ref = oracle.align(ids, 65, 16)
+    assert got.npp == ref.npp
+    assert np.array_equal(got.sorted_ids, ref.sorted_ids) and np.array_equal(got.expert_ids, ref.expert_ids)
+
+
+def test_align_eplb_permutation_is_a_relabelling():
+    """One replica per expert, physical ids a permutation over more physical
+    slots: the same as aligning the relabelled ids (numpy take), with the
+    unused physical experts empty."""
+    rng = np.random.default_rng(45)
+    ids = inputs.random_ids(200, 5, 40, seed=46)
+    perm = rng.permutation(48)[:40].astype(np.int32)
+    got = oracle.align_eplb(ids, 40, perm[:, None], np.ones(40, np.int32), 48, 8)
+    ref = _textbook_align(np.take(perm, ids), 48, 8)
+    assert got.npp == len(ref[0])
+    assert np.array_equal(got.sorted_ids, ref[0]) and np.array_equal(got.expert_ids, ref[1])
+
+
+def test_align_eplb_replicas_hand_case():
+    """Hand-worked: 4 tokens x 2 slots, expert 0 held by physical 5 and 2
+    (two replicas), expert 1 by physical 3, expert 2 by physical 0; A = 2.
+    Token t's slot of expert 0 goes to replica t mod 2 (tokens 2 and 3 hold
+    expert 0 in different slot positions, so the token, not the slot, picks):
+      ids   [[0,1],[2,0],[1,0],[0,2]]  (flat 0..7)
+      phys  [[5,3],[0,2],[3,5],[2,0]]
+    physical 0: flat 2, 7; physical 2: flat 3, 6; physical 3: flat 1, 4;
+    physical 5: flat 0, 5."""
+    ids = np.array([[0, 1], [2, 0], [1, 0], [0, 2]], np.int32)
+    mp = np.array([[5, 2], [3, -1], [0, -1]], np.int32)
+    cnt = np.array([2, 1, 1], np.int32)
+    got = oracle.align_eplb(ids, 3, mp, cnt, 6, 2)
+    assert got.npp == 8
+    assert got.sorted_ids.tolist() == [2, 7, 3, 6, 1, 4, 0, 5]
+    assert got.expert_ids.tolist() == [0, 2, 3, 5]
+    # a replica count above the table width is refused
+    with pytest.raises(ValueError):
+        oracle.align_eplb(ids, 3, mp, np.array([3, 1, 1], np.int32), 6, 2)

@@ -24,16 +24,21 @@ MUTANTS = [
     ("ties go to the highest id",
      "return (a->id < b->id) ? -1 : (a->id > b->id);", "return (a->id > b->id) ? -1 : (a->id < b->id);"),
     ("softmax not renormalised over the top-k",
-     "for (int i = 0; i < k; ++i) denom += exp(s[i].v - zmax);",
-     "for (int i = 0; i < E; ++i) denom += exp(s[i].v - zmax);"),
+     "int nden = renormalize ? k : E;", "int nden = E;"),
+    ("renormalised even when renormalize = 0",
+     "int nden = renormalize ? k : E;", "int nden = k;"),
     ("sigmoid sign flipped", "(1.0 / (1.0 + exp(-s)))", "(1.0 / (1.0 + exp(s)))"),
     ("shared scale dropped",
      "return (float)((double)scale * (1.0 / (1.0 + exp(-s))));",
      "return (float)(1.0 / (1.0 + exp(-s)));"),
-    ("shared logit rounded to bf16 before the sigmoid",
-     "w[(int64_t)t * width + k] = oracle_shared_weight(s, scale);",
-     "w[(int64_t)t * width + k] = oracle_shared_weight(oracle_bf16_to_double(oracle_bf16_from_double(s)), scale);"),
-    ("top-k on the unrounded logits", "oracle_select(E, k, zh, ids", "oracle_select(E, k, z, ids"),
+    ("shared logit rounded to bf16 before the sigmoid without the flag",
+     "double sr = shared_bf16 ? oracle_bf16_to_double(oracle_bf16_from_double(s)) : s;",
+     "double sr = oracle_bf16_to_double(oracle_bf16_from_double(s));"),
+    ("shared_bf16 flag ignored",
+     "double sr = shared_bf16 ? oracle_bf16_to_double(oracle_bf16_from_double(s)) : s;",
+     "double sr = s;"),
+    ("top-k on the unrounded logits", "oracle_select(E, k, renormalize, zh, ids",
+     "oracle_select(E, k, renormalize, z, ids"),
     ("tier boundary inclusive",
      "< (int64_t)128 * num_experts) ? 64 : 128;", "<= (int64_t)128 * num_experts) ? 64 : 128;"),
     ("capacity one row too large",
@@ -44,6 +49,10 @@ MUTANTS = [
      "off[e + 1] = off[e] + (cnt[e] + A - 1) / A * A;",
      "off[e + 1] = off[e] + (cnt[e] + A - 1) / A * A + (cnt[e] == 0 ? A : 0);"),
     ("padding sentinel 0", "sorted[p] = (int32_t)numel;", "sorted[p] = 0;"),
+    ("EPLB replica chosen by slot instead of token",
+     "int p = map[(int64_t)e * max_replicas + (int)(t % count[e])];",
+     "int p = map[(int64_t)e * max_replicas + (int)(i % count[e])];"),
+    ("EPLB remap skipped", "phys[i] = p;", "phys[i] = e;"),
     ("descending order inside an expert",
      "for (int64_t i = 0; i < numel; ++i) sorted[cur[ids[i]]++] = (int32_t)i;",
      "for (int64_t i = numel - 1; i >= 0; --i) sorted[cur[ids[i]]++] = (int32_t)i;"),
@@ -57,7 +66,7 @@ def test_pins_reject_mutant(tmp_path, name, old, new):
     mut = tmp_path / "oracle_mutant.c"
     mut.write_text(src.replace(old, new))
     lib = tmp_path / "liboracle_mutant.so"
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
                            "-ffp-contract=off", "-o", str(lib), str(mut), "-lm"])
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
