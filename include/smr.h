@@ -82,7 +82,9 @@ typedef struct smr_route_args {
     int32_t topk;            /* routed top-k, 1..E, topk + has_shared <= 32 */
     int32_t has_shared;      /* S: 1 = shared expert with id E, 0 = none */
     float shared_scale;      /* multiplies sigmoid(shared logit) */
-    int32_t renormalize;     /* must be 1 (softmax renormalised over the top-k) */
+    int32_t renormalize;     /* 1: weights = softmax renormalised over the top-k (sum 1);
+                                0: the softmax over all E routed experts read at the top-k
+                                ids (unnormalised top-k weights) */
     const void *hidden;      /* bf16 [M, ld_hidden], 16-byte aligned */
     int64_t ld_hidden;       /* row stride of hidden in elements, >= H, multiple of 8 */
     const void *gate_w;      /* bf16 [E, H] contiguous (nn.Linear layout), 16-byte aligned */
@@ -94,6 +96,12 @@ typedef struct smr_route_args {
     float *topk_weights;     /* out: fp32 [M, topk + S] */
     uint16_t *logits_out;    /* optional out: bf16 bits [M, E] of the rounded routed
                                 logits (bias included); NULL to skip */
+    int32_t shared_logit_bf16; /* 1: round the shared logit to bf16 before the sigmoid
+                                  (the shared gate as a bf16 dot product, "Netra Kernel
+                                  ...", Reusing routing work instead of recomputing it);
+                                  0: use the fp32 logit (only the routed logits are
+                                  rounded, "[AMD] One-launch small-M MoE router ...",
+                                  Modifications) */
 } smr_route_args;
 
 /* Align problem over a [num_tokens, width] id matrix. */
@@ -113,6 +121,21 @@ typedef struct smr_align_args {
     int32_t *expert_ids;          /* out: int32 [expert_cap]; [0, npp/A) defined */
     int64_t expert_cap;           /* >= ceil(smr_align_capacity(...) / A) */
     int32_t *num_tokens_post_padded;  /* out: device int32 [1] = npp */
+    /* Optional expert-parallel load-balancing (EPLB) logical->physical remap
+     * applied inside the align (the pages' guards refuse such a remap without
+     * defining it; this is the library's reading): logical expert e (an id in
+     * topk_ids) is held by eplb_count[e] in [1, eplb_max_replicas] physical
+     * replicas listed in eplb_map[e * eplb_max_replicas + r]; the slot of
+     * token t goes to replica r = t mod eplb_count[e]. Counts, padding, the
+     * capacity (numel + num_physical * (A - 1)) and expert_ids are then over
+     * the num_physical physical experts; sorted_token_ids still holds flat
+     * slot indices. An id, count or physical id out of range is skipped and
+     * sets bit 0 of the sticky device error word. eplb_map == NULL: no remap
+     * (the other three fields are ignored). Device pointers, read only. */
+    const int32_t *eplb_map;      /* int32 [num_experts, eplb_max_replicas] or NULL */
+    const int32_t *eplb_count;    /* int32 [num_experts] */
+    int32_t eplb_max_replicas;    /* 1..64 */
+    int32_t num_physical;         /* 1..1025 */
 } smr_align_args;
 
 /* M-aware alignment tier (host, no device work): 64 if
@@ -133,7 +156,7 @@ SMR_API size_t smr_align_workspace_size(const smr_align_args *args);
 SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const smr_align_args *align);
 
 /* Route only: the gate GEMM, bf16 rounding, top-k with the lowest id winning
- * ties, softmax renormalised over the selected and the shared slot
+ * ties, softmax (renormalised over the selected, or not) and the shared slot
  * ("[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950",
  * Modifications). One kernel launch for M <= 16: the gate rows are split
  * across CTAs, and one CTA selects after collecting the row groups'
@@ -160,7 +183,8 @@ SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t
  * align->num_experts == E + S; routed_topk/routed_experts are taken from the
  * route. For M <= 16 both run in ONE launch; for larger M the tcgen05 route
  * also writes each 64-row tile's expert counts and two align launches
- * follow (one when the ids fit a single align CTA). */
+ * follow (one when the ids fit a single align CTA). With an EPLB remap the
+ * align always runs as its own launches behind the route (1 or 3). */
 SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_args *align,
                            void *workspace, size_t workspace_bytes, void *stream);
 

@@ -126,7 +126,7 @@ def _workspace(ws, nbytes: int, device):
 
 
 def _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, ids, wts,
-                logits_out) -> RouteArgs:
+                logits_out, shared_logit_bf16=False) -> RouteArgs:
     torch = _torch()
     if hidden.dtype != torch.bfloat16 or gate_w.dtype != torch.bfloat16:
         raise TypeError("hidden and gate_w must be bfloat16")
@@ -155,6 +155,7 @@ def _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize,
     a.topk_ids = _ptr(ids)
     a.topk_weights = _ptr(wts)
     a.logits_out = _ptr(logits_out)
+    a.shared_logit_bf16 = 1 if shared_logit_bf16 else 0
     return a
 
 
@@ -170,14 +171,14 @@ def _route_outputs(hidden, topk, has_shared, ids, wts):
 
 
 def route(hidden, gate_w, shared_w=None, bias=None, *, topk: int, shared_scale: float = 1.0,
-          renormalize: bool = True, topk_ids=None, topk_weights=None, logits_out=None,
-          workspace=None, stream=None) -> Tuple:
+          renormalize: bool = True, shared_logit_bf16: bool = False, topk_ids=None,
+          topk_weights=None, logits_out=None, workspace=None, stream=None) -> Tuple:
     """Route M tokens: returns (topk_ids int32 [M, k+S], topk_weights fp32 [M, k+S])."""
     _disabled()
     lib = _lib.load()
     topk_ids, topk_weights = _route_outputs(hidden, topk, shared_w is not None, topk_ids, topk_weights)
     a = _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, topk_ids,
-                    topk_weights, logits_out)
+                    topk_weights, logits_out, shared_logit_bf16)
     need = lib.smr_route_workspace_size(ctypes.byref(a))
     wp, wn = _workspace(workspace, need, hidden.device)
     _check(lib.smr_route(ctypes.byref(a), wp, wn, _stream_ptr(stream)))
@@ -185,7 +186,7 @@ def route(hidden, gate_w, shared_w=None, bias=None, *, topk: int, shared_scale: 
 
 
 def _align_args(topk_ids, num_tokens, width, num_experts, block_size, routed_topk,
-                routed_experts, sorted_ids, expert_ids, npp) -> AlignArgs:
+                routed_experts, sorted_ids, expert_ids, npp, eplb=None) -> AlignArgs:
     a = AlignArgs()
     a.topk_ids = _ptr(topk_ids)
     a.num_tokens = int(num_tokens)
@@ -199,7 +200,24 @@ def _align_args(topk_ids, num_tokens, width, num_experts, block_size, routed_top
     a.expert_ids = _ptr(expert_ids)
     a.expert_cap = 0 if expert_ids is None else expert_ids.numel()
     a.num_tokens_post_padded = _ptr(npp)
+    if eplb is not None:
+        emap, ecount, nphys = eplb
+        a.eplb_map = _ptr(emap)
+        a.eplb_count = _ptr(ecount)
+        a.eplb_max_replicas = int(emap.shape[1]) if emap.dim() == 2 else 1
+        a.num_physical = int(nphys)
     return a
+
+
+def _eplb(eplb_map, eplb_count, num_physical):
+    """(map, count, num_physical) of an EPLB remap, or None."""
+    if eplb_map is None:
+        return None
+    torch = _torch()
+    for t in (eplb_map, eplb_count):
+        if t is None or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("eplb_map [E_al, R] and eplb_count [E_al] must be contiguous int32 tensors")
+    return eplb_map, eplb_count, int(num_physical)
 
 
 def _align_outputs(device, numel, num_experts, A, sorted_ids, expert_ids, npp):
@@ -216,8 +234,11 @@ def _align_outputs(device, numel, num_experts, A, sorted_ids, expert_ids, npp):
 
 def align(topk_ids, num_experts: int, block_size: int = 0, *, routed_topk: int = 0,
           routed_experts: int = 0, sorted_token_ids=None, expert_ids=None,
-          num_tokens_post_padded=None, workspace=None, stream=None) -> Tuple:
-    """moe_align_block_size of an int32 [num_tokens, width] id matrix.
+          num_tokens_post_padded=None, eplb_map=None, eplb_count=None, num_physical: int = 0,
+          workspace=None, stream=None) -> Tuple:
+    """moe_align_block_size of an int32 [num_tokens, width] id matrix,
+    optionally behind an EPLB logical->physical remap (eplb_map [E, R],
+    eplb_count [E], num_physical; see smr_align_args in include/smr.h).
 
     Returns (sorted_token_ids, expert_ids, num_tokens_post_padded); only the
     first npp / npp // A entries of the first two are defined."""
@@ -228,9 +249,11 @@ def align(topk_ids, num_experts: int, block_size: int = 0, *, routed_topk: int =
         raise ValueError("topk_ids must be a contiguous int32 [num_tokens, width] tensor")
     T, W = topk_ids.shape
     A = block_size if block_size > 0 else select_block_size(T, routed_topk, routed_experts)
-    outs = _align_outputs(topk_ids.device, T * W, num_experts, A, sorted_token_ids, expert_ids,
-                          num_tokens_post_padded)
-    a = _align_args(topk_ids, T, W, num_experts, block_size, routed_topk, routed_experts, *outs)
+    eplb = _eplb(eplb_map, eplb_count, num_physical)
+    outs = _align_outputs(topk_ids.device, T * W, num_physical if eplb else num_experts, A,
+                          sorted_token_ids, expert_ids, num_tokens_post_padded)
+    a = _align_args(topk_ids, T, W, num_experts, block_size, routed_topk, routed_experts, *outs,
+                    eplb=eplb)
     need = lib.smr_align_workspace_size(ctypes.byref(a))
     wp, wn = _workspace(workspace, need, topk_ids.device)
     _check(lib.smr_align(ctypes.byref(a), wp, wn, _stream_ptr(stream)))
@@ -238,22 +261,26 @@ def align(topk_ids, num_experts: int, block_size: int = 0, *, routed_topk: int =
 
 
 def route_align(hidden, gate_w, shared_w=None, bias=None, *, topk: int, block_size: int = 0,
-                shared_scale: float = 1.0, renormalize: bool = True, topk_ids=None,
-                topk_weights=None, logits_out=None, sorted_token_ids=None, expert_ids=None,
-                num_tokens_post_padded=None, workspace=None, stream=None) -> Tuple:
-    """Route then align (one launch for M <= 16). Returns (topk_ids,
-    topk_weights, sorted_token_ids, expert_ids, num_tokens_post_padded)."""
+                shared_scale: float = 1.0, renormalize: bool = True,
+                shared_logit_bf16: bool = False, topk_ids=None, topk_weights=None,
+                logits_out=None, sorted_token_ids=None, expert_ids=None,
+                num_tokens_post_padded=None, eplb_map=None, eplb_count=None,
+                num_physical: int = 0, workspace=None, stream=None) -> Tuple:
+    """Route then align (one launch for M <= 16 without an EPLB remap).
+    Returns (topk_ids, topk_weights, sorted_token_ids, expert_ids,
+    num_tokens_post_padded)."""
     _disabled()
     lib = _lib.load()
     S = 1 if shared_w is not None else 0
     topk_ids, topk_weights = _route_outputs(hidden, topk, S, topk_ids, topk_weights)
     ra = _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, topk_ids,
-                     topk_weights, logits_out)
+                     topk_weights, logits_out, shared_logit_bf16)
     M, E = ra.M, ra.E
     A = block_size if block_size > 0 else select_block_size(M, topk, E)
-    outs = _align_outputs(hidden.device, M * (topk + S), E + S, A, sorted_token_ids, expert_ids,
-                          num_tokens_post_padded)
-    aa = _align_args(topk_ids, M, topk + S, E + S, block_size, topk, E, *outs)
+    eplb = _eplb(eplb_map, eplb_count, num_physical)
+    outs = _align_outputs(hidden.device, M * (topk + S), num_physical if eplb else E + S, A,
+                          sorted_token_ids, expert_ids, num_tokens_post_padded)
+    aa = _align_args(topk_ids, M, topk + S, E + S, block_size, topk, E, *outs, eplb=eplb)
     need = lib.smr_route_align_workspace_size(ctypes.byref(ra), ctypes.byref(aa))
     wp, wn = _workspace(workspace, need, hidden.device)
     _check(lib.smr_route_align(ctypes.byref(ra), ctypes.byref(aa), wp, wn, _stream_ptr(stream)))
@@ -262,8 +289,9 @@ def route_align(hidden, gate_w, shared_w=None, bias=None, *, topk: int, block_si
 
 def route_align_static(hidden, gate_w, shared_w=None, bias=None, *, topk: int,
                        block_size: int = 0, shared_scale: float = 1.0, renormalize: bool = True,
-                       topk_ids=None, topk_weights=None, logits_out=None, sorted_token_ids=None,
-                       expert_ids=None, num_tokens_post_padded=None, stream=None) -> Tuple:
+                       shared_logit_bf16: bool = False, topk_ids=None, topk_weights=None,
+                       logits_out=None, sorted_token_ids=None, expert_ids=None,
+                       num_tokens_post_padded=None, stream=None) -> Tuple:
     """route_align for 1 <= M <= 16 without a workspace: the library's fixed
     device scratch array is used instead, for callers that cannot allocate
     device memory. Calls must not overlap on the GPU; the first call on a
@@ -275,7 +303,7 @@ def route_align_static(hidden, gate_w, shared_w=None, bias=None, *, topk: int,
     S = 1 if shared_w is not None else 0
     topk_ids, topk_weights = _route_outputs(hidden, topk, S, topk_ids, topk_weights)
     ra = _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, topk_ids,
-                     topk_weights, logits_out)
+                     topk_weights, logits_out, shared_logit_bf16)
     M, E = ra.M, ra.E
     A = block_size if block_size > 0 else select_block_size(M, topk, E)
     outs = _align_outputs(hidden.device, M * (topk + S), E + S, A, sorted_token_ids, expert_ids,

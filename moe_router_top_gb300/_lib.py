@@ -43,6 +43,7 @@ class RouteArgs(ctypes.Structure):
         ("gate_w", ctypes.c_void_p), ("shared_w", ctypes.c_void_p),
         ("bias", ctypes.c_void_p), ("topk_ids", ctypes.c_void_p),
         ("topk_weights", ctypes.c_void_p), ("logits_out", ctypes.c_void_p),
+        ("shared_logit_bf16", ctypes.c_int32),
     ]
 
 
@@ -54,6 +55,8 @@ class AlignArgs(ctypes.Structure):
         ("block_size", ctypes.c_int32), ("sorted_token_ids", ctypes.c_void_p),
         ("sorted_cap", ctypes.c_int64), ("expert_ids", ctypes.c_void_p),
         ("expert_cap", ctypes.c_int64), ("num_tokens_post_padded", ctypes.c_void_p),
+        ("eplb_map", ctypes.c_void_p), ("eplb_count", ctypes.c_void_p),
+        ("eplb_max_replicas", ctypes.c_int32), ("num_physical", ctypes.c_int32),
     ]
 
 

@@ -26,6 +26,20 @@ namespace smr {
 constexpr int kAlignThreads = 512;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
+// The expert the align files slot i under: its id e, or behind an EPLB remap
+// the physical replica of logical expert e that token i / width uses,
+// map[e * R + (i / width) mod count[e]]. A logical id, replica count or
+// physical id out of range gives -1, which the callers skip and flag as a
+// bad id.
+__device__ __forceinline__ int align_expert_of(const AlignLaunch &a, int e, int i) {
+    if (a.map == nullptr) return e;
+    if ((unsigned)e >= (unsigned)a.E_log) return -1;
+    const int c = __ldg(a.map_count + e);
+    if (c < 1 || c > a.map_R) return -1;
+    const int p = __ldg(a.map + (int64_t)e * a.map_R + (i / a.width) % c);
+    return (unsigned)p < (unsigned)a.E_al ? p : -1;
+}
+
 __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const AlignLaunch a) {
     extern __shared__ __align__(16) int sm[];
     griddep_launch_dependents();  // the next kernel may launch; it waits for this grid
@@ -34,6 +48,11 @@ __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const Align
     int *ids = sm;  // [kAlignSingleMax] staged ids
     AlignSmem s = align_carve(sm + kAlignSingleMax, a.E_al);
     stage_ids(ids, a.ids, a.numel);
+    if (a.map != nullptr) {  // EPLB: file each slot under its physical replica
+        for (int i = threadIdx.x; i < a.numel; i += blockDim.x) ids[i] = align_expert_of(a, ids[i], i);
+        __syncwarp();
+        __syncthreads();
+    }
     align_count(ids, a.numel, a.E_al, s, err);
     const int npp = align_offsets(s.cnt, a.E_al, a.A, s);
     align_scatter(ids, a.numel, a.E_al, 0, s, false, a.sorted, a.sorted_cap, err);
@@ -66,6 +85,9 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_count_kernel(const Al
         int v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) v[j] = __ldcg(a.ids + min(i0 + j * kTileThreads + tid, end - 1));
+        if (a.map != nullptr)  // EPLB: count physical replicas
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = align_expert_of(a, v[j], min(i0 + j * kTileThreads + tid, end - 1));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (i0 + j * kTileThreads + tid < end) {
@@ -181,6 +203,10 @@ __global__ void __launch_bounds__(kTileThreads) align_tile_scatter_kernel(const 
     auto load_ids = [&](int c0, int (&e4)[4]) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) e4[g] = __ldcg(a.ids + beg + min(c0 + warp * 128 + g * 32 + lane, n - 1));
+        if (a.map != nullptr)  // EPLB: scatter by physical replica
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                e4[g] = align_expert_of(a, e4[g], beg + min(c0 + warp * 128 + g * 32 + lane, n - 1));
     };
     int e4[4];
     load_ids(0, e4);

@@ -97,8 +97,10 @@ void check_route(const smr_route_args *a, Reasons &r) {
         r.bad("topk must be in [1, E] (got " + std::to_string(a->topk) + ")");
     else if (a->topk + S > 32)
         r.unsup("topk + has_shared must be <= 32 (got " + std::to_string(a->topk + S) + ")");
-    if (a->renormalize != 1)
-        r.unsup("only renormalize == 1 (softmax renormalised over the top-k) is implemented");
+    if (a->renormalize != 0 && a->renormalize != 1)
+        r.bad("renormalize must be 0 or 1 (got " + std::to_string(a->renormalize) + ")");
+    if (a->shared_logit_bf16 != 0 && a->shared_logit_bf16 != 1)
+        r.bad("shared_logit_bf16 must be 0 or 1 (got " + std::to_string(a->shared_logit_bf16) + ")");
     if (!std::isfinite(a->shared_scale)) r.bad("shared_scale must be finite");
     if (a->M > 0) {
         if (!a->hidden) r.bad("hidden is NULL");
@@ -135,6 +137,12 @@ int effective_block_size(const smr_align_args *a) {
     return smr_select_block_size(a->num_tokens, a->routed_topk, a->routed_experts);
 }
 
+// The experts the align counts and pads: the physical ones behind an EPLB
+// remap, else the ids' own range.
+bool has_eplb(const smr_align_args *a) { return a->eplb_map != nullptr; }
+int align_experts(const smr_align_args *a) { return has_eplb(a) ? a->num_physical : a->num_experts; }
+constexpr int kMaxReplicas = 64;
+
 void check_align(const smr_align_args *a, Reasons &r, bool ids_from_route) {
     if (a->num_tokens < 0) r.bad("num_tokens must be >= 0");
     if (a->width < 1) r.bad("width must be >= 1");
@@ -145,6 +153,15 @@ void check_align(const smr_align_args *a, Reasons &r, bool ids_from_route) {
               std::to_string(a->block_size) + ")");
     if (a->block_size == 0 && !ids_from_route && (a->routed_topk < 1 || a->routed_experts < 1))
         r.bad("block_size == 0 needs routed_topk >= 1 and routed_experts >= 1");
+    if (has_eplb(a)) {
+        if (!a->eplb_count) r.bad("eplb_count is NULL but eplb_map is set");
+        if (!aligned(a->eplb_map, 4) || (a->eplb_count && !aligned(a->eplb_count, 4)))
+            r.bad("eplb_map and eplb_count must be 4-byte aligned");
+        if (a->eplb_max_replicas < 1 || a->eplb_max_replicas > kMaxReplicas)
+            r.bad("eplb_max_replicas must be in [1, 64] (got " + std::to_string(a->eplb_max_replicas) + ")");
+        if (a->num_physical < 1 || a->num_physical > kMaxExperts + 1)
+            r.bad("num_physical must be in [1, 1025] (got " + std::to_string(a->num_physical) + ")");
+    }
     if (!r.invalid.empty()) return;
     const int64_t numel = (int64_t)a->num_tokens * a->width;
     if (numel > (int64_t)1 << 30) r.unsup("num_tokens * width must be <= 2^30");
@@ -153,7 +170,7 @@ void check_align(const smr_align_args *a, Reasons &r, bool ids_from_route) {
         r.bad("cannot derive a block size");
         return;
     }
-    const int64_t cap = smr_align_capacity(numel, a->num_experts, A);
+    const int64_t cap = smr_align_capacity(numel, align_experts(a), A);
     if (!ids_from_route) {
         if (numel > 0 && !a->topk_ids) r.bad("topk_ids is NULL");
         else if (a->topk_ids && !aligned(a->topk_ids, 4)) r.bad("topk_ids must be 4-byte aligned");
@@ -172,7 +189,7 @@ void check_align(const smr_align_args *a, Reasons &r, bool ids_from_route) {
 size_t align_scratch_bytes(const smr_align_args *a) {
     const int64_t numel = (int64_t)a->num_tokens * a->width;
     if (numel <= smr::kAlignSingleMax) return 0;
-    return round_up((size_t)smr::align_scratch_words(numel, a->num_experts) * 4, kWsAlign);
+    return round_up((size_t)smr::align_scratch_words(numel, align_experts(a)) * 4, kWsAlign);
 }
 
 smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
@@ -193,9 +210,10 @@ smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
 }
 
 // The align behind a tcgen05 route over more than kAlignSingleMax slots takes
-// its per-tile expert counts from the route (tiles of 64 token rows).
-bool align_counted_by_route(const smr_route_args *r, int64_t numel) {
-    return r->M > smr::kSmallMaxM && numel > smr::kAlignSingleMax;
+// its per-tile expert counts from the route (tiles of 64 token rows), unless
+// an EPLB remap changes what is counted.
+bool align_counted_by_route(const smr_route_args *r, const smr_align_args *a, int64_t numel) {
+    return r->M > smr::kSmallMaxM && numel > smr::kAlignSingleMax && !has_eplb(a);
 }
 int64_t route_tiles(const smr_route_args *r) {
     return (r->M + smr::kTcCountRows - 1) / smr::kTcCountRows;
@@ -207,8 +225,13 @@ smr::AlignLaunch make_align_launch(const smr_align_args *a, const int32_t *ids, 
     smr::AlignLaunch L{};
     L.ids = ids;
     L.numel = a->num_tokens * a->width;
-    L.E_al = a->num_experts;
+    L.E_al = align_experts(a);
     L.A = effective_block_size(a);
+    L.map = a->eplb_map;
+    L.map_count = a->eplb_count;
+    L.map_R = has_eplb(a) ? a->eplb_max_replicas : 1;
+    L.E_log = a->num_experts;
+    L.width = a->width;
     L.sorted = a->sorted_token_ids;
     L.expert_ids = a->expert_ids;
     L.npp = a->num_tokens_post_padded;
@@ -238,6 +261,8 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
         L.bias = a->bias;
         L.M = a->M; L.H = a->H; L.E = a->E; L.S = S; L.k = a->topk;
         L.scale = a->shared_scale;
+        L.renorm = a->renormalize;
+        L.shared_bf16 = a->shared_logit_bf16;
         L.ids = a->topk_ids;
         L.wts = a->topk_weights;
         L.logits_out = a->logits_out;
@@ -267,6 +292,8 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
     L.bias = a->bias;
     L.M = a->M; L.H = a->H; L.E = a->E; L.S = S; L.k = a->topk;
     L.scale = a->shared_scale;
+    L.renorm = a->renormalize;
+    L.shared_bf16 = a->shared_logit_bf16;
     L.ids = a->topk_ids;
     L.wts = a->topk_weights;
     L.logits_out = a->logits_out;
@@ -318,7 +345,7 @@ SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const
     al.width = route->topk + (route->has_shared ? 1 : 0);
     al.num_experts = route->E + (route->has_shared ? 1 : 0);
     const int64_t numel = (int64_t)al.num_tokens * al.width;
-    if (align_counted_by_route(route, numel))  // tiles of 64 route rows
+    if (align_counted_by_route(route, &al, numel))  // tiles of 64 route rows
         return kHeaderBytes + route_scratch_bytes(route) +
                round_up((size_t)smr::align_scratch_words_tiles(route_tiles(route), al.num_experts) * 4,
                         kWsAlign);
@@ -390,12 +417,12 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
     if ((st = check_device()) != SMR_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
-    if (route->M >= 1 && route->M <= smr::kSmallMaxM) {
+    if (route->M >= 1 && route->M <= smr::kSmallMaxM && !has_eplb(&al)) {
         st = run_route(route, workspace, s, &al, &launches);
         if (st == SMR_OK) g_last_launches = launches;
         return st;
     }
-    const bool counted = align_counted_by_route(route, (int64_t)route->M * al.width);
+    const bool counted = align_counted_by_route(route, &al, (int64_t)route->M * al.width);
     smr::AlignLaunch L = make_align_launch(&al, route->topk_ids, workspace,
                                            kHeaderBytes + route_scratch_bytes(route),
                                            counted ? smr::kTcCountRows * al.width : 0);
@@ -409,6 +436,7 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
     g_last_launches = launches;
     return SMR_OK;
 }
+
 
 SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr_align_args *align,
                                           void *stream) {
@@ -431,6 +459,7 @@ SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr
     if (route->M < 1 || route->M > smr::kSmallMaxM)
         r.unsup("the fixed-scratch entry point covers 1 <= M <= 16 (got M=" +
                 std::to_string(route->M) + ")");
+    if (has_eplb(&al)) r.unsup("the fixed-scratch entry point takes no EPLB remap");
     if (!r.ok()) return r.finish("smr_route_align_static");
     const size_t need = smr_route_align_workspace_size(route, &al);
     if (need > smr::kStaticScratchBytes) {
@@ -520,7 +549,7 @@ SMR_API const char *smr_status_string(smr_status status) {
 
 SMR_API const char *smr_last_error(void) { return g_last_error.c_str(); }
 
-SMR_API int32_t smr_version(void) { return 0x000100; }
+SMR_API int32_t smr_version(void) { return 0x000200; }
 
 SMR_API int32_t smr_last_launch_count(void) { return g_last_launches; }
 

@@ -52,6 +52,8 @@ struct SmallRouteLaunch {
     const float *bias;
     int M, H, E, S, k;
     float scale;
+    int renorm;       // 1: weights renormalised over the top-k; 0: the E-expert softmax's
+    int shared_bf16;  // 1: the shared logit is rounded to bf16 before the sigmoid
     int32_t *ids;
     float *wts;
     uint16_t *logits_out;
@@ -88,6 +90,8 @@ struct TcRouteLaunch {
     const float *bias;
     int M, H, E, S, k;
     float scale;
+    int renorm;       // as in SmallRouteLaunch
+    int shared_bf16;
     int32_t *ids;
     float *wts;
     uint16_t *logits_out;
@@ -125,6 +129,12 @@ struct AlignLaunch {
     // > 0: the tile counts were written by the tcgen05 route (tiles of
     // counted_tile slots); the count launch is skipped
     int counted_tile;
+    // optional EPLB remap (map == nullptr: none): the id e of slot i (token
+    // i / width) becomes map[e * map_R + (i / width) % map_count[e]]; E_al
+    // is then the number of physical experts, E_log that of logical ones
+    const int32_t *map;
+    const int32_t *map_count;
+    int map_R, E_log, width;
 };
 constexpr int kAlignSingleMax = 8192;   // numel handled by one CTA
 constexpr int kAlignMinTile = 1024;     // slots per CTA in the multi-CTA path, at least

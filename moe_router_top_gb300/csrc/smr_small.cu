@@ -108,7 +108,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 template <int NK>
 __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, uint32_t want,
                                               long long poll_limit, int E, int S,
-                                              int k, int32_t *ids, float *wts, uint32_t *keys_s, int flat0,
+                                              int k, int renorm, int32_t *ids, float *wts, uint32_t *keys_s,
+                                              int flat0,
                                               uint32_t *cand_s, uint32_t *tmask, uint32_t *tbits, int m,
                                               uint32_t *err) {
     const int lane = threadIdx.x & 31;
@@ -146,6 +147,23 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
 #pragma unroll
         for (int i = 0; i < h; ++i) lm[i] = max(lm[i], lm[i + h]);
     const uint32_t lmax = lm[0];
+    // without renormalisation the weights divide by the softmax denominator
+    // over all E experts: every key's exponential relative to the row's
+    // largest logit, summed as a tree (per lane, then across the warp)
+    float den_all = 0.0f;
+    if (!renorm) {
+        const float vtop = key_value(__reduce_max_sync(0xffffffffu, lmax));
+        float ex[NK];
+#pragma unroll
+        for (int i = 0; i < NK; ++i) ex[i] = key[i] ? expf(key_value(key[i]) - vtop) : 0.0f;
+#pragma unroll
+        for (int h = NK / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) ex[i] += ex[i + h];
+        den_all = ex[0];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den_all += __shfl_xor_sync(0xffffffffu, den_all, o);
+    }
     // T: the lane maximum with exactly k - 1 larger ones. Valid keys are
     // unique and nonzero; a lane without a valid key holds 0 and ranks at or
     // past min(E, 32) >= k, so exactly one lane matches.
@@ -202,17 +220,18 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
             for (int i = 0; i < NK; ++i) key[i] = (key[i] == gmax) ? 0u : key[i];
         }
     }
-    // softmax over the selected logits (renormalised top-k); every lane
-    // evaluates the exponential, lanes past k drop it. The weight is the
-    // exponential times the correctly rounded reciprocal of the sum (two
-    // roundings, within 1.5 ulp of the quotient).
+    // softmax over the selected logits (renormalised top-k), or the E-expert
+    // softmax at the selected ids; every lane evaluates the exponential, lanes
+    // past k drop it. The weight is the exponential times the correctly
+    // rounded reciprocal of the denominator (two roundings, within 1.5 ulp of
+    // the quotient).
     const float vmax = key_value(first);
     const float ex = expf(key_value(mine) - vmax);
     const float ev = (lane < k) ? ex : 0.0f;
     float sum = ev;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float inv = __frcp_rn(sum);
+    const float inv = __frcp_rn(renorm ? sum : den_all);
     if (lane < k) {
         const int id = key_id(mine);
         ids[lane] = id;
@@ -675,7 +694,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
                     p.logits_out[(int64_t)m16 * p.E + row] = (uint16_t)(__float_as_uint(zr) >> 16);
             } else {
                 p.ids[(int64_t)m16 * (p.k + 1) + p.k] = p.E;
-                p.wts[(int64_t)m16 * (p.k + 1) + p.k] = p.scale * sigmoid_stable(v);
+                p.wts[(int64_t)m16 * (p.k + 1) + p.k] = p.scale * sigmoid_stable(p.shared_bf16 ? round_bf16(v) : v);
             }
         }
     }
@@ -710,7 +729,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     const uint32_t want = p.stall ? (tag + 1u) | 0x80000000u : tag;
     const long long poll_limit = p.stall ? p.stall_limit : kSmallPollLimit;
     for (int m = warp; m < p.M; m += kSmallWarps)
-        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, want, poll_limit, p.E, p.S, p.k,
+        warp_topk_row<NK>(p.scratch + (int64_t)m * p.E, want, poll_limit, p.E, p.S, p.k, p.renorm,
                           p.ids + (int64_t)m * width,
                           p.wts + (int64_t)m * width, keys_s + m * width, m * width, cand_s + warp * 32,
                           P.mask_align ? tmask : nullptr, tbits, m, &hdr->error);

@@ -65,6 +65,8 @@ constexpr int kTcSmemLimit = 232448;  // 227 KiB opt-in per CTA
 struct TcParams {
     int M, H, E, S, k, width;
     float scale;
+    int renorm;       // 1: weights renormalised over the top-k; 0: the E-expert softmax's
+    int shared_bf16;  // 1: the shared logit is rounded to bf16 before the sigmoid
     const float *bias;
     const uint16_t *ws;
     const uint16_t *x;  // hidden states (row stride ld), read directly by the shared-logit warps
@@ -77,7 +79,7 @@ struct TcParams {
     int stall;             // failure-injection hook: the half merge waits on a barrier
     long long stall_limit; // nothing arrives on, for at most stall_limit SM cycles
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
-    uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off;
+    uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off, misc_den_off;
 };
 
 // Compensated (two-sum) accumulation of k-block partial sums.
@@ -301,6 +303,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
     int *hist = reinterpret_cast<int *>(misc + p.misc_hist_off);  // [2][E + S] counts of the CTA's two 64-row tiles
     uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
+    float2 *den_s = reinterpret_cast<float2 *>(misc + p.misc_den_off);  // [128] half 0's (sum, max)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * kTcBM;
@@ -484,6 +487,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     float *numer = reinterpret_cast<float *>(smem) + 2 * kCandCap * kTcBM;  // [32][128]
     const uint32_t rs = dump_row_bytes(ecols);
     const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
+    float den_half = 0.0f, v_half = 0.0f;  // without renormalisation: this half's denominator
     if (ok) {
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
         // 1. one sweep over this half's TMEM columns: add the bias, round to
@@ -598,8 +602,32 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             topk_from_list<kCandCap>(list + row, n, p.k);
         }
         __syncwarp();
+        // 4. without renormalisation: this half's share of the E-expert
+        //    softmax denominator, every rounded logit's exponential relative
+        //    to the half's largest (eight per group as a tree, the groups by a
+        //    compensated sum); half 1 rescales both to the row's largest
+        if (!p.renorm) {
+            v_half = key_value(list[row]);
+            float hi = 0.0f, lo = 0.0f;
+#pragma unroll 1
+            for (int g = 0; g < ng; ++g) {
+                const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                float e[kGroup];
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u)
+                    e[u] = expf(__uint_as_float((u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16)) - v_half);
+#pragma unroll
+                for (int h = kGroup / 2; h >= 1; h >>= 1)
+#pragma unroll
+                    for (int u = 0; u < h; ++u) e[u] += e[u + h];
+                two_sum_acc(hi, lo, e[0]);
+            }
+            den_half = hi + lo;
+        }
     }
     if (hf == 0) {
+        if (!p.renorm) den_s[row] = make_float2(den_half, v_half);  // posted with the top-k
         __syncwarp();
         // (under the failure-injection hook half 0 does not post: the merge's
         // wait then runs out, which sets the error bit and skips the outputs)
@@ -633,7 +661,12 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 numer[r * kTcBM + row] = ev;
                 orow[r] = key_id(m);
             }
-            const float inv = 1.0f / sum;  // one division; each weight within 1.5 ulp of ev / sum
+            float den = sum;
+            if (!p.renorm) {  // both halves' denominators at the row's largest logit
+                const float2 d0 = den_s[row];
+                den = den_half * expf(v_half - vmax) + d0.x * expf(d0.y - vmax);
+            }
+            const float inv = 1.0f / den;  // one division; each weight within 1.5 ulp of ev / den
 #pragma unroll 4
             for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] * inv;
             if (count) {
@@ -652,7 +685,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (p.S) {  // (its count is the tile's number of rows, set below)
                 const float sh = s_hi + s_lo;
                 orow[p.k] = p.E;
-                wrow[p.k] = p.scale * sigmoid_stable(sh);
+                wrow[p.k] = p.scale * sigmoid_stable(p.shared_bf16 ? round_bf16(sh) : sh);
             }
         }
         __syncwarp();
@@ -743,11 +776,12 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.stage_bytes = (uint32_t)(kTcBM * kTcSW + (E / 2) * kTcSW);
     // misc: barriers and flags (256 B: 3*stages+2 mbarriers, TMEM slot, abort
     // flag), bias [E] fp32, expert counts [2][E+S] int32, shared gate [H, padded
-    // to whole k-blocks] bf16
+    // to whole k-blocks] bf16, half 0's softmax denominators [128] (sum, max)
     p.misc_bias_off = 256;
     p.misc_hist_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
     p.misc_ws_off = p.misc_hist_off + (uint32_t)((2 * (E + S) * 4 + 15) & ~15);
-    const size_t misc = p.misc_ws_off + (S ? (size_t)p.num_kb * kTcBK * 2 : 0);
+    p.misc_den_off = p.misc_ws_off + (uint32_t)(S ? (size_t)p.num_kb * kTcBK * 2 : 0);
+    const size_t misc = p.misc_den_off + (size_t)kTcBM * sizeof(float2);
     const size_t budget = (size_t)kTcSmemLimit - 1024 - misc;
     int st = (int)(budget / p.stage_bytes);
     if (st > 6) st = 6;
@@ -812,6 +846,8 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     if (!plan_tc(a.M, a.H, a.E, a.k, a.S, &plan)) return cudaErrorNotSupported;
     TcParams &p = plan.p;
     p.scale = a.scale;
+    p.renorm = a.renorm;
+    p.shared_bf16 = a.shared_bf16;
     p.bias = a.bias;
     p.x = a.x;
     p.ld = a.ld;

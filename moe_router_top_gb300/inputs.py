@@ -60,6 +60,8 @@ class RouteInputs:
     bias: Optional[np.ndarray]       # float32 [E], or None
     block_size: int = 0              # 0 = M-aware tier
     name: str = ""
+    renormalize: bool = True         # routing variant flags (passed through, no arithmetic here)
+    shared_bf16: bool = False
 
     @property
     def width(self) -> int:
@@ -92,7 +94,8 @@ def make_route_inputs(M: int, H: int, E: int, topk: int, has_shared: int, *,
                       seed: int, dist: str = "normal", x_std: float = 1.0,
                       w_std: float = 0.02, zipf_s: Optional[float] = None,
                       shared_scale: float = 1.0, block_size: int = 0,
-                      name: str = "") -> RouteInputs:
+                      name: str = "", renormalize: bool = True,
+                      shared_bf16: bool = False) -> RouteInputs:
     rng = np.random.default_rng(seed)
     if dist == "normal":
         x = _normal_bf16(rng, (M, H), x_std)
@@ -107,7 +110,8 @@ def make_route_inputs(M: int, H: int, E: int, topk: int, has_shared: int, *,
     bias = zipf_log_prior(E, zipf_s, rng) if zipf_s is not None else None
     return RouteInputs(M=M, H=H, E=E, topk=topk, has_shared=has_shared,
                        shared_scale=float(shared_scale), x=x, w=w, ws=ws,
-                       bias=bias, block_size=block_size, name=name)
+                       bias=bias, block_size=block_size, name=name,
+                       renormalize=renormalize, shared_bf16=shared_bf16)
 
 
 # --- the five workloads -----------------------------------------------------
@@ -160,3 +164,22 @@ def random_ids(num_tokens: int, width: int, num_experts: int, *, seed: int,
         else:
             out[t] = rng.choice(num_experts, size=width, replace=True, p=p)
     return out
+
+
+def random_eplb_map(num_experts: int, max_replicas: int, num_physical: int, *,
+                    seed: int):
+    """A random expert-parallel load-balancing table: each logical expert
+    gets 1..max_replicas replicas (int32 count [num_experts]), each replica a
+    distinct physical expert (int32 map [num_experts, max_replicas], unused
+    entries -1); needs num_physical >= the replicas drawn (checked)."""
+    rng = np.random.default_rng(seed)
+    count = rng.integers(1, max_replicas + 1, size=num_experts).astype(np.int32)
+    while int(count.sum()) > num_physical:
+        count[int(np.argmax(count))] -= 1
+    phys = rng.permutation(num_physical)[: int(count.sum())].astype(np.int32)
+    emap = np.full((num_experts, max_replicas), -1, np.int32)
+    pos = 0
+    for e in range(num_experts):
+        emap[e, : count[e]] = phys[pos: pos + count[e]]
+        pos += int(count[e])
+    return emap, count

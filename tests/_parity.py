@@ -23,6 +23,11 @@ output. Acceptance rules, per token row:
    with logits_out, the GPU's logits themselves (each must be admissible);
    without, a search over the admissible values of the logits that can reach
    the top-k. The count is reported and bounded by MAX_ROUNDING_FRACTION.
+   Without renormalisation (weights = the E-expert softmax at the top-k) a
+   flip of ANY logit moves the denominator, so without logits_out such rows
+   are held to a weight bound derived from the bands instead (the oracle's
+   softmax shares times each band's exponential width); with logits_out the
+   check stays exact.
  * boundary row (the benchmark spec): the oracle's k-th and (k+1)-th rounded logits
    tie or lie within 1 bf16 ulp. The expert SET chosen may differ from the
    oracle's only on boundary rows (counted and reported).
@@ -121,7 +126,7 @@ class RouteReport:
         return dataclasses.asdict(self)
 
 
-def _explained(zhat_row, lo_row, hi_row, k, ids_row, w_row, oracle_ids) -> bool:
+def _explained(zhat_row, lo_row, hi_row, k, ids_row, w_row, oracle_ids, renorm=True) -> bool:
     """Does the oracle's selection on some admissible choice of this row's
     logits reproduce (ids_row, w_row)? Only the logits of experts that either
     selection holds can make a difference (any other expert stays out of the
@@ -139,7 +144,7 @@ def _explained(zhat_row, lo_row, hi_row, k, ids_row, w_row, oracle_ids) -> bool:
         # spans many bf16 steps; the GPU's weights then imply its value: for
         # e in slot j and another expert r in slot i, w_j / w_i =
         # exp(z_e - z_r), with z_r taken at the oracle's rounding
-        if e in ids_row.tolist() and len(ids_row) > 1:
+        if renorm and e in ids_row.tolist() and len(ids_row) > 1:
             j = ids_row.tolist().index(e)
             i = 1 if j == 0 else 0
             if w_row[j] > 0 and w_row[i] > 0:
@@ -160,7 +165,7 @@ def _explained(zhat_row, lo_row, hi_row, k, ids_row, w_row, oracle_ids) -> bool:
                 if tried > MAX_COMBOS:
                     return False
                 z[list(subset)] = combo
-                sid, sw = oracle.select(z, k)
+                sid, sw = oracle.select(z, k, renorm)
                 z[list(subset)] = zhat_row[list(subset)]
                 if np.array_equal(sid, ids_row) and weights_close(w_row, sw).all():
                     return True
@@ -178,7 +183,9 @@ def check_route(ri: inputs.RouteInputs, ids_g: np.ndarray, w_g: np.ndarray,
     k, S, E = ri.topk, ri.has_shared, ri.E
     if threads is None:
         threads = min(os.cpu_count() or 1, 32) if len(rows) >= 256 else 1
-    ref = oracle.route(ri.x, ri.w, ri.ws, ri.bias, k, ri.shared_scale, rows=rows, threads=threads)
+    renorm = ri.renormalize
+    ref = oracle.route(ri.x, ri.w, ri.ws, ri.bias, k, ri.shared_scale, rows=rows, threads=threads,
+                       renormalize=renorm, shared_bf16=ri.shared_bf16)
     n = len(rows)
     rep = RouteReport(rows=n)
 
@@ -214,7 +221,7 @@ def check_route(ri: inputs.RouteInputs, ids_g: np.ndarray, w_g: np.ndarray,
             assert rep.logit_mismatch == 0, f"{rep.logit_mismatch} logits differ on exact-arithmetic inputs"
         # the GPU's selection on its own (admissible) logits must be the
         # oracle's selection on them
-        sel_ids, sel_w = oracle.select_rows(zg, k)
+        sel_ids, sel_w = oracle.select_rows(zg, k, renorm)
         assert np.array_equal(ids_g[:, :k], sel_ids), "top-k differs from oracle selection on the GPU's logits"
         ok = weights_close(w_g[:, :k], sel_w)
         assert ok.all(), f"weights off on GPU logits: max rel {np.max(np.abs(w_g[:, :k] - sel_w) / np.maximum(np.abs(sel_w), 1e-30)):.3g}"
@@ -230,13 +237,32 @@ def check_route(ri: inputs.RouteInputs, ids_g: np.ndarray, w_g: np.ndarray,
     assert not (set_differs & ~boundary).any(), (
         f"rows {rows[set_differs & ~boundary][:8]} choose other experts than the oracle off the "
         f"k-th boundary")
+    if logits_g is None and not renorm and (~exact).any():
+        # without renormalisation every logit enters the denominator, so a
+        # legitimate rounding flip anywhere in the row moves the weights: each
+        # weight may differ relatively by its own logit's band plus the
+        # denominator's, sum over e of p_e * (exp(hi_e - lo_e) - 1), p the
+        # oracle's softmax (plus the 2e-6 of the arithmetic, and 10%)
+        zmax = ref.zhat.max(axis=1, keepdims=True)
+        pe = np.exp(ref.zhat - zmax)
+        pe /= pe.sum(axis=1, keepdims=True)
+        band = np.expm1(hi - lo)
+        den_var = (pe * band).sum(axis=1)
+        num_var = np.take_along_axis(band, ids_g[:, :k].astype(np.int64), axis=1)
+        allowed = 1.1 * (W_RTOL + num_var + den_var[:, None]) * np.abs(ref.w[:, :k]) + W_ATOL
+        same_set_rows = ~exact & same_ids
+        off = np.abs(w_g[:, :k].astype(np.float64) - ref.w[:, :k]) > allowed
+        assert not (off & same_set_rows[:, None]).any(), (
+            f"rows {rows[(off & same_set_rows[:, None]).any(axis=1)][:8]}: weights beyond the "
+            f"rounding bound of the unrenormalised softmax")
     for i in np.nonzero(~exact)[0]:
-        if logits_g is None:  # with logits_out the GPU's own logits explained it above
-            assert _explained(ref.zhat[i], lo[i], hi[i], k, ids_g[i, :k], w_g[i, :k], ref.ids[i, :k]), (
+        if logits_g is None and renorm:  # with logits_out the GPU's own logits explained it above
+            assert _explained(ref.zhat[i], lo[i], hi[i], k, ids_g[i, :k], w_g[i, :k], ref.ids[i, :k],
+                              renorm), (
                 f"row {rows[i]}: ids {ids_g[i, :k]} / weights differ from the oracle's "
                 f"{ref.ids[i, :k]} and no admissible rounding of its logits explains them")
     rep.rounding_rows = int((~exact).sum())
-    assert rep.rounding_rows <= max(MIN_ROUNDING_ROWS, int(np.ceil(MAX_ROUNDING_FRACTION * n))), (
+    assert not renorm or rep.rounding_rows <= max(MIN_ROUNDING_ROWS, int(np.ceil(MAX_ROUNDING_FRACTION * n))), (
         f"{rep.rounding_rows} of {n} rows differ by a rounding flip, above the "
         f"{MAX_ROUNDING_FRACTION:.0%} ceiling")
     if exact.any():
@@ -260,7 +286,10 @@ def check_route_properties(ri: inputs.RouteInputs, ids_g: np.ndarray, w_g: np.nd
     srt = np.sort(routed, axis=1)
     assert np.all(srt[:, 1:] != srt[:, :-1]), "duplicate expert in a row"
     w = np.asarray(w_g, np.float64)
-    assert np.all(np.abs(w[:, :k].sum(axis=1) - 1.0) <= 1e-5), "routed weights do not sum to 1"
+    if ri.renormalize:
+        assert np.all(np.abs(w[:, :k].sum(axis=1) - 1.0) <= 1e-5), "routed weights do not sum to 1"
+    else:
+        assert np.all(w[:, :k].sum(axis=1) <= 1.0 + 1e-5), "routed weights sum above 1"
     assert np.all(np.diff(w[:, :k], axis=1) <= 0), "routed weights must be non-increasing by slot"
     if S:
         assert np.all(np.asarray(ids_g)[:, k] == E)

@@ -39,14 +39,16 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_struct_layouts_match_header(lib):
     # field order and sizes as declared in include/smr.h (LP64)
-    assert ctypes.sizeof(RouteArgs) == 7 * 4 + 4 + 8 * 8
+    assert ctypes.sizeof(RouteArgs) == 7 * 4 + 4 + 8 * 8 + 8  # + shared_logit_bf16 (padded)
     assert RouteArgs.hidden.offset == 32
-    assert ctypes.sizeof(AlignArgs) == 8 + 6 * 4 + 5 * 8
+    assert RouteArgs.shared_logit_bf16.offset == 96
+    assert ctypes.sizeof(AlignArgs) == 8 + 6 * 4 + 5 * 8 + 2 * 8 + 2 * 4
     assert AlignArgs.sorted_token_ids.offset == 32
+    assert AlignArgs.eplb_map.offset == 72 and AlignArgs.num_physical.offset == 92
 
 
 def test_version_and_status_strings(lib):
-    assert lib.smr_version() == 0x000100
+    assert lib.smr_version() == 0x000200
     assert lib.smr_status_string(0) == b"SMR_OK"
     assert lib.smr_status_string(2) == b"SMR_ERR_UNSUPPORTED"
 
@@ -81,11 +83,18 @@ def test_route_refusal_lists_every_reason(lib):
     assert lib.smr_last_launch_count() == 0
 
 
-def test_route_unsupported_contract(lib):
+def test_route_variant_flags_checked(lib):
     a = _good_route()
-    a.renormalize = 0
-    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
-    assert "renormalize" in lib.smr_last_error().decode()
+    a.renormalize = 2
+    a.shared_logit_bf16 = 3
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_INVALID_ARG
+    msg = lib.smr_last_error().decode()
+    assert "renormalize must be 0 or 1" in msg and "shared_logit_bf16 must be 0 or 1" in msg
+    a.renormalize, a.shared_logit_bf16 = 0, 1  # both variants are implemented
+    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_WORKSPACE
+
+
+def test_route_unsupported_contract(lib):
     a = _good_route(M=64, E=500)      # tcgen05 path needs E % 32 == 0
     assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
     assert "E % 32 == 0" in lib.smr_last_error().decode()
@@ -272,3 +281,25 @@ def test_failure_hook_and_static_error_refusals(lib):
     assert lib.smr_test_force_wait_timeout(_lib.SMR_STALL_TC_MERGE, 0) == _lib.SMR_ERR_INVALID_ARG
     assert lib.smr_test_force_wait_timeout(_lib.SMR_STALL_NONE, 0) == _lib.SMR_OK
     assert lib.smr_get_static_device_error(None, None) == _lib.SMR_ERR_INVALID_ARG
+
+
+def test_align_eplb_arguments_checked(lib):
+    """The EPLB remap's table pointers and sizes are checked before any
+    launch, and the capacity is taken over the physical experts."""
+    a = AlignArgs()
+    a.topk_ids = 0x1000
+    a.num_tokens, a.width, a.num_experts, a.block_size = 8, 4, 17, 16
+    a.sorted_token_ids, a.expert_ids, a.num_tokens_post_padded = 0x2000, 0x3000, 0x4000
+    a.eplb_map = 0x5002            # misaligned
+    a.eplb_count = None
+    a.eplb_max_replicas = 65       # above 64
+    a.num_physical = 2000          # above 1025
+    a.sorted_cap = a.expert_cap = 1 << 20
+    assert lib.smr_align(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_INVALID_ARG
+    msg = lib.smr_last_error().decode()
+    for frag in ("eplb_count is NULL", "4-byte aligned", "eplb_max_replicas", "num_physical"):
+        assert frag in msg, msg
+    a.eplb_map, a.eplb_count, a.eplb_max_replicas, a.num_physical = 0x5000, 0x6000, 2, 40
+    a.sorted_cap = 32 + 40 * 15 - 1  # one short of numel + num_physical * (A - 1)
+    assert lib.smr_align(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_INVALID_ARG
+    assert "required 632" in lib.smr_last_error().decode()

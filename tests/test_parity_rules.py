@@ -158,7 +158,7 @@ def test_align_rules_reject(align_case, mistake):
         check_align(ids, 17, 4, srt, eids, np.array([npp], np.int32))
 
 
-def _fp32_chain_route(ri):
+def _fp32_chain_route(ri, renormalize=True):
     """A stand-in for an fp32-accumulating kernel: the dot of every 16-wide
     K block exactly, the blocks added one by one in fp32 (H/16 additions, the
     tcgen05 path's chain), the bias added in fp32, then the oracle's bf16
@@ -170,15 +170,17 @@ def _fp32_chain_route(ri):
         acc = (acc + (x[:, c:c + 16] @ w[:, c:c + 16].T).astype(np.float32)).astype(np.float32)
     if ri.bias is not None:
         acc = (acc + ri.bias).astype(np.float32)
-    return oracle.select_rows(oracle.bf16_round(acc.astype(np.float64)), ri.topk)
+    return oracle.select_rows(oracle.bf16_round(acc.astype(np.float64)), ri.topk, renormalize)
 
 
+@pytest.mark.parametrize("renormalize", [True, False])
 @pytest.mark.parametrize("M", [1024, 2048])
-def test_fp32_accumulation_stand_in_passes(M):
+def test_fp32_accumulation_stand_in_passes(M, renormalize):
     """Results of a real fp32 accumulation order differ from the fp64
-    oracle's on a few rows (a selected logit rounds the other way); the rule
-    must accept and count them, and reject none."""
+    oracle's on a few rows (a logit rounds the other way); the rule must
+    accept and count them, and reject none."""
     ri = inputs.zipf_sweep(M)
-    ids, w = _fp32_chain_route(ri)
+    ri.renormalize = renormalize
+    ids, w = _fp32_chain_route(ri, renormalize)
     rep = check_route(ri, ids, w, None)
     assert rep.rounding_rows >= 1 and rep.set_differs_rows == 0
