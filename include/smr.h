@@ -160,10 +160,11 @@ SMR_API size_t smr_route_align_workspace_size(const smr_route_args *route, const
  * ("[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950",
  * Modifications). One kernel launch for M <= 16: the gate rows are split
  * across CTAs, and one CTA selects after collecting the row groups'
- * tagged selection keys from the workspace. For M > 16, one tcgen05 GEMM
- * launch with the top-k fused into its epilogue, which requires
- * E % 32 == 0 and 32 <= E <= 512 (other E with M > 16 are refused with
- * SMR_ERR_UNSUPPORTED). M == 0 launches nothing. Refusals (SMR_ERR_*) are
+ * tagged selection keys from the workspace. For M > 16 with E % 32 == 0 and
+ * 32 <= E <= 512, one tcgen05 GEMM launch with the top-k fused into its
+ * epilogue; any other E (up to 1024) takes ceil(E / 512) tcgen05 launches
+ * that write the rounded logits into the workspace, then one select launch
+ * (one warp per row). M == 0 launches nothing. Refusals (SMR_ERR_*) are
  * returned before any launch; a failed launch returns SMR_ERR_CUDA. */
 SMR_API smr_status smr_route(const smr_route_args *args, void *workspace, size_t workspace_bytes,
                      void *stream);

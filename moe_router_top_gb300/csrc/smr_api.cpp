@@ -6,10 +6,13 @@
 // prefill: M-aware moe_align block size", Purpose, for the alignment tier):
 //   route_align, M <= 16 : 1 launch  (small route + fused align)
 //   route_align, M > 16  : 1 tcgen05 route launch (which also counts the experts of
-//                          its rows when the align is multi-CTA) + 1 or 2 align launches
+//                          its rows when the align is multi-CTA) + 1 or 2 align launches;
+//                          with E > 512 or E % 32 != 0: ceil(E / 512) logits-only
+//                          tcgen05 launches + 1 select launch + 1 or 3 align launches
 //   route        : 1 launch;  align : 1 launch (numel <= 8192) or 3.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -119,15 +122,24 @@ void check_route(const smr_route_args *a, Reasons &r) {
         else if (!aligned(a->topk_weights, 4)) r.bad("topk_weights must be 4-byte aligned");
         if (a->logits_out && !aligned(a->logits_out, 16)) r.bad("logits_out must be 16-byte aligned");
     }
-    if (a->M > smr::kSmallMaxM && r.invalid.empty() &&
-        !smr::tc_route_supported(a->H, a->E, a->topk, S))
-        r.unsup("M > 16 uses the tcgen05 path, which needs E % 32 == 0 and 32 <= E <= 512 (got E=" +
-                std::to_string(a->E) + ")");
+}
+
+// M > 16 with a gate outside the fused tcgen05 epilogue (E > 512 or E not a
+// multiple of 32): logits-only tcgen05 launches, then the select kernel.
+bool generic_route(const smr_route_args *a) {
+    return a->M > smr::kSmallMaxM && !smr::tc_route_supported(a->H, a->E, a->topk, a->has_shared ? 1 : 0);
+}
+
+size_t generic_logits_bytes(const smr_route_args *a) {
+    return round_up((size_t)a->M * (size_t)smr::generic_logits_ld(a->E) * 2, kWsAlign);
 }
 
 size_t route_scratch_bytes(const smr_route_args *a) {
-    if (a->M <= 0 || a->M > smr::kSmallMaxM) return 0;
-    return round_up((size_t)a->M * (size_t)a->E * 8, kWsAlign);  // tagged selection keys
+    if (a->M <= 0) return 0;
+    if (a->M <= smr::kSmallMaxM) return round_up((size_t)a->M * (size_t)a->E * 8, kWsAlign);  // tagged keys
+    if (generic_route(a))  // bf16 logit rows + shared logits
+        return generic_logits_bytes(a) + round_up((size_t)a->M * 4, kWsAlign);
+    return 0;
 }
 
 // --- align ------------------------------------------------------------------
@@ -213,7 +225,7 @@ smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
 // its per-tile expert counts from the route (tiles of 64 token rows), unless
 // an EPLB remap changes what is counted.
 bool align_counted_by_route(const smr_route_args *r, const smr_align_args *a, int64_t numel) {
-    return r->M > smr::kSmallMaxM && numel > smr::kAlignSingleMax && !has_eplb(a);
+    return r->M > smr::kSmallMaxM && numel > smr::kAlignSingleMax && !has_eplb(a) && !generic_route(r);
 }
 int64_t route_tiles(const smr_route_args *r) {
     return (r->M + smr::kTcCountRows - 1) / smr::kTcCountRows;
@@ -281,6 +293,47 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
         L.stall_limit = L.stall ? hook.limit : 0;
         cudaError_t e = smr::launch_small_route(L, stream);
         if (e != cudaSuccess) return cuda_fail("small-M route launch", e);
+        *launches += 1;
+        return SMR_OK;
+    }
+    if (generic_route(a)) {
+        // the logits of every 512-column range of the gate, then the top-k
+        // over whole rows
+        const int64_t ld = smr::generic_logits_ld(a->E);
+        uint16_t *lg = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + kHeaderBytes);
+        float *sv = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kHeaderBytes + generic_logits_bytes(a));
+        for (int c0 = 0; c0 < a->E; c0 += smr::kTcRangeCols) {
+            smr::TcRouteLaunch L{};
+            L.x = static_cast<const uint16_t *>(a->hidden);
+            L.ld = a->ld_hidden;
+            L.w = static_cast<const uint16_t *>(a->gate_w) + (int64_t)c0 * a->H;
+            L.ws = (c0 == 0 && S) ? static_cast<const uint16_t *>(a->shared_w) : nullptr;
+            L.bias = a->bias ? a->bias + c0 : nullptr;
+            L.M = a->M; L.H = a->H; L.E = std::min(smr::kTcRangeCols, a->E - c0);
+            L.S = (c0 == 0) ? S : 0; L.k = 1;
+            L.hdr = ws;
+            L.logits_only = true;
+            L.col0 = c0;
+            L.logits_ws = lg;
+            L.ld_logits = ld;
+            L.s_out = sv;
+            cudaError_t e = smr::launch_tc_route(L, stream);
+            if (e != cudaSuccess) return cuda_fail("tcgen05 logits launch", e);
+            *launches += 1;
+        }
+        smr::SelectLaunch L{};
+        L.logits = lg;
+        L.ld = ld;
+        L.s = sv;
+        L.M = a->M; L.E = a->E; L.S = S; L.k = a->topk;
+        L.renorm = a->renormalize;
+        L.shared_bf16 = a->shared_logit_bf16;
+        L.scale = a->shared_scale;
+        L.ids = a->topk_ids;
+        L.wts = a->topk_weights;
+        L.logits_out = a->logits_out;
+        cudaError_t e = smr::launch_select(L, stream);
+        if (e != cudaSuccess) return cuda_fail("select launch", e);
         *launches += 1;
         return SMR_OK;
     }

@@ -316,6 +316,135 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
            ((uint32_t)(m >> 4) << 24);
 }
 
+// ------------------------------------------------ warp top-k + softmax --
+
+// Lanes below this one in the warp.
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+
+// Top-k and softmax of one token row held by one warp as NK keys per lane
+// (make_key of the bf16-rounded logit and the expert id; 0 = no key), as
+// "[AMD] One-launch small-M MoE router for Qwen3.5 on gfx950", Modifications,
+// defines them: the k largest rounded logits, the lowest id first among equal
+// ones, slots ordered by (value desc, id asc); weights = softmax over the
+// selected (renorm = 1) or the softmax over every key read at the selected
+// (renorm = 0). Returns the key of slot `lane` (lanes < k) and sets its
+// weight. cand_s: 32 words of shared memory owned by the warp. key[] is
+// consumed.
+//
+// Selection by threshold instead of k serial maxima: T = the k-th largest of
+// the 32 lane maxima is a lower bound of the k-th largest key (the k lanes
+// whose maxima reach T hold k distinct keys >= T), so the top-k are among
+// the keys >= T. Those (usually k + a few) are compacted into cand_s by
+// ballots, each one ranked against the others in one shuffle pass, and
+// stored at its rank. When more than 32 keys reach T (the largest logits
+// concentrated in a few lanes), k exact rounds of a warp maximum take over.
+template <int NK>
+__device__ __forceinline__ uint32_t warp_topk_keys(uint32_t (&key)[NK], int k, int renorm, uint32_t *cand_s,
+                                                   float &weight) {
+    const int lane = threadIdx.x & 31;
+    // this lane's largest key (a tree: depth log2(NK))
+    uint32_t lm[NK / 2];
+#pragma unroll
+    for (int i = 0; i < NK / 2; ++i) lm[i] = max(key[i], key[i + NK / 2]);
+#pragma unroll
+    for (int h = NK / 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) lm[i] = max(lm[i], lm[i + h]);
+    const uint32_t lmax = lm[0];
+    // without renormalisation the weights divide by the softmax denominator
+    // over all E experts: every key's exponential relative to the row's
+    // largest logit, summed as a tree (per lane, then across the warp)
+    float den_all = 0.0f;
+    if (!renorm) {
+        const float vtop = key_value(__reduce_max_sync(0xffffffffu, lmax));
+        float ex[NK];
+#pragma unroll
+        for (int i = 0; i < NK; ++i) ex[i] = key[i] ? expf(key_value(key[i]) - vtop) : 0.0f;
+#pragma unroll
+        for (int h = NK / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) ex[i] += ex[i + h];
+        den_all = ex[0];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den_all += __shfl_xor_sync(0xffffffffu, den_all, o);
+    }
+    // T: the lane maximum with exactly k - 1 larger ones. Valid keys are
+    // unique and nonzero; a lane without a valid key holds 0 and ranks at or
+    // past min(E, 32) >= k, so exactly one lane matches.
+    int rl = 0;
+#pragma unroll
+    for (int d = 1; d < 32; ++d) rl += __shfl_xor_sync(0xffffffffu, lmax, d) > lmax;
+    const uint32_t T = __shfl_sync(0xffffffffu, lmax, __ffs(__ballot_sync(0xffffffffu, rl == k - 1)) - 1);
+    uint32_t bal[NK];
+    int tot = 0;
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+        bal[i] = __ballot_sync(0xffffffffu, key[i] >= T);
+        tot += __popc(bal[i]);
+    }
+    uint32_t mine, first;
+    if (tot <= 32) {  // warp-uniform
+        // compact the candidates, in (i, lane) order, into cand_s[0, tot)
+        const uint32_t lt = lanemask_lt();
+        int base = 0;
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+            if (key[i] >= T) cand_s[base + __popc(bal[i] & lt)] = key[i];
+            base += __popc(bal[i]);
+        }
+        __syncwarp();
+        const uint32_t c = lane < tot ? cand_s[lane] : 0u;
+        int r = 0;  // candidates above this one (0 never counts: valid keys are nonzero)
+#pragma unroll
+        for (int d = 1; d < 32; ++d) r += __shfl_xor_sync(0xffffffffu, c, d) > c;
+        __syncwarp();
+        if (lane < tot && r < k) cand_s[r] = c;  // slot r of the row
+        __syncwarp();
+        mine = cand_s[lane];  // meaningful for lanes < k
+        first = cand_s[0];
+        __syncwarp();
+    } else {
+        // k rounds: each lane's largest key, the warp's largest (redux), and
+        // the lane holding it clears it (keys are unique)
+        mine = 0u;
+        first = 0u;
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            uint32_t m2[NK / 2];
+#pragma unroll
+            for (int i = 0; i < NK / 2; ++i) m2[i] = max(key[i], key[i + NK / 2]);
+#pragma unroll
+            for (int h = NK / 4; h >= 1; h >>= 1)
+#pragma unroll
+                for (int i = 0; i < h; ++i) m2[i] = max(m2[i], m2[i + h]);
+            const uint32_t gmax = __reduce_max_sync(0xffffffffu, m2[0]);
+            first = (r == 0) ? gmax : first;
+            mine = (lane == r) ? gmax : mine;
+#pragma unroll
+            for (int i = 0; i < NK; ++i) key[i] = (key[i] == gmax) ? 0u : key[i];
+        }
+    }
+    // softmax over the selected logits (renormalised top-k), or the E-expert
+    // softmax at the selected ids; every lane evaluates the exponential, lanes
+    // past k drop it. The weight is the exponential times the correctly
+    // rounded reciprocal of the denominator (two roundings, within 1.5 ulp of
+    // the quotient).
+    const float vmax = key_value(first);
+    const float ex = expf(key_value(mine) - vmax);
+    const float ev = (lane < k) ? ex : 0.0f;
+    float sum = ev;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv = __frcp_rn(renorm ? sum : den_all);
+    weight = ev * inv;
+    return mine;
+}
+
 // ------------------------------------------------------ align building blocks --
 //
 // moe_align_block_size over flat slot indices i = t*width + s ("[ROCm][Kernel]
@@ -358,11 +487,6 @@ __device__ __forceinline__ AlignSmem align_carve(int *smem, int num_experts) {
     return s;
 }
 
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 
 // Lanes of the warp holding the same value as this lane, for values in
 // [0, 2048): eleven ballots, one per bit (a fixed cost, unlike a

@@ -103,12 +103,42 @@ struct TcRouteLaunch {
     // on a barrier nothing arrives on, giving up after stall_limit SM cycles
     int stall;
     long long stall_limit;
+    // logits-only launch (the route for E > 512 or E % 32 != 0): the gate
+    // rows [col0, col0 + E) (w, bias already offset to row col0) are
+    // computed and written, rounded to bf16 with the bias, into
+    // logits_ws[M][ld_logits] at column col0 (columns past E up to the next
+    // multiple of 32: -inf); the shared logit (ws != nullptr) into s_out[M].
+    // k, ids, wts, logits_out and tile_counts are then unused.
+    bool logits_only;
+    int col0;
+    uint16_t *logits_ws;
+    int64_t ld_logits;
+    float *s_out;
 };
 constexpr int kTcTileRows = 128;   // token rows per CTA of the tcgen05 route
 constexpr int kTcCountRows = 64;   // token rows per align tile counted by the route
 // Returns cudaErrorNotSupported when the shape is outside the tcgen05 path.
 bool tc_route_supported(int H, int E, int k, int S);
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream);
+// Gate columns per logits-only launch, and the workspace row stride (elements)
+// of the logits of E experts.
+constexpr int kTcRangeCols = 512;
+inline int64_t generic_logits_ld(int E) { return (E + 31) / 32 * 32; }
+
+// Top-k + softmax + shared slot of every token row from the logits a
+// logits-only route wrote (one warp per row).
+struct SelectLaunch {
+    const uint16_t *logits;  // [M][ld] bf16 bits, -inf past E
+    int64_t ld;
+    const float *s;          // [M] shared logit (S == 1)
+    int M, E, S, k;
+    int renorm, shared_bf16;
+    float scale;
+    int32_t *ids;
+    float *wts;
+    uint16_t *logits_out;    // optional [M][E]
+};
+cudaError_t launch_select(const SelectLaunch &a, cudaStream_t stream);
 
 // moe_align_block_size.
 struct AlignLaunch {

@@ -96,15 +96,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // shared slot k was written by its row group) and the align's
 // (expert << 10 | flat slot) keys of all k + S slots to keys_s; with tmask,
 // also marks token m in the routed experts' token masks and the
-// touched-expert bitmap tbits.
-//
-// Selection by threshold instead of k serial maxima: T = the k-th largest of
-// the 32 lane maxima is a lower bound of the k-th largest key (the k lanes
-// whose maxima reach T hold k distinct keys >= T), so the top-k are among
-// the keys >= T. Those (usually k + a few) are compacted into cand_s by
-// ballots, each one ranked against the others in one shuffle pass, and
-// stored at its rank. When more than 32 keys reach T (the largest logits
-// concentrated in a few lanes), k exact rounds of a warp maximum take over.
+// touched-expert bitmap tbits. The selection itself is warp_topk_keys.
 template <int NK>
 __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, uint32_t want,
                                               long long poll_limit, int E, int S,
@@ -138,104 +130,12 @@ __device__ __forceinline__ void warp_topk_row(const unsigned long long *krow, ui
     uint32_t key[NK];
 #pragma unroll
     for (int i = 0; i < NK; ++i) key[i] = (lane + 32 * i < E) ? (uint32_t)v[i] : 0u;
-    // this lane's largest key (a tree: depth log2(NK))
-    uint32_t lm[NK / 2];
-#pragma unroll
-    for (int i = 0; i < NK / 2; ++i) lm[i] = max(key[i], key[i + NK / 2]);
-#pragma unroll
-    for (int h = NK / 4; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) lm[i] = max(lm[i], lm[i + h]);
-    const uint32_t lmax = lm[0];
-    // without renormalisation the weights divide by the softmax denominator
-    // over all E experts: every key's exponential relative to the row's
-    // largest logit, summed as a tree (per lane, then across the warp)
-    float den_all = 0.0f;
-    if (!renorm) {
-        const float vtop = key_value(__reduce_max_sync(0xffffffffu, lmax));
-        float ex[NK];
-#pragma unroll
-        for (int i = 0; i < NK; ++i) ex[i] = key[i] ? expf(key_value(key[i]) - vtop) : 0.0f;
-#pragma unroll
-        for (int h = NK / 2; h >= 1; h >>= 1)
-#pragma unroll
-            for (int i = 0; i < h; ++i) ex[i] += ex[i + h];
-        den_all = ex[0];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den_all += __shfl_xor_sync(0xffffffffu, den_all, o);
-    }
-    // T: the lane maximum with exactly k - 1 larger ones. Valid keys are
-    // unique and nonzero; a lane without a valid key holds 0 and ranks at or
-    // past min(E, 32) >= k, so exactly one lane matches.
-    int rl = 0;
-#pragma unroll
-    for (int d = 1; d < 32; ++d) rl += __shfl_xor_sync(0xffffffffu, lmax, d) > lmax;
-    const uint32_t T = __shfl_sync(0xffffffffu, lmax, __ffs(__ballot_sync(0xffffffffu, rl == k - 1)) - 1);
-    uint32_t bal[NK];
-    int tot = 0;
-#pragma unroll
-    for (int i = 0; i < NK; ++i) {
-        bal[i] = __ballot_sync(0xffffffffu, key[i] >= T);
-        tot += __popc(bal[i]);
-    }
-    uint32_t mine, first;
-    if (tot <= 32) {  // warp-uniform
-        // compact the candidates, in (i, lane) order, into cand_s[0, tot)
-        const uint32_t lt = lanemask_lt();
-        int base = 0;
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-            if (key[i] >= T) cand_s[base + __popc(bal[i] & lt)] = key[i];
-            base += __popc(bal[i]);
-        }
-        __syncwarp();
-        const uint32_t c = lane < tot ? cand_s[lane] : 0u;
-        int r = 0;  // candidates above this one (0 never counts: valid keys are nonzero)
-#pragma unroll
-        for (int d = 1; d < 32; ++d) r += __shfl_xor_sync(0xffffffffu, c, d) > c;
-        __syncwarp();
-        if (lane < tot && r < k) cand_s[r] = c;  // slot r of the row
-        __syncwarp();
-        mine = cand_s[lane];  // meaningful for lanes < k
-        first = cand_s[0];
-        __syncwarp();
-    } else {
-        // k rounds: each lane's largest key, the warp's largest (redux), and
-        // the lane holding it clears it (keys are unique)
-        mine = 0u;
-        first = 0u;
-#pragma unroll 1
-        for (int r = 0; r < k; ++r) {
-            uint32_t m2[NK / 2];
-#pragma unroll
-            for (int i = 0; i < NK / 2; ++i) m2[i] = max(key[i], key[i + NK / 2]);
-#pragma unroll
-            for (int h = NK / 4; h >= 1; h >>= 1)
-#pragma unroll
-                for (int i = 0; i < h; ++i) m2[i] = max(m2[i], m2[i + h]);
-            const uint32_t gmax = __reduce_max_sync(0xffffffffu, m2[0]);
-            first = (r == 0) ? gmax : first;
-            mine = (lane == r) ? gmax : mine;
-#pragma unroll
-            for (int i = 0; i < NK; ++i) key[i] = (key[i] == gmax) ? 0u : key[i];
-        }
-    }
-    // softmax over the selected logits (renormalised top-k), or the E-expert
-    // softmax at the selected ids; every lane evaluates the exponential, lanes
-    // past k drop it. The weight is the exponential times the correctly
-    // rounded reciprocal of the denominator (two roundings, within 1.5 ulp of
-    // the quotient).
-    const float vmax = key_value(first);
-    const float ex = expf(key_value(mine) - vmax);
-    const float ev = (lane < k) ? ex : 0.0f;
-    float sum = ev;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float inv = __frcp_rn(renorm ? sum : den_all);
+    float weight;
+    const uint32_t mine = warp_topk_keys<NK>(key, k, renorm, cand_s, weight);
     if (lane < k) {
         const int id = key_id(mine);
         ids[lane] = id;
-        wts[lane] = ev * inv;
+        wts[lane] = weight;
         keys_s[lane] = ((uint32_t)id << 10) | (uint32_t)(flat0 + lane);  // the align's key
         if (tmask != nullptr) {
             atomicOr(tmask + id, 1u << m);

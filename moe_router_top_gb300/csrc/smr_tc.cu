@@ -78,6 +78,11 @@ struct TcParams {
     int32_t *tile_counts;  // optional: expert counts of each 64-row tile, [tiles][E + S]
     int stall;             // failure-injection hook: the half merge waits on a barrier
     long long stall_limit; // nothing arrives on, for at most stall_limit SM cycles
+    int E_valid;           // gate rows that exist (E is padded to whole swizzle atoms)
+    int col0;              // logits-only: first column of this launch in the logit rows
+    uint16_t *logits_ws;   // logits-only: [M][ld_logits] bf16
+    int64_t ld_logits;
+    float *s_out;          // logits-only: [M] shared logit
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
     uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off, misc_den_off;
 };
@@ -284,7 +289,7 @@ __device__ __noinline__ void copy_row_out(uint32_t drow, uint16_t *dst, int ng) 
     for (int g = 0; g < ng; ++g) reinterpret_cast<uint4 *>(dst)[g] = ld_shared_v4(drow + (uint32_t)(g * 16));
 }
 
-template <int NGM, int CW>
+template <int CW, bool LO>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const TcParams p) {
@@ -335,7 +340,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc_fence_before();
     cluster_arrive();
     if (warp == 2 || warp == 3) {  // bias and expert counts, read in the epilogue
-        for (int i = threadIdx.x - 64; i < p.E; i += 64) bias_s[i] = p.bias ? p.bias[i] : 0.0f;
+        for (int i = threadIdx.x - 64; i < p.E; i += 64) bias_s[i] = (p.bias && i < p.E_valid) ? p.bias[i] : 0.0f;
         for (int i = threadIdx.x - 64; i < 2 * (p.E + p.S); i += 64) hist[i] = 0;
     } else if (warp >= 4 && p.S) {  // shared gate row, zero-padded to whole k-blocks
         const int nch = p.H >> 3;
@@ -474,235 +479,269 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc_fence_after();
     ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
     __syncwarp();  // lanes left the bounded wait on different iterations
-    const int ecols = p.E / 2;
-    const int c_beg = hf * ecols;
-    const int nch = ecols / CW;       // CW-column TMEM chunks per half
-    const int ng = ecols / kGroup;    // groups of kGroup consecutive columns per half
-    // the stage ring is idle once the accumulator is complete. Per half a
-    // list column per thread ([32][128] words: group maxima, then candidates,
-    // then the half's top-k), softmax numerators of half 1, and each half's
-    // rounded logits (row stride rs)
-    uint32_t *list = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);
-    uint32_t *list0 = reinterpret_cast<uint32_t *>(smem);                 // half 0's top-k
-    float *numer = reinterpret_cast<float *>(smem) + 2 * kCandCap * kTcBM;  // [32][128]
-    const uint32_t rs = dump_row_bytes(ecols);
-    const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
-    float den_half = 0.0f, v_half = 0.0f;  // without renormalisation: this half's denominator
-    if (ok) {
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
-        // 1. one sweep over this half's TMEM columns: add the bias, round to
-        //    bf16 two at a time, keep the row in shared memory and the maximum
-        //    of each group of kGroup columns in the thread's list column
-        uint32_t ra[CW], rb[CW];
-        const bool has_bias = p.bias != nullptr;
-        auto process = [&](uint32_t (&r)[CW], int ch) {
-            const int c = c_beg + ch * CW;
-            uint32_t pair = 0u;  // ordered 16-bit maxima of two consecutive groups
-#pragma unroll
-            for (int u = 0; u < CW / kGroup; ++u) {
-                float b[kGroup];
-#pragma unroll
-                for (int t = 0; t < kGroup; ++t) b[t] = 0.0f;
-                if (has_bias) {
-                    const float4 b0 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup);
-                    const float4 b1 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup + 4);
-                    b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-                    b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
-                }
-                uint32_t wv[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int i = u * kGroup + 2 * t;
-                    wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + b[2 * t],
-                                           __uint_as_float(r[i + 1]) + b[2 * t + 1]);
-                }
-                const int g = ch * (CW / kGroup) + u;
-                st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                // the group's maximum: bf16 pair maxima, then one conversion to
-                // ordered keys; a -0 maximum counts as +0 (equal values)
-                const uint32_t bm = max_bf16x2(max_bf16x2(wv[0], wv[1]), max_bf16x2(wv[2], wv[3]));
-                const uint32_t mx = ordered_bf16x2(bm);
-                uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
-                gmax16 = (gmax16 == 0x7FFFu) ? 0x8000u : gmax16;
-                pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
-                if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
-            }
-        };
-        tmem_ld_async<CW>(taddr, ra);
-        tmem_ld_wait<CW>(ra);
-        for (int ch = 0; ch < nch; ch += 2) {  // the next chunk's load in flight
-            const bool two = ch + 1 < nch;
-            if (two) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), rb);
-            process(ra, ch);
-            if (two) {
-                tmem_ld_wait<CW>(rb);
-                if (ch + 2 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 2) * CW), ra);
-                process(rb, ch + 1);
-                if (ch + 2 < nch) tmem_ld_wait<CW>(ra);
-            }
-        }
-        __syncwarp();
-        if (__builtin_expect(p.logits_out != nullptr, 0) && valid)
-            copy_row_out(drow, p.logits_out + (int64_t)grow * p.E + c_beg, ng);
-        // the k-th largest group maximum T bounds this half's top-k from
-        // below (k groups hold a logit >= T); only groups whose maximum is
-        // >= T can hold a logit >= T. Group maxima are ordered 16-bit keys,
-        // two per word, so each of the k rounds works on 16 registers.
-        uint32_t sel = 0;
-        float T = -INFINITY;
-        if (p.k <= ng) {
-            uint32_t pw[kCandCap / 2], po[kCandCap / 2];
-#pragma unroll
-            for (int i = 0; i < kCandCap / 2; ++i) po[i] = pw[i] = (2 * i < ng) ? list[i * kTcBM + row] : 0u;
-            const uint32_t t16 = kth_largest_packed(pw, p.k);
-            T = ordered16_value(t16);
-            const uint32_t ts = t16 | (t16 << 16);
-#pragma unroll
-            for (int i = 0; i < kCandCap / 2; ++i) {
-                const uint32_t ge = __vcmpgeu2(po[i], ts);
-                sel |= ((ge & 1u) << (2 * i)) | (((ge >> 16) & 1u) << (2 * i + 1));
-            }
-            sel &= (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);
-        } else {
-            sel = (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);  // fewer groups than k: all
-        }
-        __syncwarp();
-        // 2. append every logit >= T of the selected groups (about k groups)
-        //    to the list column, over the group maxima
-        uint32_t n = 0;
-        const uint32_t cand_row = smem_u32(list + row);
+    if constexpr (LO) {
+        // logits only: this launch's columns [col0, col0 + E), the bias added
+        // and rounded to bf16 (columns past E_valid: -inf), into the rows of
+        // the workspace; the shared logit of warps 4-7's rows. A select
+        // kernel takes the top-k over whole rows afterwards.
+        if (ok) {
+            const int ecols = p.E / 2, c_beg = hf * ecols;
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
+            uint16_t *dst = p.logits_ws + (int64_t)(valid ? grow : 0) * p.ld_logits + p.col0 + c_beg;
 #pragma unroll 1
-        while (__any_sync(0xffffffffu, sel != 0u)) {
-            const uint32_t act = sel != 0u ? 1u : 0u;
-            const int g = act ? __ffs(sel) - 1 : 0;
-            sel &= sel - 1u;
-            const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int ch = 0; ch < ecols / CW; ++ch) {
+                uint32_t r[CW];
+                tmem_ld_async<CW>(taddr + (uint32_t)(ch * CW), r);
+                tmem_ld_wait<CW>(r);
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) {
-                const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
-                const uint32_t c = act & (__uint_as_float(hb) >= T ? 1u : 0u);
-                st_shared_if(cand_row + min(n, (uint32_t)(kCandCap - 1)) * (kTcBM * 4),
-                             hb | (uint32_t)(c_beg + g * kGroup + u),
-                             c & (n < (uint32_t)kCandCap ? 1u : 0u));
-                n += c;
+                for (int u = 0; u < CW / kGroup; ++u) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int i = u * kGroup + 2 * t, c = c_beg + ch * CW + i;
+                        const float lo = c < p.E_valid ? __uint_as_float(r[i]) + bias_s[c] : -INFINITY;
+                        const float hi = c + 1 < p.E_valid ? __uint_as_float(r[i + 1]) + bias_s[c + 1] : -INFINITY;
+                        wv[t] = pack_bf16x2_rn(lo, hi);
+                    }
+                    if (valid)
+                        *reinterpret_cast<uint4 *>(dst + ch * CW + u * kGroup) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
             }
+            if (hf == 1 && p.S && valid) p.s_out[grow] = s_hi + s_lo;
+        } else if (lane == 0) {
+            set_error(p.err, kErrWaitTimeout);
         }
-        asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
-        __syncwarp();
-        // 3. this half's top-k, in order, into the list column: k rounds of
-        //    the largest remaining candidate key. A row whose candidates
-        //    overflowed the list takes k passes over its rounded logits.
-        if (__all_sync(0xffffffffu, n <= 16u)) {
-            topk_from_list<16>(list + row, n, p.k);  // the common case (~0.3% of rows exceed 16)
-        } else if (__builtin_expect(__any_sync(0xffffffffu, n > (uint32_t)kCandCap), 0)) {
-            if (n > (uint32_t)kCandCap) topk_from_row(drow, ng, c_beg, p.k, list + row);
-            else topk_from_list<kCandCap>(list + row, n, p.k);
-        } else {
-            topk_from_list<kCandCap>(list + row, n, p.k);
-        }
-        __syncwarp();
-        // 4. without renormalisation: this half's share of the E-expert
-        //    softmax denominator, every rounded logit's exponential relative
-        //    to the half's largest (eight per group as a tree, the groups by a
-        //    compensated sum); half 1 rescales both to the row's largest
-        if (!p.renorm) {
-            v_half = key_value(list[row]);
-            float hi = 0.0f, lo = 0.0f;
-#pragma unroll 1
-            for (int g = 0; g < ng; ++g) {
+    } else {
+        const int ecols = p.E / 2;
+        const int c_beg = hf * ecols;
+        const int nch = ecols / CW;       // CW-column TMEM chunks per half
+        const int ng = ecols / kGroup;    // groups of kGroup consecutive columns per half
+        // the stage ring is idle once the accumulator is complete. Per half a
+        // list column per thread ([32][128] words: group maxima, then candidates,
+        // then the half's top-k), softmax numerators of half 1, and each half's
+        // rounded logits (row stride rs)
+        uint32_t *list = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);
+        uint32_t *list0 = reinterpret_cast<uint32_t *>(smem);                 // half 0's top-k
+        float *numer = reinterpret_cast<float *>(smem) + 2 * kCandCap * kTcBM;  // [32][128]
+        const uint32_t rs = dump_row_bytes(ecols);
+        const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
+        float den_half = 0.0f, v_half = 0.0f;  // without renormalisation: this half's denominator
+        if (ok) {
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
+            // 1. one sweep over this half's TMEM columns: add the bias, round to
+            //    bf16 two at a time, keep the row in shared memory and the maximum
+            //    of each group of kGroup columns in the thread's list column
+            uint32_t ra[CW], rb[CW];
+            const bool has_bias = p.bias != nullptr;
+            auto process = [&](uint32_t (&r)[CW], int ch) {
+                const int c = c_beg + ch * CW;
+                uint32_t pair = 0u;  // ordered 16-bit maxima of two consecutive groups
+    #pragma unroll
+                for (int u = 0; u < CW / kGroup; ++u) {
+                    float b[kGroup];
+    #pragma unroll
+                    for (int t = 0; t < kGroup; ++t) b[t] = 0.0f;
+                    if (has_bias) {
+                        const float4 b0 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup);
+                        const float4 b1 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup + 4);
+                        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+                    }
+                    uint32_t wv[4];
+    #pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int i = u * kGroup + 2 * t;
+                        wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + b[2 * t],
+                                               __uint_as_float(r[i + 1]) + b[2 * t + 1]);
+                    }
+                    const int g = ch * (CW / kGroup) + u;
+                    st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                    // the group's maximum: bf16 pair maxima, then one conversion to
+                    // ordered keys; a -0 maximum counts as +0 (equal values)
+                    const uint32_t bm = max_bf16x2(max_bf16x2(wv[0], wv[1]), max_bf16x2(wv[2], wv[3]));
+                    const uint32_t mx = ordered_bf16x2(bm);
+                    uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
+                    gmax16 = (gmax16 == 0x7FFFu) ? 0x8000u : gmax16;
+                    pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
+                    if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
+                }
+            };
+            tmem_ld_async<CW>(taddr, ra);
+            tmem_ld_wait<CW>(ra);
+            for (int ch = 0; ch < nch; ch += 2) {  // the next chunk's load in flight
+                const bool two = ch + 1 < nch;
+                if (two) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), rb);
+                process(ra, ch);
+                if (two) {
+                    tmem_ld_wait<CW>(rb);
+                    if (ch + 2 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 2) * CW), ra);
+                    process(rb, ch + 1);
+                    if (ch + 2 < nch) tmem_ld_wait<CW>(ra);
+                }
+            }
+            __syncwarp();
+            if (__builtin_expect(p.logits_out != nullptr, 0) && valid)
+                copy_row_out(drow, p.logits_out + (int64_t)grow * p.E + c_beg, ng);
+            // the k-th largest group maximum T bounds this half's top-k from
+            // below (k groups hold a logit >= T); only groups whose maximum is
+            // >= T can hold a logit >= T. Group maxima are ordered 16-bit keys,
+            // two per word, so each of the k rounds works on 16 registers.
+            uint32_t sel = 0;
+            float T = -INFINITY;
+            if (p.k <= ng) {
+                uint32_t pw[kCandCap / 2], po[kCandCap / 2];
+    #pragma unroll
+                for (int i = 0; i < kCandCap / 2; ++i) po[i] = pw[i] = (2 * i < ng) ? list[i * kTcBM + row] : 0u;
+                const uint32_t t16 = kth_largest_packed(pw, p.k);
+                T = ordered16_value(t16);
+                const uint32_t ts = t16 | (t16 << 16);
+    #pragma unroll
+                for (int i = 0; i < kCandCap / 2; ++i) {
+                    const uint32_t ge = __vcmpgeu2(po[i], ts);
+                    sel |= ((ge & 1u) << (2 * i)) | (((ge >> 16) & 1u) << (2 * i + 1));
+                }
+                sel &= (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);
+            } else {
+                sel = (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);  // fewer groups than k: all
+            }
+            __syncwarp();
+            // 2. append every logit >= T of the selected groups (about k groups)
+            //    to the list column, over the group maxima
+            uint32_t n = 0;
+            const uint32_t cand_row = smem_u32(list + row);
+    #pragma unroll 1
+            while (__any_sync(0xffffffffu, sel != 0u)) {
+                const uint32_t act = sel != 0u ? 1u : 0u;
+                const int g = act ? __ffs(sel) - 1 : 0;
+                sel &= sel - 1u;
                 const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
                 const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                float e[kGroup];
-#pragma unroll
-                for (int u = 0; u < kGroup; ++u)
-                    e[u] = expf(__uint_as_float((u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16)) - v_half);
-#pragma unroll
-                for (int h = kGroup / 2; h >= 1; h >>= 1)
-#pragma unroll
-                    for (int u = 0; u < h; ++u) e[u] += e[u + h];
-                two_sum_acc(hi, lo, e[0]);
-            }
-            den_half = hi + lo;
-        }
-    }
-    if (hf == 0) {
-        if (!p.renorm) den_s[row] = make_float2(den_half, v_half);  // posted with the top-k
-        __syncwarp();
-        // (under the failure-injection hook half 0 does not post: the merge's
-        // wait then runs out, which sets the error bit and skips the outputs)
-        if (lane == 0 && !p.stall) mbar_arrive(smem_u32(half_done));
-    } else {
-        // ------------------------------ half 1: merge, softmax, write -----
-        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag,
-                                                                   p.stall ? p.stall_limit : kWaitCycles));
-        __syncwarp();
-        if (ok && got && valid) {
-            int32_t *orow = p.ids + (int64_t)grow * p.width;
-            float *wrow = p.wts + (int64_t)grow * p.width;
-            int *h = hist + (row / kTcCountRows) * (p.E + p.S);
-            const bool count = p.tile_counts != nullptr;
-            // both halves' lists are sorted descending: a pointer merge of k
-            // steps gives the row's top-k; the softmax numerators go to
-            // shared memory, the ids straight out
-            int i = 0, j = 0;
-            float vmax = 0.0f, sum = 0.0f;
-#pragma unroll 1
-            for (int r = 0; r < p.k; ++r) {
-                const uint32_t x1 = i < p.k ? list[i * kTcBM + row] : 0u;
-                const uint32_t x0 = j < p.k ? list0[j * kTcBM + row] : 0u;
-                const bool take1 = x1 > x0;
-                const uint32_t m = take1 ? x1 : x0;
-                i += take1 ? 1 : 0;
-                j += take1 ? 0 : 1;
-                vmax = (r == 0) ? key_value(m) : vmax;
-                const float ev = expf(key_value(m) - vmax);
-                sum += ev;
-                numer[r * kTcBM + row] = ev;
-                orow[r] = key_id(m);
-            }
-            float den = sum;
-            if (!p.renorm) {  // both halves' denominators at the row's largest logit
-                const float2 d0 = den_s[row];
-                den = den_half * expf(v_half - vmax) + d0.x * expf(d0.y - vmax);
-            }
-            const float inv = 1.0f / den;  // one division; each weight within 1.5 ulp of ev / den
-#pragma unroll 4
-            for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] * inv;
-            if (count) {
-                // the row's experts, for the align behind the route: the top-k
-                // are the first i entries of this half's list and the first j
-                // of half 0's. All keys are loaded before the first atomic, so
-                // the atomics issue back to back (off the merge's chain).
-                uint32_t ks[kCandCap];
-#pragma unroll
-                for (int r = 0; r < kCandCap; ++r)
-                    ks[r] = (r < p.k) ? (r < i ? list[r * kTcBM + row] : list0[(r - i) * kTcBM + row]) : 0u;
-#pragma unroll
-                for (int r = 0; r < kCandCap; ++r)
-                    if (r < p.k) atomicAdd(&h[key_id(ks[r])], 1);
-            }
-            if (p.S) {  // (its count is the tile's number of rows, set below)
-                const float sh = s_hi + s_lo;
-                orow[p.k] = p.E;
-                wrow[p.k] = p.scale * sigmoid_stable(p.shared_bf16 ? round_bf16(sh) : sh);
-            }
-        }
-        __syncwarp();
-        if (p.tile_counts) {
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // the 4 warps of half 1
-            const int E_al = p.E + p.S;
-            for (int t = 0; t < kTcTileRows / kTcCountRows; ++t) {  // tiles that hold rows
-                const int r0 = m0 + t * kTcCountRows;
-                if (r0 < p.M) {
-                    const int rows_t = min(kTcCountRows, p.M - r0);  // every row has one shared slot
-                    for (int e = threadIdx.x - 128; e < E_al; e += 128)
-                        p.tile_counts[(int64_t)(blockIdx.x * (kTcTileRows / kTcCountRows) + t) * E_al + e] =
-                            (e == p.E) ? rows_t : hist[t * E_al + e];
+    #pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
+                    const uint32_t c = act & (__uint_as_float(hb) >= T ? 1u : 0u);
+                    st_shared_if(cand_row + min(n, (uint32_t)(kCandCap - 1)) * (kTcBM * 4),
+                                 hb | (uint32_t)(c_beg + g * kGroup + u),
+                                 c & (n < (uint32_t)kCandCap ? 1u : 0u));
+                    n += c;
                 }
             }
+            asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
+            __syncwarp();
+            // 3. this half's top-k, in order, into the list column: k rounds of
+            //    the largest remaining candidate key. A row whose candidates
+            //    overflowed the list takes k passes over its rounded logits.
+            if (__all_sync(0xffffffffu, n <= 16u)) {
+                topk_from_list<16>(list + row, n, p.k);  // the common case (~0.3% of rows exceed 16)
+            } else if (__builtin_expect(__any_sync(0xffffffffu, n > (uint32_t)kCandCap), 0)) {
+                if (n > (uint32_t)kCandCap) topk_from_row(drow, ng, c_beg, p.k, list + row);
+                else topk_from_list<kCandCap>(list + row, n, p.k);
+            } else {
+                topk_from_list<kCandCap>(list + row, n, p.k);
+            }
+            __syncwarp();
+            // 4. without renormalisation: this half's share of the E-expert
+            //    softmax denominator, every rounded logit's exponential relative
+            //    to the half's largest (eight per group as a tree, the groups by a
+            //    compensated sum); half 1 rescales both to the row's largest
+            if (!p.renorm) {
+                v_half = key_value(list[row]);
+                float hi = 0.0f, lo = 0.0f;
+    #pragma unroll 1
+                for (int g = 0; g < ng; ++g) {
+                    const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    float e[kGroup];
+    #pragma unroll
+                    for (int u = 0; u < kGroup; ++u)
+                        e[u] = expf(__uint_as_float((u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16)) - v_half);
+    #pragma unroll
+                    for (int h = kGroup / 2; h >= 1; h >>= 1)
+    #pragma unroll
+                        for (int u = 0; u < h; ++u) e[u] += e[u + h];
+                    two_sum_acc(hi, lo, e[0]);
+                }
+                den_half = hi + lo;
+            }
         }
-        if (!(ok && got)) set_error(p.err, kErrWaitTimeout);
+        if (hf == 0) {
+            if (!p.renorm) den_s[row] = make_float2(den_half, v_half);  // posted with the top-k
+            __syncwarp();
+            // (under the failure-injection hook half 0 does not post: the merge's
+            // wait then runs out, which sets the error bit and skips the outputs)
+            if (lane == 0 && !p.stall) mbar_arrive(smem_u32(half_done));
+        } else {
+            // ------------------------------ half 1: merge, softmax, write -----
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(half_done), 0u, abort_flag,
+                                                                       p.stall ? p.stall_limit : kWaitCycles));
+            __syncwarp();
+            if (ok && got && valid) {
+                int32_t *orow = p.ids + (int64_t)grow * p.width;
+                float *wrow = p.wts + (int64_t)grow * p.width;
+                int *h = hist + (row / kTcCountRows) * (p.E + p.S);
+                const bool count = p.tile_counts != nullptr;
+                // both halves' lists are sorted descending: a pointer merge of k
+                // steps gives the row's top-k; the softmax numerators go to
+                // shared memory, the ids straight out
+                int i = 0, j = 0;
+                float vmax = 0.0f, sum = 0.0f;
+    #pragma unroll 1
+                for (int r = 0; r < p.k; ++r) {
+                    const uint32_t x1 = i < p.k ? list[i * kTcBM + row] : 0u;
+                    const uint32_t x0 = j < p.k ? list0[j * kTcBM + row] : 0u;
+                    const bool take1 = x1 > x0;
+                    const uint32_t m = take1 ? x1 : x0;
+                    i += take1 ? 1 : 0;
+                    j += take1 ? 0 : 1;
+                    vmax = (r == 0) ? key_value(m) : vmax;
+                    const float ev = expf(key_value(m) - vmax);
+                    sum += ev;
+                    numer[r * kTcBM + row] = ev;
+                    orow[r] = key_id(m);
+                }
+                float den = sum;
+                if (!p.renorm) {  // both halves' denominators at the row's largest logit
+                    const float2 d0 = den_s[row];
+                    den = den_half * expf(v_half - vmax) + d0.x * expf(d0.y - vmax);
+                }
+                const float inv = 1.0f / den;  // one division; each weight within 1.5 ulp of ev / den
+    #pragma unroll 4
+                for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] * inv;
+                if (count) {
+                    // the row's experts, for the align behind the route: the top-k
+                    // are the first i entries of this half's list and the first j
+                    // of half 0's. All keys are loaded before the first atomic, so
+                    // the atomics issue back to back (off the merge's chain).
+                    uint32_t ks[kCandCap];
+    #pragma unroll
+                    for (int r = 0; r < kCandCap; ++r)
+                        ks[r] = (r < p.k) ? (r < i ? list[r * kTcBM + row] : list0[(r - i) * kTcBM + row]) : 0u;
+    #pragma unroll
+                    for (int r = 0; r < kCandCap; ++r)
+                        if (r < p.k) atomicAdd(&h[key_id(ks[r])], 1);
+                }
+                if (p.S) {  // (its count is the tile's number of rows, set below)
+                    const float sh = s_hi + s_lo;
+                    orow[p.k] = p.E;
+                    wrow[p.k] = p.scale * sigmoid_stable(p.shared_bf16 ? round_bf16(sh) : sh);
+                }
+            }
+            __syncwarp();
+            if (p.tile_counts) {
+                asm volatile("bar.sync 1, 128;" ::: "memory");  // the 4 warps of half 1
+                const int E_al = p.E + p.S;
+                for (int t = 0; t < kTcTileRows / kTcCountRows; ++t) {  // tiles that hold rows
+                    const int r0 = m0 + t * kTcCountRows;
+                    if (r0 < p.M) {
+                        const int rows_t = min(kTcCountRows, p.M - r0);  // every row has one shared slot
+                        for (int e = threadIdx.x - 128; e < E_al; e += 128)
+                            p.tile_counts[(int64_t)(blockIdx.x * (kTcTileRows / kTcCountRows) + t) * E_al + e] =
+                                (e == p.E) ? rows_t : hist[t * E_al + e];
+                    }
+                }
+            }
+            if (!(ok && got)) set_error(p.err, kErrWaitTimeout);
+        }
     }
     tc_fence_before();
     // both CTAs' epilogues are done with TMEM and no barrier of either CTA
@@ -760,6 +799,7 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     TcParams p{};
     p.H = H;
     p.E = E;
+    p.E_valid = E;
     p.S = S;
     p.k = k;
     p.M = M;
@@ -807,16 +847,16 @@ bool tc_route_supported(int H, int E, int k, int S) {
     return plan_tc(1, H, E, k, S, &plan);
 }
 
-template <int NGM, int CW>
+template <int CW, bool LO>
 static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const TcPlan &plan,
                              cudaStream_t stream) {
     static std::atomic<bool> configured[kMaxDevices];
     cudaError_t e = once_per_device(configured, [](int) {
-        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
+        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<CW, LO>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kTcSmemLimit);
         if (r == cudaSuccess)  // the same carveout as every other kernel of the library
-            r = cudaFuncSetAttribute(tc_route_kernel<NGM, CW>,
+            r = cudaFuncSetAttribute(tc_route_kernel<CW, LO>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         return r;
@@ -838,13 +878,21 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_route_kernel<NGM, CW>, mx, mw, plan.p);
+    return cudaLaunchKernelEx(&cfg, tc_route_kernel<CW, LO>, mx, mw, plan.p);
 }
 
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     TcPlan plan;
-    if (!plan_tc(a.M, a.H, a.E, a.k, a.S, &plan)) return cudaErrorNotSupported;
+    // a logits-only launch computes its E valid gate rows padded to whole
+    // 32-row groups (zero rows past E from the tensor map's fill)
+    const int E_pad = a.logits_only ? (a.E + 31) / 32 * 32 : a.E;
+    if (!plan_tc(a.M, a.H, E_pad, a.logits_only ? 1 : a.k, a.S, &plan)) return cudaErrorNotSupported;
     TcParams &p = plan.p;
+    p.E_valid = a.E;
+    p.col0 = a.col0;
+    p.logits_ws = a.logits_ws;
+    p.ld_logits = a.ld_logits;
+    p.s_out = a.s_out;
     p.scale = a.scale;
     p.renorm = a.renorm;
     p.shared_bf16 = a.shared_bf16;
@@ -865,12 +913,11 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     if (!make_map(&mw, a.w, (uint64_t)a.H, (uint64_t)a.E, (uint64_t)a.H * 2, kTcBK,
                   (uint32_t)(p.piece_n / 2)))
         return cudaErrorInvalidValue;
-    // 32-column TMEM chunks when each column half is a multiple of 32, else
-    // 16; at most 16 or 32 column groups per half
-    const bool wide = (a.E / 2) % 32 == 0;
-    if (a.E <= 256)
-        return wide ? launch_ng<16, 32>(mx, mw, plan, stream) : launch_ng<16, 16>(mx, mw, plan, stream);
-    return wide ? launch_ng<32, 32>(mx, mw, plan, stream) : launch_ng<32, 16>(mx, mw, plan, stream);
+    // 32-column TMEM chunks when each column half is a multiple of 32, else 16
+    const bool wide = (E_pad / 2) % 32 == 0;
+    if (a.logits_only)
+        return wide ? launch_ng<32, true>(mx, mw, plan, stream) : launch_ng<16, true>(mx, mw, plan, stream);
+    return wide ? launch_ng<32, false>(mx, mw, plan, stream) : launch_ng<16, false>(mx, mw, plan, stream);
 }
 
 }  // namespace smr

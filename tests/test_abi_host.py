@@ -95,9 +95,14 @@ def test_route_variant_flags_checked(lib):
 
 
 def test_route_unsupported_contract(lib):
-    a = _good_route(M=64, E=500)      # tcgen05 path needs E % 32 == 0
-    assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
-    assert "E % 32 == 0" in lib.smr_last_error().decode()
+    for E in (500, 1024, 40):         # outside the fused epilogue: logits + select, admitted
+        a = _good_route(M=64, E=E)
+        need = lib.smr_route_workspace_size(ctypes.byref(a))
+        ld = (E + 31) // 32 * 32      # bf16 logit rows + fp32 shared logits in the workspace
+        assert need == 256 + ((64 * ld * 2 + 255) // 256) * 256 + 256
+        assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_WORKSPACE
+    a = _good_route(M=64, E=512)      # fused epilogue: no workspace beyond the header
+    assert lib.smr_route_workspace_size(ctypes.byref(a)) == 256
     a = _good_route(k=32, S=1, E=64)  # width 33 > 32
     assert lib.smr_route(ctypes.byref(a), None, 0, None) == _lib.SMR_ERR_UNSUPPORTED
 
@@ -228,7 +233,7 @@ def _set(obj, **kw):
     (dict(bias=0x60002), _lib.SMR_ERR_INVALID_ARG, "bias must be 4-byte aligned"),
     (dict(topk_weights=0x50002), _lib.SMR_ERR_INVALID_ARG, "topk_weights must be 4-byte aligned"),
     (dict(logits_out=0x70008), _lib.SMR_ERR_INVALID_ARG, "logits_out must be 16-byte aligned"),
-    (dict(M=32, E=1024), _lib.SMR_ERR_UNSUPPORTED, "32 <= E <= 512"),
+    (dict(renormalize=5), _lib.SMR_ERR_INVALID_ARG, "renormalize must be 0 or 1"),
 ])
 def test_route_refuses_each_bad_argument(lib, change, status, fragment):
     """Every malformed route argument is refused before any launch, with its

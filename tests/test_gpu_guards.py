@@ -58,6 +58,7 @@ class Guarded:
     (9, 512, 64, 8, 1, 5),        # single launch, A < M: ranked align, direct stores
     (300, 512, 256, 8, 1, 64),    # tcgen05 route + one-CTA align
     (2049, 256, 128, 8, 1, 128),  # tcgen05 route + counted multi-tile align
+    (300, 512, 1000, 10, 1, 64),  # logits-only tcgen05 launches + select + one-CTA align
 ])
 def test_route_align_writes_stay_inside_outputs(smr, M, H, E, k, S, A):
     ri = inputs.make_route_inputs(M, H, E, k, S, seed=500 + M + E)

@@ -162,10 +162,28 @@ def test_large_batch_logits_every_tile(smr):
     (300, 512, 512, 16, 0),  # k = 16 threshold classes
     (64, 128, 32, 32, 0),    # k = E, 32 classes
     (256, 2048, 256, 1, 1),  # k = 1
+    # M > 16 outside the fused epilogue: logits-only tcgen05 launches + select
+    (300, 512, 1024, 10, 1),   # the largest E: two 512-column launches
+    (130, 200, 100, 8, 1),     # E not a multiple of 32, ragged K and tail
+    (17, 64, 8, 4, 0),         # tiny E: one 32-column launch, 24 padded columns
+    (1000, 1024, 600, 31, 1),  # a 512-column launch + an 88-column one, widest row
 ])
 def test_shapes(smr, M, H, E, k, S):
     ri = inputs.make_route_inputs(M, H, E, k, S, seed=M * 1000 + E, shared_scale=0.75)
     _full_check(smr, ri, 64)
+
+
+@pytest.mark.parametrize("M,H,E,k,S,zipf,launches", [
+    (2049, 1024, 1000, 8, 1, 1.1, 2 + 1 + 3),  # logits in two launches, select, three align launches
+    (16384, 4096, 1024, 10, 1, None, 2 + 1 + 3),
+])
+def test_generic_route_align(smr, M, H, E, k, S, zipf, launches):
+    """M > 16 with E beyond the fused epilogue, through route_align as the
+    benchmark calls it (no logits output): every row against the oracle."""
+    ri = inputs.make_route_inputs(M, H, E, k, S, seed=M + E, zipf_s=zipf)
+    rep, al, ids = _full_check(smr, ri, 128, with_logits=False, name=f"generic_M{M}_E{E}")
+    assert smr.last_launch_count() == launches
+    print(f"generic M={M} E={E}: {rep}")
 
 
 @pytest.mark.parametrize("M,H,E,k,S,zipf", [
