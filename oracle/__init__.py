@@ -71,6 +71,12 @@ def _load():
             lib.oracle_align.restype = i32
             lib.oracle_align_eplb.argtypes = [P, i64, i32, i32, P, P, i32, i32, i32, P, i64, P, i64, P]
             lib.oracle_align_eplb.restype = i32
+            lib.oracle_e4m3_from_double.argtypes = [f64]
+            lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = f64
+            lib.oracle_quant_fp8.argtypes = [i32, i32, P, i64, P, P]
+            lib.oracle_quant_fp8.restype = None
             _lib = lib
     return _lib
 
@@ -231,3 +237,24 @@ def align_eplb(ids: np.ndarray, num_experts: int, eplb_map: np.ndarray, eplb_cou
         raise ValueError("oracle_align_eplb: id, replica count or physical id out of range")
     n = int(npp[0])
     return AlignResult(sorted_ids[:n].copy(), expert_ids[: n // A].copy(), n)
+
+
+# --- hidden states to e4m3 -------------------------------------------------------
+
+def e4m3_from_double(v: float) -> int:
+    return int(_load().oracle_e4m3_from_double(float(v)))
+
+
+def e4m3_to_double(c: int) -> float:
+    return float(_load().oracle_e4m3_to_double(int(c) & 0xFF))
+
+
+def quant_fp8(x: np.ndarray):
+    """E4M3 codes [M, H] (uint8) and fp32 block scales [M, H/128] of bf16-bit
+    hidden states (see oracle_quant_fp8 in oracle.c)."""
+    x = _c(x, np.uint16)
+    M, H = x.shape
+    q = np.empty((M, H), dtype=np.uint8)
+    sc = np.empty((M, H // 128), dtype=np.float32)
+    _load().oracle_quant_fp8(M, H, _ptr(x), H, _ptr(q), _ptr(sc))
+    return q, sc

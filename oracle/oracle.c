@@ -86,6 +86,81 @@ ORACLE_API void oracle_bf16_round_array(int64_t n, const double *in, double *out
         out[i] = oracle_bf16_to_double(oracle_bf16_from_double(in[i]));
 }
 
+/* ---------------------------------------------------------------- e4m3 --- */
+
+/* E4M3 (the FP8 format of "Netra Kernel ...", Fusing the activation/
+ * quantization boundary): 1 sign bit, 4 exponent bits (bias 7), 3 stored
+ * fraction bits, no infinities; code 0x7F / 0xFF is NaN. Normal numbers carry
+ * 4 significant bits; below 2^-6 the spacing is fixed at 2^-9 (subnormals).
+ * The largest finite value is 1.75 * 2^8 = 448. Rounds to nearest even and
+ * saturates: magnitudes beyond 448 give +-448. */
+ORACLE_API uint8_t oracle_e4m3_from_double(double v)
+{
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);
+    int e = e2 - 1;                /* a in [2^e, 2^(e+1)) */
+    if (e < -6) e = -6;            /* subnormal range: fixed spacing 2^-9 */
+    double step = ldexp(1.0, e - 3);  /* spacing of e4m3 values near a */
+    double m = nearbyint(a / step);     /* exact quotient; default mode is RNE */
+    double r = m * step;
+    if (r > 448.0) r = 448.0;      /* cannot happen below 448 (448 is a code) */
+    /* encode r: exponent field and fraction */
+    if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (int)(r / ldexp(1.0, -9)));  /* subnormal */
+    int re2;
+    double f = frexp(r, &re2);     /* r = f * 2^re2, f in [0.5, 1) */
+    int exp_field = re2 - 1 + 7;
+    int frac = (int)((f * 2.0 - 1.0) * 8.0);
+    return (uint8_t)(sign | (exp_field << 3) | frac);
+}
+
+ORACLE_API double oracle_e4m3_to_double(uint8_t c)
+{
+    int sign = c & 0x80, ef = (c >> 3) & 0xF, fr = c & 7;
+    if ((c & 0x7F) == 0x7F) return NAN;
+    double mag = ef == 0 ? ldexp((double)fr, -9) : ldexp(1.0 + fr / 8.0, ef - 7);
+    return sign ? -mag : mag;
+}
+
+/* Hidden states quantised once for the expert GEMMs ("Netra Kernel ...",
+ * Fusing the activation/quantization boundary: each contiguous 128-element
+ * block to E4M3 with its block scale). Reading taken: per row t and block b
+ * of 128 elements, amax = max |x|, scale[t][b] = amax / 448 and the codes are
+ * e4m3(x * (448 / amax)), each division and the product rounded to fp32 (the
+ * precision the kernel decides the codes in: fp32 operands and results);
+ * a block of zeros has scale 0 and zero codes. H must be a multiple of 128.
+ * q [M][H] codes, scales [M][H/128]. */
+ORACLE_API void oracle_quant_fp8(int M, int H, const uint16_t *x, int64_t ld_x, uint8_t *q, float *scales)
+{
+    for (int t = 0; t < M; ++t) {
+        for (int b = 0; b < H / 128; ++b) {
+            const uint16_t *xb = x + (int64_t)t * ld_x + (int64_t)b * 128;
+            double amax = 0.0;
+            for (int i = 0; i < 128; ++i) {
+                double a = fabs(oracle_bf16_to_double(xb[i]));
+                if (a > amax) amax = a;
+            }
+            uint8_t *qb = q + (int64_t)t * H + (int64_t)b * 128;
+            if (amax == 0.0) {
+                scales[(int64_t)t * (H / 128) + b] = 0.0f;
+                for (int i = 0; i < 128; ++i) qb[i] = 0;
+                continue;
+            }
+            float scale = (float)(amax / 448.0);
+            float inv = (float)(448.0 / amax);
+            scales[(int64_t)t * (H / 128) + b] = scale;
+            for (int i = 0; i < 128; ++i) {
+                float v = (float)(oracle_bf16_to_double(xb[i]) * (double)inv);
+                qb[i] = oracle_e4m3_from_double((double)v);
+            }
+        }
+    }
+}
+
 /* --------------------------------------------------------- gate GEMM --- */
 
 /* z[t*E + e] = sum_h x[t,h]*W[e,h] + bias[e] in double; absdot (optional)

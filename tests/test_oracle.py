@@ -497,3 +497,76 @@ def test_align_eplb_replicas_hand_case():
     # a replica count above the table width is refused
     with pytest.raises(ValueError):
         oracle.align_eplb(ids, 3, mp, np.array([3, 1, 1], np.int32), 6, 2)
+
+
+# ------------------------------------------------ hidden states to e4m3 ---
+
+def _e4m3_table():
+    """All finite e4m3 values except -0, as (Fraction, code), sorted."""
+    out = []
+    for c in range(256):
+        if (c & 0x7F) == 0x7F or c == 0x80:
+            continue
+        ef, fr = (c >> 3) & 0xF, c & 7
+        mag = Fraction(fr, 8) * Fraction(1, 64) if ef == 0 else (1 + Fraction(fr, 8)) * Fraction(2) ** (ef - 7)
+        out.append((-mag if c & 0x80 else mag, c))
+    return sorted(out)
+
+
+def test_e4m3_exhaustive_brute_force():
+    """Every code, every midpoint between neighbours (ties to the even code)
+    and points just beside the midpoints, against exact rationals."""
+    table = _e4m3_table()
+    assert len(table) == 253 and table[-1][0] == 448 and table[0][0] == -448
+    for v, c in table:
+        assert oracle.e4m3_from_double(float(v)) == c
+        assert oracle.e4m3_to_double(c) == float(v)
+    for (a, ca), (b, cb) in zip(table, table[1:]):
+        mid = (a + b) / 2
+        even = ca if (ca & 1) == 0 else cb
+        if a == 0 or b == 0:  # around zero the sign of the rounded zero follows v
+            continue
+        assert oracle.e4m3_from_double(float(mid)) == even, (a, b)
+        eps = (b - a) / 1024
+        assert oracle.e4m3_from_double(float(mid - eps)) == ca
+        assert oracle.e4m3_from_double(float(mid + eps)) == cb
+
+
+def test_e4m3_saturates_and_matches_torch():
+    for v, c in ((448.0, 0x7E), (449.0, 0x7E), (479.9, 0x7E), (1e9, 0x7E), (-500.0, 0xFE),
+                 (2.0 ** -10, 0x00), (3 * 2.0 ** -11, 0x01)):
+        assert oracle.e4m3_from_double(v) == c, v
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(71)
+    v = np.concatenate([rng.uniform(-447, 447, 4000), rng.normal(0, 1, 4000),
+                        rng.normal(0, 0.01, 2000)]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_double(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_quant_fp8_closed_forms():
+    """A block whose largest magnitude is a: scale = fl(a / 448), that
+    element's code is +-448, a zero block gives scale 0 and zero codes,
+    every code decodes within half an e4m3 step of x * 448 / a."""
+    H = 256
+    xf = np.zeros((2, H), np.float32)
+    xf[0, :128] = np.linspace(-3.0, 2.5, 128)
+    xf[1, 128:] = np.random.default_rng(72).normal(0, 1, 128)
+    x = inputs.f32_to_bf16_bits(xf)
+    xv = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    q, sc = oracle.quant_fp8(x)
+    assert sc[0, 1] == 0.0 and np.all(q[0, 128:] == 0) and sc[1, 0] == 0.0 and np.all(q[1, :128] == 0)
+    for t, b in ((0, 0), (1, 1)):
+        blk = xv[t, 128 * b:128 * b + 128]
+        a = np.abs(blk).max()
+        assert sc[t, b] == np.float32(a / 448.0)
+        i = int(np.argmax(np.abs(blk)))
+        assert oracle.e4m3_to_double(q[t, 128 * b + i]) == math.copysign(448.0, blk[i])
+        dec = np.array([oracle.e4m3_to_double(c) for c in q[t, 128 * b:128 * b + 128]])
+        scaled = blk * (448.0 / a)
+        step = np.where(np.abs(scaled) < 2.0 ** -6, 2.0 ** -9,
+                        2.0 ** (np.floor(np.log2(np.maximum(np.abs(scaled), 1e-30))) - 3))
+        assert np.all(np.abs(dec - scaled) <= step / 2 * (1 + 1e-6) + 1e-9)

@@ -53,6 +53,14 @@ MUTANTS = [
      "int p = map[(int64_t)e * max_replicas + (int)(t % count[e])];",
      "int p = map[(int64_t)e * max_replicas + (int)(i % count[e])];"),
     ("EPLB remap skipped", "phys[i] = p;", "phys[i] = e;"),
+    ("e4m3 truncates", "double m = nearbyint(a / step);", "double m = trunc(a / step);"),
+    ("e4m3 overflow to NaN instead of saturating",
+     "if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 464.0) return (uint8_t)(sign | 0x7F);"),
+    ("block scale over 240 instead of 448",
+     "float scale = (float)(amax / 448.0);", "float scale = (float)(amax / 240.0);"),
+    ("codes from the unscaled values",
+     "float v = (float)(oracle_bf16_to_double(xb[i]) * (double)inv);",
+     "float v = (float)(oracle_bf16_to_double(xb[i]));"),
     ("descending order inside an expert",
      "for (int64_t i = 0; i < numel; ++i) sorted[cur[ids[i]]++] = (int32_t)i;",
      "for (int64_t i = numel - 1; i >= 0; --i) sorted[cur[ids[i]]++] = (int32_t)i;"),
