@@ -102,6 +102,15 @@ typedef struct smr_route_args {
                                   0: use the fp32 logit (only the routed logits are
                                   rounded, "[AMD] One-launch small-M MoE router ...",
                                   Modifications) */
+    /* Optional: the hidden states quantised once, in the route's launch, for
+     * the expert GEMMs ("Netra Kernel ...", Fusing the activation/quantization
+     * boundary: E4M3 with one scale per 128 contiguous values). For every row
+     * t and 128-element block b: scale = amax / 448 (amax the block's largest
+     * magnitude), codes = E4M3(x * (448 / amax)) rounded to nearest even and
+     * saturated at +-448, the divisions and the product in fp32; a block of
+     * zeros gets scale 0 and zero codes. Needs H % 128 == 0. NULL to skip. */
+    uint8_t *hidden_fp8;     /* out: e4m3 codes [M, H], 16-byte aligned */
+    float *hidden_scales;    /* out: fp32 [M, H / 128] */
 } smr_route_args;
 
 /* Align problem over a [num_tokens, width] id matrix. */

@@ -126,7 +126,7 @@ def _workspace(ws, nbytes: int, device):
 
 
 def _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, ids, wts,
-                logits_out, shared_logit_bf16=False) -> RouteArgs:
+                logits_out, shared_logit_bf16=False, hidden_fp8=None, hidden_scales=None) -> RouteArgs:
     torch = _torch()
     if hidden.dtype != torch.bfloat16 or gate_w.dtype != torch.bfloat16:
         raise TypeError("hidden and gate_w must be bfloat16")
@@ -156,6 +156,16 @@ def _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize,
     a.topk_weights = _ptr(wts)
     a.logits_out = _ptr(logits_out)
     a.shared_logit_bf16 = 1 if shared_logit_bf16 else 0
+    if hidden_fp8 is not None:
+        M, H = hidden.shape
+        if (hidden_fp8.dtype != torch.uint8 or tuple(hidden_fp8.shape) != (M, H)
+                or not hidden_fp8.is_contiguous()):
+            raise ValueError("hidden_fp8 must be a contiguous uint8 [M, H] tensor (e4m3 codes)")
+        if (hidden_scales is None or hidden_scales.dtype != torch.float32
+                or tuple(hidden_scales.shape) != (M, H // 128) or not hidden_scales.is_contiguous()):
+            raise ValueError("hidden_scales must be a contiguous float32 [M, H // 128] tensor")
+        a.hidden_fp8 = _ptr(hidden_fp8)
+        a.hidden_scales = _ptr(hidden_scales)
     return a
 
 
@@ -172,13 +182,17 @@ def _route_outputs(hidden, topk, has_shared, ids, wts):
 
 def route(hidden, gate_w, shared_w=None, bias=None, *, topk: int, shared_scale: float = 1.0,
           renormalize: bool = True, shared_logit_bf16: bool = False, topk_ids=None,
-          topk_weights=None, logits_out=None, workspace=None, stream=None) -> Tuple:
-    """Route M tokens: returns (topk_ids int32 [M, k+S], topk_weights fp32 [M, k+S])."""
+          topk_weights=None, logits_out=None, hidden_fp8=None, hidden_scales=None,
+          workspace=None, stream=None) -> Tuple:
+    """Route M tokens: returns (topk_ids int32 [M, k+S], topk_weights fp32 [M, k+S]).
+    hidden_fp8 (uint8 [M, H]) and hidden_scales (float32 [M, H/128]), when
+    given, receive the hidden states as e4m3 codes with one scale per 128
+    values, written by the same launch."""
     _disabled()
     lib = _lib.load()
     topk_ids, topk_weights = _route_outputs(hidden, topk, shared_w is not None, topk_ids, topk_weights)
     a = _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, topk_ids,
-                    topk_weights, logits_out, shared_logit_bf16)
+                    topk_weights, logits_out, shared_logit_bf16, hidden_fp8, hidden_scales)
     need = lib.smr_route_workspace_size(ctypes.byref(a))
     wp, wn = _workspace(workspace, need, hidden.device)
     _check(lib.smr_route(ctypes.byref(a), wp, wn, _stream_ptr(stream)))
@@ -265,7 +279,8 @@ def route_align(hidden, gate_w, shared_w=None, bias=None, *, topk: int, block_si
                 shared_logit_bf16: bool = False, topk_ids=None, topk_weights=None,
                 logits_out=None, sorted_token_ids=None, expert_ids=None,
                 num_tokens_post_padded=None, eplb_map=None, eplb_count=None,
-                num_physical: int = 0, workspace=None, stream=None) -> Tuple:
+                num_physical: int = 0, hidden_fp8=None, hidden_scales=None, workspace=None,
+                stream=None) -> Tuple:
     """Route then align (one launch for M <= 16 without an EPLB remap).
     Returns (topk_ids, topk_weights, sorted_token_ids, expert_ids,
     num_tokens_post_padded)."""
@@ -274,7 +289,7 @@ def route_align(hidden, gate_w, shared_w=None, bias=None, *, topk: int, block_si
     S = 1 if shared_w is not None else 0
     topk_ids, topk_weights = _route_outputs(hidden, topk, S, topk_ids, topk_weights)
     ra = _route_args(hidden, gate_w, shared_w, bias, topk, shared_scale, renormalize, topk_ids,
-                     topk_weights, logits_out, shared_logit_bf16)
+                     topk_weights, logits_out, shared_logit_bf16, hidden_fp8, hidden_scales)
     M, E = ra.M, ra.E
     A = block_size if block_size > 0 else select_block_size(M, topk, E)
     eplb = _eplb(eplb_map, eplb_count, num_physical)

@@ -44,6 +44,7 @@ class RouteArgs(ctypes.Structure):
         ("bias", ctypes.c_void_p), ("topk_ids", ctypes.c_void_p),
         ("topk_weights", ctypes.c_void_p), ("logits_out", ctypes.c_void_p),
         ("shared_logit_bf16", ctypes.c_int32),
+        ("hidden_fp8", ctypes.c_void_p), ("hidden_scales", ctypes.c_void_p),
     ]
 
 

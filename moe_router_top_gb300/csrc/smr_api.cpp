@@ -121,6 +121,12 @@ void check_route(const smr_route_args *a, Reasons &r) {
         if (!a->topk_weights) r.bad("topk_weights is NULL");
         else if (!aligned(a->topk_weights, 4)) r.bad("topk_weights must be 4-byte aligned");
         if (a->logits_out && !aligned(a->logits_out, 16)) r.bad("logits_out must be 16-byte aligned");
+        if (a->hidden_fp8) {
+            if (a->H % 128 != 0) r.bad("hidden_fp8 needs H % 128 == 0 (one scale per 128 values)");
+            if (!aligned(a->hidden_fp8, 16)) r.bad("hidden_fp8 must be 16-byte aligned");
+            if (!a->hidden_scales) r.bad("hidden_scales is NULL but hidden_fp8 is set");
+            else if (!aligned(a->hidden_scales, 4)) r.bad("hidden_scales must be 4-byte aligned");
+        }
     }
 }
 
@@ -288,6 +294,8 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
             L.sorted_cap = fused_align->sorted_cap;
             L.expert_cap = fused_align->expert_cap;
         }
+        L.xq = a->hidden_fp8;
+        L.xs = a->hidden_scales;
         const smr::StallHook hook = smr::stall_hook();
         L.stall = hook.site == smr::kStallSmallTail;
         L.stall_limit = L.stall ? hook.limit : 0;
@@ -317,6 +325,8 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
             L.logits_ws = lg;
             L.ld_logits = ld;
             L.s_out = sv;
+            L.xq = (c0 == 0) ? a->hidden_fp8 : nullptr;  // the first launch quantises x
+            L.xs = a->hidden_scales;
             cudaError_t e = smr::launch_tc_route(L, stream);
             if (e != cudaSuccess) return cuda_fail("tcgen05 logits launch", e);
             *launches += 1;
@@ -352,6 +362,8 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
     L.logits_out = a->logits_out;
     L.hdr = ws;
     L.tile_counts = tile_counts;
+    L.xq = a->hidden_fp8;
+    L.xs = a->hidden_scales;
     const smr::StallHook hook = smr::stall_hook();
     L.stall = hook.site == smr::kStallTcMerge;
     L.stall_limit = L.stall ? hook.limit : 0;

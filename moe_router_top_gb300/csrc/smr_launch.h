@@ -69,6 +69,10 @@ struct SmallRouteLaunch {
     // writes, giving up after stall_limit reloads
     int stall;
     long long stall_limit;
+    // optional: the hidden states as e4m3 codes [M][H] with one fp32 scale
+    // per 128 elements [M][H / 128] (H % 128 == 0)
+    uint8_t *xq;
+    float *xs;
 };
 constexpr int kSmallMaxM = 16;
 // Number of K ranges the gate rows are split into (the CTAs of one cluster);
@@ -114,6 +118,10 @@ struct TcRouteLaunch {
     uint16_t *logits_ws;
     int64_t ld_logits;
     float *s_out;
+    // optional: the hidden states as e4m3 codes [M][H] with one fp32 scale
+    // per 128 elements [M][H / 128] (H % 128 == 0)
+    uint8_t *xq;
+    float *xs;
 };
 constexpr int kTcTileRows = 128;   // token rows per CTA of the tcgen05 route
 constexpr int kTcCountRows = 64;   // token rows per align tile counted by the route

@@ -423,6 +423,37 @@ __device__ __forceinline__ void align_tiny(const uint32_t *keys, int n, int A, u
     report_bad_slots(bad, err);
 }
 
+// The hidden states to e4m3 ("Netra Kernel ...", Fusing the activation/
+// quantization boundary: one scale per 128 values): the kq-th of KQ CTAs
+// takes its share of the 128-element blocks, one warp per (token, block),
+// four elements per lane, re-read from L2 (this kernel loaded them already).
+// scale = amax / 448 and codes = e4m3(x * (448 / amax)) rounded to nearest
+// even and saturated, in fp32; a block of zeros gets scale 0 and zero codes.
+__device__ __noinline__ void small_quant_x(const SmallRouteLaunch &p, int kq, int KQ) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = p.H >> 7, b0 = kq * nb / KQ, b1 = (kq + 1) * nb / KQ, per = b1 - b0;
+#pragma unroll 1
+    for (int j = warp; j < p.M * per; j += kSmallWarps) {
+        const int m = j / per, b = b0 + j % per;
+        const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(p.x + (int64_t)m * p.ld + b * 128) + lane);
+        const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xFFFF0000u);
+        const float f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xFFFF0000u);
+        // magnitudes are nonnegative floats: their bit patterns order alike
+        const float amax = __uint_as_float(__reduce_max_sync(
+            0xffffffffu, __float_as_uint(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))))));
+        uint32_t codes = 0u;
+        if (amax > 0.0f) {
+            const float inv = 448.0f / amax;
+            uint16_t lo, hi;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(f1 * inv), "f"(f0 * inv));
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(f3 * inv), "f"(f2 * inv));
+            codes = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        reinterpret_cast<uint32_t *>(p.xq + (int64_t)m * p.H + b * 128)[lane] = codes;
+        if (lane == 0) p.xs[(int64_t)m * nb + b] = amax / 448.0f;
+    }
+}
+
 // NB: blocks of 8 tokens, 1 (M <= 8) or 2 (M <= 16); NK: keys per lane in
 // the top-k, 16 (E <= 512) or 32 (E <= 1024) -- one top-k per instance, so
 // the tail's code is laid out in the order it runs
@@ -570,6 +601,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         if (kq != 0) {
             st_async_cluster_f32(cluster_addr(smem_u32(slots + kq * 256 + tid), 0u), v,
                                  cluster_addr(smem_u32(&s_red_bar), 0u));
+            if (rg == 0 && p.xq != nullptr) small_quant_x(p, kq, P.KQ);
             return;
         }
         slots[tid] = v;  // read back by this thread only
@@ -600,6 +632,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
     }
     __syncwarp();
     __syncthreads();
+    if (rg == 0 && p.xq != nullptr) small_quant_x(p, 0, P.KQ);  // after this group's keys
 
     // ---- 3. hand-off: the tail CTA collects the tagged keys ----
     // No fence and no counter: every key word carries the call's tag, so

@@ -83,6 +83,8 @@ struct TcParams {
     uint16_t *logits_ws;   // logits-only: [M][ld_logits] bf16
     int64_t ld_logits;
     float *s_out;          // logits-only: [M] shared logit
+    uint8_t *xq;           // optional: hidden states as e4m3 codes [M][H]
+    float *xs;             // and their scales [M][H / 128]
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
     uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off, misc_den_off;
 };
@@ -284,6 +286,55 @@ __device__ __noinline__ void topk_from_row(uint32_t drow, int ng, int c_beg, int
     }
 }
 
+// The largest magnitude of a k-block row's 64 bf16 (eight 16-byte chunks),
+// as a packed pair of bf16 maxima.
+__device__ __forceinline__ uint32_t absmax_bf16x2(const uint4 (&a)[kTcBK / 8]) {
+    uint32_t m = 0u;  // packed bf16 magnitudes: sign bits cleared, then pair maxima
+#pragma unroll
+    for (int c = 0; c < kTcBK / 8; ++c) {
+        m = max_bf16x2(m, max_bf16x2(a[c].x & 0x7FFF7FFFu, a[c].y & 0x7FFF7FFFu));
+        m = max_bf16x2(m, max_bf16x2(a[c].z & 0x7FFF7FFFu, a[c].w & 0x7FFF7FFFu));
+    }
+    return m;
+}
+// 128 bf16 (two k-blocks' eight 16-byte chunks each, in element order) to
+// e4m3: scale = amax / 448, codes = e4m3(x * (448 / amax)) rounded to
+// nearest even and saturated (cvt.rn.satfinite), the divisions and the
+// product in fp32; a block of zeros gets scale 0 and zero codes. m: the
+// packed maxima of both halves (absmax_bf16x2). Writes 128 code bytes
+// (8-byte aligned) and the scale.
+__device__ __forceinline__ void quant_block_e4m3(const uint4 (&a)[kTcBK / 8], const uint4 (&b)[kTcBK / 8],
+                                                 uint32_t m, uint8_t *q, float *scale) {
+    const float amax = fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+    if (amax == 0.0f) {  // zero codes (also for -0 elements) and scale 0
+#pragma unroll
+        for (int i = 0; i < 8; ++i) reinterpret_cast<uint4 *>(q)[i] = make_uint4(0u, 0u, 0u, 0u);
+        *scale = 0.0f;
+        return;
+    }
+    const float inv = 448.0f / amax;
+    *scale = amax / 448.0f;
+    // one 8-element chunk at a time (8 codes, one 8-byte store), so that few
+    // products are live at once
+#pragma unroll
+    for (int c = 0; c < 2 * (kTcBK / 8); ++c) {
+        const uint4 v = c < kTcBK / 8 ? a[c] : b[c - kTcBK / 8];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t code[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint16_t lo, hi;
+            asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo)
+                         : "f"(__uint_as_float(w[2 * h] & 0xFFFF0000u) * inv), "f"(__uint_as_float(w[2 * h] << 16) * inv));
+            asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi)
+                         : "f"(__uint_as_float(w[2 * h + 1] & 0xFFFF0000u) * inv),
+                           "f"(__uint_as_float(w[2 * h + 1] << 16) * inv));
+            code[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        reinterpret_cast<uint2 *>(q)[c] = make_uint2(code[0], code[1]);
+    }
+}
+
 // Optional logits output: the row's rounded logits from shared memory.
 __device__ __noinline__ void copy_row_out(uint32_t drow, uint16_t *dst, int ng) {
     for (int g = 0; g < ng; ++g) reinterpret_cast<uint4 *>(dst)[g] = ld_shared_v4(drow + (uint32_t)(g * 16));
@@ -320,7 +371,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&mma_done[s]), 1);  // the MMA commit (multicast to both CTAs)
-            mbar_init(smem_u32(&empty[s]), 4);     // the 4 shared-logit warps
+            mbar_init(smem_u32(&empty[s]), 4);     // the 4 side warps (shared logit, e4m3 x)
         }
         mbar_init(smem_u32(accum), 1);
         mbar_init(smem_u32(half_done), 4);
@@ -353,6 +404,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    const bool side = p.S || p.xq != nullptr;  // warps 4-7 read every stage's x tile
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int hf = warp >> 2; // column half this warp takes in the epilogue
     const int row = q * 32 + lane;
@@ -389,7 +441,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (kb >= pre) {
                     // a stage is refilled once the MMAs (and, with a shared
                     // gate, the shared-logit warps) are done with it
-                    if (!mbar_wait_bounded(smem_u32(p.S ? &empty[s] : &mma_done[s]), ph ^ 1u, abort_flag)) break;
+                    if (!mbar_wait_bounded(smem_u32(side ? &empty[s] : &mma_done[s]), ph ^ 1u, abort_flag)) break;
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * p.stage_bytes);
                 }
                 tma_load_2d_pair(a_dst, &tm_x, kb * kTcBK, m_load, fb);
@@ -433,14 +485,22 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc_commit_pair(smem_u32(accum), pair_mask);
         }
         __syncwarp();
-    } else if (hf == 1 && p.S) {
-        // ------- shared-expert logit, warps 4-7, from each stage's x tile ---
+    } else if (hf == 1 && side) {
+        // ---- side warps 4-7: shared-expert logit and e4m3 hidden states ----
         // once the MMAs are done with a stage (their commit reaches both
         // CTAs) its x tile is still in place: thread = token row reads the
         // row's 64 elements of the k-block (eight 16-byte chunks, 128-byte
-        // swizzle: chunk c sits at c ^ (row & 7)), fp32 dot per k-block,
-        // compensated sum across k-blocks; each warp then releases the stage
+        // swizzle: chunk c sits at c ^ (row & 7)); then
+        //  - shared logit: fp32 dot per k-block, compensated sum across them;
+        //  - e4m3: the even k-block's elements wait in registers for the odd
+        //    one; the 128-element block's largest magnitude gives its scale
+        //    amax / 448 and the codes e4m3(x * (448 / amax)), stored with
+        //    16-byte stores ("Netra Kernel ...", Fusing the activation/
+        //    quantization boundary: E4M3 with one scale per 128 values);
+        // each warp then releases the stage
         const uint32_t swz = (uint32_t)(row & 7);
+        uint4 prev[kTcBK / 8];  // the even k-block's chunks (e4m3 only)
+        uint32_t prev_max = 0u; // and their largest magnitudes (packed bf16 pair)
         for (int kb = 0; kb < p.num_kb; ++kb) {
             const int s = kb % ST;
             const uint32_t ph = (uint32_t)(kb / ST) & 1u;
@@ -449,17 +509,37 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 break;
             }
             const uint8_t *xrow = smem + (size_t)s * p.stage_bytes + (size_t)row * kTcSW;
-            const uint4 *wsv = reinterpret_cast<const uint4 *>(ws_s) + kb * (kTcBK / 8);
-            float part = 0.0f;
+            uint4 xv[kTcBK / 8];
 #pragma unroll
-            for (int c = 0; c < kTcBK / 8; ++c) {
-                float xf[8], wf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(xrow + ((c ^ swz) << 4)), xf);
-                unpack8(wsv[c], wf);
+            for (int c = 0; c < kTcBK / 8; ++c) xv[c] = *reinterpret_cast<const uint4 *>(xrow + ((c ^ swz) << 4));
+            // every loaded value is used below before the stage is released
+            // (a release issued while shared-memory loads are still in flight
+            // may let the next TMA write overtake them)
+            if (p.S) {
+                const uint4 *wsv = reinterpret_cast<const uint4 *>(ws_s) + kb * (kTcBK / 8);
+                float part = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
+                for (int c = 0; c < kTcBK / 8; ++c) {
+                    float xf[8], wf[8];
+                    unpack8(xv[c], xf);
+                    unpack8(wsv[c], wf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
+                }
+                two_sum_acc(s_hi, s_lo, part);
             }
-            two_sum_acc(s_hi, s_lo, part);
+            if (p.xq != nullptr) {
+                const uint32_t m = absmax_bf16x2(xv);
+                if ((kb & 1) == 0) {
+#pragma unroll
+                    for (int c = 0; c < kTcBK / 8; ++c) prev[c] = xv[c];
+                    prev_max = m;
+                } else if (valid) {
+                    quant_block_e4m3(prev, xv, max_bf16x2(prev_max, m),
+                                     p.xq + (int64_t)grow * p.H + (kb >> 1) * 128,
+                                     p.xs + (int64_t)grow * (p.H >> 7) + (kb >> 1));
+                }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
@@ -893,6 +973,8 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     p.logits_ws = a.logits_ws;
     p.ld_logits = a.ld_logits;
     p.s_out = a.s_out;
+    p.xq = a.xq;
+    p.xs = a.xs;
     p.scale = a.scale;
     p.renorm = a.renorm;
     p.shared_bf16 = a.shared_bf16;

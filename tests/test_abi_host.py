@@ -39,9 +39,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_struct_layouts_match_header(lib):
     # field order and sizes as declared in include/smr.h (LP64)
-    assert ctypes.sizeof(RouteArgs) == 7 * 4 + 4 + 8 * 8 + 8  # + shared_logit_bf16 (padded)
+    assert ctypes.sizeof(RouteArgs) == 7 * 4 + 4 + 8 * 8 + 8 + 2 * 8  # + shared_logit_bf16, e4m3 outputs
     assert RouteArgs.hidden.offset == 32
-    assert RouteArgs.shared_logit_bf16.offset == 96
+    assert RouteArgs.shared_logit_bf16.offset == 96 and RouteArgs.hidden_fp8.offset == 104
     assert ctypes.sizeof(AlignArgs) == 8 + 6 * 4 + 5 * 8 + 2 * 8 + 2 * 4
     assert AlignArgs.sorted_token_ids.offset == 32
     assert AlignArgs.eplb_map.offset == 72 and AlignArgs.num_physical.offset == 92
@@ -234,6 +234,11 @@ def _set(obj, **kw):
     (dict(topk_weights=0x50002), _lib.SMR_ERR_INVALID_ARG, "topk_weights must be 4-byte aligned"),
     (dict(logits_out=0x70008), _lib.SMR_ERR_INVALID_ARG, "logits_out must be 16-byte aligned"),
     (dict(renormalize=5), _lib.SMR_ERR_INVALID_ARG, "renormalize must be 0 or 1"),
+    (dict(hidden_fp8=0x80000), _lib.SMR_ERR_INVALID_ARG, "hidden_scales is NULL"),
+    (dict(hidden_fp8=0x80008, hidden_scales=0x90000), _lib.SMR_ERR_INVALID_ARG,
+     "hidden_fp8 must be 16-byte aligned"),
+    (dict(H=4104, ld_hidden=4104, hidden_fp8=0x80000, hidden_scales=0x90000),
+     _lib.SMR_ERR_INVALID_ARG, "hidden_fp8 needs H % 128 == 0"),
 ])
 def test_route_refuses_each_bad_argument(lib, change, status, fragment):
     """Every malformed route argument is refused before any launch, with its
