@@ -5,8 +5,9 @@
 // Modifications, for the guarded single launch; "[ROCm][Kernel] W4A16 MoE
 // prefill: M-aware moe_align block size", Purpose, for the alignment tier):
 //   route_align, M <= 16 : 1 launch  (small route + fused align)
-//   route_align, M > 16  : 1 tcgen05 route launch (which also counts the experts of
-//                          its rows when the align is multi-CTA) + 1 or 2 align launches;
+//   route_align, M > 16  : 1 tcgen05 route launch whose last CTA aligns all ids when
+//                          they fit one align CTA (<= 8192), else the route (which then
+//                          counts the experts of its rows) + 2 align launches;
 //                          with E > 512 or E % 32 != 0: ceil(E / 512) logits-only
 //                          tcgen05 launches + 1 select launch + 1 or 3 align launches
 //   route        : 1 launch;  align : 1 launch (numel <= 8192) or 3.
@@ -364,6 +365,14 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
     L.tile_counts = tile_counts;
     L.xq = a->hidden_fp8;
     L.xs = a->hidden_scales;
+    if (fused_align) {  // the ids fit one align CTA: the route's last CTA aligns them
+        L.fa_A = effective_block_size(fused_align);
+        L.fa_sorted = fused_align->sorted_token_ids;
+        L.fa_eids = fused_align->expert_ids;
+        L.fa_npp = fused_align->num_tokens_post_padded;
+        L.fa_sorted_cap = fused_align->sorted_cap;
+        L.fa_eids_cap = fused_align->expert_cap;
+    }
     const smr::StallHook hook = smr::stall_hook();
     L.stall = hook.site == smr::kStallTcMerge;
     L.stall_limit = L.stall ? hook.limit : 0;
@@ -483,6 +492,13 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     if (route->M >= 1 && route->M <= smr::kSmallMaxM && !has_eplb(&al)) {
+        st = run_route(route, workspace, s, &al, &launches);
+        if (st == SMR_OK) g_last_launches = launches;
+        return st;
+    }
+    if (route->M > 0 && (int64_t)route->M * al.width <= smr::kAlignSingleMax && !has_eplb(&al) &&
+        !generic_route(route)) {
+        // mid M: one launch, the align fused into the route's last CTA
         st = run_route(route, workspace, s, &al, &launches);
         if (st == SMR_OK) g_last_launches = launches;
         return st;

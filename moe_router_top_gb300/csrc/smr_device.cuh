@@ -21,13 +21,15 @@ constexpr uint32_t kErrWaitTimeout = 2u;  // a bounded wait gave up
 constexpr uint32_t kErrBadSlot = 4u;      // an align output position fell outside its array (skipped)
 
 // First 256 bytes of every workspace. Zeroed once by the caller; afterwards
-// only the error word (set on errors, cleared by the caller) and the small
-// route's call tag (advanced by every small-M call) change.
+// only the error word (set on errors, cleared by the caller), the small
+// route's call tag (advanced by every small-M call) and the fused align's
+// ticket (back at zero after every call) change.
 struct WsHeader {
     uint32_t unused;  // zero
     uint32_t error;   // sticky error bits (kErr*)
     uint32_t epoch;   // small route: tag of the last completed call (top bit set once used)
-    uint32_t reserved[61];
+    uint32_t ticket;  // tcgen05 route with the align fused: CTAs done (back to 0 at the end)
+    uint32_t reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -85,6 +85,10 @@ struct TcParams {
     float *s_out;          // logits-only: [M] shared logit
     uint8_t *xq;           // optional: hidden states as e4m3 codes [M][H]
     float *xs;             // and their scales [M][H / 128]
+    int fa_A;              // optional fused align (fa_sorted != nullptr), see TcRouteLaunch
+    int32_t *fa_sorted, *fa_eids, *fa_npp;
+    int64_t fa_sorted_cap, fa_eids_cap;
+    uint32_t *ticket;      // the workspace header's ticket
     int num_kb, stages, n_pieces, piece_n;  // gate pieces of piece_n <= 256 columns
     uint32_t tmem_cols, stage_bytes, misc_off, misc_bias_off, misc_ws_off, misc_hist_off, misc_den_off;
 };
@@ -335,6 +339,39 @@ __device__ __forceinline__ void quant_block_e4m3(const uint4 (&a)[kTcBK / 8], co
     }
 }
 
+// The align fused into the route when the M * (k + S) ids fit one align CTA
+// ("[ROCm][Kernel] W4A16 MoE prefill: M-aware moe_align block size",
+// Purpose; the shared expert is expert E, appended to the sorted route stream
+// as "Netra Kernel ...", Reusing routing work instead of recomputing it, does
+// without a separate launch). Every thread publishes its id stores, one
+// thread per CTA takes a ticket; the last CTA to finish stages all the ids
+// from L2 into its idle stage ring and runs the single-CTA align there, then
+// sets the ticket back to zero for the next call (whose route writes nothing
+// before this grid has completed).
+// s_last: a word of shared memory (kept out of static shared memory, so that
+// the kernel's dynamic allocation can take the whole opt-in limit).
+__device__ __noinline__ void fused_align_tail(const TcParams &p, uint8_t *smem, volatile int *s_last) {
+    __threadfence();  // this thread's ids are visible device-wide before the ticket
+    __syncthreads();
+    if (threadIdx.x == 0) *s_last = atomicAdd(p.ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();  // the other CTAs' ids, published before their tickets
+    const int numel = p.M * p.width, E_al = p.E + p.S;
+    int *ids = reinterpret_cast<int *>(smem);
+    AlignSmem s = align_carve(ids + kAlignSingleMax, E_al);
+    stage_ids(ids, p.ids, numel);
+    align_count(ids, numel, E_al, s, p.err);
+    const int npp = align_offsets(s.cnt, E_al, p.fa_A, s);
+    align_scatter(ids, numel, E_al, 0, s, false, p.fa_sorted, p.fa_sorted_cap, p.err);
+    align_fill(p.fa_A, E_al, s.cnt, s, numel, p.fa_sorted, p.fa_sorted_cap, p.fa_eids, p.fa_eids_cap, p.err,
+               threadIdx.x, blockDim.x);
+    if (threadIdx.x == 0) {
+        *p.fa_npp = npp;
+        *p.ticket = 0u;
+    }
+}
+
 // Optional logits output: the row's rounded logits from shared memory.
 __device__ __noinline__ void copy_row_out(uint32_t drow, uint16_t *dst, int ng) {
     for (int g = 0; g < ng; ++g) reinterpret_cast<uint4 *>(dst)[g] = ld_shared_v4(drow + (uint32_t)(g * 16));
@@ -355,7 +392,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     uint64_t *accum = empty + ST;      // the pair MMAs of the whole K loop are done
     uint64_t *half_done = accum + 1;   // the 4 warps of column half 0 posted their top-k
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(half_done + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);  // then the fused align's flag
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
     int *hist = reinterpret_cast<int *>(misc + p.misc_hist_off);  // [2][E + S] counts of the CTA's two 64-row tiles
     uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
@@ -832,6 +869,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         tc_fence_after();
         tmem_dealloc_pair(tmem, p.tmem_cols);
     }
+    if constexpr (!LO) {
+        if (p.fa_sorted != nullptr) fused_align_tail(p, smem, abort_flag + 1);
+    }
 }
 
 // ------------------------------------------------------------------ host --
@@ -906,7 +946,7 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     int st = (int)(budget / p.stage_bytes);
     if (st > 6) st = 6;
     if (st < 2) return false;
-    static_assert(8 * (3 * 6 + 2) + 8 <= 256, "barriers fit the misc header");
+    static_assert(8 * (3 * 6 + 2) + 12 <= 256, "barriers, TMEM slot and two flags fit the misc header");
     // the epilogue (candidate lists, half 0's top-k, both halves' rounded
     // logits) reuses the stage ring; the misc block follows the larger one
     const size_t ring = (size_t)st * p.stage_bytes;
@@ -975,6 +1015,18 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     p.s_out = a.s_out;
     p.xq = a.xq;
     p.xs = a.xs;
+    p.fa_A = a.fa_A;
+    p.fa_sorted = a.fa_sorted;
+    p.fa_eids = a.fa_eids;
+    p.fa_npp = a.fa_npp;
+    p.fa_sorted_cap = a.fa_sorted_cap;
+    p.fa_eids_cap = a.fa_eids_cap;
+    p.ticket = &reinterpret_cast<WsHeader *>(a.hdr)->ticket;
+    // the fused align stages the ids and its arrays in the idle stage ring
+    if (a.fa_sorted != nullptr &&
+        (a.logits_only || (size_t)p.misc_off < (size_t)(kAlignSingleMax + align_smem_words(kTcThreads / 32,
+                                                                                             a.E + a.S)) * 4))
+        return cudaErrorNotSupported;
     p.scale = a.scale;
     p.renorm = a.renorm;
     p.shared_bf16 = a.shared_bf16;

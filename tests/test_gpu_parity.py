@@ -186,6 +186,28 @@ def test_generic_route_align(smr, M, H, E, k, S, zipf, launches):
     print(f"generic M={M} E={E}: {rep}")
 
 
+@pytest.mark.parametrize("M,E,k,S,A", [
+    (17, 64, 8, 1, 64),      # smallest tcgen05 batch
+    (128, 128, 8, 0, 0),     # the short prefill (tier: 64)
+    (744, 512, 10, 1, 128),  # 8184 slots: the most one align CTA takes
+    (1024, 128, 8, 0, 0),    # the skewed sweep's 1024 tokens
+])
+def test_mid_m_route_align_is_one_launch(smr, M, E, k, S, A):
+    """Mid M: the route's last CTA aligns all ids (the shared expert appended
+    as expert E), so route_align is one launch; three calls in a row on one
+    workspace each match the oracle and leave the ticket at zero."""
+    ri = inputs.make_route_inputs(M, 1024, E, k, S, seed=900 + M)
+    wsp = smr.Workspace()
+    Aeff = A if A > 0 else oracle.select_block_size(M, k, E)
+    for _ in range(3):
+        ids, wts, srt, eids, npp, _ = _route_align(smr, ri, A, with_logits=False, workspace=wsp)
+        assert smr.last_launch_count() == 1
+        check_route(ri, ids, wts, None)
+        check_align(ids, E + S, Aeff, srt, eids, npp)
+    assert int(wsp.buf[12:16].view(torch.int32).item()) == 0  # the ticket
+    assert smr.get_device_error(wsp) == 0
+
+
 @pytest.mark.parametrize("M,H,E,k,S,zipf", [
     (1000, 1024, 512, 10, 1, None),  # 11000 slots: the route counts 16 tiles, the last 40 rows
     (777, 512, 256, 12, 0, 1.1),     # odd CTA count (7 tiles in 4 pairs), ragged tile, bias
