@@ -527,8 +527,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_route_kernel(const Sma
         }
         // The gate weights are the layer's parameters; the hidden states may
         // come from the previous kernel in the stream: the first batch of gate
-        // loads is in flight before waiting for that kernel to complete.
+        // loads is in flight before waiting for that kernel to complete. The
+        // hidden states' lines are only prefetched into L2 before the wait (a
+        // hint, no value is read: L2 is coherent, and the loads after the wait
+        // go through L2), so that after it they are an L2 hit rather than a
+        // DRAM access queued behind the gate stream.
         if (!waited) {
+#pragma unroll
+            for (int j = 0; j < kMaxSlicesPerWarp; ++j) {
+                const int kc = min((s0 + j * kSmallWarps) * kSliceK + 8 * t, p.H - 8);
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(xa + kc));
+                if (NB > 1) asm volatile("prefetch.global.L2 [%0];" ::"l"(xb + kc));
+            }
             griddep_wait();
             waited = true;
         }
