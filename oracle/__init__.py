@@ -77,6 +77,8 @@ def _load():
             lib.oracle_e4m3_to_double.restype = f64
             lib.oracle_quant_fp8.argtypes = [i32, i32, P, i64, P, P]
             lib.oracle_quant_fp8.restype = None
+            lib.oracle_expert_gemm.argtypes = [i64, i32, i32, i32, P, P, i64, P, P, P]
+            lib.oracle_expert_gemm.restype = None
             _lib = lib
     return _lib
 
@@ -258,3 +260,22 @@ def quant_fp8(x: np.ndarray):
     sc = np.empty((M, H // 128), dtype=np.float32)
     _load().oracle_quant_fp8(M, H, _ptr(x), H, _ptr(q), _ptr(sc))
     return q, sc
+
+
+# --- consumer expert GEMM -------------------------------------------------------
+
+def expert_gemm(x: np.ndarray, ids: np.ndarray, w: np.ndarray):
+    """Exact per-slot expert products out[t*width+s] = x[t] . W[ids[t,s]]^T
+    (fp64, [numel, N]) and sum|x*W| of each, for bf16-bit x [T, H], ids
+    [T, width] and W [E, N, H]."""
+    x = _c(x, np.uint16)
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    w = _c(w, np.uint16)
+    T, H = x.shape
+    width = ids.shape[1]
+    E, N, _ = w.shape
+    numel = T * width
+    out = np.empty((numel, N), dtype=np.float64)
+    ad = np.empty((numel, N), dtype=np.float64)
+    _load().oracle_expert_gemm(numel, H, N, width, _ptr(ids), _ptr(x), H, _ptr(w), _ptr(out), _ptr(ad))
+    return out, ad

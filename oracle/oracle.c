@@ -427,3 +427,34 @@ ORACLE_API int oracle_align_eplb(const int32_t *ids, int64_t numel, int width, i
     free(phys);
     return rc;
 }
+
+/* ------------------------------------------------- consumer expert GEMM --- */
+
+/* The expert GEMM that consumes the align's output ("[ROCm][Kernel] W4A16
+ * MoE prefill: M-aware moe_align block size", Purpose: each block of A rows
+ * of sorted_token_ids runs the full K contraction against the weights of
+ * expert_ids[block]; blocks at or past num_tokens_post_padded return early),
+ * here with bf16 expert weights. Whatever the blocking, every routed slot
+ * i = t * width + s gets out[i][n] = sum_h x[t][h] * W[ids[i]][n][h], so the
+ * oracle is that plain definition per slot, in double, with absdot (optional)
+ * the sum of |x * W|. W is [num_experts][N][H]. */
+ORACLE_API void oracle_expert_gemm(int64_t numel, int H, int N, int width, const int32_t *ids,
+                                   const uint16_t *x, int64_t ld_x, const uint16_t *W, double *out,
+                                   double *absdot)
+{
+    for (int64_t i = 0; i < numel; ++i) {
+        const uint16_t *xt = x + (i / width) * ld_x;
+        const uint16_t *we = W + (int64_t)ids[i] * N * H;
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0, aacc = 0.0;
+            for (int h = 0; h < H; ++h) {
+                double p = oracle_bf16_to_double(xt[h]) * oracle_bf16_to_double(we[(int64_t)n * H + h]);
+                acc += p;
+                aacc += fabs(p);
+            }
+            out[i * N + n] = acc;
+            if (absdot) absdot[i * N + n] = aacc;
+        }
+    }
+}
+

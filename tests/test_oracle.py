@@ -570,3 +570,36 @@ def test_quant_fp8_closed_forms():
         step = np.where(np.abs(scaled) < 2.0 ** -6, 2.0 ** -9,
                         2.0 ** (np.floor(np.log2(np.maximum(np.abs(scaled), 1e-30))) - 3))
         assert np.all(np.abs(dec - scaled) <= step / 2 * (1 + 1e-6) + 1e-9)
+
+
+# ---------------------------------------------------- consumer expert GEMM ---
+
+def test_expert_gemm_matches_numpy_per_expert():
+    """Each slot's row equals x[token] @ W[expert].T (numpy fp64 matmul)."""
+    rng = np.random.default_rng(81)
+    T, width, E, N, H = 7, 3, 5, 16, 64
+    x = inputs.f32_to_bf16_bits(rng.normal(0, 1, (T, H)).astype(np.float32))
+    w = inputs.f32_to_bf16_bits(rng.normal(0, 0.05, (E, N, H)).astype(np.float32))
+    ids = inputs.random_ids(T, width, E, seed=82)
+    out, ad = oracle.expert_gemm(x, ids, w)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    wf = inputs.bf16_bits_to_f32(w).astype(np.float64)
+    ref = np.einsum("th,tsnh->tsn", xf, wf[ids]).reshape(T * width, N)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    aref = np.einsum("th,tsnh->tsn", np.abs(xf), np.abs(wf[ids])).reshape(T * width, N)
+    assert np.allclose(ad, aref, rtol=1e-12, atol=0)
+
+
+def test_expert_gemm_integer_inputs_exact():
+    """Integer entries: every product and sum is exact in double."""
+    rng = np.random.default_rng(83)
+    T, width, E, N, H = 5, 2, 3, 8, 128
+    x = inputs.f32_to_bf16_bits(rng.integers(-3, 4, (T, H)).astype(np.float32))
+    w = inputs.f32_to_bf16_bits(rng.integers(-3, 4, (E, N, H)).astype(np.float32))
+    ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1], [2, 0]], np.int32)
+    out, _ = oracle.expert_gemm(x, ids, w)
+    xi = inputs.bf16_bits_to_f32(x).astype(np.int64)
+    wi = inputs.bf16_bits_to_f32(w).astype(np.int64)
+    for t in range(T):
+        for s in range(width):
+            assert np.array_equal(out[t * width + s], (wi[ids[t, s]] @ xi[t]).astype(np.float64))

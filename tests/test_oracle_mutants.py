@@ -61,6 +61,11 @@ MUTANTS = [
     ("codes from the unscaled values",
      "float v = (float)(oracle_bf16_to_double(xb[i]) * (double)inv);",
      "float v = (float)(oracle_bf16_to_double(xb[i]));"),
+    ("expert GEMM reads the slot's expert from the wrong slot",
+     "const uint16_t *we = W + (int64_t)ids[i] * N * H;",
+     "const uint16_t *we = W + (int64_t)ids[i / width * width] * N * H;"),
+    ("expert GEMM weights read transposed",
+     "oracle_bf16_to_double(we[(int64_t)n * H + h]);", "oracle_bf16_to_double(we[(int64_t)h * N + n]);"),
     ("descending order inside an expert",
      "for (int64_t i = 0; i < numel; ++i) sorted[cur[ids[i]]++] = (int32_t)i;",
      "for (int64_t i = numel - 1; i >= 0; --i) sorted[cur[ids[i]]++] = (int32_t)i;"),
