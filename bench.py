@@ -429,6 +429,69 @@ def bench_small(torch, smr, inputs, M, l2_bytes, reps=20, calls=100):
             "bytes": bytes_moved, "launches": launches, "ring_copies": ncopies}
 
 
+def bench_consumer(torch, smr, inputs, N=1536, reps=10, calls=20):
+    """The M-aware tier end to end: route_align + the consumer expert GEMM
+    (bf16 experts [128, N, 2048], N = 1536 for a gate+up projection of 768)
+    on the skewed sweep's batches, at A = 64 and A = 128. The expert GEMM's
+    work follows npp (blocks at or past it return at once)."""
+    H_, E_, K_ = 2048, 128, 8
+    g = torch.Generator(device="cuda").manual_seed(7)
+    ew = (torch.randn((E_, N, H_), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    out_all = {}
+    for M in inputs.ZIPF_TOKENS[1:]:
+        ri = inputs.zipf_sweep(M)
+        x = to_dev_bf16(ri.x, torch)
+        w = to_dev_bf16(ri.w, torch)
+        b = torch.from_numpy(ri.bias).cuda()
+        row = {"tier_block_size": smr.select_block_size(M, K_, E_), "routed_rows": M * K_}
+        for A in (64, 128):
+            wsp = smr.Workspace()
+            ids, wts, srt, eids, npp = smr.route_align(x, w, None, b, topk=K_, block_size=A, workspace=wsp)
+            out = torch.empty((M * K_, N), dtype=torch.float32, device="cuda")
+
+            def step(gemm_only=False):
+                if not gemm_only:
+                    smr.route_align(x, w, None, b, topk=K_, block_size=A, topk_ids=ids, topk_weights=wts,
+                                    sorted_token_ids=srt, expert_ids=eids, num_tokens_post_padded=npp,
+                                    workspace=wsp)
+                smr.expert_gemm(x, ew, srt, eids, npp, width=K_, block_size=A, out=out, workspace=wsp)
+
+            def time_graph(gemm_only):
+                st = torch.cuda.Stream()
+                st.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(st):
+                    step(gemm_only)
+                torch.cuda.current_stream().wait_stream(st)
+                torch.cuda.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    for _ in range(calls):
+                        step(gemm_only)
+                gr.replay()
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(reps):
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    gr.replay()
+                    e.record()
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(e) * 1000.0 / calls)
+                return statistics.median(ts)
+
+            us_gemm = time_graph(True)
+            us_step = time_graph(False)
+            n = int(npp.item())
+            row[f"A{A}"] = {"npp": n, "padding_fraction": 1.0 - M * K_ / n,
+                            "us_route_align_plus_expert_gemm": us_step, "us_expert_gemm": us_gemm,
+                            "expert_gemm_useful_tflops": 2.0 * M * K_ * N * H_ / (us_gemm * 1e-6) / 1e12,
+                            "expert_gemm_done_tflops": 2.0 * n * N * H_ / (us_gemm * 1e-6) / 1e12}
+            assert smr.get_device_error(wsp) == 0
+        out_all[f"M{M}"] = row
+    return {"workload": f"skewed sweep (H=2048, E=128, top-8, Zipf 1.1 bias), expert GEMM N={N} bf16",
+            "timing": f"CUDA graph of {calls} steps, median of {reps} replays", "by_tokens": out_all}
+
+
 def cpu_baseline_large():
     """The C oracle on the large batch: all 16384 rows split over every host
     core (median of 3 runs), and single-threaded on the first
@@ -550,6 +613,8 @@ def run_smr(args):
             if not args.no_cpu:
                 small[f"M{M}"]["cpu_baseline"] = cpu_baseline_small(M)
         line["small_m"] = small
+    if rank == 0 and not args.no_consumer:
+        line["consumer_tier"] = bench_consumer(torch, smr, inputs)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline_large()
     if rank == 0:
@@ -642,6 +707,8 @@ def main():
     ap.add_argument("--impl", choices=("smr", "reference"), default="smr")
     ap.add_argument("--no-small", action="store_true", help="skip the M=4/8 small-batch timings")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-consumer", action="store_true",
+                    help="skip the route_align + expert GEMM timings at both block sizes")
     ap.add_argument("--no-large", action="store_true",
                     help="only the M=4/8 small-batch timings (prints a partial line)")
     ap.add_argument("--profile-m", type=int, default=0,

@@ -147,6 +147,25 @@ typedef struct smr_align_args {
     int32_t num_physical;         /* 1..1025 */
 } smr_align_args;
 
+/* The consumer of the align: the expert GEMM. */
+typedef struct smr_expert_gemm_args {
+    const void *hidden;            /* bf16 [num_tokens, ld_hidden], 16-byte aligned */
+    int64_t ld_hidden;             /* row stride in elements, >= H, multiple of 8 */
+    int32_t num_tokens;            /* T >= 0 */
+    int32_t width;                 /* slots per token (the align's width), >= 1 */
+    int32_t H;                     /* hidden size, multiple of 64, <= 16384 */
+    const void *expert_w;          /* bf16 [num_experts, N, H] (each expert's [N, H] rows), 16-byte aligned */
+    int32_t num_experts;           /* the align's num_experts (or num_physical), 1..1025 */
+    int32_t N;                     /* output columns per expert, multiple of 128, <= 16384 */
+    int32_t block_size;            /* A used by the align: 64 or 128 */
+    const int32_t *sorted_token_ids;  /* the align's outputs (device) */
+    int64_t sorted_cap;            /* its length: the grid covers ceil(sorted_cap / A) blocks */
+    const int32_t *expert_ids;
+    const int32_t *num_tokens_post_padded;
+    float *out;                    /* out: fp32 [num_tokens * width, N], row = flat slot index
+                                      t * width + s; 16-byte aligned */
+} smr_expert_gemm_args;
+
 /* M-aware alignment tier (host, no device work): 64 if
  * num_tokens * topk < 128 * num_experts (fewer than one full 128-row block of
  * routed rows per expert), else 128. Returns -1 on non-positive topk or
@@ -217,6 +236,22 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
  *    SMR_ERR_UNSUPPORTED. Outputs are as for smr_route_align. */
 SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr_align_args *align,
                                           void *stream);
+
+/* The expert GEMM that consumes the align ("[ROCm][Kernel] W4A16 MoE
+ * prefill: M-aware moe_align block size (1.6x TTFT)", Purpose), with bf16
+ * expert weights: for every block b of A rows of sorted_token_ids with
+ * b * A < num_tokens_post_padded, the rows' hidden states (slot / width =
+ * token) against expert expert_ids[b]'s [N, H] weights; every routed slot i
+ * gets out[i] = hidden[i / width] . W[e]^T (fp32 accumulation and output).
+ * Padding rows are computed as zeros and not stored; blocks at or past npp
+ * return at once (the early exit whose work the M-aware tier shrinks).
+ * One launch of ceil(sorted_cap / A) x N / 256 (or 128) CTAs. The workspace
+ * (>= 256 bytes, zeroed once) only carries the sticky error word: bit 0 for
+ * an expert id out of range, bit 2 for a sorted entry that is neither a slot
+ * nor the sentinel (both from a corrupted align output), bit 1 for a wait
+ * that gave up (the block's outputs are then not written). */
+SMR_API smr_status smr_expert_gemm(const smr_expert_gemm_args *args, void *workspace, size_t workspace_bytes,
+                                   void *stream);
 
 /* Sticky device error word of a workspace: synchronises `stream`, then copies
  * the word to *code_out (0 = no error; bit 0 = an id out of range in align,

@@ -14,11 +14,11 @@ import os
 from typing import Optional, Tuple
 
 from . import _lib
-from ._lib import AlignArgs, RouteArgs
+from ._lib import AlignArgs, ExpertGemmArgs, RouteArgs
 
 __all__ = [
     "SmrError", "SmrUnsupported", "Workspace", "route", "align", "route_align",
-    "route_align_static",
+    "route_align_static", "expert_gemm",
     "select_block_size", "align_capacity", "route_workspace_size", "align_workspace_size",
     "route_align_workspace_size", "get_device_error", "clear_device_error",
     "get_static_device_error", "clear_static_device_error", "test_force_wait_timeout",
@@ -326,6 +326,38 @@ def route_align_static(hidden, gate_w, shared_w=None, bias=None, *, topk: int,
     aa = _align_args(topk_ids, M, topk + S, E + S, block_size, topk, E, *outs)
     _check(lib.smr_route_align_static(ctypes.byref(ra), ctypes.byref(aa), _stream_ptr(stream)))
     return (topk_ids, topk_weights) + tuple(outs)
+
+
+def expert_gemm(hidden, expert_w, sorted_token_ids, expert_ids, num_tokens_post_padded, *,
+                width: int, block_size: int, out=None, workspace=None, stream=None):
+    """The consumer expert GEMM over the align's outputs: returns out fp32
+    [num_tokens * width, N], row t * width + s = hidden[t] . W[e]^T for the
+    slot's expert e (expert_w bf16 [num_experts, N, H]); blocks at or past
+    num_tokens_post_padded do no work."""
+    _disabled()
+    torch = _torch()
+    lib = _lib.load()
+    if hidden.dtype != torch.bfloat16 or hidden.dim() != 2 or hidden.stride(1) != 1:
+        raise ValueError("hidden must be a bfloat16 [T, H] tensor with unit stride along H")
+    if expert_w.dtype != torch.bfloat16 or expert_w.dim() != 3 or not expert_w.is_contiguous():
+        raise ValueError("expert_w must be a contiguous bfloat16 [num_experts, N, H] tensor")
+    T, H = hidden.shape
+    E, N, H2 = expert_w.shape
+    if H2 != H:
+        raise ValueError("expert_w's last dimension must be H")
+    if out is None:
+        out = torch.empty((T * width, N), dtype=torch.float32, device=hidden.device)
+    a = ExpertGemmArgs()
+    a.hidden, a.ld_hidden = _ptr(hidden), (hidden.stride(0) if T > 1 else H)
+    a.num_tokens, a.width, a.H = T, int(width), H
+    a.expert_w, a.num_experts, a.N = _ptr(expert_w), E, N
+    a.block_size = int(block_size)
+    a.sorted_token_ids, a.sorted_cap = _ptr(sorted_token_ids), sorted_token_ids.numel()
+    a.expert_ids, a.num_tokens_post_padded = _ptr(expert_ids), _ptr(num_tokens_post_padded)
+    a.out = _ptr(out)
+    wp, wn = _workspace(workspace, 256, hidden.device)
+    _check(lib.smr_expert_gemm(ctypes.byref(a), wp, wn, _stream_ptr(stream)))
+    return out
 
 
 def select_block_size(num_tokens: int, topk: int, num_experts: int) -> int:

@@ -27,6 +27,7 @@ EXPORTED = (
     "smr_route_align", "smr_get_device_error", "smr_clear_device_error", "smr_status_string",
     "smr_last_error", "smr_version", "smr_last_launch_count", "smr_route_align_static",
     "smr_get_static_device_error", "smr_clear_static_device_error", "smr_test_force_wait_timeout",
+    "smr_expert_gemm",
 )
 
 SMR_STALL_NONE = 0
@@ -58,6 +59,17 @@ class AlignArgs(ctypes.Structure):
         ("expert_cap", ctypes.c_int64), ("num_tokens_post_padded", ctypes.c_void_p),
         ("eplb_map", ctypes.c_void_p), ("eplb_count", ctypes.c_void_p),
         ("eplb_max_replicas", ctypes.c_int32), ("num_physical", ctypes.c_int32),
+    ]
+
+
+class ExpertGemmArgs(ctypes.Structure):
+    _fields_ = [
+        ("hidden", ctypes.c_void_p), ("ld_hidden", ctypes.c_int64),
+        ("num_tokens", ctypes.c_int32), ("width", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("expert_w", ctypes.c_void_p), ("num_experts", ctypes.c_int32), ("N", ctypes.c_int32),
+        ("block_size", ctypes.c_int32), ("sorted_token_ids", ctypes.c_void_p),
+        ("sorted_cap", ctypes.c_int64), ("expert_ids", ctypes.c_void_p),
+        ("num_tokens_post_padded", ctypes.c_void_p), ("out", ctypes.c_void_p),
     ]
 
 
@@ -96,6 +108,7 @@ def load(path: str = LIB_PATH):
             "smr_get_static_device_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
             "smr_clear_static_device_error": ([P], ctypes.c_int),
             "smr_test_force_wait_timeout": ([i32, i64], ctypes.c_int),
+            "smr_expert_gemm": ([ctypes.POINTER(ExpertGemmArgs), P, sz, P], ctypes.c_int),
         }
         for name, (argtypes, restype) in sigs.items():
             fn = getattr(lib, name)

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsmr.so")
-SOURCES = ["smr_api.cpp", "smr_small.cu", "smr_align.cu", "smr_tc.cu", "smr_select.cu"]
+SOURCES = ["smr_api.cpp", "smr_small.cu", "smr_align.cu", "smr_tc.cu", "smr_select.cu", "smr_expert.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("smr_device.cuh", "smr_launch.h")] + [
     os.path.join(INCLUDE, "smr.h")]
 

@@ -559,6 +559,62 @@ SMR_API smr_status smr_route_align_static(const smr_route_args *route, const smr
     return st;
 }
 
+SMR_API smr_status smr_expert_gemm(const smr_expert_gemm_args *a, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    g_last_launches = 0;
+    if (!a) {
+        g_last_error = "smr_expert_gemm: args is NULL";
+        return SMR_ERR_INVALID_ARG;
+    }
+    Reasons r;
+    if (a->num_tokens < 0) r.bad("num_tokens must be >= 0");
+    if (a->width < 1) r.bad("width must be >= 1");
+    if (a->H < 64 || a->H > kMaxH || a->H % 64 != 0)
+        r.bad("H must be a multiple of 64 in [64, 16384] (got " + std::to_string(a->H) + ")");
+    if (a->N < 128 || a->N > kMaxH || a->N % 128 != 0)
+        r.bad("N must be a multiple of 128 in [128, 16384] (got " + std::to_string(a->N) + ")");
+    if (a->num_experts < 1 || a->num_experts > kMaxExperts + 1)
+        r.bad("num_experts must be in [1, 1025] (got " + std::to_string(a->num_experts) + ")");
+    if (a->block_size != 64 && a->block_size != 128)
+        r.unsup("block_size must be 64 or 128 (the MMA's rows; got " + std::to_string(a->block_size) + ")");
+    const int64_t numel = (int64_t)a->num_tokens * a->width;
+    if (numel > 0) {
+        if (!a->hidden || !aligned(a->hidden, 16)) r.bad("hidden must be a 16-byte aligned pointer");
+        if (a->ld_hidden < a->H || a->ld_hidden % 8 != 0) r.bad("ld_hidden must be >= H and a multiple of 8");
+        if (!a->expert_w || !aligned(a->expert_w, 16)) r.bad("expert_w must be a 16-byte aligned pointer");
+        if (!a->sorted_token_ids || !a->expert_ids || !a->num_tokens_post_padded)
+            r.bad("sorted_token_ids, expert_ids and num_tokens_post_padded must be set");
+        if (!a->out || !aligned(a->out, 16)) r.bad("out must be a 16-byte aligned pointer");
+        if (a->sorted_cap < 1) r.bad("sorted_cap must be >= 1");
+        if (numel * (int64_t)a->N > ((int64_t)1 << 40)) r.unsup("num_tokens * width * N too large");
+    }
+    if (!r.ok()) return r.finish("smr_expert_gemm");
+    if (numel == 0) return SMR_OK;
+    smr_status st = check_ws(workspace, workspace_bytes, kHeaderBytes, "smr_expert_gemm");
+    if (st != SMR_OK) return st;
+    if ((st = check_device()) != SMR_OK) return st;
+    smr::ExpertGemmLaunch L{};
+    L.x = static_cast<const uint16_t *>(a->hidden);
+    L.ld = a->ld_hidden;
+    L.width = a->width;
+    L.H = a->H;
+    L.N = a->N;
+    L.A = a->block_size;
+    L.num_experts = a->num_experts;
+    L.numel = numel;
+    L.max_blocks = (a->sorted_cap + a->block_size - 1) / a->block_size;
+    L.w = static_cast<const uint16_t *>(a->expert_w);
+    L.sorted = a->sorted_token_ids;
+    L.eids = a->expert_ids;
+    L.npp = a->num_tokens_post_padded;
+    L.out = a->out;
+    L.hdr = workspace;
+    cudaError_t e = smr::launch_expert_gemm(L, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("expert GEMM launch", e);
+    g_last_launches = 1;
+    return SMR_OK;
+}
+
 SMR_API smr_status smr_get_device_error(const void *workspace, void *stream, int32_t *code_out) {
     if (!workspace || !code_out) {
         g_last_error = "smr_get_device_error: workspace or code_out is NULL";

@@ -2,6 +2,7 @@
 // (smr_api.cpp) and the kernel translation units. Host-only types.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -152,6 +153,26 @@ struct SelectLaunch {
     uint16_t *logits_out;    // optional [M][E]
 };
 cudaError_t launch_select(const SelectLaunch &a, cudaStream_t stream);
+// A 2-D bf16 tensor map with the 128-byte swizzle (rows of row_bytes; boxes
+// of box_inner x box_outer elements); false if it cannot be encoded.
+bool make_tma_map_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// The consumer expert GEMM over the align's output: for every block b of A
+// rows of sorted_token_ids below num_tokens_post_padded, expert
+// expert_ids[b]'s [N, H] weights against the gathered hidden-state rows;
+// out[slot][N] fp32 for every routed slot (padding rows are not written).
+struct ExpertGemmLaunch {
+    const uint16_t *x;
+    int64_t ld;
+    int width, H, N, A, num_experts;
+    int64_t numel, max_blocks;
+    const uint16_t *w;       // [num_experts][N][H]
+    const int32_t *sorted, *eids, *npp;
+    float *out;
+    void *hdr;               // workspace header (sticky error word)
+};
+cudaError_t launch_expert_gemm(const ExpertGemmLaunch &a, cudaStream_t stream);
 
 // moe_align_block_size.
 struct AlignLaunch {

@@ -891,7 +891,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
+bool make_tma_map_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -1042,9 +1042,9 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     p.stall = a.stall;
     p.stall_limit = a.stall_limit > 0 ? a.stall_limit : kWaitCycles;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, a.x, (uint64_t)a.H, (uint64_t)a.M, (uint64_t)a.ld * 2, kTcBK, kTcBM))
+    if (!make_tma_map_2d(&mx, a.x, (uint64_t)a.H, (uint64_t)a.M, (uint64_t)a.ld * 2, kTcBK, kTcBM))
         return cudaErrorInvalidValue;
-    if (!make_map(&mw, a.w, (uint64_t)a.H, (uint64_t)a.E, (uint64_t)a.H * 2, kTcBK,
+    if (!make_tma_map_2d(&mw, a.w, (uint64_t)a.H, (uint64_t)a.E, (uint64_t)a.H * 2, kTcBK,
                   (uint32_t)(p.piece_n / 2)))
         return cudaErrorInvalidValue;
     // 32-column TMEM chunks when each column half is a multiple of 32, else 16
