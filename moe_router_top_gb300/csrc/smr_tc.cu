@@ -377,7 +377,7 @@ __device__ __noinline__ void copy_row_out(uint32_t drow, uint16_t *dst, int ng) 
     for (int g = 0; g < ng; ++g) reinterpret_cast<uint4 *>(dst)[g] = ld_shared_v4(drow + (uint32_t)(g * 16));
 }
 
-template <int CW, bool LO>
+template <int CW, bool LO, bool XQ>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const TcParams p) {
@@ -441,7 +441,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const bool side = p.S || p.xq != nullptr;  // warps 4-7 read every stage's x tile
+    const bool side = p.S || XQ;  // warps 4-7 read every stage's x tile
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int hf = warp >> 2; // column half this warp takes in the epilogue
     const int row = q * 32 + lane;
@@ -565,7 +565,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 two_sum_acc(s_hi, s_lo, part);
             }
-            if (p.xq != nullptr) {
+            if constexpr (XQ) {
                 const uint32_t m = absmax_bf16x2(xv);
                 if ((kb & 1) == 0) {
 #pragma unroll
@@ -967,16 +967,16 @@ bool tc_route_supported(int H, int E, int k, int S) {
     return plan_tc(1, H, E, k, S, &plan);
 }
 
-template <int CW, bool LO>
+template <int CW, bool LO, bool XQ>
 static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const TcPlan &plan,
                              cudaStream_t stream) {
     static std::atomic<bool> configured[kMaxDevices];
     cudaError_t e = once_per_device(configured, [](int) {
-        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<CW, LO>,
+        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<CW, LO, XQ>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kTcSmemLimit);
         if (r == cudaSuccess)  // the same carveout as every other kernel of the library
-            r = cudaFuncSetAttribute(tc_route_kernel<CW, LO>,
+            r = cudaFuncSetAttribute(tc_route_kernel<CW, LO, XQ>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         return r;
@@ -998,7 +998,7 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_route_kernel<CW, LO>, mx, mw, plan.p);
+    return cudaLaunchKernelEx(&cfg, tc_route_kernel<CW, LO, XQ>, mx, mw, plan.p);
 }
 
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
@@ -1049,9 +1049,16 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     // 32-column TMEM chunks when each column half is a multiple of 32, else 16
     const bool wide = (E_pad / 2) % 32 == 0;
+    // the e4m3 hidden states are a separate instantiation, so that a route
+    // without them keeps the plain kernel's registers and code
+    if (a.xq != nullptr) {
+        if (a.logits_only)
+            return wide ? launch_ng<32, true, true>(mx, mw, plan, stream) : launch_ng<16, true, true>(mx, mw, plan, stream);
+        return wide ? launch_ng<32, false, true>(mx, mw, plan, stream) : launch_ng<16, false, true>(mx, mw, plan, stream);
+    }
     if (a.logits_only)
-        return wide ? launch_ng<32, true>(mx, mw, plan, stream) : launch_ng<16, true>(mx, mw, plan, stream);
-    return wide ? launch_ng<32, false>(mx, mw, plan, stream) : launch_ng<16, false>(mx, mw, plan, stream);
+        return wide ? launch_ng<32, true, false>(mx, mw, plan, stream) : launch_ng<16, true, false>(mx, mw, plan, stream);
+    return wide ? launch_ng<32, false, false>(mx, mw, plan, stream) : launch_ng<16, false, false>(mx, mw, plan, stream);
 }
 
 }  // namespace smr
