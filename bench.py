@@ -699,6 +699,28 @@ def run_profile(args):
     print(f"profile run: {args.steps} steps at M={args.profile_m}")
 
 
+def run_profile_expert(args):
+    """A few route_align + expert GEMM steps on the skewed sweep's shapes at
+    --profile-expert tokens (A = 128, N = 1536), for ncu captures."""
+    import torch
+    import moe_router_top_gb300 as smr
+    from moe_router_top_gb300 import build, inputs
+    build.build()
+    torch.cuda.set_device(0)
+    ri = inputs.zipf_sweep(args.profile_expert)
+    x, w = to_dev_bf16(ri.x, torch), to_dev_bf16(ri.w, torch)
+    b = torch.from_numpy(ri.bias).cuda()
+    g = torch.Generator(device="cuda").manual_seed(7)
+    ew = (torch.randn((128, 1536, 2048), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    wsp = smr.Workspace()
+    for _ in range(args.warmup + args.steps):
+        ids, wts, srt, eids, npp = smr.route_align(x, w, None, b, topk=8, block_size=128, workspace=wsp)
+        smr.expert_gemm(x, ew, srt, eids, npp, width=8, block_size=128, workspace=wsp)
+    torch.cuda.synchronize()
+    assert smr.get_device_error(wsp) == 0
+    print(f"profile run: {args.steps} steps of route_align + expert GEMM at M={args.profile_expert}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,10 +736,15 @@ def main():
     ap.add_argument("--profile-m", type=int, default=0,
                     help="profiling aid: run `--steps` route+align steps of the large-batch "
                          "shapes at this many tokens and exit (no JSON line)")
+    ap.add_argument("--profile-expert", type=int, default=0,
+                    help="profiling aid: route_align + expert GEMM steps on the skewed sweep's "
+                         "shapes at this many tokens, then exit (no JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.profile_m:
+    if args.profile_expert:
+        run_profile_expert(args)
+    elif args.profile_m:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)
