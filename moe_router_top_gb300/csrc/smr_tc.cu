@@ -507,10 +507,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc_fence_after();
                 const uint32_t a_base = smem_u32(smem + (size_t)s * p.stage_bytes);
                 const uint32_t b_base = a_base + kTcBM * kTcSW;
+                // piece-major: a piece's four K=16 steps back to back into its
+                // accumulator, then the next piece (alternating the two
+                // accumulators step by step ran the pair MMAs ~15% slower:
+                // 65.5 against 55.5 us per 16384-token launch)
+                for (int pc = 0; pc < p.n_pieces; ++pc) {
 #pragma unroll
-                for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                    const uint64_t adesc = smem_desc_sw<kTcSW>(a_base + kk * 32);
-                    for (int pc = 0; pc < p.n_pieces; ++pc) {
+                    for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                        const uint64_t adesc = smem_desc_sw<kTcSW>(a_base + kk * 32);
                         const uint64_t bdesc =
                             smem_desc_sw<kTcSW>(b_base + (uint32_t)pc * half * kTcSW + kk * 32);
                         tc_mma_bf16_pair(tmem + (uint32_t)(pc * p.piece_n), adesc, bdesc, idesc,
