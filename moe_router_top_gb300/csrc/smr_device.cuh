@@ -639,6 +639,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
     return excl;
 }
 
+// c rounded up to a multiple of A (c >= 0; a mask when A is a power of two).
+__device__ __forceinline__ int pad_to_blocks(int c, int A) {
+    return (A & (A - 1)) == 0 ? (c + A - 1) & -A : (c + A - 1) / A * A;
+}
+
 // Padded segment offsets from per-expert totals tot[]: off[e] = sum over
 // e' < e of ceil(tot[e']/A)*A; returns npp = off[E_al]. Each thread scans a
 // contiguous run of experts so the order of the sum is fixed.
@@ -646,13 +651,13 @@ __device__ __forceinline__ int align_offsets(const int *tot, int E_al, int A, co
     const int per = (E_al + blockDim.x - 1) / blockDim.x;
     const int e0 = threadIdx.x * per, e1 = min(e0 + per, E_al);
     int local = 0;
-    for (int e = e0; e < e1; ++e) local += (tot[e] + A - 1) / A * A;
+    for (int e = e0; e < e1; ++e) local += pad_to_blocks(tot[e], A);
     __syncwarp();
     int total;
     int run = block_exclusive_scan(local, s.scratch, &total);
     for (int e = e0; e < e1; ++e) {
         s.off[e] = run;
-        run += (tot[e] + A - 1) / A * A;
+        run += pad_to_blocks(tot[e], A);
     }
     if (threadIdx.x == 0) s.off[E_al] = total;
     __syncwarp();

@@ -803,7 +803,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const bool count = p.tile_counts != nullptr;
                 // both halves' lists are sorted descending: a pointer merge of k
                 // steps gives the row's top-k; the softmax numerators go to
-                // shared memory, the ids straight out
+                // shared memory, the ids straight out, and (for the align
+                // behind the route) each expert's count up by one -- a
+                // shared-memory reduction whose result nothing here waits for
                 int i = 0, j = 0;
                 float vmax = 0.0f, sum = 0.0f;
     #pragma unroll 1
@@ -819,6 +821,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     sum += ev;
                     numer[r * kTcBM + row] = ev;
                     orow[r] = key_id(m);
+                    if (count) atomicAdd(&h[key_id(m)], 1);
                 }
                 float den = sum;
                 if (!p.renorm) {  // both halves' denominators at the row's largest logit
@@ -828,19 +831,6 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const float inv = 1.0f / den;  // one division; each weight within 1.5 ulp of ev / den
     #pragma unroll 4
                 for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] * inv;
-                if (count) {
-                    // the row's experts, for the align behind the route: the top-k
-                    // are the first i entries of this half's list and the first j
-                    // of half 0's. All keys are loaded before the first atomic, so
-                    // the atomics issue back to back (off the merge's chain).
-                    uint32_t ks[kCandCap];
-    #pragma unroll
-                    for (int r = 0; r < kCandCap; ++r)
-                        ks[r] = (r < p.k) ? (r < i ? list[r * kTcBM + row] : list0[(r - i) * kTcBM + row]) : 0u;
-    #pragma unroll
-                    for (int r = 0; r < kCandCap; ++r)
-                        if (r < p.k) atomicAdd(&h[key_id(ks[r])], 1);
-                }
                 if (p.S) {  // (its count is the tile's number of rows, set below)
                     const float sh = s_hi + s_lo;
                     orow[p.k] = p.E;

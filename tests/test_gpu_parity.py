@@ -222,6 +222,45 @@ def test_route_align_counts_from_route(smr, M, H, E, k, S, zipf):
     assert smr.last_launch_count() == 3  # route + tile scan + tile scatter
 
 
+def test_counted_align_after_other_calls_on_one_workspace(smr):
+    """The counted align's tile arrays share the workspace with every other
+    call's scratch (the logit rows of the generic route, the small route's
+    tagged keys, the standalone align's tile arrays): any call sequence on one
+    workspace gives the oracle's results, and the header's ticket and error
+    word end at zero."""
+    wsp = smr.Workspace()
+    big = inputs.make_route_inputs(2049, 512, 256, 8, 1, seed=77)
+    x, w, ws, b = _dev(big)
+    ref = None
+    for step in range(3):
+        # something else writes where the group totals live
+        if step == 0:
+            gen = inputs.make_route_inputs(2049, 256, 1000, 8, 1, seed=78)  # generic: logit rows
+            gx, gw, gws, gb = _dev(gen)
+            smr.route_align(gx, gw, gws, gb, topk=8, block_size=64, workspace=wsp)
+        elif step == 1:
+            ids0 = torch.from_numpy(inputs.random_ids(3000, 9, 257, seed=5)).cuda()
+            smr.align(ids0, 257, 16, workspace=wsp)  # standalone multi-tile align
+        else:
+            sm = inputs.make_route_inputs(16, 1024, 1024, 8, 1, seed=79)  # tagged keys
+            sx, sw, sws, sb = _dev(sm)
+            smr.route_align(sx, sw, sws, sb, topk=8, block_size=64, workspace=wsp)
+        out = smr.route_align(x, w, ws, b, topk=8, block_size=128, workspace=wsp)
+        torch.cuda.synchronize()
+        assert smr.last_launch_count() == 3
+        ids, wts, srt, eids, npp = (t.cpu().numpy() for t in out)
+        check_route(big, ids, wts, None)
+        check_align(ids, 257, 128, srt, eids, npp)
+        n = int(npp[0])  # only the first npp (npp / A) entries are defined
+        got = (ids.copy(), srt[:n].copy(), eids[: n // 128].copy(), npp.copy())
+        if ref is None:
+            ref = got
+        for a, r in zip(got, ref):
+            assert np.array_equal(a, r)
+        hdr = wsp.buf[:32].view(torch.int32).cpu().numpy()
+        assert hdr[1] == 0 and hdr[3] == 0  # error, ticket
+
+
 @pytest.mark.parametrize("M", [4, 40])
 def test_all_equal_logits_lowest_ids_win(smr, M):
     ri = inputs.make_route_inputs(M, 256, 128, 8, 1, seed=3)
