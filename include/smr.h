@@ -200,7 +200,7 @@ SMR_API smr_status smr_route(const smr_route_args *args, void *workspace, size_t
 /* Align only: moe_align_block_size ("[ROCm][Kernel] W4A16 MoE prefill:
  * M-aware moe_align block size (1.6x TTFT)", Purpose). Reads topk_ids,
  * writes sorted_token_ids, expert_ids and num_tokens_post_padded. One launch
- * for num_tokens * width <= 8192, else three (tile counts, tile starts,
+ * for num_tokens * width <= 2048, else three (tile counts, tile starts,
  * scatter). An id outside [0, num_experts) is skipped and sets the sticky
  * device error word (see smr_get_device_error). */
 SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t workspace_bytes,

@@ -191,6 +191,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w));
 }
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -377,7 +382,7 @@ __device__ __noinline__ void copy_row_out(uint32_t drow, uint16_t *dst, int ng) 
     for (int g = 0; g < ng; ++g) reinterpret_cast<uint4 *>(dst)[g] = ld_shared_v4(drow + (uint32_t)(g * 16));
 }
 
-template <int CW, bool LO, bool XQ>
+template <int CW, bool LO, bool XQ, bool QD>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const TcParams p) {
@@ -647,6 +652,11 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const uint32_t rs = dump_row_bytes(ecols);
         const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
         float den_half = 0.0f, v_half = 0.0f;  // without renormalisation: this half's denominator
+        // threshold units: groups of kGroup columns, or for a half of at most
+        // 128 columns quads of 4 (with few groups, k of them would select
+        // nearly every group and overflow the candidate list)
+        constexpr bool quads = QD;  // (QD only with ecols <= 128)
+        const int nu = quads ? ecols / 4 : ng;
         if (ok) {
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c_beg;
             // 1. one sweep over this half's TMEM columns: add the bias, round to
@@ -677,14 +687,22 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     const int g = ch * (CW / kGroup) + u;
                     st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                    // the group's maximum: bf16 pair maxima, then one conversion to
+                    // the unit maxima: bf16 pair maxima, then one conversion to
                     // ordered keys; a -0 maximum counts as +0 (equal values)
-                    const uint32_t bm = max_bf16x2(max_bf16x2(wv[0], wv[1]), max_bf16x2(wv[2], wv[3]));
-                    const uint32_t mx = ordered_bf16x2(bm);
-                    uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
-                    gmax16 = (gmax16 == 0x7FFFu) ? 0x8000u : gmax16;
-                    pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
-                    if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
+                    const uint32_t qa = max_bf16x2(wv[0], wv[1]), qb = max_bf16x2(wv[2], wv[3]);
+                    if (quads) {  // the group's two quads, one word
+                        const uint32_t oa = ordered_bf16x2(qa), ob = ordered_bf16x2(qb);
+                        uint32_t m0 = max(oa & 0xFFFFu, oa >> 16), m1 = max(ob & 0xFFFFu, ob >> 16);
+                        m0 = (m0 == 0x7FFFu) ? 0x8000u : m0;
+                        m1 = (m1 == 0x7FFFu) ? 0x8000u : m1;
+                        list[g * kTcBM + row] = m0 | (m1 << 16);
+                    } else {
+                        const uint32_t mx = ordered_bf16x2(max_bf16x2(qa, qb));
+                        uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
+                        gmax16 = (gmax16 == 0x7FFFu) ? 0x8000u : gmax16;
+                        pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
+                        if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
+                    }
                 }
             };
             tmem_ld_async<CW>(taddr, ra);
@@ -703,16 +721,16 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             __syncwarp();
             if (__builtin_expect(p.logits_out != nullptr, 0) && valid)
                 copy_row_out(drow, p.logits_out + (int64_t)grow * p.E + c_beg, ng);
-            // the k-th largest group maximum T bounds this half's top-k from
-            // below (k groups hold a logit >= T); only groups whose maximum is
-            // >= T can hold a logit >= T. Group maxima are ordered 16-bit keys,
+            // the k-th largest unit maximum T bounds this half's top-k from
+            // below (k units hold a logit >= T); only units whose maximum is
+            // >= T can hold a logit >= T. Unit maxima are ordered 16-bit keys,
             // two per word, so each of the k rounds works on 16 registers.
             uint32_t sel = 0;
             float T = -INFINITY;
-            if (p.k <= ng) {
+            if (p.k <= nu) {
                 uint32_t pw[kCandCap / 2], po[kCandCap / 2];
     #pragma unroll
-                for (int i = 0; i < kCandCap / 2; ++i) po[i] = pw[i] = (2 * i < ng) ? list[i * kTcBM + row] : 0u;
+                for (int i = 0; i < kCandCap / 2; ++i) po[i] = pw[i] = (2 * i < nu) ? list[i * kTcBM + row] : 0u;
                 const uint32_t t16 = kth_largest_packed(pw, p.k);
                 T = ordered16_value(t16);
                 const uint32_t ts = t16 | (t16 << 16);
@@ -721,28 +739,36 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     const uint32_t ge = __vcmpgeu2(po[i], ts);
                     sel |= ((ge & 1u) << (2 * i)) | (((ge >> 16) & 1u) << (2 * i + 1));
                 }
-                sel &= (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);
+                sel &= (nu >= 32) ? 0xFFFFFFFFu : ((1u << nu) - 1u);
             } else {
-                sel = (ng >= 32) ? 0xFFFFFFFFu : ((1u << ng) - 1u);  // fewer groups than k: all
+                sel = (nu >= 32) ? 0xFFFFFFFFu : ((1u << nu) - 1u);  // fewer units than k: all
             }
             __syncwarp();
-            // 2. append every logit >= T of the selected groups (about k groups)
-            //    to the list column, over the group maxima
+            // 2. append every logit >= T of the selected units (about k units)
+            //    to the list column, over the unit maxima
             uint32_t n = 0;
             const uint32_t cand_row = smem_u32(list + row);
     #pragma unroll 1
             while (__any_sync(0xffffffffu, sel != 0u)) {
                 const uint32_t act = sel != 0u ? 1u : 0u;
-                const int g = act ? __ffs(sel) - 1 : 0;
+                const int g = act ? __ffs(sel) - 1 : 0;  // the unit
                 sel &= sel - 1u;
-                const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                uint32_t wv[4];
+                if (quads) {
+                    const uint2 v = ld_shared_v2(drow + (uint32_t)(g * 8));
+                    wv[0] = v.x; wv[1] = v.y; wv[2] = 0u; wv[3] = 0u;
+                } else {
+                    const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
+                    wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
+                }
+                const uint32_t nv = quads ? 4u : (uint32_t)kGroup;
+                const int col = c_beg + g * (int)nv;
     #pragma unroll
                 for (int u = 0; u < kGroup; ++u) {
                     const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
-                    const uint32_t c = act & (__uint_as_float(hb) >= T ? 1u : 0u);
+                    const uint32_t c = act & ((uint32_t)u < nv ? 1u : 0u) & (__uint_as_float(hb) >= T ? 1u : 0u);
                     st_shared_if(cand_row + min(n, (uint32_t)(kCandCap - 1)) * (kTcBM * 4),
-                                 hb | (uint32_t)(c_beg + g * kGroup + u),
+                                 hb | (uint32_t)(col + u),
                                  c & (n < (uint32_t)kCandCap ? 1u : 0u));
                     n += c;
                 }
@@ -961,16 +987,16 @@ bool tc_route_supported(int H, int E, int k, int S) {
     return plan_tc(1, H, E, k, S, &plan);
 }
 
-template <int CW, bool LO, bool XQ>
+template <int CW, bool LO, bool XQ, bool QD>
 static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const TcPlan &plan,
                              cudaStream_t stream) {
     static std::atomic<bool> configured[kMaxDevices];
     cudaError_t e = once_per_device(configured, [](int) {
-        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<CW, LO, XQ>,
+        cudaError_t r = cudaFuncSetAttribute(tc_route_kernel<CW, LO, XQ, QD>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kTcSmemLimit);
         if (r == cudaSuccess)  // the same carveout as every other kernel of the library
-            r = cudaFuncSetAttribute(tc_route_kernel<CW, LO, XQ>,
+            r = cudaFuncSetAttribute(tc_route_kernel<CW, LO, XQ, QD>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         return r;
@@ -992,7 +1018,7 @@ static cudaError_t launch_ng(const CUtensorMap &mx, const CUtensorMap &mw, const
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_route_kernel<CW, LO, XQ>, mx, mw, plan.p);
+    return cudaLaunchKernelEx(&cfg, tc_route_kernel<CW, LO, XQ, QD>, mx, mw, plan.p);
 }
 
 cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
@@ -1045,14 +1071,26 @@ cudaError_t launch_tc_route(const TcRouteLaunch &a, cudaStream_t stream) {
     const bool wide = (E_pad / 2) % 32 == 0;
     // the e4m3 hidden states are a separate instantiation, so that a route
     // without them keeps the plain kernel's registers and code
+    // quads (QD) as the threshold units for column halves of at most 128
+    const bool qd = !a.logits_only && E_pad / 2 <= 128;
     if (a.xq != nullptr) {
         if (a.logits_only)
-            return wide ? launch_ng<32, true, true>(mx, mw, plan, stream) : launch_ng<16, true, true>(mx, mw, plan, stream);
-        return wide ? launch_ng<32, false, true>(mx, mw, plan, stream) : launch_ng<16, false, true>(mx, mw, plan, stream);
+            return wide ? launch_ng<32, true, true, false>(mx, mw, plan, stream)
+                        : launch_ng<16, true, true, false>(mx, mw, plan, stream);
+        if (qd)
+            return wide ? launch_ng<32, false, true, true>(mx, mw, plan, stream)
+                        : launch_ng<16, false, true, true>(mx, mw, plan, stream);
+        return wide ? launch_ng<32, false, true, false>(mx, mw, plan, stream)
+                    : launch_ng<16, false, true, false>(mx, mw, plan, stream);
     }
     if (a.logits_only)
-        return wide ? launch_ng<32, true, false>(mx, mw, plan, stream) : launch_ng<16, true, false>(mx, mw, plan, stream);
-    return wide ? launch_ng<32, false, false>(mx, mw, plan, stream) : launch_ng<16, false, false>(mx, mw, plan, stream);
+        return wide ? launch_ng<32, true, false, false>(mx, mw, plan, stream)
+                    : launch_ng<16, true, false, false>(mx, mw, plan, stream);
+    if (qd)
+        return wide ? launch_ng<32, false, false, true>(mx, mw, plan, stream)
+                    : launch_ng<16, false, false, true>(mx, mw, plan, stream);
+    return wide ? launch_ng<32, false, false, false>(mx, mw, plan, stream)
+                : launch_ng<16, false, false, false>(mx, mw, plan, stream);
 }
 
 }  // namespace smr

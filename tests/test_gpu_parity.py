@@ -189,8 +189,8 @@ def test_generic_route_align(smr, M, H, E, k, S, zipf, launches):
 @pytest.mark.parametrize("M,E,k,S,A", [
     (17, 64, 8, 1, 64),      # smallest tcgen05 batch
     (128, 128, 8, 0, 0),     # the short prefill (tier: 64)
-    (744, 512, 10, 1, 128),  # 8184 slots: the most one align CTA takes
-    (1024, 128, 8, 0, 0),    # the skewed sweep's 1024 tokens
+    (186, 512, 10, 1, 128),  # 2046 slots: the most one align CTA takes
+    (256, 128, 8, 0, 0),     # 2048 slots at k = 8
 ])
 def test_mid_m_route_align_is_one_launch(smr, M, E, k, S, A):
     """Mid M: the route's last CTA aligns all ids (the shared expert appended
@@ -212,12 +212,13 @@ def test_mid_m_route_align_is_one_launch(smr, M, E, k, S, A):
     (1000, 1024, 512, 10, 1, None),  # 11000 slots: the route counts 16 tiles, the last 40 rows
     (777, 512, 256, 12, 0, 1.1),     # odd CTA count (7 tiles in 4 pairs), ragged tile, bias
     (2049, 256, 128, 8, 1, None),    # 33 count tiles, last one a single row
+    (300, 512, 128, 8, 0, 1.1),      # 2400 slots: just above one align CTA, 5 count tiles
 ])
 def test_route_align_counts_from_route(smr, M, H, E, k, S, zipf):
     """route_align above one CTA's align: the tcgen05 route writes each
     64-row tile's expert counts and the align scans and scatters from them."""
     ri = inputs.make_route_inputs(M, H, E, k, S, seed=M + E, zipf_s=zipf)
-    assert M * (k + S) > 8192
+    assert M * (k + S) > 2048
     _full_check(smr, ri, 128)
     assert smr.last_launch_count() == 3  # route + tile scan + tile scatter
 
@@ -259,6 +260,17 @@ def test_counted_align_after_other_calls_on_one_workspace(smr):
             assert np.array_equal(a, r)
         hdr = wsp.buf[:32].view(torch.int32).cpu().numpy()
         assert hdr[1] == 0 and hdr[3] == 0  # error, ticket
+
+
+@pytest.mark.parametrize("M,E,k", [(200, 128, 8), (300, 256, 10), (150, 64, 8), (40, 96, 12)])
+def test_quad_threshold_integer_ties(smr, M, E, k):
+    """Column halves of at most 128 experts take their threshold over
+    4-column maxima: integer inputs (exact fp32 sums, many equal logits,
+    k as large as the number of quads) must give the oracle's ids, weights
+    and align outputs bit for bit."""
+    ri = inputs.make_route_inputs(M, 256, E, k, 1, seed=40 + M + E, dist="int")
+    rep, al, ids = _full_check(smr, ri, 64, exact=True)
+    assert rep.exact_rows == rep.rows
 
 
 @pytest.mark.parametrize("M", [4, 40])
@@ -394,8 +406,9 @@ def test_back_to_back_small_calls_share_a_workspace(smr):
     (0, 11, 513, 64, None),        # empty input
     (1, 1, 1, 1, None),
     (4, 11, 513, 64, None),
-    (700, 11, 513, 64, 1.1),       # single CTA near its limit (7700 slots)
-    (745, 11, 513, 128, None),     # just above: two tiles
+    (186, 11, 513, 64, 1.1),       # single CTA near its limit (2046 slots)
+    (187, 11, 513, 128, None),     # just above: the three multi-CTA launches
+    (700, 11, 513, 64, 1.1),       # 7700 slots, one tile
     (16384, 11, 513, 128, 1.1),    # the large batch's shape
     (2048, 8, 128, 128, 2.0),      # very hot experts
     (3000, 3, 7, 200, None),       # odd block size, few experts
@@ -408,7 +421,7 @@ def test_align_standalone(smr, T, W, E_al, A, skew):
     srt, eids, npp = smr.align(dids, E_al, A)
     torch.cuda.synchronize()
     check_align(ids, E_al, A, srt.cpu().numpy(), eids.cpu().numpy(), npp.cpu().numpy())
-    assert smr.last_launch_count() == (1 if T * W <= 8192 else 3)
+    assert smr.last_launch_count() == (1 if T * W <= 2048 else 3)
 
 
 def test_align_reused_workspace_back_to_back(smr):

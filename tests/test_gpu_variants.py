@@ -133,7 +133,7 @@ def test_route_align_eplb(smr, M, H, E, k, S, R, P):
                                                 eplb_count=dcnt, num_physical=P)
     torch.cuda.synchronize()
     launches = smr.last_launch_count()
-    assert launches == 1 + (1 if M * (k + S) <= 8192 else 3)
+    assert launches == 1 + (1 if M * (k + S) <= 2048 else 3)
     ids = ids.cpu().numpy()
     check_route(ri, ids, wts.cpu().numpy(), None)
     ref = oracle.align_eplb(ids, E + S, emap, cnt, P, A)
