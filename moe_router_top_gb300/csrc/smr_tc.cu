@@ -663,27 +663,32 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             //    bf16 two at a time, keep the row in shared memory and the maximum
             //    of each group of kGroup columns in the thread's list column
             uint32_t ra[CW], rb[CW];
-            const bool has_bias = p.bias != nullptr;
-            auto process = [&](uint32_t (&r)[CW], int ch) {
+            // (without a bias the logits are rounded as they are: no bias
+            // loads and adds in this issue-bound sweep)
+            auto process = [&](uint32_t (&r)[CW], int ch, auto with_bias) {
                 const int c = c_beg + ch * CW;
                 uint32_t pair = 0u;  // ordered 16-bit maxima of two consecutive groups
     #pragma unroll
                 for (int u = 0; u < CW / kGroup; ++u) {
-                    float b[kGroup];
-    #pragma unroll
-                    for (int t = 0; t < kGroup; ++t) b[t] = 0.0f;
-                    if (has_bias) {
+                    uint32_t wv[4];
+                    if constexpr (decltype(with_bias)::value) {
+                        float b[kGroup];
                         const float4 b0 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup);
                         const float4 b1 = *reinterpret_cast<const float4 *>(bias_s + c + u * kGroup + 4);
                         b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
                         b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
-                    }
-                    uint32_t wv[4];
     #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int i = u * kGroup + 2 * t;
-                        wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + b[2 * t],
-                                               __uint_as_float(r[i + 1]) + b[2 * t + 1]);
+                        for (int t = 0; t < 4; ++t) {
+                            const int i = u * kGroup + 2 * t;
+                            wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]) + b[2 * t],
+                                                   __uint_as_float(r[i + 1]) + b[2 * t + 1]);
+                        }
+                    } else {
+    #pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int i = u * kGroup + 2 * t;
+                            wv[t] = pack_bf16x2_rn(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                        }
                     }
                     const int g = ch * (CW / kGroup) + u;
                     st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
@@ -705,19 +710,25 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             };
-            tmem_ld_async<CW>(taddr, ra);
-            tmem_ld_wait<CW>(ra);
-            for (int ch = 0; ch < nch; ch += 2) {  // the next chunk's load in flight
-                const bool two = ch + 1 < nch;
-                if (two) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), rb);
-                process(ra, ch);
-                if (two) {
-                    tmem_ld_wait<CW>(rb);
-                    if (ch + 2 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 2) * CW), ra);
-                    process(rb, ch + 1);
-                    if (ch + 2 < nch) tmem_ld_wait<CW>(ra);
+            auto sweep = [&](auto with_bias) {
+                tmem_ld_async<CW>(taddr, ra);
+                tmem_ld_wait<CW>(ra);
+                for (int ch = 0; ch < nch; ch += 2) {  // the next chunk's load in flight
+                    const bool two = ch + 1 < nch;
+                    if (two) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 1) * CW), rb);
+                    process(ra, ch, with_bias);
+                    if (two) {
+                        tmem_ld_wait<CW>(rb);
+                        if (ch + 2 < nch) tmem_ld_async<CW>(taddr + (uint32_t)((ch + 2) * CW), ra);
+                        process(rb, ch + 1, with_bias);
+                        if (ch + 2 < nch) tmem_ld_wait<CW>(ra);
+                    }
                 }
-            }
+            };
+            if (p.bias != nullptr)
+                sweep(std::true_type{});
+            else
+                sweep(std::false_type{});
             __syncwarp();
             if (__builtin_expect(p.logits_out != nullptr, 0) && valid)
                 copy_row_out(drow, p.logits_out + (int64_t)grow * p.E + c_beg, ng);
