@@ -400,7 +400,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);  // then the fused align's flag
     float *bias_s = reinterpret_cast<float *>(misc + p.misc_bias_off);
     int *hist = reinterpret_cast<int *>(misc + p.misc_hist_off);  // [2][E + S] counts of the CTA's two 64-row tiles
-    uint16_t *ws_s = reinterpret_cast<uint16_t *>(misc + p.misc_ws_off);
+    float *ws_s = reinterpret_cast<float *>(misc + p.misc_ws_off);  // the shared gate row in fp32
     float2 *den_s = reinterpret_cast<float2 *>(misc + p.misc_den_off);  // [128] half 0's (sum, max)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -435,11 +435,16 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (warp == 2 || warp == 3) {  // bias and expert counts, read in the epilogue
         for (int i = threadIdx.x - 64; i < p.E; i += 64) bias_s[i] = (p.bias && i < p.E_valid) ? p.bias[i] : 0.0f;
         for (int i = threadIdx.x - 64; i < 2 * (p.E + p.S); i += 64) hist[i] = 0;
-    } else if (warp >= 4 && p.S) {  // shared gate row, zero-padded to whole k-blocks
+    } else if (warp >= 4 && p.S) {
+        // the shared gate row in fp32 (converted once here rather than per
+        // stage), zero-padded to whole k-blocks
         const int nch = p.H >> 3;
-        for (int c = threadIdx.x - 128; c < p.num_kb * (kTcBK / 8); c += 128)
-            reinterpret_cast<uint4 *>(ws_s)[c] =
-                c < nch ? reinterpret_cast<const uint4 *>(p.ws)[c] : make_uint4(0u, 0u, 0u, 0u);
+        for (int c = threadIdx.x - 128; c < p.num_kb * (kTcBK / 8); c += 128) {
+            float f[8];
+            unpack8(c < nch ? reinterpret_cast<const uint4 *>(p.ws)[c] : make_uint4(0u, 0u, 0u, 0u), f);
+            reinterpret_cast<float4 *>(ws_s)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
+            reinterpret_cast<float4 *>(ws_s)[2 * c + 1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
         asm volatile("bar.sync 2, 128;" ::: "memory");  // the 4 shared-logit warps read all of it
     }
     cluster_wait();
@@ -562,13 +567,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // (a release issued while shared-memory loads are still in flight
             // may let the next TMA write overtake them)
             if (p.S) {
-                const uint4 *wsv = reinterpret_cast<const uint4 *>(ws_s) + kb * (kTcBK / 8);
+                const float4 *wsv = reinterpret_cast<const float4 *>(ws_s) + kb * (kTcBK / 4);
                 float part = 0.0f;
 #pragma unroll
                 for (int c = 0; c < kTcBK / 8; ++c) {
-                    float xf[8], wf[8];
+                    float xf[8];
                     unpack8(xv[c], xf);
-                    unpack8(wsv[c], wf);
+                    const float4 w0 = wsv[2 * c], w1 = wsv[2 * c + 1];
+                    const float wf[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e) part = fmaf(xf[e], wf[e], part);
                 }
@@ -967,11 +973,11 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.stage_bytes = (uint32_t)(kTcBM * kTcSW + (E / 2) * kTcSW);
     // misc: barriers and flags (256 B: 3*stages+2 mbarriers, TMEM slot, abort
     // flag), bias [E] fp32, expert counts [2][E+S] int32, shared gate [H, padded
-    // to whole k-blocks] bf16, half 0's softmax denominators [128] (sum, max)
+    // to whole k-blocks] fp32, half 0's softmax denominators [128] (sum, max)
     p.misc_bias_off = 256;
     p.misc_hist_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
     p.misc_ws_off = p.misc_hist_off + (uint32_t)((2 * (E + S) * 4 + 15) & ~15);
-    p.misc_den_off = p.misc_ws_off + (uint32_t)(S ? (size_t)p.num_kb * kTcBK * 2 : 0);
+    p.misc_den_off = p.misc_ws_off + (uint32_t)(S ? (size_t)p.num_kb * kTcBK * 4 : 0);
     const size_t misc = p.misc_den_off + (size_t)kTcBM * sizeof(float2);
     const size_t budget = (size_t)kTcSmemLimit - 1024 - misc;
     int st = (int)(budget / p.stage_bytes);
