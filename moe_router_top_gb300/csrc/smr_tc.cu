@@ -402,6 +402,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     int *hist = reinterpret_cast<int *>(misc + p.misc_hist_off);  // [2][E + S] counts of the CTA's two 64-row tiles
     float *ws_s = reinterpret_cast<float *>(misc + p.misc_ws_off);  // the shared gate row in fp32
     float2 *den_s = reinterpret_cast<float2 *>(misc + p.misc_den_off);  // [128] half 0's (sum, max)
+    float *sh_s = reinterpret_cast<float *>(misc + p.misc_den_off + kTcBM * sizeof(float2));  // [128] shared logits
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * kTcBM;
@@ -432,14 +433,21 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     // stage what only later steps read (overlapping the first loads)
     tc_fence_before();
     cluster_arrive();
-    if (warp == 2 || warp == 3) {  // bias and expert counts, read in the epilogue
-        for (int i = threadIdx.x - 64; i < p.E; i += 64) bias_s[i] = (p.bias && i < p.E_valid) ? p.bias[i] : 0.0f;
-        for (int i = threadIdx.x - 64; i < 2 * (p.E + p.S); i += 64) hist[i] = 0;
-    } else if (warp >= 4 && p.S) {
+    // warp roles in the K loop: 0 the TMA producer, 3 the MMA issuer (alone
+    // on its scheduler: warp w runs on scheduler w % 4), 2 and 4-6 the side
+    // warps (shared logit, e4m3 hidden states; side rows si * 32 + lane),
+    // 1 and 7 stage the bias and clear the expert counts first
+    const bool is_side = warp == 2 || (warp >= 4 && warp <= 6);
+    const int si = warp == 2 ? 3 : warp - 4;
+    if (warp == 1 || warp == 7) {  // bias and expert counts, read in the epilogue
+        const int j = (warp == 1 ? 0 : 32) + lane;
+        for (int i = j; i < p.E; i += 64) bias_s[i] = (p.bias && i < p.E_valid) ? p.bias[i] : 0.0f;
+        for (int i = j; i < 2 * (p.E + p.S); i += 64) hist[i] = 0;
+    } else if (is_side && p.S) {
         // the shared gate row in fp32 (converted once here rather than per
         // stage), zero-padded to whole k-blocks
         const int nch = p.H >> 3;
-        for (int c = threadIdx.x - 128; c < p.num_kb * (kTcBK / 8); c += 128) {
+        for (int c = si * 32 + lane; c < p.num_kb * (kTcBK / 8); c += 128) {
             float f[8];
             unpack8(c < nch ? reinterpret_cast<const uint4 *>(p.ws)[c] : make_uint4(0u, 0u, 0u, 0u), f);
             reinterpret_cast<float4 *>(ws_s)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
@@ -457,7 +465,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int row = q * 32 + lane;
     const int grow = m0 + row;
     const bool valid = grow < p.M;
-    float s_hi = 0.0f, s_lo = 0.0f;  // shared-expert logit (warps 4-7)
+    float s_hi = 0.0f, s_lo = 0.0f;  // shared-expert logit of a side warp's row (compensated sum)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
@@ -502,7 +510,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (kb < p.num_kb) set_error(p.err, kErrWaitTimeout);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 3) {
         // ------------------------------------------ MMA issuer (leader) ----
         if (leader && lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(2 * kTcBM, p.piece_n);
@@ -536,8 +544,8 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc_commit_pair(smem_u32(accum), pair_mask);
         }
         __syncwarp();
-    } else if (hf == 1 && side) {
-        // ---- side warps 4-7: shared-expert logit and e4m3 hidden states ----
+    } else if (is_side && side) {
+        // ---- side warps 2, 4-6: shared-expert logit and e4m3 hidden states ----
         // once the MMAs are done with a stage (their commit reaches both
         // CTAs) its x tile is still in place: thread = token row reads the
         // row's 64 elements of the k-block (eight 16-byte chunks, 128-byte
@@ -549,7 +557,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         //    16-byte stores ("Netra Kernel ...", Fusing the activation/
         //    quantization boundary: E4M3 with one scale per 128 values);
         // each warp then releases the stage
-        const uint32_t swz = (uint32_t)(row & 7);
+        const int srow = si * 32 + lane, sgrow = m0 + srow;
+        const bool svalid = sgrow < p.M;
+        const uint32_t swz = (uint32_t)(srow & 7);
         uint4 prev[kTcBK / 8];  // the even k-block's chunks (e4m3 only)
         uint32_t prev_max = 0u; // and their largest magnitudes (packed bf16 pair)
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -559,7 +569,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 set_error(p.err, kErrWaitTimeout);
                 break;
             }
-            const uint8_t *xrow = smem + (size_t)s * p.stage_bytes + (size_t)row * kTcSW;
+            const uint8_t *xrow = smem + (size_t)s * p.stage_bytes + (size_t)srow * kTcSW;
             uint4 xv[kTcBK / 8];
 #pragma unroll
             for (int c = 0; c < kTcBK / 8; ++c) xv[c] = *reinterpret_cast<const uint4 *>(xrow + ((c ^ swz) << 4));
@@ -586,16 +596,17 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                     for (int c = 0; c < kTcBK / 8; ++c) prev[c] = xv[c];
                     prev_max = m;
-                } else if (valid) {
+                } else if (svalid) {
                     quant_block_e4m3(prev, xv, max_bf16x2(prev_max, m),
-                                     p.xq + (int64_t)grow * p.H + (kb >> 1) * 128,
-                                     p.xs + (int64_t)grow * (p.H >> 7) + (kb >> 1));
+                                     p.xq + (int64_t)sgrow * p.H + (kb >> 1) * 128,
+                                     p.xs + (int64_t)sgrow * (p.H >> 7) + (kb >> 1));
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
         __syncwarp();
+        if (p.S) sh_s[srow] = s_hi + s_lo;  // read by the merge after the epilogue's first barrier
     }
 
     // ---------------------------------- epilogue: all 8 warps ----------
@@ -639,7 +650,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         *reinterpret_cast<uint4 *>(dst + ch * CW + u * kGroup) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
-            if (hf == 1 && p.S && valid) p.s_out[grow] = s_hi + s_lo;
+            if (hf == 1 && p.S && valid) p.s_out[grow] = sh_s[row];
         } else if (lane == 0) {
             set_error(p.err, kErrWaitTimeout);
         }
@@ -875,7 +886,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     #pragma unroll 4
                 for (int r = 0; r < p.k; ++r) wrow[r] = numer[r * kTcBM + row] * inv;
                 if (p.S) {  // (its count is the tile's number of rows, set below)
-                    const float sh = s_hi + s_lo;
+                    const float sh = sh_s[row];
                     orow[p.k] = p.E;
                     wrow[p.k] = p.scale * sigmoid_stable(p.shared_bf16 ? round_bf16(sh) : sh);
                 }
@@ -973,12 +984,13 @@ static bool plan_tc(int M, int H, int E, int k, int S, TcPlan *out) {
     p.stage_bytes = (uint32_t)(kTcBM * kTcSW + (E / 2) * kTcSW);
     // misc: barriers and flags (256 B: 3*stages+2 mbarriers, TMEM slot, abort
     // flag), bias [E] fp32, expert counts [2][E+S] int32, shared gate [H, padded
-    // to whole k-blocks] fp32, half 0's softmax denominators [128] (sum, max)
+    // to whole k-blocks] fp32, half 0's softmax denominators [128] (sum, max),
+    // the shared logits [128]
     p.misc_bias_off = 256;
     p.misc_hist_off = 256 + (uint32_t)((E * 4 + 15) & ~15);
     p.misc_ws_off = p.misc_hist_off + (uint32_t)((2 * (E + S) * 4 + 15) & ~15);
     p.misc_den_off = p.misc_ws_off + (uint32_t)(S ? (size_t)p.num_kb * kTcBK * 4 : 0);
-    const size_t misc = p.misc_den_off + (size_t)kTcBM * sizeof(float2);
+    const size_t misc = p.misc_den_off + (size_t)kTcBM * (sizeof(float2) + sizeof(float));
     const size_t budget = (size_t)kTcSmemLimit - 1024 - misc;
     int st = (int)(budget / p.stage_bytes);
     if (st > 6) st = 6;
