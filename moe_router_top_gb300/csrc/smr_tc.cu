@@ -433,14 +433,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     // stage what only later steps read (overlapping the first loads)
     tc_fence_before();
     cluster_arrive();
-    // warp roles in the K loop: 0 the TMA producer, 3 the MMA issuer (alone
-    // on its scheduler: warp w runs on scheduler w % 4), 2 and 4-6 the side
-    // warps (shared logit, e4m3 hidden states; side rows si * 32 + lane),
-    // 1 and 7 stage the bias and clear the expert counts first
-    const bool is_side = warp == 2 || (warp >= 4 && warp <= 6);
-    const int si = warp == 2 ? 3 : warp - 4;
-    if (warp == 1 || warp == 7) {  // bias and expert counts, read in the epilogue
-        const int j = (warp == 1 ? 0 : 32) + lane;
+    // warp roles in the K loop: 0 the TMA producer and 3 the MMA issuer,
+    // each alone on its scheduler (warp w runs on scheduler w % 4); 1, 2, 5
+    // and 6 the side warps (shared logit, e4m3 hidden states; side rows
+    // si * 32 + lane); 4 and 7 stage the bias and clear the expert counts
+    const bool is_side = warp == 1 || warp == 2 || warp == 5 || warp == 6;
+    const int si = warp < 4 ? warp - 1 : warp - 3;
+    if (warp == 4 || warp == 7) {  // bias and expert counts, read in the epilogue
+        const int j = (warp == 4 ? 0 : 32) + lane;
         for (int i = j; i < p.E; i += 64) bias_s[i] = (p.bias && i < p.E_valid) ? p.bias[i] : 0.0f;
         for (int i = j; i < 2 * (p.E + p.S); i += 64) hist[i] = 0;
     } else if (is_side && p.S) {
@@ -545,7 +545,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
         __syncwarp();
     } else if (is_side && side) {
-        // ---- side warps 2, 4-6: shared-expert logit and e4m3 hidden states ----
+        // ---- side warps 1, 2, 5, 6: shared-expert logit and e4m3 hidden states ----
         // once the MMAs are done with a stage (their commit reaches both
         // CTAs) its x tile is still in place: thread = token row reads the
         // row's 64 elements of the k-block (eight 16-byte chunks, 128-byte
