@@ -106,7 +106,7 @@ class ClockSampler:
                 self.samples.append(clk.value)
             if self._reasons_fn(h, ctypes.byref(rs)) == 0:
                 self.reasons |= rs.value
-            time.sleep(0.002)
+            time.sleep(0.0002)
 
     def __enter__(self):
         if self._nvml is not None:
