@@ -235,24 +235,42 @@ __device__ __forceinline__ float ordered16_value(uint32_t o) {
     return __uint_as_float(b << 16);
 }
 
+// Lane-wise (16-bit halves) wrapping add and unsigned maximum.
+__device__ __forceinline__ uint32_t add_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // A value of rank <= k among the 32 ordered 16-bit keys packed in pw (0 =
-// empty): k rounds of taking the maximum and clearing every half equal to it.
-// Equal keys leave together, so the result is at most the k-th largest; it
-// stays a valid lower bound for "at least k keys are >= it".
-__device__ __forceinline__ uint32_t kth_largest_packed(uint32_t (&pw)[kCandCap / 2], int k) {
-    uint32_t last = 0u;
+// empty): the maximum, then k - 1 steps to the largest key below the current
+// one. A step adds 2^16 - m to every half (mod 2^16): keys >= m land in
+// [0, 2^16 - m) and keys < m in [2^16 - m, 2^16), in their own order, so one
+// maximum over the shifted halves, shifted back, is the next key down; it is
+// 0 (an empty half) or >= m when no key below m is left, and m stays. Equal
+// keys count once, so the result is at
+// most the k-th largest; it stays a valid lower bound for "at least k keys
+// are >= it".
+__device__ __forceinline__ uint32_t kth_largest_packed(const uint32_t (&pw)[kCandCap / 2], int k) {
+    uint32_t m2 = pw[0];
+#pragma unroll
+    for (int i = 1; i < kCandCap / 2; ++i) m2 = max_u16x2(m2, pw[i]);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        uint32_t m2 = pw[0];
+    for (int r = 1; r < k; ++r) {
+        const uint32_t d = (0x10000u - m) & 0xFFFFu, dd = d | (d << 16);
+        uint32_t z2 = add_u16x2(pw[0], dd);
 #pragma unroll
-        for (int i = 1; i < kCandCap / 2; ++i) m2 = __vmaxu2(m2, pw[i]);
-        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-        last = m ? m : last;
-        const uint32_t ms = m | (m << 16);
-#pragma unroll
-        for (int i = 0; i < kCandCap / 2; ++i) pw[i] &= ~__vcmpeq2(pw[i], ms);
+        for (int i = 1; i < kCandCap / 2; ++i) z2 = max_u16x2(z2, add_u16x2(pw[i], dd));
+        const uint32_t nx = (max(z2 & 0xFFFFu, z2 >> 16) + m) & 0xFFFFu;
+        m = (nx != 0u && nx < m) ? nx : m;  // (nx >= m: every key is >= m)
     }
-    return last;
+    return m;
 }
 
 // A thread's n <= SLOTS candidate entries (list column, stride kTcBM words)
@@ -262,13 +280,22 @@ __device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k)
     uint32_t a[SLOTS];
 #pragma unroll
     for (int j = 0; j < SLOTS; ++j) a[j] = (j < (int)n) ? entry_key(col[j * kTcBM]) : 0u;
+    // keys are distinct: after the maximum, each round takes the largest key
+    // below the previous one as the maximum of a[i] - m (mod 2^32), which
+    // puts keys >= m below every key < m, shifted back; the result is >= m
+    // (every slot holds a key >= m) or 0 (an empty slot) when no key is left,
+    // and then 0 stays
+    uint32_t m = a[0];
+#pragma unroll
+    for (int i = 1; i < SLOTS; ++i) m = max(m, a[i]);
+    col[0] = m;
 #pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        uint32_t m = 0u;
+    for (int r = 1; r < k; ++r) {
+        uint32_t z = a[0] - m;
 #pragma unroll
-        for (int i = 0; i < SLOTS; ++i) m = max(m, a[i]);
-#pragma unroll
-        for (int i = 0; i < SLOTS; ++i) a[i] = (a[i] == m) ? 0u : a[i];
+        for (int i = 1; i < SLOTS; ++i) z = max(z, a[i] - m);
+        const uint32_t nxt = z + m;
+        m = nxt < m ? nxt : 0u;
         col[r * kTcBM] = m;
     }
 }
@@ -752,19 +779,19 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // the k-th largest unit maximum T bounds this half's top-k from
             // below (k units hold a logit >= T); only units whose maximum is
             // >= T can hold a logit >= T. Unit maxima are ordered 16-bit keys,
-            // two per word, so each of the k rounds works on 16 registers.
+            // two per word, so each of the k steps works on 16 registers.
             uint32_t sel = 0;
             float T = -INFINITY;
             if (p.k <= nu) {
-                uint32_t pw[kCandCap / 2], po[kCandCap / 2];
+                uint32_t pw[kCandCap / 2];
     #pragma unroll
-                for (int i = 0; i < kCandCap / 2; ++i) po[i] = pw[i] = (2 * i < nu) ? list[i * kTcBM + row] : 0u;
+                for (int i = 0; i < kCandCap / 2; ++i) pw[i] = (2 * i < nu) ? list[i * kTcBM + row] : 0u;
                 const uint32_t t16 = kth_largest_packed(pw, p.k);
                 T = ordered16_value(t16);
                 const uint32_t ts = t16 | (t16 << 16);
     #pragma unroll
                 for (int i = 0; i < kCandCap / 2; ++i) {
-                    const uint32_t ge = __vcmpgeu2(po[i], ts);
+                    const uint32_t ge = __vcmpgeu2(pw[i], ts);
                     sel |= ((ge & 1u) << (2 * i)) | (((ge >> 16) & 1u) << (2 * i + 1));
                 }
                 sel &= (nu >= 32) ? 0xFFFFFFFFu : ((1u << nu) - 1u);
