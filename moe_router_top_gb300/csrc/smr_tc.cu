@@ -59,7 +59,11 @@ constexpr int kTcSW = kTcBK * 2;
 constexpr int kTcThreads = 256;
 constexpr int kCandCap = 32;
 constexpr int kGroup = 8;             // consecutive columns per group (one 16-byte bf16 group)
-constexpr int kEpiListBytes = 3 * kCandCap * kTcBM * 4;  // two candidate lists + half 0's top-k
+// epilogue lists: half 0's candidates (then its top-k), the softmax
+// numerators, half 1's candidates, and kGroup slots of room after each list
+// for a unit's entries past kCandCap (the numerators are written only after
+// the candidates are dead)
+constexpr int kEpiListBytes = (3 * kCandCap + kGroup) * kTcBM * 4;
 constexpr int kTcSmemLimit = 232448;  // 227 KiB opt-in per CTA
 
 struct TcParams {
@@ -132,36 +136,44 @@ __device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, uint32_t
                  ::"r"(addr), "r"(v), "r"(c));
 }
 
-// Descending sort of N unsigned keys (bitonic network, N a power of two).
-// Only the first N entries of the array take part.
-template <int N, int CAP>
-__device__ __forceinline__ void sort_keys_desc(uint32_t (&a)[CAP]) {
-    static_assert(N <= CAP, "prefix within the array");
+// Descending sort of N unsigned keys: Batcher's odd-even merge sort (merges
+// of sorted runs of p = 1, 2, 4, ... keys; each merge compares keys k apart
+// for k = p, p/2, ..., 1, only within one run pair). The comparator list is
+// built at compile time and the network fully unrolled: 63 compare-exchanges
+// for N = 16.
+template <int N>
+struct OddEvenNet {
+    int x[N * N], y[N * N], count;
+    constexpr OddEvenNet() : x(), y(), count(0) {
+        for (int p = 1; p < N; p <<= 1)
+            for (int k = p; k >= 1; k >>= 1)
+                for (int j = k % p; j + k < N; j += 2 * k)
+                    for (int i = 0; i < k; ++i)
+                        if (i + j + k < N && (i + j) / (2 * p) == (i + j + k) / (2 * p)) {
+                            x[count] = i + j;
+                            y[count] = i + j + k;
+                            ++count;
+                        }
+    }
+};
+template <int N>
+__device__ __forceinline__ void sort_desc_oddeven(uint32_t (&a)[N]) {
+    constexpr OddEvenNet<N> net{};
 #pragma unroll
-    for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = ((i & size) == 0);
-                    const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
-                    a[i] = desc ? hi : lo;
-                    a[j] = desc ? lo : hi;
-                }
-            }
-        }
+    for (int c = 0; c < net.count; ++c) {
+        const uint32_t hi = max(a[net.x[c]], a[net.y[c]]), lo = min(a[net.x[c]], a[net.y[c]]);
+        a[net.x[c]] = hi;
+        a[net.y[c]] = lo;
     }
 }
 
 // Candidate entry (bf16 bits of the rounded logit in the high half, expert id
 // in the low half) -> ordered selection key.
 __device__ __forceinline__ uint32_t entry_key(uint32_t entry) {
-    uint32_t b = entry >> 16;
-    b = (b == 0x8000u) ? 0u : b;  // a rounded -0 ranks (and ties) as +0
-    const uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
-    return (ord << 16) | (0xFFFFu - (entry & 0xFFFFu));
+    // a value >= +0 flips its sign bit, a negative one all its bits; the id
+    // becomes 0xFFFF - id either way
+    const uint32_t key = entry ^ ((uint32_t)((int32_t)entry >> 31) | 0x8000FFFFu);
+    return key + ((key >> 16) == 0x7FFFu ? 0x10000u : 0u);  // a rounded -0 ranks (and ties) as +0
 }
 
 // TMEM loads of CW columns (CW = 32 or 16) for one warp's 32 lanes.
@@ -206,23 +218,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // Row stride of the rounded-logit copy in shared memory: an odd multiple of
 // 16 bytes, so eight consecutive rows' 16-byte groups fall in distinct banks.
 __host__ __device__ constexpr uint32_t dump_row_bytes(int ecols) { return (uint32_t)ecols * 2u + 16u; }
-
-// Bitonic merge of a bitonic sequence of N keys into descending order.
-template <int N>
-__device__ __forceinline__ void bitonic_merge_desc(uint32_t (&a)[N]) {
-#pragma unroll
-    for (int stride = N >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const int j = i ^ stride;
-            if (j > i) {
-                const uint32_t hi = max(a[i], a[j]), lo = min(a[i], a[j]);
-                a[i] = hi;
-                a[j] = lo;
-            }
-        }
-    }
-}
 
 // bf16 pair -> ordered unsigned 16-bit keys (numeric order as unsigned order).
 __device__ __forceinline__ uint32_t ordered_bf16x2(uint32_t x) {
@@ -280,6 +275,14 @@ __device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k)
     uint32_t a[SLOTS];
 #pragma unroll
     for (int j = 0; j < SLOTS; ++j) a[j] = (j < (int)n) ? entry_key(col[j * kTcBM]) : 0u;
+    if constexpr (SLOTS == 16) {  // the common case: one sorting network
+        sort_desc_oddeven(a);
+#pragma unroll
+        for (int r = 0; r < SLOTS; ++r)
+            if (r < k) col[r * kTcBM] = a[r];
+        for (int r = SLOTS; r < k; ++r) col[r * kTcBM] = 0u;
+        return;
+    }
     // keys are distinct: after the maximum, each round takes the largest key
     // below the previous one as the maximum of a[i] - m (mod 2^32), which
     // puts keys >= m below every key < m, shifted back; the result is >= m
@@ -690,9 +693,9 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // list column per thread ([32][128] words: group maxima, then candidates,
         // then the half's top-k), softmax numerators of half 1, and each half's
         // rounded logits (row stride rs)
-        uint32_t *list = reinterpret_cast<uint32_t *>(smem) + hf * (kCandCap * kTcBM);
+        uint32_t *list = reinterpret_cast<uint32_t *>(smem) + hf * (2 * kCandCap * kTcBM);
         uint32_t *list0 = reinterpret_cast<uint32_t *>(smem);                 // half 0's top-k
-        float *numer = reinterpret_cast<float *>(smem) + 2 * kCandCap * kTcBM;  // [32][128]
+        float *numer = reinterpret_cast<float *>(smem) + kCandCap * kTcBM;  // [32][128], between the lists
         const uint32_t rs = dump_row_bytes(ecols);
         const uint32_t drow = smem_u32(smem) + (uint32_t)(kEpiListBytes + (hf * kTcBM + row) * rs);
         float den_half = 0.0f, v_half = 0.0f;  // without renormalisation: this half's denominator
@@ -800,13 +803,16 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
             __syncwarp();
             // 2. append every logit >= T of the selected units (about k units)
-            //    to the list column, over the unit maxima
-            uint32_t n = 0;
-            const uint32_t cand_row = smem_u32(list + row);
+            //    to the list column, over the unit maxima. A unit adds at most
+            //    kGroup entries, so while n <= kCandCap it is taken without a
+            //    bound check (the kGroup slots past a list are room for it);
+            //    n > kCandCap marks an overflow
+            constexpr uint32_t nv = quads ? 4u : (uint32_t)kGroup;  // columns per unit
+            uint32_t *cand = list + row;
     #pragma unroll 1
             while (__any_sync(0xffffffffu, sel != 0u)) {
-                const uint32_t act = sel != 0u ? 1u : 0u;
-                const int g = act ? __ffs(sel) - 1 : 0;  // the unit
+                const bool on = sel != 0u && cand <= list + row + kCandCap * kTcBM;
+                const int g = sel != 0u ? __ffs(sel) - 1 : 0;  // the unit
                 sel &= sel - 1u;
                 uint32_t wv[4];
                 if (quads) {
@@ -816,23 +822,21 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     const uint4 v = ld_shared_v4(drow + (uint32_t)(g * 16));
                     wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
                 }
-                const uint32_t nv = quads ? 4u : (uint32_t)kGroup;
-                const int col = c_beg + g * (int)nv;
+                const uint32_t col = (uint32_t)(c_beg + g * (int)nv);  // a multiple of nv
     #pragma unroll
-                for (int u = 0; u < kGroup; ++u) {
+                for (int u = 0; u < (int)nv; ++u) {
                     const uint32_t hb = (u & 1) ? (wv[u >> 1] & 0xFFFF0000u) : (wv[u >> 1] << 16);
-                    const uint32_t c = act & ((uint32_t)u < nv ? 1u : 0u) & (__uint_as_float(hb) >= T ? 1u : 0u);
-                    st_shared_if(cand_row + min(n, (uint32_t)(kCandCap - 1)) * (kTcBM * 4),
-                                 hb | (uint32_t)(col + u),
-                                 c & (n < (uint32_t)kCandCap ? 1u : 0u));
-                    n += c;
+                    const bool c = on && __uint_as_float(hb) >= T;
+                    if (c) *cand = hb | col | (uint32_t)u;
+                    cand += c ? kTcBM : 0;
                 }
             }
-            asm volatile("" ::: "memory");  // the predicated stores above precede the reads below
+            const uint32_t n = (uint32_t)(cand - (list + row)) / kTcBM;
             __syncwarp();
-            // 3. this half's top-k, in order, into the list column: k rounds of
-            //    the largest remaining candidate key. A row whose candidates
-            //    overflowed the list takes k passes over its rounded logits.
+            // 3. this half's top-k, in order, into the list column: a sorting
+            //    network over up to 16 candidate keys, else k rounds of the
+            //    largest remaining key. A row whose candidates overflowed the
+            //    list takes k passes over its rounded logits.
             if (__all_sync(0xffffffffu, n <= 16u)) {
                 topk_from_list<16>(list + row, n, p.k);  // the common case (~0.3% of rows exceed 16)
             } else if (__builtin_expect(__any_sync(0xffffffffu, n > (uint32_t)kCandCap), 0)) {
