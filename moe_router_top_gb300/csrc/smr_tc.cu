@@ -219,15 +219,21 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // 16 bytes, so eight consecutive rows' 16-byte groups fall in distinct banks.
 __host__ __device__ constexpr uint32_t dump_row_bytes(int ecols) { return (uint32_t)ecols * 2u + 16u; }
 
-// bf16 pair -> ordered unsigned 16-bit keys (numeric order as unsigned order).
+// bf16 pair -> ordered unsigned 16-bit keys (numeric order as unsigned
+// order, -0 and +0 both 0x8000): a value >= +0 sets its sign bit, a negative
+// one b becomes 2^16 - b. (The negative half's +1 never carries out of it.)
 __device__ __forceinline__ uint32_t ordered_bf16x2(uint32_t x) {
     const uint32_t neg = (x >> 15) & 0x00010001u;  // sign bit of each half
-    return x ^ ((neg * 0xFFFFu) | 0x80008000u);
+    return (x ^ ((neg * 0xFFFFu) | 0x80008000u)) + neg;
 }
 // Ordered 16-bit key -> the bf16 value as a float.
 __device__ __forceinline__ float ordered16_value(uint32_t o) {
-    const uint32_t b = (o & 0x8000u) ? (o & 0x7FFFu) : (~o & 0xFFFFu);
+    const uint32_t b = (o & 0x8000u) ? (o & 0x7FFFu) : ((0x10000u - o) & 0xFFFFu);
     return __uint_as_float(b << 16);
+}
+// The larger halves of two bf16 pairs' halves: (max of a's halves, max of b's).
+__device__ __forceinline__ uint32_t halves_max_bf16x2(uint32_t a, uint32_t b) {
+    return max_bf16x2(__byte_perm(a, b, 0x5410), __byte_perm(a, b, 0x7632));
 }
 
 // Lane-wise (16-bit halves) wrapping add and unsigned maximum.
@@ -259,9 +265,14 @@ __device__ __forceinline__ uint32_t kth_largest_packed(const uint32_t (&pw)[kCan
 #pragma unroll 1
     for (int r = 1; r < k; ++r) {
         const uint32_t d = (0x10000u - m) & 0xFFFFu, dd = d | (d << 16);
-        uint32_t z2 = add_u16x2(pw[0], dd);
+        uint32_t z[kCandCap / 2];
 #pragma unroll
-        for (int i = 1; i < kCandCap / 2; ++i) z2 = max_u16x2(z2, add_u16x2(pw[i], dd));
+        for (int i = 0; i < kCandCap / 2; ++i) z[i] = add_u16x2(pw[i], dd);
+#pragma unroll
+        for (int w = kCandCap / 4; w >= 1; w >>= 1)  // a tree of maxima
+#pragma unroll
+            for (int i = 0; i < w; ++i) z[i] = max_u16x2(z[i], z[i + w]);
+        const uint32_t z2 = z[0];
         const uint32_t nx = (max(z2 & 0xFFFFu, z2 >> 16) + m) & 0xFFFFu;
         m = (nx != 0u && nx < m) ? nx : m;  // (nx >= m: every key is >= m)
     }
@@ -281,25 +292,27 @@ __device__ __forceinline__ void topk_from_list(uint32_t *col, uint32_t n, int k)
         for (int r = 0; r < SLOTS; ++r)
             if (r < k) col[r * kTcBM] = a[r];
         for (int r = SLOTS; r < k; ++r) col[r * kTcBM] = 0u;
-        return;
-    }
-    // keys are distinct: after the maximum, each round takes the largest key
-    // below the previous one as the maximum of a[i] - m (mod 2^32), which
-    // puts keys >= m below every key < m, shifted back; the result is >= m
-    // (every slot holds a key >= m) or 0 (an empty slot) when no key is left,
-    // and then 0 stays
-    uint32_t m = a[0];
+    } else {
+        // k rounds. Keys are distinct: after the maximum, each round takes
+        // the largest key below the previous one as the maximum of a[i] - m
+        // (mod 2^32), which puts keys >= m below every key < m, shifted back;
+        // the result is >= m (every slot holds a key >= m) or 0 (an empty
+        // slot) when no key is left, and then 0 stays. (Rolled: this path's
+        // instructions are fetched cold, and a network over both halves of
+        // the list measured slower in the whole step.)
+        uint32_t m = a[0];
 #pragma unroll
-    for (int i = 1; i < SLOTS; ++i) m = max(m, a[i]);
-    col[0] = m;
+        for (int i = 1; i < SLOTS; ++i) m = max(m, a[i]);
+        col[0] = m;
 #pragma unroll 1
-    for (int r = 1; r < k; ++r) {
-        uint32_t z = a[0] - m;
+        for (int r = 1; r < k; ++r) {
+            uint32_t z = a[0] - m;
 #pragma unroll
-        for (int i = 1; i < SLOTS; ++i) z = max(z, a[i] - m);
-        const uint32_t nxt = z + m;
-        m = nxt < m ? nxt : 0u;
-        col[r * kTcBM] = m;
+            for (int i = 1; i < SLOTS; ++i) z = max(z, a[i] - m);
+            const uint32_t nxt = z + m;
+            m = nxt < m ? nxt : 0u;
+            col[r * kTcBM] = m;
+        }
     }
 }
 
@@ -714,7 +727,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // loads and adds in this issue-bound sweep)
             auto process = [&](uint32_t (&r)[CW], int ch, auto with_bias) {
                 const int c = c_beg + ch * CW;
-                uint32_t pair = 0u;  // ordered 16-bit maxima of two consecutive groups
+                uint32_t pair = 0u;  // the even group's pair maxima
     #pragma unroll
                 for (int u = 0; u < CW / kGroup; ++u) {
                     uint32_t wv[4];
@@ -740,20 +753,14 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     const int g = ch * (CW / kGroup) + u;
                     st_shared_v4(drow + (uint32_t)(g * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
                     // the unit maxima: bf16 pair maxima, then one conversion to
-                    // ordered keys; a -0 maximum counts as +0 (equal values)
+                    // ordered keys per two units (a -0 maximum ranks as +0)
                     const uint32_t qa = max_bf16x2(wv[0], wv[1]), qb = max_bf16x2(wv[2], wv[3]);
                     if (quads) {  // the group's two quads, one word
-                        const uint32_t oa = ordered_bf16x2(qa), ob = ordered_bf16x2(qb);
-                        uint32_t m0 = max(oa & 0xFFFFu, oa >> 16), m1 = max(ob & 0xFFFFu, ob >> 16);
-                        m0 = (m0 == 0x7FFFu) ? 0x8000u : m0;
-                        m1 = (m1 == 0x7FFFu) ? 0x8000u : m1;
-                        list[g * kTcBM + row] = m0 | (m1 << 16);
-                    } else {
-                        const uint32_t mx = ordered_bf16x2(max_bf16x2(qa, qb));
-                        uint32_t gmax16 = max(mx & 0xFFFFu, mx >> 16);
-                        gmax16 = (gmax16 == 0x7FFFu) ? 0x8000u : gmax16;
-                        pair = (u & 1) ? (pair | (gmax16 << 16)) : gmax16;
-                        if (u & 1) list[(g >> 1) * kTcBM + row] = pair;
+                        list[g * kTcBM + row] = ordered_bf16x2(halves_max_bf16x2(qa, qb));
+                    } else {      // two groups, one word
+                        const uint32_t m = max_bf16x2(qa, qb);  // (even columns' maximum, odd columns')
+                        if (u & 1) list[(g >> 1) * kTcBM + row] = ordered_bf16x2(halves_max_bf16x2(pair, m));
+                        pair = m;
                     }
                 }
             };
