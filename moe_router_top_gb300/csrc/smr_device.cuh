@@ -173,6 +173,13 @@ __device__ __forceinline__ void cluster_wait() {
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
+// A hint: the box of a 2-D tensor map at {c0, c1} (c0 as for a load: a
+// multiple of 16 bytes) into L2; nothing lands in shared memory and no
+// value is read.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0), "r"(c1)
+                 : "memory");
+}
 
 // ------------------------------------------------------------- tcgen05 ---
 

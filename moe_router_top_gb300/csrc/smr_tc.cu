@@ -519,7 +519,10 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int m_load = m0 < p.M ? m0 : 0;
             // the gate pieces of the first stages (layer parameters) are
             // requested before waiting for the previous kernel in the stream
-            // (programmatic dependent launch), the hidden states after it
+            // (programmatic dependent launch), the hidden states after it;
+            // their first stages are only prefetched into L2 before the wait
+            // (a hint: no value is read, L2 is coherent and the loads after
+            // the wait go through it), so that those loads hit L2
             const int pre = min(ST, p.num_kb);
             for (int kb = 0; kb < pre; ++kb) {
                 const uint32_t fb = cluster_addr(smem_u32(&full[kb]), 0u);  // leader's barrier
@@ -529,6 +532,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     tma_load_2d_pair(b_dst + (uint32_t)pc * half * kTcSW, &tm_w, kb * kTcBK,
                                      pc * p.piece_n + (int)(rank * half), fb);
             }
+            for (int kb = 0; kb < pre; ++kb) tma_prefetch_l2_2d(&tm_x, kb * kTcBK, m_load);
             griddep_wait();
             int kb = 0;
             for (; kb < p.num_kb; ++kb) {
