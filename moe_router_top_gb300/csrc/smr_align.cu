@@ -114,8 +114,11 @@ __global__ void __launch_bounds__(EPB * 32) align_tile_scan_kernel(const AlignLa
     __shared__ int part[32][EPB + 1];
     __shared__ int tot_s[EPB];
     const int el = threadIdx.x % EPB, c = threadIdx.x / EPB;
-    griddep_launch_dependents();
     griddep_wait();  // the tile counts come from the previous kernel
+    // the next kernel launches only after every CTA got here, so once the
+    // previous kernel (and everything before it) has completed: the scatter
+    // behind the route reads the route's ids before its own wait
+    griddep_launch_dependents();
     const int e = blockIdx.x * EPB + el;
     const int ec = min(e, a.E_al - 1);  // clamped: every load stays in bounds
     const int tpc = (ntiles + 31) / 32;
@@ -319,28 +322,13 @@ __global__ void __launch_bounds__(kTileThreads) align_rows_scatter_kernel(const 
     const int tile = kTcCountRows * width;
     const int beg = t * tile, n = min(beg + tile, a.numel) - beg;
     griddep_launch_dependents();  // the next kernel may launch; it waits for this grid
-    griddep_wait();  // the tile starts and totals come from the previous kernel
+    // The ids are the route's: the scan before this kernel let it launch only
+    // after waiting for the route, so they are complete already, and the
+    // per-expert row masks are built before waiting for the scan
     int ev[kRowsMaxSlots];
 #pragma unroll
     for (int j = 0; j < kRowsMaxSlots; ++j) ev[j] = __ldcg(a.ids + beg + min(tid + j * kTileThreads, n - 1));
-    constexpr int kPerThread = (kMaxExpertsAl + kTileThreads - 1) / kTileThreads;
-    int bse[kPerThread], tt[kPerThread];
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        const int e = min(tid + j * kTileThreads, E_al - 1);
-        bse[j] = __ldcg(a.tile_base + (int64_t)t * E_al + e);
-        tt[j] = __ldcg(a.totals + e);
-    }
     for (int q = tid; q < 2 * E_al; q += kTileThreads) mask[q] = 0u;
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        const int e = tid + j * kTileThreads;
-        if (e < E_al) {
-            base[e] = bse[j];
-            tot[e] = tt[j];
-        }
-    }
-    __syncwarp();
     __syncthreads();
     int rw[kRowsMaxSlots];  // the slot's row in the tile, or -1
 #pragma unroll
@@ -351,7 +339,24 @@ __global__ void __launch_bounds__(kTileThreads) align_rows_scatter_kernel(const 
         rw[j] = ok ? i / width : -1;
         if (ok) atomicOr(&mask[2 * ev[j] + (rw[j] >> 5)], 1u << (rw[j] & 31));
     }
-    __syncwarp();
+    griddep_wait();  // the tile starts and totals come from the scan
+    constexpr int kPerThread = (kMaxExpertsAl + kTileThreads - 1) / kTileThreads;
+    int bse[kPerThread], tt[kPerThread];
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int e = min(tid + j * kTileThreads, E_al - 1);
+        bse[j] = __ldcg(a.tile_base + (int64_t)t * E_al + e);
+        tt[j] = __ldcg(a.totals + e);
+    }
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int e = tid + j * kTileThreads;
+        if (e < E_al) {
+            base[e] = bse[j];
+            tot[e] = tt[j];
+        }
+    }
+    __syncthreads();  // base and tot (read by align_offsets) and the masks are complete
     AlignSmem s;
     s.off = off;
     s.scratch = scratch;
