@@ -211,9 +211,10 @@ SMR_API smr_status smr_align(const smr_align_args *args, void *workspace, size_t
  * route->topk_ids, align->num_tokens == route->M, align->width == topk + S,
  * align->num_experts == E + S; routed_topk/routed_experts are taken from the
  * route. For M <= 16 both run in ONE launch; for larger M the tcgen05 route
- * also writes each 64-row tile's expert counts and two align launches
- * follow (one when the ids fit a single align CTA). With an EPLB remap the
- * align always runs as its own launches behind the route (1 or 3). */
+ * aligns in its last CTA when M * width <= 704 (one launch), else it also
+ * writes each 64-row tile's expert counts and two align launches follow.
+ * With an EPLB remap the align always runs as its own launches behind the
+ * route (1 or 3). */
 SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_args *align,
                            void *workspace, size_t workspace_bytes, void *stream);
 

@@ -421,7 +421,7 @@ static cudaError_t launch_dependent(void (*kern)(Args...), int grid, int block, 
 
 cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream) {
     cudaError_t e;
-    if (a.numel <= kAlignSingleMax) {
+    if (a.numel <= kAlignSingleMax && a.counted_tile == 0) {
         const size_t smem = (size_t)(kAlignSingleMax + align_smem_words(kAlignWarps, a.E_al)) * 4;
         const size_t smem_max = (size_t)(kAlignSingleMax + align_smem_words(kAlignWarps, 1025)) * 4;
         if ((e = configure((const void *)align_single_kernel, 0, smem_max)) != cudaSuccess) return e;

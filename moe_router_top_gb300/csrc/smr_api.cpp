@@ -228,11 +228,11 @@ smr_status check_ws(void *ws, size_t bytes, size_t need, const char *what) {
     return SMR_OK;
 }
 
-// The align behind a tcgen05 route over more than kAlignSingleMax slots takes
+// The align behind a tcgen05 route over more than kFusedAlignMax slots takes
 // its per-tile expert counts from the route (tiles of 64 token rows), unless
 // an EPLB remap changes what is counted.
 bool align_counted_by_route(const smr_route_args *r, const smr_align_args *a, int64_t numel) {
-    return r->M > smr::kSmallMaxM && numel > smr::kAlignSingleMax && !has_eplb(a) && !generic_route(r);
+    return r->M > smr::kSmallMaxM && numel > smr::kFusedAlignMax && !has_eplb(a) && !generic_route(r);
 }
 int64_t route_tiles(const smr_route_args *r) {
     return (r->M + smr::kTcCountRows - 1) / smr::kTcCountRows;
@@ -496,7 +496,7 @@ SMR_API smr_status smr_route_align(const smr_route_args *route, const smr_align_
         if (st == SMR_OK) g_last_launches = launches;
         return st;
     }
-    if (route->M > 0 && (int64_t)route->M * al.width <= smr::kAlignSingleMax && !has_eplb(&al) &&
+    if (route->M > 0 && (int64_t)route->M * al.width <= smr::kFusedAlignMax && !has_eplb(&al) &&
         !generic_route(route)) {
         // mid M: one launch, the align fused into the route's last CTA
         st = run_route(route, workspace, s, &al, &launches);

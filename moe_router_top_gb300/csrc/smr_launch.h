@@ -203,6 +203,12 @@ struct AlignLaunch {
 // numel handled by one CTA: above ~2000 slots the three multi-CTA launches
 // measured faster (8184 slots: 33 us in one CTA, 12 us in three launches)
 constexpr int kAlignSingleMax = 2048;
+// route_align behind a tcgen05 route over at most this many slots aligns in
+// the route's last CTA (one launch); above it the route's 64-row tile counts
+// feed the scan and the rows scatter, whose first round trip runs under the
+// scan (measured per call, E = 128, H = 2048: 26.0 against 27.6 us at 360
+// slots, 27.4 against 25.9 at 1152, 30.0 against 25.9 at 1800)
+constexpr int kFusedAlignMax = 704;
 constexpr int kAlignMinTile = 1024;     // slots per CTA in the multi-CTA path, at least
 constexpr int kAlignMaxTiles = 2048;    // tiles, at most (larger inputs take larger tiles)
 inline int align_tile_size(int64_t numel) {
@@ -221,7 +227,7 @@ inline int64_t align_scratch_words(int64_t numel, int E_al) {
 }
 // Launches of launch_align for these inputs.
 inline int align_launches(int64_t numel, bool counted) {
-    return numel <= kAlignSingleMax ? 1 : (counted ? 2 : 3);
+    return counted ? 2 : (numel <= kAlignSingleMax ? 1 : 3);
 }
 cudaError_t launch_align(const AlignLaunch &a, cudaStream_t stream);
 

@@ -188,9 +188,9 @@ def test_generic_route_align(smr, M, H, E, k, S, zipf, launches):
 
 @pytest.mark.parametrize("M,E,k,S,A", [
     (17, 64, 8, 1, 64),      # smallest tcgen05 batch
-    (128, 128, 8, 0, 0),     # the short prefill (tier: 64)
-    (186, 512, 10, 1, 128),  # 2046 slots: the most one align CTA takes
-    (256, 128, 8, 0, 0),     # 2048 slots at k = 8
+    (40, 256, 12, 1, 0),     # 520 slots, tier block size
+    (64, 512, 10, 1, 128),   # 704 slots: the most the route's last CTA aligns
+    (88, 128, 8, 0, 0),      # 704 slots at k = 8
 ])
 def test_mid_m_route_align_is_one_launch(smr, M, E, k, S, A):
     """Mid M: the route's last CTA aligns all ids (the shared expert appended
@@ -212,13 +212,16 @@ def test_mid_m_route_align_is_one_launch(smr, M, E, k, S, A):
     (1000, 1024, 512, 10, 1, None),  # 11000 slots: the route counts 16 tiles, the last 40 rows
     (777, 512, 256, 12, 0, 1.1),     # odd CTA count (7 tiles in 4 pairs), ragged tile, bias
     (2049, 256, 128, 8, 1, None),    # 33 count tiles, last one a single row
-    (300, 512, 128, 8, 0, 1.1),      # 2400 slots: just above one align CTA, 5 count tiles
+    (300, 512, 128, 8, 0, 1.1),      # 2400 slots, 5 count tiles
+    (65, 1024, 512, 10, 1, None),    # 715 slots: just above the fused align, 2 count tiles
+    (128, 1024, 128, 8, 0, None),    # the short prefill: 1024 slots, 2 count tiles
+    (186, 1024, 512, 10, 1, 1.1),    # 2046 slots, a ragged count tile
 ])
 def test_route_align_counts_from_route(smr, M, H, E, k, S, zipf):
-    """route_align above one CTA's align: the tcgen05 route writes each
+    """route_align above the align fused into the route: the tcgen05 route writes each
     64-row tile's expert counts and the align scans and scatters from them."""
     ri = inputs.make_route_inputs(M, H, E, k, S, seed=M + E, zipf_s=zipf)
-    assert M * (k + S) > 2048
+    assert M * (k + S) > 704  # above the align fused into the route
     _full_check(smr, ri, 128)
     assert smr.last_launch_count() == 3  # route + tile scan + tile scatter
 
