@@ -171,6 +171,24 @@ def test_align_workspace_sizes(lib):
     assert lib.smr_align_workspace_size(ctypes.byref(a)) == 256 + ((words * 4 + 255) // 256) * 256
 
 
+def test_route_align_workspace_follows_the_fused_align_cut_over(lib):
+    """Behind a tcgen05 route, up to 704 slots are aligned by the route's last
+    CTA in shared memory (no align scratch); above, the route counts its
+    64-row tiles and the scan and scatter keep [tiles][E_al] counts and starts
+    and [E_al] totals in the workspace."""
+    def need(M):
+        r = _good_route(M=M, H=1024, E=512, k=10, S=1)
+        a = _set(_good_align(T=M, W=11, E_al=513, A=128), topk_ids=r.topk_ids)
+        return lib.smr_route_align_workspace_size(ctypes.byref(r), ctypes.byref(a))
+    assert need(64) == 256                      # 704 slots: fused
+    tiles = -(-65 // 64)                        # 715 slots: counted, 2 tiles
+    words = 2 * tiles * 513 + 513
+    assert need(65) == 256 + ((words * 4 + 255) // 256) * 256
+    tiles = -(-16384 // 64)
+    words = 2 * tiles * 513 + 513
+    assert need(16384) == 256 + ((words * 4 + 255) // 256) * 256
+
+
 def test_route_align_consistency_checks(lib):
     r = _good_route()
     a = _good_align()
