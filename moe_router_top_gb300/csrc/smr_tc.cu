@@ -16,34 +16,38 @@
 // plus MMA operand reads reach the SM's shared-memory bandwidth, while the
 // pair form halves the gate bytes per SM.
 //
-// Per CTA, 256 threads (8 warps):
+// Per CTA, 256 threads (8 warps); warp w issues on scheduler w % 4:
 //   warp 0     TMA producer: x tile [128 x 64] and this CTA's half of each
 //              N<=256 gate piece [E/2 x 64] per k-block (128-byte swizzle),
 //              into a ring of shared-memory stages; loads of both CTAs
 //              complete the leader CTA's "full" barrier;
-//   warp 1     allocates TMEM for the pair (E fp32 columns x 128 lanes per
-//              CTA); in the leader CTA one thread issues the pair MMAs and
-//              commits (multicast to both CTAs) to free each stage;
-//   warps 4-7  meanwhile compute the shared-expert logit of their row from
-//              the x tile of each stage (CUDA cores, fp32 per k-block,
+//   warp 3     in the leader CTA, one thread issues the pair MMAs and commits
+//              (multicast to both CTAs) to free each stage; warps 0 and 3
+//              are alone on their schedulers;
+//   warp 1     also allocates TMEM for the pair (E fp32 columns x 128 lanes
+//              per CTA);
+//   warps 1, 2, 5, 6  meanwhile compute the shared-expert logit of their row
+//              from the x tile of each stage (CUDA cores, fp32 per k-block,
 //              compensated sum across k-blocks), read once the MMAs are done
-//              with the stage and before it is refilled.
+//              with the stage and before it is refilled;
+//   warps 4, 7 stage the bias and clear the expert counts.
 // Epilogue, all 8 warps: warp w reads TMEM lane quarter w%4 (thread = token
 // row) and column half w/4 (E/2 experts). Each half selects its own exact
 // top-k of bf16-rounded logits in three steps:
 //   1. one sweep over TMEM: add the bias, round to bf16 two at a time, keep
 //      the rounded row in the (now idle) stage ring, and take the maximum of
-//      each group of 8 consecutive columns; T = k-th largest group maximum
-//      (k groups hold a logit >= T, so every top-k logit, ties included, is
-//      >= T, and only groups whose maximum is >= T -- about k of them -- can
-//      hold one);
-//   2. append the logits >= T of those groups to a per-thread shared list
+//      each unit of 8 (or 4) consecutive columns; T = k-th largest unit
+//      maximum (k units hold a logit >= T, so every top-k logit, ties
+//      included, is >= T, and only units whose maximum is >= T -- about k of
+//      them -- can hold one);
+//   2. append the logits >= T of those units to a per-thread shared list
 //      with predicated stores (about 1.2k entries on random data);
-//   3. sort the list as ordered keys in registers (exact k-pass fallback over
-//      the half's rounded logits if the list overflows).
+//   3. order the list as keys in registers (a sorting network up to 16
+//      entries; exact k-pass fallback over the half's rounded logits if the
+//      list overflows).
 // Half 0 posts its top-k to shared memory; half 1 merges the two sorted lists
-// (bitonic merge), applies the softmax and writes the row with its shared
-// slot. Every mbarrier wait is bounded; on timeout the kernel sets the
+// (a k-step pointer merge), applies the softmax and writes the row with its
+// shared slot. Every mbarrier wait is bounded; on timeout the kernel sets the
 // workspace's error bit, skips its outputs and still frees TMEM and leaves
 // through the cluster barriers. Warps hand off through mbarriers only.
 #include <cudaTypedefs.h>
@@ -502,7 +506,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const bool side = p.S || XQ;  // warps 4-7 read every stage's x tile
+    const bool side = p.S || XQ;  // the side warps read every stage's x tile
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int hf = warp >> 2; // column half this warp takes in the epilogue
     const int row = q * 32 + lane;
@@ -661,10 +665,11 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     // expert columns [hf*E/2, (hf+1)*E/2); each half finds its own exact
     // top-k, half 1 merges both lists and writes the row. The epilogue runs
     // once per CTA after other kernels have used the SM, so its instructions
-    // are fetched cold: it is written as short rolled loops (k rounds of a
-    // 32-key maximum, a pointer merge) rather than unrolled sorting networks.
+    // are fetched cold and its code size counts next to its instruction
+    // count: short rolled loops (k steps to the next key, a pointer merge),
+    // with one 16-key sorting network as the only long straight-line part.
     griddep_wait();   // outputs and counts are written only after the previous kernel completed
-    __syncthreads();  // the bias and count staging of warps 2-3 is visible to every warp
+    __syncthreads();  // the bias and count staging of warps 4 and 7 is visible to every warp
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(accum), 0u, abort_flag));
     tc_fence_after();
     ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;  // one decision per warp
@@ -672,7 +677,7 @@ tc_route_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if constexpr (LO) {
         // logits only: this launch's columns [col0, col0 + E), the bias added
         // and rounded to bf16 (columns past E_valid: -inf), into the rows of
-        // the workspace; the shared logit of warps 4-7's rows. A select
+        // the workspace; the shared logit of the side warps' rows. A select
         // kernel takes the top-k over whole rows afterwards.
         if (ok) {
             const int ecols = p.E / 2, c_beg = hf * ecols;
