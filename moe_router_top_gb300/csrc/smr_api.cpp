@@ -6,11 +6,11 @@
 // prefill: M-aware moe_align block size", Purpose, for the alignment tier):
 //   route_align, M <= 16 : 1 launch  (small route + fused align)
 //   route_align, M > 16  : 1 tcgen05 route launch whose last CTA aligns all ids when
-//                          they fit one align CTA (<= 8192), else the route (which then
-//                          counts the experts of its rows) + 2 align launches;
+//                          there are at most kFusedAlignMax (704), else the route (which
+//                          then counts the experts of its rows) + 2 align launches;
 //                          with E > 512 or E % 32 != 0: ceil(E / 512) logits-only
 //                          tcgen05 launches + 1 select launch + 1 or 3 align launches
-//   route        : 1 launch;  align : 1 launch (numel <= 8192) or 3.
+//   route        : 1 launch;  align : 1 launch (numel <= kAlignSingleMax, 2048) or 3.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -365,7 +365,7 @@ smr_status run_route(const smr_route_args *a, void *ws, cudaStream_t stream,
     L.tile_counts = tile_counts;
     L.xq = a->hidden_fp8;
     L.xs = a->hidden_scales;
-    if (fused_align) {  // the ids fit one align CTA: the route's last CTA aligns them
+    if (fused_align) {  // at most kFusedAlignMax ids: the route's last CTA aligns them
         L.fa_A = effective_block_size(fused_align);
         L.fa_sorted = fused_align->sorted_token_ids;
         L.fa_eids = fused_align->expert_ids;

@@ -123,8 +123,8 @@ struct TcRouteLaunch {
     // per 128 elements [M][H / 128] (H % 128 == 0)
     uint8_t *xq;
     float *xs;
-    // optional: the align fused into the route (fa_sorted != nullptr; the
-    // M * (k + S) ids fit one align CTA): the last CTA to finish aligns them
+    // optional: the align fused into the route (fa_sorted != nullptr; at
+    // most kFusedAlignMax ids): the last CTA to finish aligns them
     int fa_A;
     int32_t *fa_sorted, *fa_eids, *fa_npp;
     int64_t fa_sorted_cap, fa_eids_cap;

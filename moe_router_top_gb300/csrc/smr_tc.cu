@@ -391,7 +391,7 @@ __device__ __forceinline__ void quant_block_e4m3(const uint4 (&a)[kTcBK / 8], co
     }
 }
 
-// The align fused into the route when the M * (k + S) ids fit one align CTA
+// The align fused into the route for at most kFusedAlignMax ids
 // ("[ROCm][Kernel] W4A16 MoE prefill: M-aware moe_align block size",
 // Purpose; the shared expert is expert E, appended to the sorted route stream
 // as "Netra Kernel ...", Reusing routing work instead of recomputing it, does
