@@ -110,36 +110,6 @@ __device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
     lo += err;
 }
 
-// Descending sort of N floats (bitonic network, N a power of two).
-template <int N>
-__device__ __forceinline__ void sort_desc(float (&a)[N]) {
-#pragma unroll
-    for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = ((i & size) == 0);
-                    const float x = a[i], y = a[j];
-                    const float hi = fmaxf(x, y), lo = fminf(x, y);
-                    a[i] = desc ? hi : lo;
-                    a[j] = desc ? lo : hi;
-                }
-            }
-        }
-    }
-}
-
-// Predicated shared store (no branch): writes v to addr only if c != 0. No
-// memory clobber, so surrounding loads can still be scheduled freely; callers
-// put one compiler barrier after their store loop.
-__device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, uint32_t c) {
-    asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %2, 0;\n @p st.shared.u32 [%0], %1;\n}"
-                 ::"r"(addr), "r"(v), "r"(c));
-}
-
 // Descending sort of N unsigned keys: Batcher's odd-even merge sort (merges
 // of sorted runs of p = 1, 2, 4, ... keys; each merge compares keys k apart
 // for k = p, p/2, ..., 1, only within one run pair). The comparator list is
